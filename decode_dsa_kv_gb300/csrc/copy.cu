@@ -1,0 +1,179 @@
+// Row movement of the decode-step KV path: dsa_gather_kv serves one layer's
+// selected rows (GLM-5.2 shared-Indexer KV Cache Offload, §5 DsaServe and
+// §5.1; the base design's GatherSelectionKvCache, §2.1), dsa_refill_pool
+// installs one layer's missed rows into their FIFO victim slots and, at the
+// group's last layer, updates the pool metadata (§4.4 refill after SFA, §5
+// DsaInstall, §5.1 metadata update at the group's last layer).
+//
+// Both are pure 16-byte copies. The gather is flattened over every 16-byte
+// piece of the selection (72 per 1152-byte row), so consecutive threads move
+// consecutive bytes of a row whichever source it comes from: HBM for pool
+// hits, pinned host memory read in place over the host link for misses. Each
+// thread keeps several loads in flight before its stores.
+#include <climits>
+
+#include "common.cuh"
+
+namespace dsakv {
+namespace {
+
+constexpr int kGatherThreads = 256;
+constexpr int kUnroll = 4;
+
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_v4(uint4* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(
+    const int32_t* __restrict__ src_map, int k, int64_t total, const uint4* __restrict__ pool,
+    int P, const uint4* __restrict__ host, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
+    uint4* __restrict__ sel, int32_t* err) {
+  const int64_t step = int64_t(gridDim.x) * kGatherThreads * kUnroll;
+  int bad = 0;
+  for (int64_t base = int64_t(blockIdx.x) * kGatherThreads * kUnroll + threadIdx.x; base < total;
+       base += step) {
+    uint4 v[kUnroll];
+    bool ok[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t c = base + int64_t(u) * kGatherThreads;
+      ok[u] = false;
+      if (c < total) {
+        const int64_t row = c / DSA_ROW_CHUNKS;
+        const int part = static_cast<int>(c - row * DSA_ROW_CHUNKS);
+        const int b = static_cast<int>(row / k);
+        const int src = __ldg(src_map + row);
+        const uint4* from = nullptr;
+        if (src >= 0) {
+          if (src < P) from = pool + (int64_t(b) * P + src) * DSA_ROW_CHUNKS + part;
+          else bad |= TS_DEVERR_SLOT_RANGE;
+        } else {
+          const int64_t t = -1 - int64_t(src);
+          if (t < __ldg(ctx_len + b)) from = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS + part;
+          else bad |= TS_DEVERR_ID_RANGE;
+        }
+        if (from) {
+          v[u] = ld_nc_v4(from);
+          ok[u] = true;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (ok[u]) st_v4(sel + base + int64_t(u) * kGatherThreads, v[u]);
+  }
+  if (bad) report(err, bad);
+}
+
+// One warp per (request, miss) pair: 72 pieces, lanes stride by 32.
+__global__ void __launch_bounds__(256) refill_kernel(
+    const int32_t* __restrict__ miss_ids, const int32_t* __restrict__ miss_pos,
+    const int32_t* __restrict__ victim, const uint8_t* __restrict__ install,
+    const int32_t* __restrict__ miss_count, int B, int k, const uint4* __restrict__ sel,
+    uint4* __restrict__ pool, int P, int update_metadata, int32_t* __restrict__ pool_tags,
+    int32_t* __restrict__ fifo_ptr, const int32_t* __restrict__ ptr_next, int S, int W,
+    int32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t r = warp; r < int64_t(B) * k; r += nwarps) {
+    const int b = static_cast<int>(r / k);
+    const int i = static_cast<int>(r - int64_t(b) * k);
+    if (i >= __ldg(miss_count + b)) continue;
+    if (!__ldg(install + r)) continue;
+    const int v = __ldg(victim + r);
+    const int j = __ldg(miss_pos + r);
+    if (v < 0 || v >= P || j < 0 || j >= k) {
+      if (lane == 0) report(err, TS_DEVERR_SLOT_RANGE);
+      continue;
+    }
+    const uint4* from = sel + (int64_t(b) * k + j) * DSA_ROW_CHUNKS;
+    uint4* to = pool + (int64_t(b) * P + v) * DSA_ROW_CHUNKS;
+    uint4 a = ld_nc_v4(from + lane);
+    uint4 c = ld_nc_v4(from + lane + 32);
+    uint4 d;
+    if (lane < DSA_ROW_CHUNKS - 64) d = ld_nc_v4(from + lane + 64);
+    st_v4(to + lane, a);
+    st_v4(to + lane + 32, c);
+    if (lane < DSA_ROW_CHUNKS - 64) st_v4(to + lane + 64, d);
+    if (update_metadata && lane == 0) pool_tags[int64_t(b) * P + v] = __ldg(miss_ids + r);
+  }
+  if (update_metadata) {
+    const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nth = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t q = tid; q < int64_t(B) * S; q += nth) {
+      const int p = __ldg(ptr_next + q);
+      if (p < 0 || p >= W) {
+        report(err, TS_DEVERR_PTR_RANGE);
+        continue;
+      }
+      fifo_ptr[q] = p;
+    }
+  }
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+}  // namespace dsakv
+
+using namespace dsakv;
+
+extern "C" ts_status dsa_gather_kv(const int32_t* src_map, int B, int k, const void* pool_l, int P,
+                                   const void* host_l, int64_t ctx_stride, const int32_t* ctx_len,
+                                   void* sel_l, int32_t* err, cudaStream_t stream) {
+  if (!src_map || !pool_l || !host_l || !ctx_len || !sel_l) return TS_ERR_INVALID_ARG;
+  if (B <= 0 || k <= 0 || P <= 0 || ctx_stride <= 0) return TS_ERR_INVALID_ARG;
+  if (!aligned16(pool_l) || !aligned16(host_l) || !aligned16(sel_l)) return TS_ERR_INVALID_ARG;
+  const int64_t total = int64_t(B) * k * DSA_ROW_CHUNKS;
+  const int64_t per_block = int64_t(kGatherThreads) * kUnroll;
+  int64_t blocks = (total + per_block - 1) / per_block;
+  const int64_t cap = int64_t(sm_count()) * 8;  // 8 resident CTAs of 256 threads per SM
+  if (blocks > cap) blocks = cap;
+  gather_kernel<<<static_cast<unsigned>(blocks), kGatherThreads, 0, stream>>>(
+      src_map, k, total, static_cast<const uint4*>(pool_l), P, static_cast<const uint4*>(host_l),
+      ctx_stride, ctx_len, static_cast<uint4*>(sel_l), err);
+  return launch_status();
+}
+
+extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* miss_pos,
+                                     const int32_t* victim, const uint8_t* install,
+                                     const int32_t* miss_count, int B, int k, const void* sel_l,
+                                     void* pool_l, int P, int update_metadata, int32_t* pool_tags,
+                                     int32_t* fifo_ptr, const int32_t* ptr_next, int S, int W,
+                                     int32_t* err, cudaStream_t stream) {
+  if (!miss_ids || !miss_pos || !victim || !install || !miss_count || !sel_l || !pool_l)
+    return TS_ERR_INVALID_ARG;
+  if (B <= 0 || k <= 0 || P <= 0) return TS_ERR_INVALID_ARG;
+  if (update_metadata && (!pool_tags || !fifo_ptr || !ptr_next || S <= 0 || W <= 0 || S * W != P))
+    return TS_ERR_INVALID_ARG;
+  if (!aligned16(sel_l) || !aligned16(pool_l)) return TS_ERR_INVALID_ARG;
+  const int64_t warps = int64_t(B) * k;
+  int64_t blocks = (warps * 32 + 255) / 256;
+  const int64_t cap = int64_t(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  refill_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      miss_ids, miss_pos, victim, install, miss_count, B, k, static_cast<const uint4*>(sel_l),
+      static_cast<uint4*>(pool_l), P, update_metadata, pool_tags, fifo_ptr, ptr_next, S, W, err);
+  return launch_status();
+}

@@ -1,0 +1,290 @@
+// dsa_plan: the shared plan of one IndexShare group (GLM-5.2 shared-Indexer KV
+// Cache Offload, §4.2 shared planning and §5 DsaPlan; pool policy §4.3).
+//
+// One CTA per request. The request's pool tags are staged in shared memory;
+// every selected id is looked up in the W ways of its set (token mod S); the
+// misses are compacted in ascending id (warp ballots + a block scan when the
+// ids arrive sorted and distinct, a shared-memory bitonic sort otherwise),
+// counted per set, bucketed by set, and ranked inside their set to get the
+// FIFO victim slot and whether the miss survives a same-step overflow.
+#include <climits>
+
+#include "common.cuh"
+
+namespace dsakv {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kMaxK = 4096;
+constexpr size_t kMaxSmem = 200 * 1024;
+
+struct PlanSmem {
+  int* tags;      // [P]
+  int* cnt;       // [S]  misses per set
+  int* off;       // [S]  exclusive prefix of cnt
+  int* fill;      // [S]  bucket fill counters
+  int* mids;      // [k]  miss ids, ascending
+  int* mpos;      // [k]  first position of each miss
+  int* bucket;    // [k]  miss ids grouped by set
+  int* src;       // [k]  this request's src_map
+  uint64_t* key;  // [pow2(k)] sort keys (general path)
+  int* scratch;   // [64]
+  int* flags;     // [4]
+};
+
+__host__ __device__ inline int pow2_at_least(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// sort keys first (8-byte entries, at least 16 bytes so the int region that
+// follows stays 16-byte aligned for the int4 tag reads)
+__host__ __device__ inline size_t key_bytes(int k) {
+  return size_t(pow2_at_least(k < 2 ? 2 : k)) * 8;
+}
+
+__host__ __device__ inline size_t plan_smem_bytes(int P, int S, int k) {
+  return key_bytes(k) + size_t(P) * 4 + size_t(S) * 12 + size_t(k) * 16 + 64 * 4 + 4 * 4 + 64;
+}
+
+__device__ PlanSmem carve(char* base, int P, int S, int k) {
+  PlanSmem s;
+  uint64_t* key = reinterpret_cast<uint64_t*>(base);  // 8-byte aligned first
+  s.key = key;
+  int* p = reinterpret_cast<int*>(base + key_bytes(k));
+  s.tags = p;
+  p += P;
+  s.cnt = p;
+  p += S;
+  s.off = p;
+  p += S;
+  s.fill = p;
+  p += S;
+  s.mids = p;
+  p += k;
+  s.mpos = p;
+  p += k;
+  s.bucket = p;
+  p += k;
+  s.src = p;
+  p += k;
+  s.scratch = p;
+  p += 64;
+  s.flags = p;
+  return s;
+}
+
+// Lowest way of set `set` whose tag equals t, or -1.
+__device__ __forceinline__ int lookup(const int* tags, int set, int W, int t) {
+  const int* row = tags + set * W;
+  if ((W & 3) == 0) {
+    for (int w = 0; w < W; w += 4) {
+      int4 v = *reinterpret_cast<const int4*>(row + w);
+      if (v.x == t) return w;
+      if (v.y == t) return w + 1;
+      if (v.z == t) return w + 2;
+      if (v.w == t) return w + 3;
+    }
+    return -1;
+  }
+  for (int w = 0; w < W; ++w)
+    if (row[w] == t) return w;
+  return -1;
+}
+
+__global__ void __launch_bounds__(kThreads) dsa_plan_kernel(
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ ctx_len, int k,
+    const int32_t* __restrict__ pool_tags, const int32_t* __restrict__ fifo_ptr, int S, int W,
+    int32_t* __restrict__ src_map, int32_t* __restrict__ miss_ids, int32_t* __restrict__ miss_pos,
+    int32_t* __restrict__ victim, uint8_t* __restrict__ install, int32_t* __restrict__ miss_count,
+    int32_t* __restrict__ ptr_next, int32_t* err) {
+  extern __shared__ __align__(16) char smem_raw[];
+  const int P = S * W;
+  PlanSmem sm = carve(smem_raw, P, S, k);
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int n = ctx_len[b];
+  const int32_t* id_row = ids + int64_t(b) * k;
+  const int32_t* tag_row = pool_tags + int64_t(b) * P;
+  const int32_t* ptr_row = fifo_ptr + int64_t(b) * S;
+
+  // stage tags, clear per-set counters
+  if ((P & 3) == 0 && aligned16(tag_row)) {
+    for (int i = tid; i < P / 4; i += kThreads)
+      reinterpret_cast<int4*>(sm.tags)[i] = __ldg(reinterpret_cast<const int4*>(tag_row) + i);
+  } else {
+    for (int i = tid; i < P; i += kThreads) sm.tags[i] = __ldg(tag_row + i);
+  }
+  for (int s = tid; s < S; s += kThreads) {
+    sm.cnt[s] = 0;
+    sm.fill[s] = 0;
+    const int p = ptr_row[s];
+    if (p < 0 || p >= W) report(err, TS_DEVERR_PTR_RANGE);
+  }
+  __syncthreads();
+
+  // classify, and check whether the ids are strictly ascending
+  bool ascending = true;
+  bool bad_id = false;
+  for (int j = tid; j < k; j += kThreads) {
+    const int t = id_row[j];
+    if (j + 1 < k && !(t < id_row[j + 1])) ascending = false;
+    int src;
+    if (t < 0 || t >= n) {
+      src = INT_MIN;
+      bad_id = true;
+    } else {
+      const int set = t % S;
+      const int way = lookup(sm.tags, set, W, t);
+      src = way >= 0 ? set * W + way : -1 - t;
+    }
+    src_map[int64_t(b) * k + j] = src;
+    sm.src[j] = src;
+  }
+  if (bad_id) report(err, TS_DEVERR_ID_RANGE);
+  ascending = __syncthreads_and(ascending);
+
+  int M;
+  if (ascending) {
+    // misses in position order are already ascending and distinct: an
+    // ordered compaction. Each thread owns a contiguous run of positions.
+    const int per = (k + kThreads - 1) / kThreads;
+    const int j0 = tid * per, j1 = min(j0 + per, k);
+    int c = 0;
+    for (int j = j0; j < j1; ++j) {
+      const int src = sm.src[j];
+      c += (src < 0 && src != INT_MIN);
+    }
+    int total;
+    int o = block_exclusive_scan(c, sm.scratch, &total);
+    for (int j = j0; j < j1; ++j) {
+      const int src = sm.src[j];
+      if (src < 0 && src != INT_MIN) {
+        sm.mids[o] = -1 - src;
+        sm.mpos[o] = j;
+        ++o;
+      }
+    }
+    M = total;
+  } else {
+    // general ids: sort (id, position) pairs of the misses, keep the first of
+    // every id
+    const int np2 = pow2_at_least(k);
+    for (int j = tid; j < np2; j += kThreads) {
+      uint64_t key = ~0ull;
+      if (j < k) {
+        const int src = sm.src[j];
+        if (src < 0 && src != INT_MIN)
+          key = (static_cast<uint64_t>(static_cast<uint32_t>(-1 - src)) << 32) | uint32_t(j);
+      }
+      sm.key[j] = key;
+    }
+    __syncthreads();
+    for (int size = 2; size <= np2; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < np2 / 2; i += kThreads) {
+          const int lo = 2 * i - (i & (stride - 1));
+          const int hi = lo + stride;
+          const bool up = (lo & size) == 0;
+          const uint64_t a = sm.key[lo], c2 = sm.key[hi];
+          if ((a > c2) == up) {
+            sm.key[lo] = c2;
+            sm.key[hi] = a;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    const int per = (np2 + kThreads - 1) / kThreads;
+    const int j0 = tid * per, j1 = min(j0 + per, np2);
+    auto keep = [&](int j) {
+      const uint64_t e = sm.key[j];
+      if (e == ~0ull) return false;
+      return j == 0 || (sm.key[j - 1] >> 32) != (e >> 32);
+    };
+    int c = 0;
+    for (int j = j0; j < j1; ++j) c += keep(j);
+    int total;
+    int o = block_exclusive_scan(c, sm.scratch, &total);
+    for (int j = j0; j < j1; ++j) {
+      if (keep(j)) {
+        sm.mids[o] = static_cast<int>(sm.key[j] >> 32);
+        sm.mpos[o] = static_cast<int>(sm.key[j] & 0xffffffffu);
+        ++o;
+      }
+    }
+    M = total;
+  }
+  __syncthreads();
+
+  // misses per set, set offsets, buckets
+  for (int i = tid; i < M; i += kThreads) atomicAdd(&sm.cnt[sm.mids[i] % S], 1);
+  __syncthreads();
+  {
+    const int per = (S + kThreads - 1) / kThreads;
+    const int s0 = tid * per, s1 = min(s0 + per, S);
+    int c = 0;
+    for (int s = s0; s < s1; ++s) c += sm.cnt[s];
+    int total;
+    int o = block_exclusive_scan(c, sm.scratch, &total);
+    for (int s = s0; s < s1; ++s) {
+      sm.off[s] = o;
+      o += sm.cnt[s];
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < M; i += kThreads) {
+    const int t = sm.mids[i], set = t % S;
+    sm.bucket[sm.off[set] + atomicAdd(&sm.fill[set], 1)] = t;
+  }
+  __syncthreads();
+
+  // rank inside the set (ascending id) -> victim slot and survival
+  for (int i = tid; i < M; i += kThreads) {
+    const int t = sm.mids[i], set = t % S;
+    const int c = sm.cnt[set], o = sm.off[set];
+    int r = 0;
+    for (int e = 0; e < c; ++e) r += sm.bucket[o + e] < t;
+    const int p = ptr_row[set];
+    const int pp = (p >= 0 && p < W) ? p : 0;
+    const int64_t g = int64_t(b) * k + i;
+    miss_ids[g] = t;
+    miss_pos[g] = sm.mpos[i];
+    victim[g] = set * W + (pp + r) % W;
+    install[g] = r >= c - W ? 1 : 0;
+  }
+  for (int s = tid; s < S; s += kThreads) {
+    const int p = ptr_row[s];
+    const int pp = (p >= 0 && p < W) ? p : 0;
+    ptr_next[int64_t(b) * S + s] = (pp + sm.cnt[s]) % W;
+  }
+  if (tid == 0) miss_count[b] = M;
+}
+
+}  // namespace
+}  // namespace dsakv
+
+using namespace dsakv;
+
+extern "C" ts_status dsa_plan(const int32_t* ids, const int32_t* ctx_len, int B, int k,
+                              const int32_t* pool_tags, const int32_t* fifo_ptr, int S, int W,
+                              int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
+                              int32_t* victim, uint8_t* install, int32_t* miss_count,
+                              int32_t* ptr_next, int32_t* err, cudaStream_t stream) {
+  if (!ids || !ctx_len || !pool_tags || !fifo_ptr || !src_map || !miss_ids || !miss_pos ||
+      !victim || !install || !miss_count || !ptr_next)
+    return TS_ERR_INVALID_ARG;
+  if (B <= 0 || k <= 0 || S <= 0 || W <= 0) return TS_ERR_INVALID_ARG;
+  if (W > 32 || k > kMaxK || B > 2147483647 / 2) return TS_ERR_UNSUPPORTED;
+  if (int64_t(S) * W > (1 << 24)) return TS_ERR_UNSUPPORTED;
+  const size_t smem = plan_smem_bytes(S * W, S, k);
+  if (smem > kMaxSmem) return TS_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(dsa_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(smem)) != cudaSuccess)
+    return TS_ERR_CUDA;
+  dsa_plan_kernel<<<B, kThreads, smem, stream>>>(ids, ctx_len, k, pool_tags, fifo_ptr, S, W,
+                                                 src_map, miss_ids, miss_pos, victim, install,
+                                                 miss_count, ptr_next, err);
+  return launch_status();
+}

@@ -1,0 +1,378 @@
+// sfa_mla_decode: sparse absorbed-MLA decode attention over the selected rows
+// (GLM-5.2 shared-Indexer KV Cache Offload, §2.1: SFA runs only over the
+// 2048 rows the indexer selected; TokenSpeed engine audit, MLA section: one
+// latent row of 512 latent + 64 rope values is both K and V, and decode is
+// split over the KV rows with fp32 partials merged by log-sum-exp).
+//
+// One CTA per (request b, head tile of 128 heads, chunk of 256 selected rows),
+// on the 5th-generation tensor cores:
+//   warp 0  : TMA producer (one thread): Q and K tiles for the score product,
+//             then V tiles for the value product, through a 3-stage ring of
+//             48 KB stages (128-byte swizzle).
+//   warp 1  : allocates 512 TMEM columns; one thread issues tcgen05.mma.
+//   warps 2-5: softmax and epilogue, one TMEM lane (= one head) per thread.
+// Steps inside the CTA:
+//   S[128 x 256] = Q[128 x 576] K[256 x 576]^T   -> TMEM columns 0..255
+//   p = exp2(S*scale*log2e - max)  rounded to bf16, written to shared memory
+//       in the K-major 128-byte-swizzled layout the MMA reads
+//   O[:, 0:256]   = P V[:, 0:256]    -> TMEM columns 256..511
+//   O[:, 256:512] = P V[:, 256:512]  -> TMEM columns 0..255 (S is dead by then)
+//   O, max and row sum of the chunk -> fp32 workspace
+// A second kernel merges the chunks of a request: out = sum_c w_c O_c /
+// sum_c w_c l_c with w_c = exp2(m_c - max_c m_c).
+#include <cmath>
+
+#include "common.cuh"
+
+namespace dsakv {
+namespace {
+
+constexpr int kHeads = 128;  // MMA M
+constexpr int kChunk = 256;  // rows per CTA: N of the score product, K of the value product
+constexpr int kKB = 9;       // 64-wide blocks of the 576 dims
+constexpr int kStages = 3;
+constexpr uint32_t kQBytes = kHeads * 128;           // 128 heads x 64 dims
+constexpr uint32_t kKBytes = kChunk * 128;           // 256 rows x 64 dims
+constexpr uint32_t kStageBytes = kQBytes + kKBytes;  // 48 KB
+constexpr uint32_t kVBox = 64 * 128;                 // 64 rows x 64 dims
+constexpr uint32_t kVBytes = 4 * kVBox;              // 64 rows x 256 dims
+constexpr uint32_t kPBlock = kHeads * 128;           // 128 heads x 64 rows
+constexpr uint32_t kPBytes = 4 * kPBlock;            // 128 heads x 256 rows
+constexpr int kLoads = kKB + 8;                      // 9 score stages + 8 value stages
+constexpr int kThreads = 192;
+constexpr uint32_t kBarBytes = 256;
+constexpr uint32_t kSmemBytes = 1024 + kPBytes + kStages * kStageBytes + kBarBytes;
+constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s of global timer per wait
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct Bars {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t s_full;
+  uint64_t p_full;
+  uint64_t o_full;
+  uint64_t drain;
+  uint32_t tmem_slot;
+  int abort;
+  int issued;
+};
+static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
+
+// Wait by lane 0 of the warp, result shared by the whole warp (which is then
+// converged for the .sync.aligned tcgen05 instructions that follow).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort, kWaitLimit) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  return ok != 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sfa_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, int H, int k, int HG, int C,
+                     float scale_log2, float* __restrict__ opart, float2* __restrict__ ml,
+                     int32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* p_tile = base;
+  uint8_t* stages = base + kPBytes;
+  Bars* bars = reinterpret_cast<Bars*>(stages + kStages * kStageBytes);
+  volatile int* abort = &bars->abort;
+
+  const int c = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    bars->issued = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      for (int it = 0; it < kLoads; ++it) {
+        const int s = it % kStages;
+        if (it >= kStages &&
+            !mbar_wait_bounded(&bars->empty[s], ((it / kStages) - 1) & 1, abort, kWaitLimit))
+          break;
+        uint8_t* st = stages + s * kStageBytes;
+        if (it < kKB) {
+          mbar_expect_tx(&bars->full[s], kStageBytes);
+          tma_load_3d(st, &tm_q, &bars->full[s], it * 64, hg * kHeads, b);
+          tma_load_3d(st + kQBytes, &tm_k, &bars->full[s], it * 64, c * kChunk, b);
+        } else {
+          const int v = it - kKB, half = v >> 2, rb = v & 3;
+          mbar_expect_tx(&bars->full[s], kVBytes);
+          for (int j = 0; j < 4; ++j)
+            tma_load_3d(st + j * kVBox, &tm_v, &bars->full[s], half * 256 + j * 64,
+                        c * kChunk + rb * 64, b);
+        }
+        bars->issued = it + 1;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(kHeads, kChunk, false, false);
+      const uint32_t id_pv = idesc_bf16_f32(kHeads, 256, false, true);
+      bool ok = true;
+      for (int it = 0; it < kKB && ok; ++it) {
+        const int s = it % kStages;
+        ok = mbar_wait_bounded(&bars->full[s], (it / kStages) & 1, abort, kWaitLimit);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qa = smem_addr(stages + s * kStageBytes);
+        const uint32_t ka = qa + kQBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_bf16(tmem, smem_desc_sw128(qa + kk * 32, 16, 1024),
+                      smem_desc_sw128(ka + kk * 32, 16, 1024), id_s, (it | kk) != 0);
+        tc_commit(&bars->empty[s]);
+      }
+      if (ok) {
+        tc_commit(&bars->s_full);
+        ok = mbar_wait_bounded(&bars->p_full, 0, abort, kWaitLimit);
+      }
+      if (ok) tc_fence_after();
+      for (int it = kKB; it < kLoads && ok; ++it) {
+        const int s = it % kStages;
+        ok = mbar_wait_bounded(&bars->full[s], (it / kStages) & 1, abort, kWaitLimit);
+        if (!ok) break;
+        tc_fence_after();
+        const int v = it - kKB, half = v >> 2, rb = v & 3;
+        const uint32_t d = tmem + (half == 0 ? 256u : 0u);
+        const uint32_t pa = smem_addr(p_tile) + rb * kPBlock;
+        const uint32_t va = smem_addr(stages + s * kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_bf16(d, smem_desc_sw128(pa + kk * 32, 16, 1024),
+                      smem_desc_sw128(va + kk * 2048, kVBox, 1024), id_pv, (rb | kk) != 0);
+        tc_commit(&bars->empty[s]);
+      }
+      if (ok) tc_commit(&bars->o_full);
+    }
+  } else {
+    // ---------------- softmax + epilogue: one head per thread ----------------
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    const int nvalid = min(kChunk, k - c * kChunk);
+    float m = -INFINITY, l = 0.f;
+    bool ok = warp_wait(&bars->s_full, 0, abort);
+    if (ok) {
+      tc_fence_after();
+      uint32_t r[32];
+      for (int cb = 0; cb < kChunk / 32; ++cb) {
+        tmem_ld32(trow + cb * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (cb * 32 + i < nvalid) m = fmaxf(m, __uint_as_float(r[i]) * scale_log2);
+      }
+      for (int cb = 0; cb < kChunk / 32; ++cb) {
+        tmem_ld32(trow + cb * 32, r);
+        tmem_wait_ld();
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c0 = cb * 32 + 2 * i;
+          const float p0 = c0 < nvalid ? exp2f(__uint_as_float(r[2 * i]) * scale_log2 - m) : 0.f;
+          const float p1 =
+              c0 + 1 < nvalid ? exp2f(__uint_as_float(r[2 * i + 1]) * scale_log2 - m) : 0.f;
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          l += __low2float(h2) + __high2float(h2);
+          packed[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        uint8_t* blk = p_tile + (cb >> 1) * kPBlock + row * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int chunk = (cb & 1) * 4 + j;
+          *reinterpret_cast<uint4*>(blk + ((chunk ^ (row & 7)) << 4)) =
+              make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+      ok = warp_wait(&bars->o_full, 0, abort);
+    }
+    if (ok) {
+      tc_fence_after();
+      const int head = hg * kHeads + row;
+      const size_t slot = ((size_t(b) * HG + hg) * C + c) * kHeads + row;
+      float* orow = opart + slot * DSA_DV;
+      uint32_t r[32];
+      for (int cb = 0; cb < DSA_DV / 32; ++cb) {
+        const int v0 = cb * 32;
+        const uint32_t col = v0 < 256 ? 256u + v0 : uint32_t(v0 - 256);
+        tmem_ld32(trow + col, r);
+        tmem_wait_ld();
+        if (head < H) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(orow + v0 + 4 * j) =
+                make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+      if (head < H) ml[slot] = make_float2(m, l);
+    }
+  }
+
+  // ---------------- teardown ----------------
+  tc_fence_before();
+  __syncthreads();
+  if (bars->abort) {
+    if (threadIdx.x == 0) report(err, TS_DEVERR_TIMEOUT);
+    if (warp == 0 && lane == 0) {
+      // let the copies already issued land before the CTA exits
+      const int issued = bars->issued;
+      for (int it = issued - kStages < 0 ? 0 : issued - kStages; it < issued; ++it)
+        mbar_wait_timed(&bars->full[it % kStages], (it / kStages) & 1, kWaitLimit);
+    }
+    if (warp == 1 && lane == 0) {
+      // every tcgen05 operation this thread issued completes before the free
+      tc_commit(&bars->drain);
+      mbar_wait_timed(&bars->drain, 0, kWaitLimit);
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge the chunks of one (request, head): out = sum_c w_c O_c / sum_c w_c l_c.
+__global__ void __launch_bounds__(128) sfa_combine_kernel(const float* __restrict__ opart,
+                                                          const float2* __restrict__ ml, int H,
+                                                          int HG, int C,
+                                                          __nv_bfloat16* __restrict__ out,
+                                                          float* __restrict__ lse) {
+  const int bh = blockIdx.x;
+  const int b = bh / H, h = bh - b * H;
+  const int hg = h / kHeads, row = h - hg * kHeads;
+  const size_t slot0 = ((size_t(b) * HG + hg) * C) * kHeads + row;
+  float mx = -INFINITY;
+  for (int c = 0; c < C; ++c) mx = fmaxf(mx, ml[slot0 + size_t(c) * kHeads].x);
+  float denom = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int v = threadIdx.x * 4;
+  for (int c = 0; c < C; ++c) {
+    const size_t slot = slot0 + size_t(c) * kHeads;
+    const float2 e = ml[slot];
+    const float w = exp2f(e.x - mx);
+    denom += w * e.y;
+    const float4 o = *reinterpret_cast<const float4*>(opart + slot * DSA_DV + v);
+    acc.x += w * o.x;
+    acc.y += w * o.y;
+    acc.z += w * o.z;
+    acc.w += w * o.w;
+  }
+  const float inv = 1.f / denom;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  __nv_bfloat16* o = out + (size_t(b) * H + h) * DSA_DV + v;
+  *reinterpret_cast<__nv_bfloat162*>(o) = lo;
+  *reinterpret_cast<__nv_bfloat162*>(o + 2) = hi;
+  if (lse && threadIdx.x == 0) lse[size_t(b) * H + h] = mx * kLn2 + logf(denom);
+}
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+// 3-D map over rows of 576 bf16: dims {576, rows, batch}; box {64, box_rows, 1}.
+bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t batch, uint32_t box_rows) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {DSA_D, rows, batch};
+  const cuuint64_t strides[2] = {DSA_ROW_BYTES, rows * DSA_ROW_BYTES};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace dsakv
+
+using namespace dsakv;
+
+extern "C" size_t sfa_workspace_size(int B, int H, int k) {
+  if (B <= 0 || H <= 0 || k <= 0) return 0;
+  const size_t HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
+  const size_t slots = size_t(B) * HG * C * kHeads;
+  return align256(slots * DSA_DV * 4) + align256(slots * 8);
+}
+
+extern "C" ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int H, int k,
+                                    float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                                    int32_t* err, cudaStream_t stream) {
+  if (!q || !sel_l || !out || !ws) return TS_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || k <= 0 || !std::isfinite(scale)) return TS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(sel_l) || !aligned16(out)) return TS_ERR_INVALID_ARG;
+  if (B > 65535 || H > 65535 * kHeads || int64_t(B) * H > 2147483647) return TS_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < sfa_workspace_size(B, H, k))
+    return TS_ERR_WORKSPACE;
+  const int HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!make_map(&tm_q, q, H, B, kHeads) || !make_map(&tm_k, sel_l, k, B, kChunk) ||
+      !make_map(&tm_v, sel_l, k, B, 64))
+    return TS_ERR_CUDA;
+  const size_t slots = size_t(B) * HG * C * kHeads;
+  float* opart = static_cast<float*>(ws);
+  float2* ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + align256(slots * DSA_DV * 4));
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(sfa_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return TS_ERR_CUDA;
+    attr = true;
+  }
+  sfa_chunk_kernel<<<dim3(C, HG, B), kThreads, kSmemBytes, stream>>>(
+      tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, err);
+  if (cudaGetLastError() != cudaSuccess) return TS_ERR_CUDA;
+  sfa_combine_kernel<<<unsigned(int64_t(B) * H), 128, 0, stream>>>(
+      opart, ml, H, HG, C, static_cast<__nv_bfloat16*>(out), lse);
+  return launch_status();
+}

@@ -1,0 +1,197 @@
+/*
+ * dsakv.h -- C ABI of the decode-step KV path of DeepSeek-Sparse-Attention
+ * style serving with host-offloaded KV and a set-associative FIFO device pool,
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * Sources the operations follow:
+ *   [GLM] "GLM-5.2 shared-Indexer KV Cache Offload" (CANN cann-recipes-infer
+ *         guide): §2.1 Lightning-Indexer top-k and sparse flash attention,
+ *         §4.2 shared planning, §4.3 set-associative FIFO pool, §4.4 SFA first
+ *         and refill later, §5 the DsaPlan / DsaServe / DsaInstall split,
+ *         §5.1 model-side orchestration.
+ *   [TS]  "TokenSpeed" engine audit, MLA kernel section: the latent row
+ *         (512 latent + 64 rope values) is stored once and serves as K and V.
+ *
+ * Shapes: B requests, k selected positions per request, S sets of W ways
+ * (pool of P = S*W entries per request and layer), H query heads, latent
+ * rows of D = 576 bf16 values (1152 bytes: 512 latent + 64 rope).
+ *
+ * Conventions for every call:
+ *   - Ownership: the caller owns every buffer. The library keeps no state
+ *     between calls and allocates no memory (workspaces are passed in).
+ *   - Pointers are device pointers unless stated otherwise; host KV is pinned
+ *     host memory, passed as the device-accessible address of that memory
+ *     (see ts_host_register).
+ *   - Streams: a call only enqueues work on `stream`; it never synchronizes.
+ *     Ordering between streams is the caller's (events).
+ *   - Errors: shapes, sizes and alignment are checked on the host before
+ *     anything is launched (TS_ERR_INVALID_ARG / TS_ERR_UNSUPPORTED /
+ *     TS_ERR_WORKSPACE, nothing enqueued). A failed launch returns
+ *     TS_ERR_CUDA. Data found wrong on the device (an id outside the context,
+ *     a slot outside the pool, a NaN score, a wait that gave up) sets bits of
+ *     the caller's int32 error word `err` (TS_DEVERR_*) and the offending
+ *     element is skipped; nothing traps. `err` may be NULL to skip reporting.
+ *     The caller clears it and reads it after the stream's work completes
+ *     (ts_read_error does both the wait and the read).
+ */
+#ifndef DSAKV_H
+#define DSAKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TS_OK = 0,
+  TS_ERR_INVALID_ARG = -1,
+  TS_ERR_UNSUPPORTED = -2,
+  TS_ERR_WORKSPACE = -3,
+  TS_ERR_CUDA = -4,
+  TS_ERR_DEVICE_CHECK = -5
+} ts_status;
+
+/* Bits of the device error word. */
+#define TS_DEVERR_ID_RANGE 0x01   /* token id outside [0, ctx_len) */
+#define TS_DEVERR_NAN 0x02        /* NaN indexer score */
+#define TS_DEVERR_SLOT_RANGE 0x04 /* pool slot / selection position out of range */
+#define TS_DEVERR_PTR_RANGE 0x08  /* FIFO pointer outside [0, W) */
+#define TS_DEVERR_CTX 0x10        /* ctx_len outside [k, max_ctx] */
+#define TS_DEVERR_TIMEOUT 0x20    /* a bounded wait inside a kernel gave up */
+#define TS_DEVERR_COUNT 0x40      /* a selection did not come out at size k */
+
+#define TS_D 576        /* values per latent row */
+#define TS_D_LATENT 512 /* latent ("nope") part, also the V part */
+
+/* Text for a status code (static storage). */
+const char* ts_status_string(ts_status status);
+
+/* Page-lock and map caller-owned host memory [host, host + bytes) so that
+ * kernels can read it in place (zero-copy), and return the device-accessible
+ * address in *dev. Pair with ts_host_unregister. Host only; no device work. */
+ts_status ts_host_register(void* host, size_t bytes, void** dev);
+ts_status ts_host_unregister(void* host);
+
+/* Wait for `stream`, read the error word into *bits (host), clear it on the
+ * device. Returns TS_ERR_DEVICE_CHECK when any bit was set. */
+ts_status ts_read_error(int32_t* err, int32_t* bits, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * ts_topk -- top-k of the Lightning-Indexer scores ([GLM] §2.1: the indexer
+ * picks the history positions most relevant to the current query; SFA runs on
+ * those only).
+ *
+ *   scores   float  [B][ctx_stride]  row b valid on [0, ctx_len[b])
+ *   ctx_len  int32  [B]              device; k <= ctx_len[b] <= max_ctx
+ *   ids      int32  [B][k]           out: the k positions of largest score,
+ *                                    ties to the lower position, -0.0 == +0.0,
+ *                                    in ascending position order
+ *   ws       workspace of ts_topk_workspace_size(B, max_ctx, k) bytes,
+ *            256-byte aligned, contents need not be preserved
+ * Requires scores 16-byte aligned and ctx_stride a multiple of 4, max_ctx <=
+ * ctx_stride, 1 <= k <= 8192. A NaN score sets TS_DEVERR_NAN (the NaN ranks
+ * lowest); a ctx_len outside [k, max_ctx] sets TS_DEVERR_CTX and that
+ * request's ids are all -1.
+ * ------------------------------------------------------------------------- */
+size_t ts_topk_workspace_size(int B, int max_ctx, int k);
+ts_status ts_topk(const float* scores, int64_t ctx_stride, const int32_t* ctx_len,
+                  int B, int max_ctx, int k, int32_t* ids, void* ws, size_t ws_bytes,
+                  int32_t* err, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * dsa_plan -- the shared plan of an IndexShare group ([GLM] §4.2, §5 DsaPlan;
+ * pool policy §4.3). Once per group: classify every selected id as a pool hit
+ * or a host miss, list the distinct misses compactly, and choose the slot each
+ * miss replaces under the set-associative FIFO policy.
+ *
+ *   ids        int32 [B][k]   selected token ids (any order, repeats allowed)
+ *   ctx_len    int32 [B]      an id t is valid when 0 <= t < ctx_len[b]
+ *   pool_tags  int32 [B][P]   token held by each slot, -1 = empty; slot
+ *                             s*W + w is way w of set s; token t lives in set
+ *                             t mod S
+ *   fifo_ptr   int32 [B][S]   per-set FIFO pointer, in [0, W)
+ * Outputs (entries at and past miss_count[b] are left untouched):
+ *   src_map    int32 [B][k]   hit: the slot (>= 0); miss of token t: -1 - t;
+ *                             invalid id: INT32_MIN (and TS_DEVERR_ID_RANGE)
+ *   miss_ids   int32 [B][k]   distinct missed tokens, ascending
+ *   miss_pos   int32 [B][k]   first position of each missed token in ids
+ *   victim     int32 [B][k]   slot the miss replaces: set*W + (ptr + rank) mod W,
+ *                             rank = order of the miss among its set's misses
+ *   install    uint8 [B][k]   1 when the miss survives the step (the last W
+ *                             misses of a set); 0 when a later miss of the same
+ *                             set in the same step replaces it
+ *   miss_count int32 [B]
+ *   ptr_next   int32 [B][S]   (ptr + misses in the set) mod W
+ * Hits never move a pointer; a hit slot may be chosen as a victim (plain FIFO),
+ * which is safe because every layer reads its rows before its own refill.
+ * Requires 1 <= W <= 32, P*4 + 12*S + 16*k bytes <= 200 KiB, k <= 4096.
+ * ------------------------------------------------------------------------- */
+ts_status dsa_plan(const int32_t* ids, const int32_t* ctx_len, int B, int k,
+                   const int32_t* pool_tags, const int32_t* fifo_ptr, int S, int W,
+                   int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
+                   int32_t* victim, uint8_t* install, int32_t* miss_count,
+                   int32_t* ptr_next, int32_t* err, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * dsa_gather_kv -- serve one layer's selected rows ([GLM] §5 DsaServe, §5.1;
+ * base design §2.1 GatherSelectionKvCache). Row j of request b is copied from
+ * the device pool when src_map >= 0 and read in place from pinned host memory
+ * (zero-copy) when src_map = -1 - t.
+ *
+ *   pool_l  bf16 [B][P][576]          device, this layer's pool
+ *   host_l  bf16 [B][ctx_stride][576] device-accessible address of pinned host
+ *                                     memory, this layer's full latent KV
+ *   sel_l   bf16 [B][k][576]          out: the selection buffer SFA reads
+ * All three 16-byte aligned. Out-of-range slots or host rows set
+ * TS_DEVERR_SLOT_RANGE / TS_DEVERR_ID_RANGE and leave that row untouched.
+ * ------------------------------------------------------------------------- */
+ts_status dsa_gather_kv(const int32_t* src_map, int B, int k, const void* pool_l,
+                        int P, const void* host_l, int64_t ctx_stride,
+                        const int32_t* ctx_len, void* sel_l, int32_t* err,
+                        cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * dsa_refill_pool -- the deferred refill of one layer's pool ([GLM] §4.4, §5
+ * DsaInstall, §5.1). For every installed miss i of request b:
+ *   pool_l[b][victim[i]] = sel_l[b][miss_pos[i]]   (the missed row's bytes)
+ * and, when update_metadata != 0 (the group's last layer):
+ *   pool_tags[b][victim[i]] = miss_ids[i];  fifo_ptr[b][:] = ptr_next[b][:].
+ * Must run after this layer's dsa_gather_kv (it evicts slots the gather reads)
+ * and, with update_metadata, after the refills of every layer of the group.
+ * ------------------------------------------------------------------------- */
+ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* miss_pos,
+                          const int32_t* victim, const uint8_t* install,
+                          const int32_t* miss_count, int B, int k, const void* sel_l,
+                          void* pool_l, int P, int update_metadata, int32_t* pool_tags,
+                          int32_t* fifo_ptr, const int32_t* ptr_next, int S, int W,
+                          int32_t* err, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * sfa_mla_decode -- sparse absorbed-MLA decode attention over the selection
+ * ([GLM] §2.1 SFA; [TS] MLA section: one latent row is both K and V). For each
+ * request b and head h, over the k selected rows K_j (576 values):
+ *   s_j = scale * q[b][h] . K_j ;  p = softmax(s) ;
+ *   out[b][h][:] = sum_j p_j K_j[0:512] ;  lse[b][h] = log(sum_j exp(s_j))
+ * bf16 inputs, fp32 accumulation (tcgen05 tensor cores, TMEM accumulators),
+ * the softmax weights rounded to bf16 for the second product, bf16 output.
+ *
+ *   q     bf16 [B][H][576]    16-byte aligned
+ *   sel_l bf16 [B][k][576]    16-byte aligned
+ *   out   bf16 [B][H][512]
+ *   lse   float [B][H] or NULL
+ *   ws    workspace of sfa_workspace_size(B, H, k) bytes, 256-byte aligned
+ * A kernel wait that gives up sets TS_DEVERR_TIMEOUT.
+ * ------------------------------------------------------------------------- */
+size_t sfa_workspace_size(int B, int H, int k);
+ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int H, int k,
+                         float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                         int32_t* err, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSAKV_H */

@@ -1,0 +1,42 @@
+"""The C-ABI library loads without a GPU and exports every function the
+header declares; the Python binding wraps each under the same name."""
+import ctypes
+
+import pytest
+
+from _util import ensure_library, header_functions
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ctypes.CDLL(ensure_library())
+
+
+def test_header_declares_the_path():
+    names = header_functions()
+    for n in ("ts_topk", "dsa_plan", "dsa_gather_kv", "dsa_refill_pool", "sfa_mla_decode"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in header_functions():
+        assert hasattr(lib, n), n
+
+
+def test_binding_has_the_same_names():
+    import decode_dsa_kv_gb300 as d
+    for n in header_functions():
+        assert callable(getattr(d, n)), n
+        assert n in d.EXPORTS
+
+
+def test_host_side_validation_without_gpu():
+    import decode_dsa_kv_gb300 as d
+    from decode_dsa_kv_gb300 import _abi
+    # argument checks return before touching a device
+    assert d.ts_topk(None, 64, None, 1, 64, 8, None, None, 0, None, 0) == _abi.TS_ERR_INVALID_ARG
+    assert d.sfa_mla_decode(None, None, 1, 1, 1, 1.0, None, None, None, 0, None, 0) == \
+        _abi.TS_ERR_INVALID_ARG
+    assert d.ts_status_string(_abi.TS_ERR_WORKSPACE).startswith("workspace")
+    assert d.ts_topk_workspace_size(2, 1000, 16) > 2 * 1000 * 8
+    assert d.sfa_workspace_size(1, 128, 2048) >= 8 * 128 * 512 * 4

@@ -1,0 +1,105 @@
+"""Whole decode steps through the per-step schedule (top-k, one plan per group,
+per-layer gather + SFA on the main stream, refill on the side stream, metadata
+at the group's last layer), compared with the oracle run step by step on the
+same seeded inputs: bit-exact ids, plan, selection bytes and pool state; SFA
+within tolerance."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workload as wl
+from _util import SFA_ABS_TOL, SFA_MEAN_REL_TOL, ensure_library, sfa_errors
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def d():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_library()
+    import decode_dsa_kv_gb300 as d
+    return d
+
+
+def run_steps(d, w, steps, sample=None, sfa_layers=None, sfa_heads=None):
+    """Run `steps` decode steps of workload `w` on the GPU and, for the
+    requests in `sample` (default: all), on the oracle; compare after each
+    step. Returns per-step hit rates of the GPU plan."""
+    lens = wl.ctx_lens(w)
+    host = d.HostKV(w.layers, w.B, w.ctx_stride)
+    wl.fill_host_kv(w, host.array)
+    g = d.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host)
+    sample = list(range(w.B)) if sample is None else sample
+    sfa_layers = list(range(w.layers)) if sfa_layers is None else sfa_layers
+    states = {b: oracle.init_state(w.layers, w.S, w.W) for b in sample}
+    scores_stream = wl.ScoreStream(w)
+    scale = 1 / math.sqrt(576)
+    hit_rates = []
+    for step in range(steps):
+        scores = scores_stream.next()
+        q = wl.queries(w, step)
+        g.step(torch.from_numpy(scores).cuda(), torch.from_numpy(q.view(np.int16)).cuda())
+        assert g.synchronize() == 0, f"device error bits at step {step}"
+        ids = g.ids.cpu().numpy()
+        src = g.src_map.cpu().numpy()
+        mc = g.miss_count.cpu().numpy()
+        hit_rates.append(float((src >= 0).mean()))
+        for b in sample:
+            r = oracle.decode_step(states[b], scores[b], int(lens[b]), w.k, w.S, w.W,
+                                   host.array[:, b], q[:, b], scale, with_sfa=False)
+            plan = r["plan"]
+            M = plan.miss_count
+            assert np.array_equal(ids[b], r["ids"]), (step, b)
+            assert np.array_equal(src[b], plan.src_map), (step, b)
+            assert mc[b] == M
+            assert np.array_equal(g.miss_ids[b, :M].cpu().numpy(), plan.miss_ids)
+            assert np.array_equal(g.victim[b, :M].cpu().numpy(), plan.victim)
+            assert np.array_equal(g.install[b, :M].cpu().numpy().astype(bool), plan.install)
+            assert np.array_equal(g.tags[b].cpu().numpy(), states[b].tags), (step, b)
+            assert np.array_equal(g.fifo_ptr[b].cpu().numpy(), states[b].fifo_ptr)
+            for l in range(w.layers):
+                sel = g.sel[l, b].cpu().numpy().view(np.uint16)
+                assert np.array_equal(sel, r["sel"][l]), (step, b, l)
+                assert np.array_equal(g.pool[l, b].cpu().numpy().view(np.uint16),
+                                      states[b].pool[l]), (step, b, l)
+            for l in sfa_layers:
+                heads = slice(None) if sfa_heads is None else sfa_heads
+                o, _ = oracle.sfa_decode(q[l, b][heads], r["sel"][l], scale)
+                got = g.out[l, b].cpu().view(torch.int16).numpy().view(np.uint16)[heads]
+                a, rel = sfa_errors(got, oracle.round_to_bf16_bits(o))
+                assert a <= SFA_ABS_TOL and rel <= SFA_MEAN_REL_TOL, (step, b, l, a, rel)
+    host.close()
+    return hit_rates
+
+
+def test_tiny_all_steps(d):
+    rates = run_steps(d, wl.TINY, wl.TINY.steps)
+    assert rates[0] == 0.0 and max(rates[1:]) > 0.3
+
+
+def test_decode_batch_scaled(d):
+    w = wl.scaled(wl.DECODE_BATCH, B=3)
+    rates = run_steps(d, w, 5, sfa_layers=[0, 3])
+    assert rates[-1] > 0.5
+
+
+def test_long_context_scaled(d):
+    w = wl.scaled(wl.LONG_CONTEXT, B=2)
+    run_steps(d, w, 4, sfa_layers=[1])
+
+
+def test_adversarial_scaled_overflow(d):
+    w = wl.scaled(wl.ADVERSARIAL, ctx=1 << 17)
+    run_steps(d, w, 3, sfa_layers=[2])
+
+
+def test_decode_batch_full_size_sampled(d):
+    # the full workload (32 requests x 65,536 tokens x 4 layers) in the bench's
+    # launch configuration; the oracle follows four of the requests
+    w = wl.DECODE_BATCH
+    run_steps(d, w, 3, sample=[0, 13, 31], sfa_layers=[0, 3], sfa_heads=slice(0, 128, 9))
