@@ -91,24 +91,27 @@ def bf16_to_f32(x: np.ndarray) -> np.ndarray:
 # Context lengths, latent KV rows, queries
 # --------------------------------------------------------------------------
 
-def ctx_lens(w: Workload) -> np.ndarray:
-    """Context length of each request (int32 [B])."""
+def ctx_lens(w: Workload, first_request: int = 0) -> np.ndarray:
+    """Context length of requests first_request .. first_request+B-1 (int32 [B])."""
     if w.ctx_lo == w.ctx:
         return np.full(w.B, w.ctx, dtype=np.int32)
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([w.seed, 11])))
-    return rng.integers(w.ctx_lo, w.ctx + 1, size=w.B).astype(np.int32)
+    return rng.integers(w.ctx_lo, w.ctx + 1,
+                        size=first_request + w.B)[first_request:].astype(np.int32)
 
 
-def fill_host_kv(w: Workload, out: np.ndarray, layers=None, requests=None) -> None:
+def fill_host_kv(w: Workload, out: np.ndarray, layers=None, requests=None,
+                 first_request: int = 0) -> None:
     """Write the latent rows of every (layer, request) into `out`
     ([layers][B][ctx_stride][576] uint16); rows past a request's context are
-    left as they are."""
+    left as they are. Request b of `out` is request first_request + b of the
+    workload."""
     assert out.shape == (w.layers, w.B, w.ctx_stride, D) and out.dtype == np.uint16
-    lens = ctx_lens(w)
+    lens = ctx_lens(w, first_request)
     for l in (range(w.layers) if layers is None else layers):
         for b in (range(w.B) if requests is None else requests):
             n = int(lens[b])
-            normal_bf16(n, D, w.seed, DOMAIN_KV, l, b, 0, out[l, b, :n])
+            normal_bf16(n, D, w.seed, DOMAIN_KV, l, first_request + b, 0, out[l, b, :n])
 
 
 def host_kv_rows(w: Workload, layer: int, b: int, rows) -> np.ndarray:
@@ -120,13 +123,15 @@ def host_kv_rows(w: Workload, layer: int, b: int, rows) -> np.ndarray:
     return out
 
 
-def queries(w: Workload, step: int, out: np.ndarray | None = None) -> np.ndarray:
+def queries(w: Workload, step: int, out: np.ndarray | None = None,
+            first_request: int = 0) -> np.ndarray:
     """Queries of one decode step: uint16 [layers][B][H][576]."""
     if out is None:
         out = np.empty((w.layers, w.B, w.H, D), dtype=np.uint16)
     for l in range(w.layers):
         for b in range(w.B):
-            normal_bf16(w.H, D, w.seed, DOMAIN_Q, step, (l << 32) | b, 0, out[l, b])
+            normal_bf16(w.H, D, w.seed, DOMAIN_Q, step, (l << 32) | (first_request + b), 0,
+                        out[l, b])
     return out
 
 
@@ -189,12 +194,12 @@ class ScoreStream:
                    overflow_set (position mod S) each step.
     """
 
-    def __init__(self, w: Workload):
+    def __init__(self, w: Workload, first_request: int = 0):
         self.w = w
-        self.lens = ctx_lens(w)
+        self.lens = ctx_lens(w, first_request)
         self.step = 0
         self.rngs = [np.random.Generator(np.random.PCG64(
-            np.random.SeedSequence([w.seed, 7, b]))) for b in range(w.B)]
+            np.random.SeedSequence([w.seed, 7, first_request + b]))) for b in range(w.B)]
         self.state = [None] * w.B
         self.hot = [None] * w.B
         self.rho = [0.0] * w.B
