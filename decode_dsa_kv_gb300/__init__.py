@@ -12,7 +12,7 @@ import importlib
 
 _ABI_NAMES = {
     "ts_status_string", "ts_host_register", "ts_host_unregister", "ts_read_error",
-    "ts_topk_workspace_size", "ts_topk", "dsa_plan", "dsa_gather_kv", "dsa_refill_pool",
+    "ts_topk_workspace_size", "ts_topk", "ts_topk_noalloc", "dsa_plan", "dsa_gather_kv", "dsa_refill_pool",
     "sfa_workspace_size", "sfa_mla_decode", "DsaKvError", "check", "status_string", "EXPORTS",
     "LIB_PATH",
 }

@@ -45,6 +45,7 @@ _SIGS = {
     "ts_read_error": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "ts_topk_workspace_size": (_SZ, [_I, _I, _I]),
     "ts_topk": (_I, [_P, _I64, _P, _I, _I, _I, _P, _P, _SZ, _P, _P]),
+    "ts_topk_noalloc": (_I, [_P, _I64, _P, _I, _I, _I, _P, _P, _P]),
     "dsa_plan": (_I, [_P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dsa_gather_kv": (_I, [_P, _I, _I, _P, _I, _P, _I64, _P, _P, _P, _P]),
     "dsa_refill_pool": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _I, _I,
@@ -130,6 +131,14 @@ def ts_topk(scores, ctx_stride, ctx_len, B, max_ctx, k, ids, ws, ws_bytes, err=N
             stream=None) -> int:
     return _lib.ts_topk(ptr(scores), ctx_stride, ptr(ctx_len), B, max_ctx, k, ptr(ids),
                         ptr(ws), ws_bytes, ptr(err), stream_handle(stream))
+
+
+def ts_topk_noalloc(scores, ctx_stride, ctx_len, B, max_ctx, k, ids, err=None,
+                    stream=None) -> int:
+    """ts_topk with the library's fixed scratch array instead of a caller
+    workspace, for callers that cannot allocate device memory."""
+    return _lib.ts_topk_noalloc(ptr(scores), ctx_stride, ptr(ctx_len), B, max_ctx, k, ptr(ids),
+                                ptr(err), stream_handle(stream))
 
 
 def dsa_plan(ids, ctx_len, B, k, pool_tags, fifo_ptr, S, W, src_map, miss_ids, miss_pos,

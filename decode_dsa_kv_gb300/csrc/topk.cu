@@ -351,3 +351,72 @@ extern "C" ts_status ts_topk(const float* scores, int64_t ctx_stride, const int3
   topk_finish_kernel<<<B, kFinishThreads, 0, stream>>>(ctx_len, k, max_ctx, w, ids, err);
   return launch_status();
 }
+
+// ---------------------------------------------------------------------------
+// ts_topk_noalloc: the same top-k with its scratch in a fixed device array, for
+// callers that cannot allocate device memory.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace dsakv {
+namespace {
+
+constexpr int kNoAllocMaxB = 128;
+constexpr int64_t kNoAllocMaxPositions = int64_t(1) << 22;  // B * max_ctx
+constexpr size_t kNoAllocScratchBytes =
+    ((size_t(kNoAllocMaxB) * kBins * 4 + 255) & ~size_t(255)) +
+    ((size_t(kNoAllocMaxB) * 4 + 255) & ~size_t(255)) +
+    ((size_t(kNoAllocMaxPositions) * 8 + 255) & ~size_t(255)) +
+    ((size_t(kNoAllocMaxPositions / 32 + kNoAllocMaxB) * 4 + 255) & ~size_t(255));
+
+// Module-scope scratch: every device that loads the library holds it (about
+// 34.5 MiB) until the process exits. Host code must not pass the symbol
+// itself to a kernel; it takes the device address from cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_topk_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device.
+void* scratch_on_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace
+}  // namespace dsakv
+
+extern "C" ts_status ts_topk_noalloc(const float* scores, int64_t ctx_stride,
+                                     const int32_t* ctx_len, int B, int max_ctx, int k,
+                                     int32_t* ids, int32_t* err, cudaStream_t stream) {
+  if (!scores || !ctx_len || !ids) return TS_ERR_INVALID_ARG;
+  if (B <= 0 || k <= 0 || max_ctx < k || ctx_stride < max_ctx) return TS_ERR_INVALID_ARG;
+  if (k > kMaxK || B > kNoAllocMaxB || int64_t(B) * max_ctx > kNoAllocMaxPositions)
+    return TS_ERR_UNSUPPORTED;
+  if (!aligned16(scores) || (ctx_stride & 3) != 0) return TS_ERR_INVALID_ARG;
+  if (ts_topk_workspace_size(B, max_ctx, k) > kNoAllocScratchBytes) return TS_ERR_UNSUPPORTED;
+  void* ws = scratch_on_current_device();
+  if (!ws) return TS_ERR_CUDA;
+  TopkWs w = carve(ws, B, max_ctx);
+  // the histograms and list counters left by the previous call are cleared
+  if (cudaMemsetAsync(ws, 0, align256(size_t(B) * kBins * 4) + align256(size_t(B) * 4), stream) !=
+      cudaSuccess)
+    return TS_ERR_CUDA;
+  const dim3 grid((max_ctx + kChunk - 1) / kChunk, B);
+  topk_hist_kernel<<<grid, kThreads, 0, stream>>>(scores, ctx_stride, ctx_len, k, max_ctx, w, err);
+  topk_select_kernel<<<grid, kThreads, 0, stream>>>(scores, ctx_stride, ctx_len, k, max_ctx, w);
+  topk_finish_kernel<<<B, kFinishThreads, 0, stream>>>(ctx_len, k, max_ctx, w, ids, err);
+  return launch_status();
+}

@@ -101,6 +101,24 @@ ts_status ts_topk(const float* scores, int64_t ctx_stride, const int32_t* ctx_le
                   int B, int max_ctx, int k, int32_t* ids, void* ws, size_t ws_bytes,
                   int32_t* err, cudaStream_t stream);
 
+/* ts_topk_noalloc -- ts_topk for callers that cannot allocate device memory
+ * (a plugin inside a host engine that owns every allocation, a process whose
+ * device memory is reserved before it starts, code that runs where
+ * cudaMalloc is not allowed). The pages have no counterpart; it is an
+ * interface variant only. Same arguments, results and errors as ts_topk,
+ * minus the workspace: the scratch is one fixed device array inside this
+ * library (about 34.5 MiB, held on every GPU that loads the library until the
+ * process exits). Limits: B <= 128 and B * max_ctx <= 4,194,304; beyond them
+ * the call returns TS_ERR_UNSUPPORTED before enqueuing anything. The call
+ * allocates nothing. Its first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture. Every call uses the same array and clears
+ * the parts that must start at zero; calls whose work overlaps on the GPU
+ * (other streams, other host threads) race on it, so serialize them. */
+ts_status ts_topk_noalloc(const float* scores, int64_t ctx_stride, const int32_t* ctx_len,
+                          int B, int max_ctx, int k, int32_t* ids, int32_t* err,
+                          cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * dsa_plan -- the shared plan of an IndexShare group ([GLM] §4.2, §5 DsaPlan;
  * pool policy §4.3). Once per group: classify every selected id as a pool hit
