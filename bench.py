@@ -55,6 +55,10 @@ def parse(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--only", choices=KERNELS, default=None,
+                    help="after the warm-up steps, launch only this kernel --steps times "
+                         "(on the state the warm-up left) and report its time per launch")
+    ap.add_argument("--B", type=int, default=None, help="override the workload's request count")
     return ap.parse_args(argv)
 
 
@@ -187,9 +191,11 @@ def measured_peaks():
 
 def link_peak_gbs(torch, nbytes=1 << 30, reps=5):
     """Host-to-device bandwidth of this machine's host link: DMA copy of pinned
-    host memory (best of `reps`, CUDA events)."""
-    src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
-    src.fill_(1)
+    (registered) host memory (best of `reps`, CUDA events)."""
+    from decode_dsa_kv_gb300 import PinnedHost
+    buf = PinnedHost((nbytes,), np.uint8)
+    buf.array[:] = 1
+    src = buf.tensor()
     dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     best = 0.0
     for _ in range(reps):
@@ -201,6 +207,7 @@ def link_peak_gbs(torch, nbytes=1 << 30, reps=5):
         b.synchronize()
         best = max(best, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
     del src, dst
+    buf.close()
     return best
 
 
@@ -353,11 +360,13 @@ def run_native(args, w, rank, world, local):
     wl.fill_host_kv(w, host.array, first_request=first)
     T = max(1, min(args.period, args.warmup + args.steps))
     stream = wl.ScoreStream(w, first)
-    scores_h = torch.empty((T, w.B, w.ctx_stride), dtype=torch.float32, pin_memory=True)
-    q_h = torch.empty((T, w.layers, w.B, w.H, 576), dtype=torch.int16, pin_memory=True)
+    scores_pin = dk.PinnedHost((T, w.B, w.ctx_stride), np.float32)
+    q_pin = dk.PinnedHost((T, w.layers, w.B, w.H, 576), np.int16)
     for t in range(T):
-        scores_h[t].copy_(torch.from_numpy(stream.next()))
-        wl.queries(w, t, out=q_h[t].numpy().view(np.uint16), first_request=first)
+        scores_pin.array[t] = stream.next()
+        wl.queries(w, t, out=q_pin.array[t].view(np.uint16), first_request=first)
+    scores_h, q_h = scores_pin.tensor(), q_pin.tensor()
+    pinned_ok = scores_h.is_pinned()
     scores_d = scores_h.cuda()
     q_d = q_h.cuda()
     g = dk.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host)
@@ -375,6 +384,10 @@ def run_native(args, w, rank, world, local):
     torch.cuda.synchronize()
     if g.synchronize():
         raise RuntimeError("device error during warm-up")
+
+    if args.only:
+        return run_only(args, w, g, scores_d[palindrome_index(args.warmup, T)],
+                        q_d[palindrome_index(args.warmup, T)], peaks, link, lens, host, rank)
 
     # timed region: K steps, per-kernel events on the launching streams
     miss_log = torch.zeros((args.steps, w.B), dtype=torch.int32, device="cuda")
@@ -438,7 +451,8 @@ def run_native(args, w, rank, world, local):
     if not args.no_e2e:
         ins_s = torch.empty((w.B, w.ctx_stride), dtype=torch.float32, device="cuda")
         ins_q = torch.empty((w.layers, w.B, w.H, 576), dtype=torch.int16, device="cuda")
-        out_h = torch.empty((w.layers, w.B, w.H, 512), dtype=torch.bfloat16, pin_memory=True)
+        out_pin = dk.PinnedHost((w.layers, w.B, w.H, 512 * 2), np.uint8)
+        out_h = out_pin.tensor().view(torch.bfloat16).view(w.layers, w.B, w.H, 512)
         n_e2e = min(args.e2e_steps, args.steps)
         torch.cuda.synchronize()
         barrier(world)
@@ -460,10 +474,12 @@ def run_native(args, w, rank, world, local):
         e2e = {"value": rows_step / (e2e_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": int(ins_s.numel() * 4 + ins_q.numel() * 2),
                "d2h_bytes_per_step": int(out_h.numel() * 2), "steps": n_e2e,
-               "ms_per_step": e2e_ms}
+               "ms_per_step": e2e_ms, "host_buffers_pinned": bool(pinned_ok)}
 
     clocks = sampler.summary(t_wall0, t_wall1)
     host.close()
+    scores_pin.close()
+    q_pin.close()
 
     if rank != 0:
         return
@@ -498,10 +514,58 @@ def run_native(args, w, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def run_only(args, w, g, scores, q, peaks, link, lens, host, rank):
+    """One kernel, --steps launches on the main stream, on the pool state and
+    plan the warm-up left (each launch is idempotent on that state)."""
+    import torch
+
+    from decode_dsa_kv_gb300 import _abi as abi
+    B, k = w.B, w.k
+    m = g.main
+    launch = {
+        "topk": lambda: abi.ts_topk(scores, g.ctx_stride, g.ctx_len, B, g.max_ctx, k, g.ids,
+                                    g.topk_ws, g.topk_ws_bytes, g.err, m),
+        "plan": lambda: abi.dsa_plan(g.ids, g.ctx_len, B, k, g.tags, g.fifo_ptr, g.S, g.W,
+                                     g.src_map, g.miss_ids, g.miss_pos, g.victim, g.install,
+                                     g.miss_count, g.miss_rows, g.ptr_next, g.err, m),
+        "gather": lambda: abi.dsa_gather_kv(g.src_map, g.miss_ids, g.miss_pos, g.miss_count,
+                                            g.miss_rows, B, k, g.pool[0], g.P, host.layer_ptr(0),
+                                            g.ctx_stride, g.ctx_len, g.sel[0], g.err, m),
+        "sfa": lambda: abi.sfa_mla_decode(q[0], g.sel[0], B, g.H, k, g.scale, g.out[0],
+                                          g.lse[0], g.sfa_ws, g.sfa_ws_bytes, g.err, m),
+        "refill": lambda: abi.dsa_refill_pool(g.miss_ids, g.miss_pos, g.victim, g.install,
+                                              g.miss_count, B, k, g.sel[0], g.pool[0], g.P, 0,
+                                              g.tags, g.fifo_ptr, g.ptr_next, g.S, g.W, g.err,
+                                              m),
+    }[args.only]
+    abi.check(launch(), args.only)
+    torch.cuda.synchronize()
+    misses = g.miss_count.double().sum().item()
+    hit = 1.0 - misses / (B * k)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(m)
+    for _ in range(args.steps):
+        abi.check(launch(), args.only)
+    e1.record(m)
+    torch.cuda.synchronize()
+    if g.synchronize():
+        raise RuntimeError("device error")
+    ms = e0.elapsed_time(e1) / args.steps
+    alg = algorithmic(w, lens, hit, 1.0 - hit)[args.only]
+    rf = roofline_of(args.only, alg, ms, peaks, link)
+    host.close()
+    if rank == 0:
+        print(json.dumps({"only": args.only, "workload": w.name, "B": B, "launches": args.steps,
+                          "hit_rate": hit, "link_peak_gbs": link, **rf}), flush=True)
+
+
 def main(argv=None):
     args = parse(argv)
     rank, world, local = dist_env()
     w = wl.get(args.workload)
+    if args.B:
+        w = wl.scaled(w, B=args.B)
     if args.impl == "reference":
         run_reference(args, w, rank, world)
         return

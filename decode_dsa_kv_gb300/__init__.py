@@ -16,7 +16,7 @@ _ABI_NAMES = {
     "sfa_workspace_size", "sfa_mla_decode", "DsaKvError", "check", "status_string", "EXPORTS",
     "LIB_PATH",
 }
-_RUNTIME_NAMES = {"HostKV", "DecodeGroup"}
+_RUNTIME_NAMES = {"HostKV", "DecodeGroup", "PinnedHost"}
 
 
 def __getattr__(name):

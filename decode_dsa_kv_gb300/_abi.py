@@ -46,8 +46,8 @@ _SIGS = {
     "ts_topk_workspace_size": (_SZ, [_I, _I, _I]),
     "ts_topk": (_I, [_P, _I64, _P, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "ts_topk_noalloc": (_I, [_P, _I64, _P, _I, _I, _I, _P, _P, _P]),
-    "dsa_plan": (_I, [_P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
-    "dsa_gather_kv": (_I, [_P, _I, _I, _P, _I, _P, _I64, _P, _P, _P, _P]),
+    "dsa_plan": (_I, [_P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "dsa_gather_kv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _I, _P, _I64, _P, _P, _P, _P]),
     "dsa_refill_pool": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _I, _I,
                              _P, _P]),
     "sfa_workspace_size": (_SZ, [_I, _I, _I]),
@@ -142,15 +142,17 @@ def ts_topk_noalloc(scores, ctx_stride, ctx_len, B, max_ctx, k, ids, err=None,
 
 
 def dsa_plan(ids, ctx_len, B, k, pool_tags, fifo_ptr, S, W, src_map, miss_ids, miss_pos,
-             victim, install, miss_count, ptr_next, err=None, stream=None) -> int:
+             victim, install, miss_count, miss_rows, ptr_next, err=None, stream=None) -> int:
     return _lib.dsa_plan(ptr(ids), ptr(ctx_len), B, k, ptr(pool_tags), ptr(fifo_ptr), S, W,
                          ptr(src_map), ptr(miss_ids), ptr(miss_pos), ptr(victim), ptr(install),
-                         ptr(miss_count), ptr(ptr_next), ptr(err), stream_handle(stream))
+                         ptr(miss_count), ptr(miss_rows), ptr(ptr_next), ptr(err),
+                         stream_handle(stream))
 
 
-def dsa_gather_kv(src_map, B, k, pool_l, P, host_l, ctx_stride, ctx_len, sel_l, err=None,
-                  stream=None) -> int:
-    return _lib.dsa_gather_kv(ptr(src_map), B, k, ptr(pool_l), P, ptr(host_l), ctx_stride,
+def dsa_gather_kv(src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, pool_l, P, host_l,
+                  ctx_stride, ctx_len, sel_l, err=None, stream=None) -> int:
+    return _lib.dsa_gather_kv(ptr(src_map), ptr(miss_ids), ptr(miss_pos), ptr(miss_count),
+                              ptr(miss_rows), B, k, ptr(pool_l), P, ptr(host_l), ctx_stride,
                               ptr(ctx_len), ptr(sel_l), ptr(err), stream_handle(stream))
 
 

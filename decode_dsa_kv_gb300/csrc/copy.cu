@@ -17,8 +17,7 @@
 namespace dsakv {
 namespace {
 
-constexpr int kGatherThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kGatherThreads = 1024;
 
 __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
   uint4 v;
@@ -34,45 +33,122 @@ __device__ __forceinline__ void st_v4(uint4* p, uint4 v) {
                : "memory");
 }
 
-__global__ void __launch_bounds__(kGatherThreads) gather_kernel(
-    const int32_t* __restrict__ src_map, int k, int64_t total, const uint4* __restrict__ pool,
-    int P, const uint4* __restrict__ host, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
-    uint4* __restrict__ sel, int32_t* err) {
-  const int64_t step = int64_t(gridDim.x) * kGatherThreads * kUnroll;
-  int bad = 0;
-  for (int64_t base = int64_t(blockIdx.x) * kGatherThreads * kUnroll + threadIdx.x; base < total;
-       base += step) {
-    uint4 v[kUnroll];
-    bool ok[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c = base + int64_t(u) * kGatherThreads;
-      ok[u] = false;
-      if (c < total) {
-        const int64_t row = c / DSA_ROW_CHUNKS;
-        const int part = static_cast<int>(c - row * DSA_ROW_CHUNKS);
-        const int b = static_cast<int>(row / k);
-        const int src = __ldg(src_map + row);
-        const uint4* from = nullptr;
-        if (src >= 0) {
-          if (src < P) from = pool + (int64_t(b) * P + src) * DSA_ROW_CHUNKS + part;
-          else bad |= TS_DEVERR_SLOT_RANGE;
-        } else {
-          const int64_t t = -1 - int64_t(src);
-          if (t < __ldg(ctx_len + b)) from = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS + part;
-          else bad |= TS_DEVERR_ID_RANGE;
-        }
-        if (from) {
-          v[u] = ld_nc_v4(from);
-          ok[u] = true;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (ok[u]) st_v4(sel + base + int64_t(u) * kGatherThreads, v[u]);
+// Copy up to two 1152-byte rows with one warp: every lane moves the pieces
+// lane, lane+32 and lane+64 (< 72) of each row; all loads are issued before
+// any store, so a warp keeps up to 6 x 16 bytes per lane in flight.
+__device__ __forceinline__ void warp_copy_rows2(const uint4* from0, uint4* to0, const uint4* from1,
+                                                uint4* to1, int lane) {
+  uint4 a0, a1, a2, b0, b1, b2;
+  const bool third = lane < DSA_ROW_CHUNKS - 64;
+  if (from0) {
+    a0 = ld_nc_v4(from0 + lane);
+    a1 = ld_nc_v4(from0 + lane + 32);
+    if (third) a2 = ld_nc_v4(from0 + lane + 64);
   }
-  if (bad) report(err, bad);
+  if (from1) {
+    b0 = ld_nc_v4(from1 + lane);
+    b1 = ld_nc_v4(from1 + lane + 32);
+    if (third) b2 = ld_nc_v4(from1 + lane + 64);
+  }
+  if (from0) {
+    st_v4(to0 + lane, a0);
+    st_v4(to0 + lane + 32, a1);
+    if (third) st_v4(to0 + lane + 64, a2);
+  }
+  if (from1) {
+    st_v4(to1 + lane, b0);
+    st_v4(to1 + lane + 32, b1);
+    if (third) st_v4(to1 + lane + 64, b2);
+  }
+}
+
+// First position of token t among request b's misses, or -1: binary search of
+// the ascending miss list.
+__device__ __forceinline__ int first_pos_of(const int32_t* mids, const int32_t* mpos, int M, int t) {
+  int lo = 0, hi = M;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(mids + mid) < t) lo = mid + 1;
+    else hi = mid;
+  }
+  return (lo < M && __ldg(mids + lo) == t) ? __ldg(mpos + lo) : -1;
+}
+
+// One launch, two kinds of warps (alternating), each moving two rows per step:
+//   even warps walk the compact miss list: host row miss_ids[i] ->
+//     sel[miss_pos[i]] (the host-link reads, which set the kernel's time);
+//   odd warps walk the positions: pool row for a hit; for a miss, the host row
+//     only when that token repeats in the selection and this is not its first
+//     position (the even warps serve first positions). Requests without
+//     repeats (miss_rows == miss_count) skip misses outright.
+// The two kinds write disjoint positions and run side by side, so the HBM
+// copies of the hits hide under the host-link time of the misses.
+__global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(
+    const int32_t* __restrict__ src_map, const int32_t* __restrict__ miss_ids,
+    const int32_t* __restrict__ miss_pos, const int32_t* __restrict__ miss_count,
+    const int32_t* __restrict__ miss_rows, int B, int k, const uint4* __restrict__ pool, int P,
+    const uint4* __restrict__ host, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
+    uint4* __restrict__ sel, int32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (int64_t(blockIdx.x) * kGatherThreads + threadIdx.x) >> 5;
+  const int64_t nw = (int64_t(gridDim.x) * kGatherThreads) >> 5;
+  const int64_t rows = int64_t(B) * k;
+  const bool miss_warp = (gw & 1) == 0;
+  const int64_t w = gw >> 1;
+  const int64_t nrole = miss_warp ? (nw + 1) >> 1 : nw >> 1;
+  int bad = 0;
+  if (miss_warp) {
+    for (int64_t r0 = w * 2; r0 < rows; r0 += nrole * 2) {
+      const uint4* from[2] = {nullptr, nullptr};
+      uint4* to[2] = {nullptr, nullptr};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int64_t r = r0 + e;
+        if (r >= rows) continue;
+        const int b = static_cast<int>(r / k);
+        const int i = static_cast<int>(r - int64_t(b) * k);
+        if (i >= __ldg(miss_count + b)) continue;
+        const int t = __ldg(miss_ids + r), j = __ldg(miss_pos + r);
+        if (t < 0 || t >= __ldg(ctx_len + b) || j < 0 || j >= k) {
+          bad |= TS_DEVERR_ID_RANGE;
+          continue;
+        }
+        from[e] = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
+        to[e] = sel + (int64_t(b) * k + j) * DSA_ROW_CHUNKS;
+      }
+      warp_copy_rows2(from[0], to[0], from[1], to[1], lane);
+    }
+  } else {
+    for (int64_t r0 = w * 2; r0 < rows; r0 += nrole * 2) {
+      const uint4* from[2] = {nullptr, nullptr};
+      uint4* to[2] = {nullptr, nullptr};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int64_t r = r0 + e;
+        if (r >= rows) continue;
+        const int b = static_cast<int>(r / k);
+        const int j = static_cast<int>(r - int64_t(b) * k);
+        const int src = __ldg(src_map + r);
+        if (src >= 0) {
+          if (src < P) from[e] = pool + (int64_t(b) * P + src) * DSA_ROW_CHUNKS;
+          else bad |= TS_DEVERR_SLOT_RANGE;
+        } else if (src != INT_MIN) {
+          const int M = __ldg(miss_count + b);
+          if (__ldg(miss_rows + b) == M) continue;  // no repeats: served by a miss warp
+          const int t = -1 - src;
+          const int64_t base = int64_t(b) * k;
+          if (first_pos_of(miss_ids + base, miss_pos + base, M, t) == j) continue;
+          if (t < __ldg(ctx_len + b)) from[e] = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
+          else bad |= TS_DEVERR_ID_RANGE;
+        } else {
+          bad |= TS_DEVERR_ID_RANGE;
+        }
+        if (from[e]) to[e] = sel + r * DSA_ROW_CHUNKS;
+      }
+      warp_copy_rows2(from[0], to[0], from[1], to[1], lane);
+    }
+  }
+  if (bad && lane == 0) report(err, bad);
 }
 
 // One warp per (request, miss) pair: 72 pieces, lanes stride by 32.
@@ -138,20 +214,29 @@ int sm_count() {
 
 using namespace dsakv;
 
-extern "C" ts_status dsa_gather_kv(const int32_t* src_map, int B, int k, const void* pool_l, int P,
-                                   const void* host_l, int64_t ctx_stride, const int32_t* ctx_len,
-                                   void* sel_l, int32_t* err, cudaStream_t stream) {
-  if (!src_map || !pool_l || !host_l || !ctx_len || !sel_l) return TS_ERR_INVALID_ARG;
+extern "C" ts_status dsa_gather_kv(const int32_t* src_map, const int32_t* miss_ids,
+                                   const int32_t* miss_pos, const int32_t* miss_count,
+                                   const int32_t* miss_rows, int B, int k, const void* pool_l,
+                                   int P, const void* host_l, int64_t ctx_stride,
+                                   const int32_t* ctx_len, void* sel_l, int32_t* err,
+                                   cudaStream_t stream) {
+  if (!src_map || !miss_ids || !miss_pos || !miss_count || !miss_rows || !pool_l || !host_l ||
+      !ctx_len || !sel_l)
+    return TS_ERR_INVALID_ARG;
   if (B <= 0 || k <= 0 || P <= 0 || ctx_stride <= 0) return TS_ERR_INVALID_ARG;
   if (!aligned16(pool_l) || !aligned16(host_l) || !aligned16(sel_l)) return TS_ERR_INVALID_ARG;
-  const int64_t total = int64_t(B) * k * DSA_ROW_CHUNKS;
-  const int64_t per_block = int64_t(kGatherThreads) * kUnroll;
-  int64_t blocks = (total + per_block - 1) / per_block;
-  const int64_t cap = int64_t(sm_count()) * 8;  // 8 resident CTAs of 256 threads per SM
+  // A quarter of the SMs, one 1024-thread CTA each, keep a few MB of loads in
+  // flight, which saturates the host link (measured); the other SMs stay free
+  // for the attention of the previous layer, which runs beside the gather
+  // (an SM holding a gather CTA cannot also take an attention CTA).
+  const int64_t rows = int64_t(B) * k;
+  int64_t blocks = (rows + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
+  const int64_t cap = sm_count() / 4 > 8 ? sm_count() / 4 : 8;
   if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
   gather_kernel<<<static_cast<unsigned>(blocks), kGatherThreads, 0, stream>>>(
-      src_map, k, total, static_cast<const uint4*>(pool_l), P, static_cast<const uint4*>(host_l),
-      ctx_stride, ctx_len, static_cast<uint4*>(sel_l), err);
+      src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, static_cast<const uint4*>(pool_l), P,
+      static_cast<const uint4*>(host_l), ctx_stride, ctx_len, static_cast<uint4*>(sel_l), err);
   return launch_status();
 }
 

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads) dsa_plan_kernel(
     const int32_t* __restrict__ pool_tags, const int32_t* __restrict__ fifo_ptr, int S, int W,
     int32_t* __restrict__ src_map, int32_t* __restrict__ miss_ids, int32_t* __restrict__ miss_pos,
     int32_t* __restrict__ victim, uint8_t* __restrict__ install, int32_t* __restrict__ miss_count,
-    int32_t* __restrict__ ptr_next, int32_t* err) {
+    int32_t* __restrict__ miss_rows, int32_t* __restrict__ ptr_next, int32_t* err) {
   extern __shared__ __align__(16) char smem_raw[];
   const int P = S * W;
   PlanSmem sm = carve(smem_raw, P, S, k);
@@ -144,6 +144,14 @@ __global__ void __launch_bounds__(kThreads) dsa_plan_kernel(
   }
   if (bad_id) report(err, TS_DEVERR_ID_RANGE);
   ascending = __syncthreads_and(ascending);
+  {
+    // positions that miss, repeats included
+    int c = 0;
+    for (int j = tid; j < k; j += kThreads) c += (sm.src[j] < 0 && sm.src[j] != INT_MIN);
+    int total;
+    block_exclusive_scan(c, sm.scratch, &total);
+    if (tid == 0) miss_rows[b] = total;
+  }
 
   int M;
   if (ascending) {
@@ -271,9 +279,10 @@ extern "C" ts_status dsa_plan(const int32_t* ids, const int32_t* ctx_len, int B,
                               const int32_t* pool_tags, const int32_t* fifo_ptr, int S, int W,
                               int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
                               int32_t* victim, uint8_t* install, int32_t* miss_count,
-                              int32_t* ptr_next, int32_t* err, cudaStream_t stream) {
+                              int32_t* miss_rows, int32_t* ptr_next, int32_t* err,
+                              cudaStream_t stream) {
   if (!ids || !ctx_len || !pool_tags || !fifo_ptr || !src_map || !miss_ids || !miss_pos ||
-      !victim || !install || !miss_count || !ptr_next)
+      !victim || !install || !miss_count || !miss_rows || !ptr_next)
     return TS_ERR_INVALID_ARG;
   if (B <= 0 || k <= 0 || S <= 0 || W <= 0) return TS_ERR_INVALID_ARG;
   if (W > 32 || k > kMaxK || B > 2147483647 / 2) return TS_ERR_UNSUPPORTED;
@@ -285,6 +294,6 @@ extern "C" ts_status dsa_plan(const int32_t* ids, const int32_t* ctx_len, int B,
     return TS_ERR_CUDA;
   dsa_plan_kernel<<<B, kThreads, smem, stream>>>(ids, ctx_len, k, pool_tags, fifo_ptr, S, W,
                                                  src_map, miss_ids, miss_pos, victim, install,
-                                                 miss_count, ptr_next, err);
+                                                 miss_count, miss_rows, ptr_next, err);
   return launch_status();
 }

@@ -6,18 +6,20 @@
 //
 // One CTA per (request b, head tile of 128 heads, chunk of 256 selected rows),
 // on the 5th-generation tensor cores:
-//   warp 0  : TMA producer (one thread): Q and K tiles for the score product,
-//             then V tiles for the value product, through a 3-stage ring of
-//             48 KB stages (128-byte swizzle).
-//   warp 1  : allocates 512 TMEM columns; one thread issues tcgen05.mma.
-//   warps 2-5: softmax and epilogue, one TMEM lane (= one head) per thread.
+//   warp 0   : TMA producer (one thread): Q and K tiles for the score product,
+//              then V tiles for the value product, through a 3-stage ring of
+//              48 KB stages (128-byte swizzle).
+//   warp 1   : allocates 512 TMEM columns; one thread issues tcgen05.mma.
+//   warps 2-9: softmax and epilogue; two threads per head (TMEM lane), each
+//              with half of the chunk's columns.
 // Steps inside the CTA:
 //   S[128 x 256] = Q[128 x 576] K[256 x 576]^T   -> TMEM columns 0..255
 //   p = exp2(S*scale*log2e - max)  rounded to bf16, written to shared memory
 //       in the K-major 128-byte-swizzled layout the MMA reads
 //   O[:, 0:256]   = P V[:, 0:256]    -> TMEM columns 256..511
 //   O[:, 256:512] = P V[:, 256:512]  -> TMEM columns 0..255 (S is dead by then)
-//   O, max and row sum of the chunk -> fp32 workspace
+//   O (unnormalised), the row max and the row sum -> fp32 workspace, staged
+//       through shared memory so that every global store is a coalesced run.
 // A second kernel merges the chunks of a request: out = sum_c w_c O_c /
 // sum_c w_c l_c with w_c = exp2(m_c - max_c m_c).
 #include <cmath>
@@ -39,12 +41,15 @@ constexpr uint32_t kVBytes = 4 * kVBox;              // 64 rows x 256 dims
 constexpr uint32_t kPBlock = kHeads * 128;           // 128 heads x 64 rows
 constexpr uint32_t kPBytes = 4 * kPBlock;            // 128 heads x 256 rows
 constexpr int kLoads = kKB + 8;                      // 9 score stages + 8 value stages
-constexpr int kThreads = 192;
-constexpr uint32_t kBarBytes = 256;
+constexpr int kSoftmaxThreads = 256;                 // warps 2..9
+constexpr int kThreads = 64 + kSoftmaxThreads;
+constexpr uint32_t kBarBytes = 2048;
+constexpr int kOutStride = 256 + 4;  // floats per head row of the epilogue staging
 constexpr uint32_t kSmemBytes = 1024 + kPBytes + kStages * kStageBytes + kBarBytes;
 constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s of global timer per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+static_assert(kHeads * kOutStride * 4 <= kPBytes + kStages * kStageBytes, "epilogue staging");
 
 struct Bars {
   uint64_t full[kStages];
@@ -56,6 +61,7 @@ struct Bars {
   uint32_t tmem_slot;
   int abort;
   int issued;
+  float red[2][kHeads];  // the two column halves' row max, then row sum
 };
 static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
 
@@ -66,6 +72,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort, kWaitLimit) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   return ok != 0;
+}
+
+// Barrier among the softmax warps only (named barrier 1, 256 threads).
+__device__ __forceinline__ void softmax_sync() {
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+// 2^x on the special-function unit (relative error far below the bf16
+// rounding the weights then get).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -90,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->p_full, kSoftmaxThreads);
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -174,41 +193,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) tc_commit(&bars->o_full);
     }
   } else {
-    // ---------------- softmax + epilogue: one head per thread ----------------
-    const int q4 = warp & 3;
-    const int row = q4 * 32 + lane;
+    // ---------------- softmax and epilogue: two threads per head ----------------
+    // Every softmax_sync below is reached by all 256 softmax threads whatever
+    // happened before it (a wait that gave up only skips work).
+    const int q4 = warp & 3;            // TMEM lane quarter this warp may access
+    const int part = (warp - 2) >> 2;   // which half of the chunk's columns
+    const int row = q4 * 32 + lane;     // head within the tile
+    const int t = threadIdx.x - 64;     // 0..255
     const uint32_t trow = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
     const int nvalid = min(kChunk, k - c * kChunk);
+    const int col0 = part * (kChunk / 2);
     float m = -INFINITY, l = 0.f;
     bool ok = warp_wait(&bars->s_full, 0, abort);
     if (ok) {
       tc_fence_after();
-      uint32_t r[32];
-      for (int cb = 0; cb < kChunk / 32; ++cb) {
-        tmem_ld32(trow + cb * 32, r);
+      uint32_t r[32], r2[32];
+      for (int cb = 0; cb < kChunk / 2; cb += 64) {
+        tmem_ld32(trow + col0 + cb, r);
+        tmem_ld32(trow + col0 + cb + 32, r2);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (cb * 32 + i < nvalid) m = fmaxf(m, __uint_as_float(r[i]) * scale_log2);
+        for (int i = 0; i < 32; ++i) {
+          if (col0 + cb + i < nvalid) m = fmaxf(m, __uint_as_float(r[i]) * scale_log2);
+          if (col0 + cb + 32 + i < nvalid) m = fmaxf(m, __uint_as_float(r2[i]) * scale_log2);
+        }
       }
-      for (int cb = 0; cb < kChunk / 32; ++cb) {
-        tmem_ld32(trow + cb * 32, r);
+      bars->red[part][row] = m;
+    }
+    softmax_sync();
+    if (ok) {
+      m = fmaxf(bars->red[0][row], bars->red[1][row]);  // finite: column 0 is valid
+      uint32_t r[32];
+      for (int cb = 0; cb < kChunk / 2; cb += 32) {
+        tmem_ld32(trow + col0 + cb, r);
         tmem_wait_ld();
         uint32_t packed[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int c0 = cb * 32 + 2 * i;
-          const float p0 = c0 < nvalid ? exp2f(__uint_as_float(r[2 * i]) * scale_log2 - m) : 0.f;
+          const int c0 = col0 + cb + 2 * i;
+          const float p0 =
+              c0 < nvalid ? fast_exp2(__uint_as_float(r[2 * i]) * scale_log2 - m) : 0.f;
           const float p1 =
-              c0 + 1 < nvalid ? exp2f(__uint_as_float(r[2 * i + 1]) * scale_log2 - m) : 0.f;
+              c0 + 1 < nvalid ? fast_exp2(__uint_as_float(r[2 * i + 1]) * scale_log2 - m) : 0.f;
           const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
           l += __low2float(h2) + __high2float(h2);
           packed[i] = *reinterpret_cast<const uint32_t*>(&h2);
         }
-        uint8_t* blk = p_tile + (cb >> 1) * kPBlock + row * 128;
+        const int cc = col0 + cb;  // first of these 32 columns
+        uint8_t* blk = p_tile + (cc >> 6) * kPBlock + row * 128;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int chunk = (cb & 1) * 4 + j;
+          const int chunk = ((cc & 63) >> 3) + j;
           *reinterpret_cast<uint4*>(blk + ((chunk ^ (row & 7)) << 4)) =
               make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
         }
@@ -216,29 +251,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->p_full);
+    }
+    softmax_sync();  // every thread has read both halves' max
+    if (ok) bars->red[part][row] = l;
+    softmax_sync();
+    if (ok) {
+      l = bars->red[0][row] + bars->red[1][row];
       ok = warp_wait(&bars->o_full, 0, abort);
     }
-    if (ok) {
-      tc_fence_after();
-      const int head = hg * kHeads + row;
-      const size_t slot = ((size_t(b) * HG + hg) * C + c) * kHeads + row;
-      float* orow = opart + slot * DSA_DV;
-      uint32_t r[32];
-      for (int cb = 0; cb < DSA_DV / 32; ++cb) {
-        const int v0 = cb * 32;
-        const uint32_t col = v0 < 256 ? 256u + v0 : uint32_t(v0 - 256);
-        tmem_ld32(trow + col, r);
-        tmem_wait_ld();
-        if (head < H) {
+    // Epilogue: O goes through the (now idle) P tile and stage ring, 256 dims
+    // at a time, so that every store to the workspace is a coalesced run.
+    const bool live = ok && !*abort;
+    float* stage_o = reinterpret_cast<float*>(base);  // [128][kOutStride]
+    const size_t slot0 = ((size_t(b) * HG + hg) * C + c) * kHeads;
+    const int rows_valid = min(kHeads, H - hg * kHeads);
+    if (live) tc_fence_after();
+    for (int half = 0; half < 2; ++half) {
+      if (live) {
+        uint32_t r[32];
+        for (int qq = 0; qq < 4; ++qq) {
+          const int d = 128 * part + 32 * qq;  // dim within this half
+          tmem_ld32(trow + (half == 0 ? 256u + d : uint32_t(d)), r);
+          tmem_wait_ld();
+          float* dst = stage_o + row * kOutStride + d;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<float4*>(orow + v0 + 4 * j) =
+            *reinterpret_cast<float4*>(dst + 4 * j) =
                 make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                             __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
         }
       }
-      if (head < H) ml[slot] = make_float2(m, l);
+      softmax_sync();
+      if (live) {
+        // 128 rows x 64 float4 of this half; thread t moves float4 f = t + 256 i
+        for (int i = 0; i < 32; ++i) {
+          const int f = t + kSoftmaxThreads * i;
+          const int rr = f >> 6, c4 = f & 63;
+          if (rr < rows_valid)
+            *reinterpret_cast<float4*>(opart + (slot0 + rr) * DSA_DV + 256 * half + 4 * c4) =
+                *reinterpret_cast<const float4*>(stage_o + rr * kOutStride + 4 * c4);
+        }
+      }
+      softmax_sync();
     }
+    if (live && part == 0 && row < rows_valid) ml[slot0 + row] = make_float2(m, l);
   }
 
   // ---------------- teardown ----------------
@@ -266,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge the chunks of one (request, head): out = sum_c w_c O_c / sum_c w_c l_c.
+// Loads of up to eight chunks are issued together before they are summed.
 __global__ void __launch_bounds__(128) sfa_combine_kernel(const float* __restrict__ opart,
                                                           const float2* __restrict__ ml, int H,
                                                           int HG, int C,
@@ -275,21 +332,40 @@ __global__ void __launch_bounds__(128) sfa_combine_kernel(const float* __restric
   const int b = bh / H, h = bh - b * H;
   const int hg = h / kHeads, row = h - hg * kHeads;
   const size_t slot0 = ((size_t(b) * HG + hg) * C) * kHeads + row;
+  const int v = threadIdx.x * 4;
   float mx = -INFINITY;
-  for (int c = 0; c < C; ++c) mx = fmaxf(mx, ml[slot0 + size_t(c) * kHeads].x);
+  for (int c0 = 0; c0 < C; c0 += 8) {
+    float2 e[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      e[i] = c0 + i < C ? __ldg(ml + slot0 + size_t(c0 + i) * kHeads) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx = fmaxf(mx, e[i].x);
+  }
   float denom = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int v = threadIdx.x * 4;
-  for (int c = 0; c < C; ++c) {
-    const size_t slot = slot0 + size_t(c) * kHeads;
-    const float2 e = ml[slot];
-    const float w = exp2f(e.x - mx);
-    denom += w * e.y;
-    const float4 o = *reinterpret_cast<const float4*>(opart + slot * DSA_DV + v);
-    acc.x += w * o.x;
-    acc.y += w * o.y;
-    acc.z += w * o.z;
-    acc.w += w * o.w;
+  for (int c0 = 0; c0 < C; c0 += 8) {
+    float2 e[8];
+    float4 o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (c0 + i < C) {
+        const size_t slot = slot0 + size_t(c0 + i) * kHeads;
+        e[i] = __ldg(ml + slot);
+        o[i] = __ldcs(reinterpret_cast<const float4*>(opart + slot * DSA_DV + v));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (c0 + i < C) {
+        const float w = exp2f(e[i].x - mx);
+        denom += w * e[i].y;
+        acc.x += w * o[i].x;
+        acc.y += w * o[i].y;
+        acc.z += w * o[i].z;
+        acc.w += w * o[i].w;
+      }
+    }
   }
   const float inv = 1.f / denom;
   __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
@@ -369,10 +445,10 @@ extern "C" ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int
       return TS_ERR_CUDA;
     attr = true;
   }
+  __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(out);
   sfa_chunk_kernel<<<dim3(C, HG, B), kThreads, kSmemBytes, stream>>>(
       tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, err);
   if (cudaGetLastError() != cudaSuccess) return TS_ERR_CUDA;
-  sfa_combine_kernel<<<unsigned(int64_t(B) * H), 128, 0, stream>>>(
-      opart, ml, H, HG, C, static_cast<__nv_bfloat16*>(out), lse);
+  sfa_combine_kernel<<<unsigned(int64_t(B) * H), 128, 0, stream>>>(opart, ml, H, HG, C, outp, lse);
   return launch_status();
 }

@@ -3,31 +3,42 @@
 // history positions most relevant to the query, and sparse attention reads
 // only those). Ties go to the lower position; output in ascending position.
 //
-// Radix select in three passes, many CTAs per request:
-//   hist   : every CTA histograms the top 12 bits of the order-preserving
-//            32-bit key of its chunk and adds it to the request's histogram.
-//   select : every CTA finds the threshold bin (the bin holding the k-th
-//            largest key), marks the positions of higher bins in a bitmap
-//            (one 32-bit word per 32 positions, built by a warp ballot), and
-//            appends the threshold bin's (key, position) pairs to a list.
-//   finish : one CTA per request resolves the threshold inside that list
-//            (two more 10-bit digits, then the lowest positions among exact
-//            ties), sets their bits, and writes the set positions of the
-//            bitmap in order: the output comes out sorted without a sort.
+// Radix select on the order-preserving 32-bit key of every score:
+//   hist   : histogram of the top 12 bits of the key;
+//   select : find the threshold bin (the bin holding the k-th largest key),
+//            mark the positions of higher bins in a bitmap (one 32-bit word per
+//            32 positions, built by a warp ballot) and list the threshold
+//            bin's (key, position) pairs as candidates;
+//   finish : resolve the threshold inside the candidate list (two more 10-bit
+//            digits, then the lowest positions among exact ties), set their
+//            bits, and write the set positions of the bitmap in order: the
+//            output comes out sorted without a sort.
+// With many requests (>= 96) of up to 131,072 positions, all three run in one
+// CTA per request, with the histogram, bitmap and candidates in shared memory
+// (one launch). Otherwise hist and select spread over many CTAs per request
+// (8,192 positions each); the last select CTA of a request to finish (a
+// completion counter) runs the finish.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace dsakv {
 namespace {
 
-constexpr int kBins = 4096;          // top 12 bits of the key
-constexpr int kChunk = 16384;        // positions per CTA in hist / select
-constexpr int kThreads = 512;
-constexpr int kFinishThreads = 1024;
+constexpr int kBins = 4096;    // top 12 bits of the key
+constexpr int kChunk = 8192;   // positions per CTA in the multi-CTA hist / select
+constexpr int kThreads = 512;  // multi-CTA kernels
 constexpr int kMaxK = 8192;
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallMaxCtx = 131072;  // one CTA per request up to here ...
+constexpr int kSmallMinB = 96;        // ... when the requests alone fill the GPU
+constexpr int kSmallCandCap = 8192;   // candidates kept in shared memory
+constexpr int kFinishCandCap = 4096;  // ... by the multi-CTA finish
+constexpr uint32_t kAll = 0xFFFFFFFFu;
 
 struct TopkWs {
   uint32_t* hist;        // [B][kBins]
-  uint32_t* cand_count;  // [B]
+  uint32_t* cand_count;  // [B] candidates listed, then [B] select CTAs done
   uint64_t* cand;        // [B][max_ctx]  (key << 32 | position)
   uint32_t* bitmap;      // [B][words]
   int64_t words;
@@ -41,12 +52,16 @@ inline TopkWs carve(void* ws, int B, int max_ctx) {
   w.hist = reinterpret_cast<uint32_t*>(p);
   p += align256(size_t(B) * kBins * 4);
   w.cand_count = reinterpret_cast<uint32_t*>(p);
-  p += align256(size_t(B) * 4);
+  p += align256(size_t(B) * 8);
   w.cand = reinterpret_cast<uint64_t*>(p);
   p += align256(size_t(B) * max_ctx * 8);
   w.bitmap = reinterpret_cast<uint32_t*>(p);
   w.words = (max_ctx + 31) / 32;
   return w;
+}
+
+inline size_t counters_bytes(int B) {
+  return align256(size_t(B) * kBins * 4) + align256(size_t(B) * 8);
 }
 
 // Order-preserving key: a larger float gives a larger unsigned key. -0.0 is
@@ -63,244 +78,149 @@ __device__ __forceinline__ uint32_t score_key(float f, bool& nan) {
 
 __device__ __forceinline__ bool ctx_ok(int n, int k, int max_ctx) { return n >= k && n <= max_ctx; }
 
-// Threshold bin of the 4096-bin histogram: the bin t with
-// above(t) < k <= above(t) + hist[t], above(t) = count in bins > t.
-// Block-wide; every thread gets the result. smem: >= 2 * blockDim ints.
-__device__ void find_threshold_bin(const uint32_t* hist, int k, int* sbuf, int* bin_out,
-                                   int* above_out) {
-  const int nt = blockDim.x;
-  const int per = kBins / nt;  // 8 (512 threads) or 4 (1024 threads)
-  const int lo = threadIdx.x * per;
+// Add one to hist[bin] for every lane of the warp with bin >= 0, one atomic
+// per distinct bin (the lanes of a warp agree on few bins: scores cluster).
+__device__ __forceinline__ void warp_hist_add(uint32_t* hist, int bin) {
+  const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+  const int lane = threadIdx.x & 31;
+  if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+}
+
+// The bin t of an nbins histogram (walked from the preferred end: high bins
+// first when high_first) with before(t) < need <= before(t) + hist[t]; also
+// returns before(t) and hist[t]. Block-wide; every thread gets the result.
+// sbuf holds >= 44 ints.
+__device__ void select_bin(const uint32_t* hist, int nbins, bool high_first, int need, int* sbuf,
+                           int* bin_out, int* before_out, int* count_out) {
+  const int per = (nbins + blockDim.x - 1) / blockDim.x;
   int tot = 0;
-  for (int i = 0; i < per; ++i) tot += static_cast<int>(hist[lo + i]);
-  // exclusive suffix sum over threads = total - inclusive prefix
+  for (int j = 0; j < per; ++j) {
+    const int r = threadIdx.x * per + j;  // rank in preference order
+    if (r < nbins) tot += static_cast<int>(hist[high_first ? nbins - 1 - r : r]);
+  }
   int total;
-  int ex = block_exclusive_scan(tot, sbuf, &total);
-  int above = total - ex - tot;  // count in bins above this thread's range
+  const int ex = block_exclusive_scan(tot, sbuf, &total);
   if (threadIdx.x == 0) {
     sbuf[40] = -1;
     sbuf[41] = 0;
+    sbuf[42] = 0;
   }
   __syncthreads();
-  int cum = above;
-  for (int i = per - 1; i >= 0; --i) {
-    int h = static_cast<int>(hist[lo + i]);
-    if (cum < k && cum + h >= k) {
-      sbuf[40] = lo + i;
+  int cum = ex;
+  for (int j = 0; j < per; ++j) {
+    const int r = threadIdx.x * per + j;
+    if (r >= nbins) break;
+    const int bin = high_first ? nbins - 1 - r : r;
+    const int h = static_cast<int>(hist[bin]);
+    if (cum < need && cum + h >= need) {
+      sbuf[40] = bin;
       sbuf[41] = cum;
+      sbuf[42] = h;
     }
     cum += h;
   }
   __syncthreads();
   *bin_out = sbuf[40];
-  *above_out = sbuf[41];
+  *before_out = sbuf[41];
+  *count_out = sbuf[42];
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __restrict__ scores,
-                                                             int64_t ctx_stride,
-                                                             const int32_t* __restrict__ ctx_len,
-                                                             int k, int max_ctx, TopkWs ws,
-                                                             int32_t* err) {
-  __shared__ uint32_t h[kBins];
-  const int b = blockIdx.y;
-  const int n = ctx_len[b];
-  if (!ctx_ok(n, k, max_ctx)) return;
-  const int64_t start = int64_t(blockIdx.x) * kChunk;
-  if (start >= n) return;
-  const int64_t end = min(start + int64_t(kChunk), int64_t(n));
-  for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0;
-  __syncthreads();
-  const float* row = scores + int64_t(b) * ctx_stride;
-  bool nan = false;
-  for (int64_t i = start + int64_t(threadIdx.x) * 4; i < end; i += int64_t(kThreads) * 4) {
-    if (i + 4 <= end) {
-      float4 v = __ldg(reinterpret_cast<const float4*>(row + i));
-      atomicAdd(&h[score_key(v.x, nan) >> 20], 1u);
-      atomicAdd(&h[score_key(v.y, nan) >> 20], 1u);
-      atomicAdd(&h[score_key(v.z, nan) >> 20], 1u);
-      atomicAdd(&h[score_key(v.w, nan) >> 20], 1u);
-    } else {
-      for (int64_t j = i; j < end; ++j) atomicAdd(&h[score_key(__ldg(row + j), nan) >> 20], 1u);
-    }
+// Candidate lists: the first `cap` entries in shared memory, the rest in the
+// global workspace (cap = 0: all global).
+struct Cands {
+  const uint64_t* smem;
+  const uint64_t* glob;
+  uint32_t cap;
+  __device__ __forceinline__ uint64_t operator()(uint32_t i) const {
+    return i < cap ? smem[i] : __ldcg(glob + i);
   }
-  if (nan) report(err, TS_DEVERR_NAN);
-  __syncthreads();
-  uint32_t* gh = ws.hist + int64_t(b) * kBins;
-  for (int i = threadIdx.x; i < kBins; i += kThreads)
-    if (h[i]) atomicAdd(&gh[i], h[i]);
-}
+};
 
-__global__ void __launch_bounds__(kThreads) topk_select_kernel(const float* __restrict__ scores,
-                                                               int64_t ctx_stride,
-                                                               const int32_t* __restrict__ ctx_len,
-                                                               int k, int max_ctx, TopkWs ws) {
-  __shared__ int sbuf[64];
-  const int b = blockIdx.y;
-  const int n = ctx_len[b];
-  if (!ctx_ok(n, k, max_ctx)) return;
-  const int64_t start = int64_t(blockIdx.x) * kChunk;
-  if (start >= n) return;
-  int t1, above;
-  find_threshold_bin(ws.hist + int64_t(b) * kBins, k, sbuf, &t1, &above);
-  const int64_t end = min(start + int64_t(kChunk), int64_t(n));
-  const float* row = scores + int64_t(b) * ctx_stride;
-  uint32_t* bits = ws.bitmap + int64_t(b) * ws.words;
-  uint64_t* cand = ws.cand + int64_t(b) * max_ctx;
-  const int lane = threadIdx.x & 31;
-  // each warp covers 32 consecutive positions per iteration: one bitmap word
-  for (int64_t base = start + (threadIdx.x & ~31); base < end; base += kThreads) {
-    const int64_t i = base + lane;
-    bool nan = false;
-    uint32_t key = 0;
-    int bin = -1;
-    if (i < end) {
-      key = score_key(__ldg(row + i), nan);
-      bin = static_cast<int>(key >> 20);
-    }
-    const uint32_t above_mask = __ballot_sync(0xffffffffu, bin > t1);
-    const uint32_t tie_mask = __ballot_sync(0xffffffffu, bin == t1);
-    if (lane == 0) bits[base >> 5] = above_mask;
-    if (tie_mask) {
-      uint32_t pos0 = 0;
-      if (lane == 0) pos0 = atomicAdd(ws.cand_count + b, __popc(tie_mask));
-      pos0 = __shfl_sync(0xffffffffu, pos0, 0);
-      if (bin == t1) {
-        const uint32_t off = __popc(tie_mask & ((1u << lane) - 1u));
-        cand[pos0 + off] = (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(i);
-      }
-    }
-  }
-}
-
-// Among the candidates selected by `pred`, find the digit value t of
-// (value >> shift) & (nbins-1) such that the candidates with a digit
-// preferred to t number fewer than `need` and those preferred or equal
-// reach it. `high_first` prefers larger digits (keys), else smaller
-// (positions). Returns t and the count strictly preferred.
+// Histogram of a digit of the candidates satisfying pred, then select_bin.
 template <typename Pred, typename Digit>
-__device__ void radix_digit(const uint64_t* cand, uint32_t c, int nbins, bool high_first, int need,
-                            Pred pred, Digit digit, uint32_t* hist, int* sbuf, int* t_out,
-                            int* before_out) {
+__device__ void cand_digit(const Cands& cand, uint32_t c, int nbins, bool high_first, int need,
+                           Pred pred, Digit digit, uint32_t* hist, int* sbuf, int* t_out,
+                           int* before_out, int* count_out) {
   for (int i = threadIdx.x; i < nbins; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   for (uint32_t i = threadIdx.x; i < c; i += blockDim.x) {
-    uint64_t e = __ldcg(cand + i);
+    const uint64_t e = cand(i);
     if (pred(e)) atomicAdd(&hist[digit(e)], 1u);
   }
   __syncthreads();
-  // scan bins in preference order; nbins <= 2048 and blockDim = 1024
-  const int per = (nbins + blockDim.x - 1) / blockDim.x;
-  int tot = 0;
-  for (int j = 0; j < per; ++j) {
-    int r = threadIdx.x * per + j;  // rank in preference order
-    if (r < nbins) tot += hist[high_first ? nbins - 1 - r : r];
-  }
-  int total;
-  int ex = block_exclusive_scan(tot, sbuf, &total);
-  if (threadIdx.x == 0) {
-    sbuf[40] = -1;
-    sbuf[41] = 0;
-  }
-  __syncthreads();
-  int cum = ex;
-  for (int j = 0; j < per; ++j) {
-    int r = threadIdx.x * per + j;
-    if (r >= nbins) break;
-    int bin = high_first ? nbins - 1 - r : r;
-    int h = hist[bin];
-    if (cum < need && cum + h >= need) {
-      sbuf[40] = bin;
-      sbuf[41] = cum;
-    }
-    cum += h;
-  }
-  __syncthreads();
-  *t_out = sbuf[40];
-  *before_out = sbuf[41];
-  __syncthreads();
+  select_bin(hist, nbins, high_first, need, sbuf, t_out, before_out, count_out);
 }
 
-__global__ void __launch_bounds__(kFinishThreads) topk_finish_kernel(
-    const int32_t* __restrict__ ctx_len, int k, int max_ctx, TopkWs ws, int32_t* __restrict__ ids,
-    int32_t* err) {
-  __shared__ uint32_t hist[2048];
-  __shared__ int sbuf[64];
-  const int b = blockIdx.x;
-  const int n = ctx_len[b];
-  int32_t* out = ids + int64_t(b) * k;
-  if (!ctx_ok(n, k, max_ctx)) {
-    for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
-    if (threadIdx.x == 0) report(err, TS_DEVERR_CTX);
-    return;
+// Resolve the threshold inside the candidate list of one request, set the
+// chosen candidates' bits, and write the set positions in ascending order.
+// t1 = the 12-bit threshold bin, need1 = candidates to take. `bits` is the
+// request's bitmap (shared or global memory), n its context. hist: >= 2048
+// words of shared memory.
+template <bool kSharedBits>
+__device__ void finish_request(const Cands& cand, uint32_t c, int t1, int need1, uint32_t* bits,
+                               int n, int k, int32_t* out, uint32_t* hist, int* sbuf,
+                               int32_t* err) {
+  uint32_t T = 0, cut = kAll;  // take key > T, and key == T with position <= cut
+  if (need1 < static_cast<int>(c)) {
+    int t2, before2, cnt2, t3, before3, cnt3;
+    cand_digit(
+        cand, c, 1024, true, need1, [](uint64_t) { return true; },
+        [](uint64_t e) { return static_cast<int>((e >> 42) & 1023u); }, hist, sbuf, &t2, &before2,
+        &cnt2);
+    const int need2 = need1 - before2;
+    cand_digit(
+        cand, c, 1024, true, need2,
+        [t2](uint64_t e) { return static_cast<int>((e >> 42) & 1023u) == t2; },
+        [](uint64_t e) { return static_cast<int>((e >> 32) & 1023u); }, hist, sbuf, &t3,
+        &before3, &cnt3);
+    const int need3 = need2 - before3;  // exact ties to take
+    T = (static_cast<uint32_t>(t1) << 20) | (static_cast<uint32_t>(t2) << 10) |
+        static_cast<uint32_t>(t3);
+    if (need3 < cnt3) {
+      // the lowest positions among the exact ties: three digits of the position
+      auto is_tie = [T](uint64_t e) { return static_cast<uint32_t>(e >> 32) == T; };
+      int pa, ba, ca, pb, bb, cb, pc, bc, cc;
+      cand_digit(
+          cand, c, 2048, false, need3, is_tie,
+          [](uint64_t e) { return static_cast<int>((static_cast<uint32_t>(e) >> 20) & 2047u); },
+          hist, sbuf, &pa, &ba, &ca);
+      cand_digit(
+          cand, c, 1024, false, need3 - ba,
+          [is_tie, pa](uint64_t e) {
+            return is_tie(e) && static_cast<int>((static_cast<uint32_t>(e) >> 20) & 2047u) == pa;
+          },
+          [](uint64_t e) { return static_cast<int>((static_cast<uint32_t>(e) >> 10) & 1023u); },
+          hist, sbuf, &pb, &bb, &cb);
+      cand_digit(
+          cand, c, 1024, false, need3 - ba - bb,
+          [is_tie, pa, pb](uint64_t e) {
+            const uint32_t p = static_cast<uint32_t>(e);
+            return is_tie(e) && static_cast<int>((p >> 20) & 2047u) == pa &&
+                   static_cast<int>((p >> 10) & 1023u) == pb;
+          },
+          [](uint64_t e) { return static_cast<int>(static_cast<uint32_t>(e) & 1023u); }, hist,
+          sbuf, &pc, &bc, &cc);
+      cut = (static_cast<uint32_t>(pa) << 20) | (static_cast<uint32_t>(pb) << 10) |
+            static_cast<uint32_t>(pc);
+    }
   }
-  // the 12-bit threshold bin, as the select pass found it
-  int t1, above1;
-  {
-    // find_threshold_bin wants kBins / blockDim bins per thread: 4 here
-    find_threshold_bin(ws.hist + int64_t(b) * kBins, k, sbuf, &t1, &above1);
-  }
-  const uint64_t* cand = ws.cand + int64_t(b) * max_ctx;
-  const uint32_t c = __ldcg(ws.cand_count + b);
-  const int need1 = k - above1;  // >= 1 candidates to take from the list
-
-  // digit 2: key bits [19:10]
-  int t2, before2;
-  radix_digit(
-      cand, c, 1024, true, need1, [](uint64_t) { return true; },
-      [](uint64_t e) { return static_cast<int>((e >> 42) & 1023u); }, hist, sbuf, &t2, &before2);
-  const int need2 = need1 - before2;
-  // digit 3: key bits [9:0] among digit-2 == t2
-  int t3, before3;
-  radix_digit(
-      cand, c, 1024, true, need2,
-      [t2](uint64_t e) { return static_cast<int>((e >> 42) & 1023u) == t2; },
-      [](uint64_t e) { return static_cast<int>((e >> 32) & 1023u); }, hist, sbuf, &t3, &before3);
-  const int need3 = need2 - before3;  // ties to take at the exact threshold key
-  const uint32_t T = (static_cast<uint32_t>(t1) << 20) | (static_cast<uint32_t>(t2) << 10) |
-                     static_cast<uint32_t>(t3);
-  // lowest positions among the exact ties: three digits of the position
-  auto is_tie = [T](uint64_t e) { return static_cast<uint32_t>(e >> 32) == T; };
-  int pa, ba, pb, bb, pc, bc;
-  radix_digit(
-      cand, c, 2048, false, need3, is_tie,
-      [](uint64_t e) { return static_cast<int>((static_cast<uint32_t>(e) >> 20) & 2047u); }, hist,
-      sbuf, &pa, &ba);
-  radix_digit(
-      cand, c, 1024, false, need3 - ba,
-      [is_tie, pa](uint64_t e) {
-        return is_tie(e) && static_cast<int>((static_cast<uint32_t>(e) >> 20) & 2047u) == pa;
-      },
-      [](uint64_t e) { return static_cast<int>((static_cast<uint32_t>(e) >> 10) & 1023u); }, hist,
-      sbuf, &pb, &bb);
-  radix_digit(
-      cand, c, 1024, false, need3 - ba - bb,
-      [is_tie, pa, pb](uint64_t e) {
-        const uint32_t p = static_cast<uint32_t>(e);
-        return is_tie(e) && static_cast<int>((p >> 20) & 2047u) == pa &&
-               static_cast<int>((p >> 10) & 1023u) == pb;
-      },
-      [](uint64_t e) { return static_cast<int>(static_cast<uint32_t>(e) & 1023u); }, hist, sbuf,
-      &pc, &bc);
-  const uint32_t cut = (static_cast<uint32_t>(pa) << 20) | (static_cast<uint32_t>(pb) << 10) |
-                       static_cast<uint32_t>(pc);
-
-  // mark the chosen candidates
-  uint32_t* bits = ws.bitmap + int64_t(b) * ws.words;
+  // T = 0 with cut = all takes every candidate (need1 >= c)
   for (uint32_t i = threadIdx.x; i < c; i += blockDim.x) {
-    const uint64_t e = __ldcg(cand + i);
+    const uint64_t e = cand(i);
     const uint32_t key = static_cast<uint32_t>(e >> 32), pos = static_cast<uint32_t>(e);
     if (key > T || (key == T && pos <= cut)) atomicOr(bits + (pos >> 5), 1u << (pos & 31));
   }
   __syncthreads();
 
   // ordered write-out of the set bits
-  const int64_t nwords = (n + 31) / 32;
+  const int64_t nwords = (int64_t(n) + 31) / 32;
   const int64_t per = (nwords + blockDim.x - 1) / blockDim.x;
   const int64_t w0 = int64_t(threadIdx.x) * per;
   const int64_t w1 = min(w0 + per, nwords);
+  auto word = [&](int64_t w) { return kSharedBits ? bits[w] : __ldcg(bits + w); };
   int cnt = 0;
-  for (int64_t w = w0; w < w1; ++w) cnt += __popc(__ldcg(bits + w));
+  for (int64_t w = w0; w < w1; ++w) cnt += __popc(word(w));
   int total;
   int pos = block_exclusive_scan(cnt, sbuf, &total);
   if (total != k) {
@@ -309,13 +229,283 @@ __global__ void __launch_bounds__(kFinishThreads) topk_finish_kernel(
     return;
   }
   for (int64_t w = w0; w < w1; ++w) {
-    uint32_t m = __ldcg(bits + w);
+    uint32_t m = word(w);
     while (m) {
       const int bit = __ffs(m) - 1;
       m &= m - 1;
       out[pos++] = static_cast<int32_t>(w * 32 + bit);
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// one CTA per request (contexts up to kSmallMaxCtx)
+// ---------------------------------------------------------------------------
+struct SmallSmem {
+  uint32_t hist[kBins];
+  uint32_t bits[kSmallMaxCtx / 32];
+  uint64_t cand[kSmallCandCap];
+  int sbuf[64];
+  uint32_t ncand;
+};
+
+__global__ void __launch_bounds__(kSmallThreads) topk_small_kernel(
+    const float* __restrict__ scores, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
+    int k, int max_ctx, TopkWs ws, int32_t* __restrict__ ids, int32_t* err) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SmallSmem& sm = *reinterpret_cast<SmallSmem*>(smem_raw);
+  const int b = blockIdx.x;
+  const int n = ctx_len[b];
+  int32_t* out = ids + int64_t(b) * k;
+  if (!ctx_ok(n, k, max_ctx)) {
+    for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
+    if (threadIdx.x == 0) report(err, TS_DEVERR_CTX);
+    return;
+  }
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) sm.hist[i] = 0;
+  if (threadIdx.x == 0) sm.ncand = 0;
+  __syncthreads();
+  const float* row = scores + int64_t(b) * ctx_stride;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  bool nan = false;
+
+  // pass 1: histogram; each warp walks 4 x 32 consecutive positions per step
+  for (int base = warp * 128; base < n; base += nwarps * 128) {
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * 32 + lane;
+      v[u] = i < n ? __ldg(row + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * 32 + lane;
+      const int bin = i < n ? static_cast<int>(score_key(v[u], nan) >> 20) : -1;
+      warp_hist_add(sm.hist, bin);
+    }
+  }
+  if (nan) report(err, TS_DEVERR_NAN);
+  __syncthreads();
+  int t1, above, cnt1;
+  select_bin(sm.hist, kBins, true, k, sm.sbuf, &t1, &above, &cnt1);
+
+  // pass 2: bitmap words of the positions above the threshold bin, and the
+  // candidate list of the threshold bin
+  uint64_t* gcand = ws.cand + int64_t(b) * max_ctx;
+  for (int base = warp * 128; base < n; base += nwarps * 128) {
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * 32 + lane;
+      v[u] = i < n ? __ldg(row + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * 32 + lane;
+      bool nan2 = false;
+      uint32_t key = 0;
+      int bin = -1;
+      if (i < n) {
+        key = score_key(v[u], nan2);
+        bin = static_cast<int>(key >> 20);
+      }
+      const uint32_t above_mask = __ballot_sync(0xffffffffu, bin > t1);
+      const uint32_t tie_mask = __ballot_sync(0xffffffffu, bin == t1);
+      if (lane == 0 && base + u * 32 < n) sm.bits[(base + u * 32) >> 5] = above_mask;
+      if (tie_mask) {
+        uint32_t pos0 = 0;
+        if (lane == 0) pos0 = atomicAdd(&sm.ncand, __popc(tie_mask));
+        pos0 = __shfl_sync(0xffffffffu, pos0, 0);
+        if (bin == t1) {
+          const uint32_t at = pos0 + __popc(tie_mask & ((1u << lane) - 1u));
+          const uint64_t e = (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(i);
+          if (at < kSmallCandCap) sm.cand[at] = e;
+          else gcand[at] = e;
+        }
+      }
+    }
+  }
+  __threadfence_block();
+  __syncthreads();
+  const uint32_t c = sm.ncand;
+  Cands cand{sm.cand, gcand, kSmallCandCap};
+  finish_request<true>(cand, c, t1, k - above, sm.bits, n, k, out, sm.hist, sm.sbuf, err);
+}
+
+// ---------------------------------------------------------------------------
+// many CTAs per request
+// ---------------------------------------------------------------------------
+// Scores cluster in few bins, so shared-memory atomics on one histogram
+// collide; every pair of warps counts into its own copy (8 copies, 128 KB of
+// dynamic shared memory) and the copies are summed when flushed.
+constexpr int kHistCopies = kThreads / 64;
+
+__global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __restrict__ scores,
+                                                             int64_t ctx_stride,
+                                                             const int32_t* __restrict__ ctx_len,
+                                                             int k, int max_ctx, TopkWs ws,
+                                                             int32_t* err) {
+  extern __shared__ __align__(16) uint32_t hcopies[];  // [kHistCopies][kBins]
+  const int b = blockIdx.y;
+  const int n = ctx_len[b];
+  if (!ctx_ok(n, k, max_ctx)) return;
+  const int64_t start = int64_t(blockIdx.x) * kChunk;
+  if (start >= n) return;
+  const int64_t end = min(start + int64_t(kChunk), int64_t(n));
+  for (int i = threadIdx.x; i < kHistCopies * kBins; i += kThreads) hcopies[i] = 0;
+  __syncthreads();
+  const float* row = scores + int64_t(b) * ctx_stride;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* h = hcopies + (warp >> 1) * kBins;
+  bool nan = false;
+  for (int64_t base = start + warp * 256; base < end; base += (kThreads / 32) * 256) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t i = base + u * 32 + lane;
+      v[u] = i < end ? __ldg(row + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t i = base + u * 32 + lane;
+      const int bin = i < end ? static_cast<int>(score_key(v[u], nan) >> 20) : -1;
+      warp_hist_add(h, bin);
+    }
+  }
+  if (nan) report(err, TS_DEVERR_NAN);
+  __syncthreads();
+  uint32_t* gh = ws.hist + int64_t(b) * kBins;
+  for (int i = threadIdx.x; i < kBins; i += kThreads) {
+    uint32_t sum = 0;
+#pragma unroll
+    for (int cpy = 0; cpy < kHistCopies; ++cpy) sum += hcopies[cpy * kBins + i];
+    if (sum) atomicAdd(&gh[i], sum);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) topk_select_kernel(
+    const float* __restrict__ scores, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
+    int k, int max_ctx, TopkWs ws, int32_t* __restrict__ ids, int32_t* err) {
+  __shared__ int sbuf[64];
+  __shared__ uint32_t dig[2048];
+  __shared__ uint64_t cand_s[kFinishCandCap];
+  __shared__ int last;
+  const int b = blockIdx.y;
+  const int n = ctx_len[b];
+  if (!ctx_ok(n, k, max_ctx)) {
+    if (blockIdx.x == 0) {
+      int32_t* out = ids + int64_t(b) * k;
+      for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
+      if (threadIdx.x == 0) report(err, TS_DEVERR_CTX);
+    }
+    return;
+  }
+  const int64_t start = int64_t(blockIdx.x) * kChunk;
+  if (start >= n) return;
+  // threshold bin from the request's histogram
+  int t1, above, cnt1;
+  select_bin(ws.hist + int64_t(b) * kBins, kBins, true, k, sbuf, &t1, &above, &cnt1);
+  const int64_t end = min(start + int64_t(kChunk), int64_t(n));
+  const float* row = scores + int64_t(b) * ctx_stride;
+  uint32_t* bits = ws.bitmap + int64_t(b) * ws.words;
+  uint64_t* cand = ws.cand + int64_t(b) * max_ctx;
+  const int lane = threadIdx.x & 31;
+  // each warp covers 4 x 32 consecutive positions per iteration: 4 bitmap words
+  const int warp = threadIdx.x >> 5;
+  for (int64_t base = start + warp * 128; base < end; base += (kThreads / 32) * 128) {
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = base + u * 32 + lane;
+      v[u] = i < end ? __ldg(row + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = base + u * 32 + lane;
+      bool nan = false;
+      uint32_t key = 0;
+      int bin = -1;
+      if (i < end) {
+        key = score_key(v[u], nan);
+        bin = static_cast<int>(key >> 20);
+      }
+      const uint32_t above_mask = __ballot_sync(0xffffffffu, bin > t1);
+      const uint32_t tie_mask = __ballot_sync(0xffffffffu, bin == t1);
+      if (lane == 0 && base + u * 32 < end) bits[(base + u * 32) >> 5] = above_mask;
+      if (tie_mask) {
+        uint32_t pos0 = 0;
+        if (lane == 0) pos0 = atomicAdd(ws.cand_count + b, __popc(tie_mask));
+        pos0 = __shfl_sync(0xffffffffu, pos0, 0);
+        if (bin == t1) {
+          const uint32_t off = __popc(tie_mask & ((1u << lane) - 1u));
+          cand[pos0 + off] = (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(i);
+        }
+      }
+    }
+  }
+  // the last CTA of this request to get here runs the finish
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t chunks = static_cast<uint32_t>((int64_t(n) + kChunk - 1) / kChunk);
+    last = atomicAdd(ws.cand_count + gridDim.y + b, 1u) == chunks - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const uint32_t c = __ldcg(ws.cand_count + b);
+  // the finish reads the candidate list several times: keep its head in
+  // shared memory
+  for (uint32_t i = threadIdx.x; i < c && i < kFinishCandCap; i += blockDim.x)
+    cand_s[i] = __ldcg(cand + i);
+  __syncthreads();
+  Cands cl{cand_s, cand, kFinishCandCap};
+  finish_request<false>(cl, c, t1, k - above, bits, n, k, ids + int64_t(b) * k, dig, sbuf, err);
+}
+
+size_t small_smem_bytes() { return sizeof(SmallSmem); }
+
+// Launch the top-k on a workspace laid out by carve().
+ts_status launch_topk(const float* scores, int64_t ctx_stride, const int32_t* ctx_len, int B,
+                      int max_ctx, int k, int32_t* ids, void* ws, int32_t* err,
+                      cudaStream_t stream) {
+  TopkWs w = carve(ws, B, max_ctx);
+  if (max_ctx <= kSmallMaxCtx && B >= kSmallMinB) {
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(topk_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(small_smem_bytes())) != cudaSuccess)
+        return TS_ERR_CUDA;
+      attr = true;
+    }
+    topk_small_kernel<<<B, kSmallThreads, small_smem_bytes(), stream>>>(
+        scores, ctx_stride, ctx_len, k, max_ctx, w, ids, err);
+    return launch_status();
+  }
+  // histograms, list counters and completion counters start at zero
+  if (cudaMemsetAsync(ws, 0, counters_bytes(B), stream) != cudaSuccess) return TS_ERR_CUDA;
+  const dim3 grid((max_ctx + kChunk - 1) / kChunk, B);
+  static bool hist_attr = false;
+  if (!hist_attr) {
+    if (cudaFuncSetAttribute(topk_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kHistCopies * kBins * 4) != cudaSuccess)
+      return TS_ERR_CUDA;
+    hist_attr = true;
+  }
+  topk_hist_kernel<<<grid, kThreads, kHistCopies * kBins * 4, stream>>>(scores, ctx_stride,
+                                                                        ctx_len, k, max_ctx, w, err);
+  topk_select_kernel<<<grid, kThreads, 0, stream>>>(scores, ctx_stride, ctx_len, k, max_ctx, w,
+                                                    ids, err);
+  return launch_status();
+}
+
+ts_status check_topk_args(const float* scores, int64_t ctx_stride, const int32_t* ctx_len, int B,
+                          int max_ctx, int k, int32_t* ids) {
+  if (!scores || !ctx_len || !ids) return TS_ERR_INVALID_ARG;
+  if (B <= 0 || k <= 0 || max_ctx < k || ctx_stride < max_ctx) return TS_ERR_INVALID_ARG;
+  if (k > kMaxK || B > 65535) return TS_ERR_UNSUPPORTED;
+  if (!aligned16(scores) || (ctx_stride & 3) != 0) return TS_ERR_INVALID_ARG;
+  return TS_OK;
 }
 
 }  // namespace
@@ -327,37 +517,26 @@ extern "C" size_t ts_topk_workspace_size(int B, int max_ctx, int k) {
   (void)k;
   if (B <= 0 || max_ctx <= 0) return 0;
   const int64_t words = (int64_t(max_ctx) + 31) / 32;
-  return align256(size_t(B) * kBins * 4) + align256(size_t(B) * 4) +
+  return align256(size_t(B) * kBins * 4) + align256(size_t(B) * 8) +
          align256(size_t(B) * max_ctx * 8) + align256(size_t(B) * words * 4);
 }
 
 extern "C" ts_status ts_topk(const float* scores, int64_t ctx_stride, const int32_t* ctx_len, int B,
                              int max_ctx, int k, int32_t* ids, void* ws, size_t ws_bytes,
                              int32_t* err, cudaStream_t stream) {
-  if (!scores || !ctx_len || !ids || !ws) return TS_ERR_INVALID_ARG;
-  if (B <= 0 || k <= 0 || max_ctx < k || ctx_stride < max_ctx) return TS_ERR_INVALID_ARG;
-  if (k > kMaxK || B > 65535) return TS_ERR_UNSUPPORTED;
-  if (!aligned16(scores) || (ctx_stride & 3) != 0) return TS_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < ts_topk_workspace_size(B, max_ctx, k))
+  const ts_status st = check_topk_args(scores, ctx_stride, ctx_len, B, max_ctx, k, ids);
+  if (st != TS_OK) return st;
+  if (!ws) return TS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0 ||
+      ws_bytes < ts_topk_workspace_size(B, max_ctx, k))
     return TS_ERR_WORKSPACE;
-  TopkWs w = carve(ws, B, max_ctx);
-  // histograms and list counters start at zero on every call
-  if (cudaMemsetAsync(ws, 0, align256(size_t(B) * kBins * 4) + align256(size_t(B) * 4), stream) !=
-      cudaSuccess)
-    return TS_ERR_CUDA;
-  const dim3 grid((max_ctx + kChunk - 1) / kChunk, B);
-  topk_hist_kernel<<<grid, kThreads, 0, stream>>>(scores, ctx_stride, ctx_len, k, max_ctx, w, err);
-  topk_select_kernel<<<grid, kThreads, 0, stream>>>(scores, ctx_stride, ctx_len, k, max_ctx, w);
-  topk_finish_kernel<<<B, kFinishThreads, 0, stream>>>(ctx_len, k, max_ctx, w, ids, err);
-  return launch_status();
+  return launch_topk(scores, ctx_stride, ctx_len, B, max_ctx, k, ids, ws, err, stream);
 }
 
 // ---------------------------------------------------------------------------
 // ts_topk_noalloc: the same top-k with its scratch in a fixed device array, for
 // callers that cannot allocate device memory.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 namespace dsakv {
 namespace {
 
@@ -365,7 +544,7 @@ constexpr int kNoAllocMaxB = 128;
 constexpr int64_t kNoAllocMaxPositions = int64_t(1) << 22;  // B * max_ctx
 constexpr size_t kNoAllocScratchBytes =
     ((size_t(kNoAllocMaxB) * kBins * 4 + 255) & ~size_t(255)) +
-    ((size_t(kNoAllocMaxB) * 4 + 255) & ~size_t(255)) +
+    ((size_t(kNoAllocMaxB) * 8 + 255) & ~size_t(255)) +
     ((size_t(kNoAllocMaxPositions) * 8 + 255) & ~size_t(255)) +
     ((size_t(kNoAllocMaxPositions / 32 + kNoAllocMaxB) * 4 + 255) & ~size_t(255));
 
@@ -401,22 +580,12 @@ void* scratch_on_current_device() {
 extern "C" ts_status ts_topk_noalloc(const float* scores, int64_t ctx_stride,
                                      const int32_t* ctx_len, int B, int max_ctx, int k,
                                      int32_t* ids, int32_t* err, cudaStream_t stream) {
-  if (!scores || !ctx_len || !ids) return TS_ERR_INVALID_ARG;
-  if (B <= 0 || k <= 0 || max_ctx < k || ctx_stride < max_ctx) return TS_ERR_INVALID_ARG;
-  if (k > kMaxK || B > kNoAllocMaxB || int64_t(B) * max_ctx > kNoAllocMaxPositions)
-    return TS_ERR_UNSUPPORTED;
-  if (!aligned16(scores) || (ctx_stride & 3) != 0) return TS_ERR_INVALID_ARG;
+  const ts_status st = check_topk_args(scores, ctx_stride, ctx_len, B, max_ctx, k, ids);
+  if (st != TS_OK) return st;
+  if (B > kNoAllocMaxB || int64_t(B) * max_ctx > kNoAllocMaxPositions) return TS_ERR_UNSUPPORTED;
   if (ts_topk_workspace_size(B, max_ctx, k) > kNoAllocScratchBytes) return TS_ERR_UNSUPPORTED;
   void* ws = scratch_on_current_device();
   if (!ws) return TS_ERR_CUDA;
-  TopkWs w = carve(ws, B, max_ctx);
-  // the histograms and list counters left by the previous call are cleared
-  if (cudaMemsetAsync(ws, 0, align256(size_t(B) * kBins * 4) + align256(size_t(B) * 4), stream) !=
-      cudaSuccess)
-    return TS_ERR_CUDA;
-  const dim3 grid((max_ctx + kChunk - 1) / kChunk, B);
-  topk_hist_kernel<<<grid, kThreads, 0, stream>>>(scores, ctx_stride, ctx_len, k, max_ctx, w, err);
-  topk_select_kernel<<<grid, kThreads, 0, stream>>>(scores, ctx_stride, ctx_len, k, max_ctx, w);
-  topk_finish_kernel<<<B, kFinishThreads, 0, stream>>>(ctx_len, k, max_ctx, w, ids, err);
-  return launch_status();
+  // every call clears what must start at zero before its kernels read it
+  return launch_topk(scores, ctx_stride, ctx_len, B, max_ctx, k, ids, ws, err, stream);
 }

@@ -5,19 +5,25 @@ The schedule is the one of the GLM-5.2 shared-Indexer KV Cache Offload page,
 refill on a side stream synchronised by events, metadata update at the group's
 last layer):
 
-  main stream : ts_topk -> [wait refill_done of the previous step] -> dsa_plan
-                -> for each layer l: dsa_gather_kv(l) -> record gathered[l]
-                                     -> sfa_mla_decode(l)
-  side stream : for each layer l: wait gathered[l] -> dsa_refill_pool(l)
-                (the last layer also updates tags and FIFO pointers)
-                -> record refill_done
+  main stream   : ts_topk -> [wait refill_done of the previous step] -> dsa_plan
+                  -> record planned
+                  -> for each layer l: [wait gathered[l]] -> sfa_mla_decode(l)
+  gather stream : [wait planned] -> dsa_gather_kv(0..3), recording gathered[l]
+                  after each layer
+  side stream   : for each layer l: [wait gathered[l]] -> dsa_refill_pool(l)
+                  (the last layer also updates tags and FIFO pointers)
+                  -> record refill_done
 
-Ordering argument: refill(l) overwrites pool slots that gather(l) reads, so it
-waits for gather(l); the next step's plan reads the tags the last refill
-writes and rewrites the miss list every refill reads, so it waits for
-refill_done; the next step's gather(l) rewrites sel[l], which refill(l) reads,
-and it comes after that plan. Memory comes from PyTorch; the arithmetic runs
-in libdsakv's kernels only.
+The plan is shared by the group, so every layer's gather can start as soon as
+it exists: the host-link transfers of layer l+1 overlap the attention of
+layer l, and each layer's attention still starts the moment its own rows are
+in (SFA first). Ordering argument: refill(l) overwrites pool slots that
+gather(l) reads, so it waits for gather(l); the next step's plan reads the
+tags the last refill writes and rewrites the plan every gather and refill
+reads, so it waits for refill_done and comes after the last SFA, which waited
+for the last gather; the next step's gather(l) rewrites sel[l], which SFA(l)
+and refill(l) read, and it waits for that plan. Memory comes from PyTorch;
+the arithmetic runs in libdsakv's kernels only.
 """
 from __future__ import annotations
 
@@ -30,6 +36,34 @@ from . import _abi as abi
 
 D = 576
 DV = 512
+
+
+class PinnedHost:
+    """A page-locked host buffer owned by numpy and registered with the CUDA
+    driver (cudaHostRegister through ts_host_register). Used instead of
+    cudaHostAlloc'd memory for every host buffer the device touches: on this
+    GB300 platform the first zero-copy read after a large DMA from
+    cudaHostAlloc'd memory stalled for about a hundred milliseconds, which
+    registered memory does not do."""
+
+    def __init__(self, shape, dtype):
+        self.array = np.zeros(shape, dtype=dtype)
+        self._host = self.array.ctypes.data
+        self.dev = abi.ts_host_register(self._host, self.array.nbytes) if self.array.nbytes else 0
+
+    def tensor(self) -> torch.Tensor:
+        return torch.from_numpy(self.array)
+
+    def close(self):
+        if self._host and self.array.nbytes:
+            abi.ts_host_unregister(self._host)
+        self._host = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class HostKV:
@@ -88,6 +122,7 @@ class DecodeGroup:
         self.victim = torch.empty((B, k), **i32)
         self.install = torch.empty((B, k), dtype=torch.uint8, device=dev)
         self.miss_count = torch.zeros((B,), **i32)
+        self.miss_rows = torch.zeros((B,), **i32)
         self.ptr_next = torch.empty((B, S), **i32)
         # per-layer selection buffers and attention outputs
         self.sel = torch.empty((layers, B, k, D), dtype=torch.int16, device=dev)
@@ -101,7 +136,9 @@ class DecodeGroup:
         self.err = torch.zeros((1,), **i32)
         # streams and events
         self.main = torch.cuda.Stream(device=dev)
+        self.gstream = torch.cuda.Stream(device=dev)
         self.side = torch.cuda.Stream(device=dev)
+        self.planned = torch.cuda.Event()
         self.gathered = [torch.cuda.Event() for _ in range(layers)]
         self.refill_done = torch.cuda.Event()
         self.refill_done.record(self.side)
@@ -137,12 +174,19 @@ class DecodeGroup:
         abi.check(timed("plan", m, lambda: abi.dsa_plan(
             ids, self.ctx_len, B, k, self.tags, self.fifo_ptr, self.S, self.W, self.src_map,
             self.miss_ids, self.miss_pos, self.victim, self.install, self.miss_count,
-            self.ptr_next, self.err, m)), "dsa_plan")
+            self.miss_rows, self.ptr_next, self.err, m)), "dsa_plan")
+        self.planned.record(m)
+        gs = self.gstream
+        gs.wait_event(self.planned)
         for l in range(L):
-            abi.check(timed("gather", m, lambda: abi.dsa_gather_kv(
-                self.src_map, B, k, self.pool[l], self.P, self.host.layer_ptr(l),
-                self.ctx_stride, self.ctx_len, self.sel[l], self.err, m)), "dsa_gather_kv")
-            self.gathered[l].record(m)
+            abi.check(timed("gather", gs, lambda: abi.dsa_gather_kv(
+                self.src_map, self.miss_ids, self.miss_pos, self.miss_count, self.miss_rows, B, k,
+                self.pool[l],
+                self.P, self.host.layer_ptr(l),
+                self.ctx_stride, self.ctx_len, self.sel[l], self.err, gs)), "dsa_gather_kv")
+            self.gathered[l].record(gs)
+        for l in range(L):
+            m.wait_event(self.gathered[l])
             abi.check(timed("sfa", m, lambda: abi.sfa_mla_decode(
                 q[l], self.sel[l], B, self.H, k, self.scale, self.out[l], self.lse[l],
                 self.sfa_ws, self.sfa_ws_bytes, self.err, m)), "sfa_mla_decode")
@@ -158,10 +202,12 @@ class DecodeGroup:
         """Make `stream` (default: the current stream) wait for all step work."""
         st = torch.cuda.current_stream() if stream is None else stream
         st.wait_stream(self.main)
+        st.wait_stream(self.gstream)
         st.wait_stream(self.side)
 
     def synchronize(self) -> int:
         """Wait for everything and return (and clear) the device error bits."""
         self.main.synchronize()
+        self.gstream.synchronize()
         self.side.synchronize()
         return abi.ts_read_error(self.err, self.main)

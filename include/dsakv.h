@@ -141,7 +141,10 @@ ts_status ts_topk_noalloc(const float* scores, int64_t ctx_stride, const int32_t
  *   install    uint8 [B][k]   1 when the miss survives the step (the last W
  *                             misses of a set); 0 when a later miss of the same
  *                             set in the same step replaces it
- *   miss_count int32 [B]
+ *   miss_count int32 [B]      distinct missed tokens
+ *   miss_rows  int32 [B]      positions that miss (a repeated missed token counts
+ *                             at every position; equals miss_count when no
+ *                             token repeats)
  *   ptr_next   int32 [B][S]   (ptr + misses in the set) mod W
  * Hits never move a pointer; a hit slot may be chosen as a victim (plain FIFO),
  * which is safe because every layer reads its rows before its own refill.
@@ -151,14 +154,18 @@ ts_status dsa_plan(const int32_t* ids, const int32_t* ctx_len, int B, int k,
                    const int32_t* pool_tags, const int32_t* fifo_ptr, int S, int W,
                    int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
                    int32_t* victim, uint8_t* install, int32_t* miss_count,
-                   int32_t* ptr_next, int32_t* err, cudaStream_t stream);
+                   int32_t* miss_rows, int32_t* ptr_next, int32_t* err, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * dsa_gather_kv -- serve one layer's selected rows ([GLM] §5 DsaServe, §5.1;
  * base design §2.1 GatherSelectionKvCache). Row j of request b is copied from
  * the device pool when src_map >= 0 and read in place from pinned host memory
- * (zero-copy) when src_map = -1 - t.
+ * (zero-copy) when src_map = -1 - t. The host rows are read first, from the
+ * plan's compact miss list (miss_ids / miss_pos / miss_count of dsa_plan for
+ * the same ids), so the host-link transfers start at once; the pool rows and
+ * any repeated miss follow.
  *
+ *   src_map, miss_ids, miss_pos, miss_count, miss_rows   outputs of dsa_plan
  *   pool_l  bf16 [B][P][576]          device, this layer's pool
  *   host_l  bf16 [B][ctx_stride][576] device-accessible address of pinned host
  *                                     memory, this layer's full latent KV
@@ -166,8 +173,10 @@ ts_status dsa_plan(const int32_t* ids, const int32_t* ctx_len, int B, int k,
  * All three 16-byte aligned. Out-of-range slots or host rows set
  * TS_DEVERR_SLOT_RANGE / TS_DEVERR_ID_RANGE and leave that row untouched.
  * ------------------------------------------------------------------------- */
-ts_status dsa_gather_kv(const int32_t* src_map, int B, int k, const void* pool_l,
-                        int P, const void* host_l, int64_t ctx_stride,
+ts_status dsa_gather_kv(const int32_t* src_map, const int32_t* miss_ids,
+                        const int32_t* miss_pos, const int32_t* miss_count,
+                        const int32_t* miss_rows, int B, int k,
+                        const void* pool_l, int P, const void* host_l, int64_t ctx_stride,
                         const int32_t* ctx_len, void* sel_l, int32_t* err,
                         cudaStream_t stream);
 

@@ -40,6 +40,11 @@ class Plan:
     def miss_count(self) -> int:
         return int(self.miss_ids.size)
 
+    @property
+    def miss_rows(self) -> int:
+        """Positions that miss, a repeated missed id counted at each position."""
+        return int(np.sum((self.src_map < 0) & (self.src_map != np.iinfo(np.int32).min)))
+
 
 def dsa_plan(ids, ctx_len: int, tags, fifo_ptr, S: int, W: int) -> Plan:
     ids = [int(t) for t in ids]

@@ -74,6 +74,15 @@ def test_topk_all_equal_and_k_equals_ctx(d):
     _check_topk(d, scores, lens, 2048)
     scores2 = np.random.default_rng(2).standard_normal((1, 3000)).astype(np.float32)
     _check_topk(d, scores2, np.array([3000], np.int32), 3000)
+    # many requests (one CTA each): every score tied in some of them, so the
+    # candidate list outgrows shared memory
+    rng = np.random.default_rng(3)
+    scores4 = np.round(rng.standard_normal((96, 10000)) * 2).astype(np.float32)
+    scores4[::7] = 0.5
+    _check_topk(d, scores4, np.full(96, 10000, np.int32), 2048)
+    # past the one-CTA-per-request size: the many-CTA path, every score tied
+    scores3 = np.full((2, 150016), -2.25, np.float32)
+    _check_topk(d, scores3, np.array([150016, 140001], np.int32), 2048)
 
 
 def test_topk_errors(d):
@@ -118,11 +127,11 @@ def run_plan(d, ids, lens, tags, ptr, S, W):
     i32 = lambda *s: torch.full(s, -7, dtype=torch.int32, device="cuda")
     out = dict(src_map=i32(B, k), miss_ids=i32(B, k), miss_pos=i32(B, k), victim=i32(B, k),
                install=torch.zeros((B, k), dtype=torch.uint8, device="cuda"),
-               miss_count=i32(B), ptr_next=i32(B, S))
+               miss_count=i32(B), miss_rows=i32(B), ptr_next=i32(B, S))
     err = _err()
     st = d.dsa_plan(t(ids), t(lens), B, k, t(tags), t(ptr), S, W, out["src_map"],
                     out["miss_ids"], out["miss_pos"], out["victim"], out["install"],
-                    out["miss_count"], out["ptr_next"], err)
+                    out["miss_count"], out["miss_rows"], out["ptr_next"], err)
     assert st == 0
     bits = d.ts_read_error(err)
     return {n: v.cpu().numpy() for n, v in out.items()}, bits
@@ -135,6 +144,7 @@ def _check_plan(d, ids, lens, tags, ptr, S, W):
         want = oracle.dsa_plan(ids[b], int(lens[b]), tags[b], ptr[b], S, W)
         M = want.miss_count
         assert got["miss_count"][b] == M
+        assert got["miss_rows"][b] == want.miss_rows
         assert np.array_equal(got["src_map"][b], want.src_map)
         assert np.array_equal(got["miss_ids"][b, :M], want.miss_ids)
         assert np.array_equal(got["miss_pos"][b, :M], want.miss_pos)
@@ -211,8 +221,9 @@ def test_gather_and_refill_bytes(d):
     sel = torch.zeros((B, k, 576), dtype=torch.int16, device="cuda")
     err = _err()
     ln = t(lens)
-    assert d.dsa_gather_kv(t(got["src_map"]), B, k, pool_t, P, host.layer_ptr(0), ctx, ln, sel,
-                           err) == 0
+    assert d.dsa_gather_kv(t(got["src_map"]), t(got["miss_ids"]), t(got["miss_pos"]),
+                           t(got["miss_count"]), t(got["miss_rows"]), B, k, pool_t, P,
+                           host.layer_ptr(0), ctx, ln, sel, err) == 0
     assert d.ts_read_error(err) == 0
     sel_np = sel.cpu().numpy().view(np.uint16)
     for b in range(B):
@@ -244,11 +255,45 @@ def test_gather_flags_bad_rows(d):
     pool = torch.zeros((1, 8, 576), dtype=torch.int16, device="cuda")
     sel = torch.zeros((1, 4, 576), dtype=torch.int16, device="cuda")
     src = torch.tensor([[0, 9, -1 - 70, -1 - 3]], dtype=torch.int32, device="cuda")
+    mids = torch.tensor([[3, 70, 0, 0]], dtype=torch.int32, device="cuda")
+    mpos = torch.tensor([[3, 2, 0, 0]], dtype=torch.int32, device="cuda")
+    mcnt = torch.tensor([2], dtype=torch.int32, device="cuda")
     err = _err()
     ln = torch.tensor([64], dtype=torch.int32, device="cuda")
-    assert d.dsa_gather_kv(src, 1, 4, pool, 8, host.layer_ptr(0), 64, ln, sel, err) == 0
+    assert d.dsa_gather_kv(src, mids, mpos, mcnt, mcnt, 1, 4, pool, 8, host.layer_ptr(0), 64, ln,
+                           sel, err) == 0
     bits = d.ts_read_error(err)
     assert bits & 0x04 and bits & 0x01
+    host.close()
+
+
+def test_gather_repeated_ids(d):
+    """Caller-supplied ids with repeats: every copy of a missed token gets its
+    host row (the miss list serves the first position, the second pass the
+    others)."""
+    from decode_dsa_kv_gb300 import HostKV
+    rng = np.random.default_rng(8)
+    S, W, k, ctx = 16, 2, 200, 300
+    host = HostKV(1, 1, ctx)
+    host.array[...] = rng.integers(0, 65536, size=host.array.shape, dtype=np.uint16)
+    tags, ptr = _random_state(rng, 1, S, W, ctx)
+    pool = np.zeros((1, S * W, 576), np.uint16)
+    for slot in np.flatnonzero(tags[0] >= 0):
+        pool[0, slot] = host.array[0, 0, tags[0, slot]]
+    ids = rng.integers(0, 120, size=(1, k)).astype(np.int32)
+    lens = np.array([ctx], np.int32)
+    got, bits = run_plan(d, ids, lens, tags, ptr, S, W)
+    assert bits == 0
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    sel = torch.zeros((1, k, 576), dtype=torch.int16, device="cuda")
+    err = _err()
+    assert got["miss_rows"][0] > got["miss_count"][0]      # the ids do repeat
+    assert d.dsa_gather_kv(t(got["src_map"]), t(got["miss_ids"]), t(got["miss_pos"]),
+                           t(got["miss_count"]), t(got["miss_rows"]), 1, k,
+                           t(pool.view(np.int16)), S * W, host.layer_ptr(0), ctx, t(lens), sel,
+                           err) == 0
+    assert d.ts_read_error(err) == 0
+    assert np.array_equal(sel.cpu().numpy().view(np.uint16)[0], host.array[0, 0][ids[0]])
     host.close()
 
 
@@ -272,7 +317,8 @@ def run_sfa(d, q_bits, rows_bits, scale):
 
 
 @pytest.mark.parametrize("B,H,k", [(1, 16, 256), (2, 128, 2048), (3, 128, 300), (1, 128, 1),
-                                   (2, 20, 513), (1, 256, 1000), (4, 128, 4096)])
+                                   (2, 20, 513), (1, 256, 1000), (4, 128, 4096), (2, 128, 1800),
+                                   (3, 64, 1279)])
 def test_sfa_parity(d, B, H, k):
     rng = np.random.default_rng(B * 1000 + H + k)
     q = wl.normal_bf16(B * H, 576, 77, 9, B, H).reshape(B, H, 576)

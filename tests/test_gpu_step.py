@@ -57,6 +57,7 @@ def run_steps(d, w, steps, sample=None, sfa_layers=None, sfa_heads=None):
             assert np.array_equal(ids[b], r["ids"]), (step, b)
             assert np.array_equal(src[b], plan.src_map), (step, b)
             assert mc[b] == M
+            assert int(g.miss_rows[b]) == plan.miss_rows
             assert np.array_equal(g.miss_ids[b, :M].cpu().numpy(), plan.miss_ids)
             assert np.array_equal(g.victim[b, :M].cpu().numpy(), plan.victim)
             assert np.array_equal(g.install[b, :M].cpu().numpy().astype(bool), plan.install)

@@ -93,6 +93,7 @@ def test_duplicates_listed_once():
     ids = [9, 5, 9, 13, 5, 9]
     plan = _check_against_simulator(ids, 20, tags, [1, 1, 0, 0], S, W)
     assert plan.src_map.tolist() == [-10, 2, -10, -14, 2, -10]
+    assert plan.miss_rows == 4                      # 9 three times, 13 once
     assert plan.miss_ids.tolist() == [9, 13]
     assert plan.miss_pos.tolist() == [0, 3]
 
