@@ -37,8 +37,13 @@ import workload as wl  # noqa: E402
 METRIC = "selected KV rows/s per decode step (plan+gather+SFA); % of HBM/link roofline"
 UNIT = "rows/s"
 KERNELS = ("topk", "plan", "gather", "sfa", "refill")
-# our kernels per step: top-k 3 + plan 1 + layers x (gather 1 + sfa 2 + refill 1)
-LAUNCHES_TOPK, LAUNCHES_PLAN, LAUNCHES_PER_LAYER = 3, 1, 4
+# our kernels per step: top-k (1: one CTA per request, or 2: histogram + select)
+# + plan 1 + layers x (gather 1 + sfa 2 + refill 1)
+LAUNCHES_PLAN, LAUNCHES_PER_LAYER = 1, 4
+
+
+def topk_launches(w) -> int:
+    return 1 if (w.ctx <= 131072 and w.B >= 96) else 2
 
 
 def parse(argv=None):
@@ -59,6 +64,8 @@ def parse(argv=None):
                     help="after the warm-up steps, launch only this kernel --steps times "
                          "(on the state the warm-up left) and report its time per launch")
     ap.add_argument("--B", type=int, default=None, help="override the workload's request count")
+    ap.add_argument("--no-kernel-events", action="store_true",
+                    help="time the steps without per-kernel events (no per-kernel roofline)")
     return ap.parse_args(argv)
 
 
@@ -366,7 +373,6 @@ def run_native(args, w, rank, world, local):
         scores_pin.array[t] = stream.next()
         wl.queries(w, t, out=q_pin.array[t].view(np.uint16), first_request=first)
     scores_h, q_h = scores_pin.tensor(), q_pin.tensor()
-    pinned_ok = scores_h.is_pinned()
     scores_d = scores_h.cuda()
     q_d = q_h.cuda()
     g = dk.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host)
@@ -392,7 +398,7 @@ def run_native(args, w, rank, world, local):
     # timed region: K steps, per-kernel events on the launching streams
     miss_log = torch.zeros((args.steps, w.B), dtype=torch.int32, device="cuda")
     inst_log = torch.zeros((args.steps,), dtype=torch.int64, device="cuda")
-    kev = {n: [] for n in KERNELS}
+    kev = None if args.no_kernel_events else {n: [] for n in KERNELS}
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -402,10 +408,12 @@ def run_native(args, w, rank, world, local):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(g.main)
+    t_enq0 = time.perf_counter()
     for s in range(args.steps):
         step(args.warmup + s, kev)
         with torch.cuda.stream(g.main):
             miss_log[s].copy_(g.miss_count, non_blocking=True)
+    t_enq1 = time.perf_counter()
     g.main.wait_stream(g.side)
     e1.record(g.main)
     torch.cuda.synchronize()
@@ -429,30 +437,34 @@ def run_native(args, w, rank, world, local):
     per_kernel = {}
     alg = algorithmic(w, lens, hit_frac, install_frac)
     for n in KERNELS:
-        evs = kev[n]
+        evs = kev[n] if kev else []
         if not evs:
             continue
         ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
         per_kernel[n] = roofline_of(n, alg[n], ms, peaks, link)
         per_kernel[n]["launches_per_step"] = len(evs) / args.steps
-    dom = max(per_kernel, key=lambda n: per_kernel[n]["ms_per_launch"]
-              * per_kernel[n]["launches_per_step"])
-    rf = dict(per_kernel[dom])
-    rf_line = {"kernel": dom, "bound": rf["bound"], "achieved": rf["achieved"],
-               "peak": rf["peak"], "unit": rf["unit"], "frac": rf["frac"],
-               "traffic": traffic_record(dom, w.name),
-               "peak_source": peaks["source"] if rf["bound"] != "host_link"
-               else "H2D DMA copy of pinned memory, measured in this run"}
+    rf_line = None
+    if per_kernel:
+        dom = max(per_kernel, key=lambda n: per_kernel[n]["ms_per_launch"]
+                  * per_kernel[n]["launches_per_step"])
+        rf = dict(per_kernel[dom])
+        rf_line = {"kernel": dom, "bound": rf["bound"], "achieved": rf["achieved"],
+                   "peak": rf["peak"], "unit": rf["unit"], "frac": rf["frac"],
+                   "traffic": traffic_record(dom, w.name),
+                   "peak_source": peaks["source"] if rf["bound"] != "host_link"
+                   else "H2D DMA copy of registered host memory, measured in this run"}
 
     # end to end through the same schedule with host buffers: per step the
     # scores and queries are copied in from pinned host memory and the
     # attention output copied back
     e2e = None
     if not args.no_e2e:
+        from decode_dsa_kv_gb300 import _abi as abi
         ins_s = torch.empty((w.B, w.ctx_stride), dtype=torch.float32, device="cuda")
         ins_q = torch.empty((w.layers, w.B, w.H, 576), dtype=torch.int16, device="cuda")
-        out_pin = dk.PinnedHost((w.layers, w.B, w.H, 512 * 2), np.uint8)
-        out_h = out_pin.tensor().view(torch.bfloat16).view(w.layers, w.B, w.H, 512)
+        out_pin = dk.PinnedHost((w.layers, w.B, w.H, 512), np.int16)
+        s_bytes, q_bytes = ins_s.numel() * 4, ins_q.numel() * 2
+        o_bytes = g.out.numel() * 2
         n_e2e = min(args.e2e_steps, args.steps)
         torch.cuda.synchronize()
         barrier(world)
@@ -461,20 +473,22 @@ def run_native(args, w, rank, world, local):
         f0.record(g.main)
         for s in range(n_e2e):
             i = palindrome_index(args.warmup + args.steps + s, T)
-            with torch.cuda.stream(g.main):
-                ins_s.copy_(scores_h[i], non_blocking=True)
-                ins_q.copy_(q_h[i], non_blocking=True)
+            # the step's inputs in and its attention output out, through the SMs
+            abi.check(abi.ts_copy(ins_s, scores_pin.dev + i * s_bytes, s_bytes, g.main), "ts_copy")
+            abi.check(abi.ts_copy(ins_q, q_pin.dev + i * q_bytes, q_bytes, g.main), "ts_copy")
             g.step(ins_s, ins_q)
-            with torch.cuda.stream(g.main):
-                out_h.copy_(g.out, non_blocking=True)
+            abi.check(abi.ts_copy(out_pin.dev, g.out, o_bytes, g.main), "ts_copy")
         g.main.wait_stream(g.side)
         f1.record(g.main)
         torch.cuda.synchronize()
+        if g.synchronize():
+            raise RuntimeError("device error in the end-to-end steps")
         e2e_ms = max_over_ranks(f0.elapsed_time(f1) / n_e2e, world, "cuda")
         e2e = {"value": rows_step / (e2e_ms * 1e-3), "unit": UNIT,
-               "h2d_bytes_per_step": int(ins_s.numel() * 4 + ins_q.numel() * 2),
-               "d2h_bytes_per_step": int(out_h.numel() * 2), "steps": n_e2e,
-               "ms_per_step": e2e_ms, "host_buffers_pinned": bool(pinned_ok)}
+               "h2d_bytes_per_step": int(s_bytes + q_bytes), "d2h_bytes_per_step": int(o_bytes),
+               "steps": n_e2e, "ms_per_step": e2e_ms,
+               "copies": "ts_copy (SM copies) from / to registered host memory"}
+        out_pin.close()
 
     clocks = sampler.summary(t_wall0, t_wall1)
     host.close()
@@ -503,10 +517,11 @@ def run_native(args, w, rank, world, local):
         "roofline": rf_line,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * (LAUNCHES_TOPK + LAUNCHES_PLAN
+        "gpu_launches": args.steps * (topk_launches(w) + LAUNCHES_PLAN
                                       + w.layers * LAUNCHES_PER_LAYER),
         "clocks": clocks,
         "hit_rate": hit_frac,
+        "host_enqueue_ms_per_step": (t_enq1 - t_enq0) * 1e3 / args.steps,
         "link_peak_gbs": link,
         "kernels": {n: {k2: (round(v, 4) if isinstance(v, float) else v)
                         for k2, v in per_kernel[n].items()} for n in per_kernel},

@@ -42,6 +42,7 @@ _SIGS = {
     "ts_status_string": (ctypes.c_char_p, [_I]),
     "ts_host_register": (_I, [_P, _SZ, ctypes.POINTER(ctypes.c_void_p)]),
     "ts_host_unregister": (_I, [_P]),
+    "ts_copy": (_I, [_P, _P, _SZ, _P]),
     "ts_read_error": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "ts_topk_workspace_size": (_SZ, [_I, _I, _I]),
     "ts_topk": (_I, [_P, _I64, _P, _I, _I, _I, _P, _P, _SZ, _P, _P]),
@@ -112,6 +113,10 @@ def ts_host_register(host_addr: int, nbytes: int) -> int:
 
 def ts_host_unregister(host_addr: int) -> int:
     return _lib.ts_host_unregister(host_addr)
+
+
+def ts_copy(dst, src, nbytes: int, stream=None) -> int:
+    return _lib.ts_copy(ptr(dst), ptr(src), nbytes, stream_handle(stream))
 
 
 def ts_read_error(err, stream=None) -> int:

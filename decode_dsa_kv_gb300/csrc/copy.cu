@@ -262,3 +262,40 @@ extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* mis
       static_cast<uint4*>(pool_l), P, update_metadata, pool_tags, fifo_ptr, ptr_next, S, W, err);
   return launch_status();
 }
+
+// ---------------------------------------------------------------------------
+// ts_copy: a byte copy done by the SMs (16-byte loads and stores), between any
+// two device-accessible buffers: device memory or registered host memory.
+// ---------------------------------------------------------------------------
+namespace dsakv {
+namespace {
+
+__global__ void __launch_bounds__(512) sm_copy_kernel(const uint4* __restrict__ src,
+                                                      uint4* __restrict__ dst, int64_t n16) {
+  const int64_t step = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += step * 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * step < n16) v[u] = ld_nc_v4(src + i + u * step);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * step < n16) st_v4(dst + i + u * step, v[u]);
+  }
+}
+
+}  // namespace
+}  // namespace dsakv
+
+extern "C" ts_status ts_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
+  if (!dst || !src) return TS_ERR_INVALID_ARG;
+  if (!aligned16(dst) || !aligned16(src) || (bytes & 15u) != 0) return TS_ERR_INVALID_ARG;
+  if (bytes == 0) return TS_OK;
+  const int64_t n16 = static_cast<int64_t>(bytes / 16);
+  int64_t blocks = (n16 + 4 * 512 - 1) / (4 * 512);
+  const int64_t cap = int64_t(sm_count()) * 2;
+  if (blocks > cap) blocks = cap;
+  sm_copy_kernel<<<static_cast<unsigned>(blocks), 512, 0, stream>>>(
+      static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+  return launch_status();
+}

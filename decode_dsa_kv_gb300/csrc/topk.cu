@@ -368,8 +368,7 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int64_t i = base + u * 32 + lane;
-      const int bin = i < end ? static_cast<int>(score_key(v[u], nan) >> 20) : -1;
-      warp_hist_add(h, bin);
+      if (i < end) atomicAdd(&h[score_key(v[u], nan) >> 20], 1u);
     }
   }
   if (nan) report(err, TS_DEVERR_NAN);

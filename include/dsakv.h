@@ -75,6 +75,15 @@ const char* ts_status_string(ts_status status);
 ts_status ts_host_register(void* host, size_t bytes, void** dev);
 ts_status ts_host_unregister(void* host);
 
+/* Copy `bytes` bytes from src to dst with the SMs (16-byte loads and stores).
+ * Either side may be device memory or registered host memory (its device-
+ * accessible address). For moving a step's inputs and outputs across the host
+ * link: on GB300 systems, DMA copies from many distinct host buffers were seen
+ * to slow the zero-copy gathers that run at the same time, where SM copies
+ * were not. Both pointers 16-byte aligned, bytes a multiple of 16. Enqueues
+ * on `stream`; no allocation. */
+ts_status ts_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream);
+
 /* Wait for `stream`, read the error word into *bits (host), clear it on the
  * device. Returns TS_ERR_DEVICE_CHECK when any bit was set. */
 ts_status ts_read_error(int32_t* err, int32_t* bits, cudaStream_t stream);

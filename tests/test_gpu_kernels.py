@@ -343,3 +343,21 @@ def test_sfa_constant_rows_exact(d):
     q = wl.normal_bf16(128, 576, 6, 9, 0, 0).reshape(1, 128, 576)
     out, lse = run_sfa(d, q, rows, 1 / 24)
     assert np.array_equal(out[0], np.repeat(row[:, :512], 128, axis=0))
+
+
+def test_ts_copy_between_device_and_registered_host(d):
+    from decode_dsa_kv_gb300 import PinnedHost
+    rng = np.random.default_rng(12)
+    n = 3 * 1024 * 1024 + 48
+    h_in = PinnedHost((n,), np.uint8)
+    h_in.array[:] = rng.integers(0, 256, n, dtype=np.uint8)
+    dev = torch.empty(n, dtype=torch.uint8, device="cuda")
+    h_out = PinnedHost((n,), np.uint8)
+    assert d.ts_copy(dev, h_in.dev, n) == 0            # host -> device
+    assert d.ts_copy(h_out.dev, dev, n) == 0           # device -> host
+    torch.cuda.synchronize()
+    assert np.array_equal(dev.cpu().numpy(), h_in.array)
+    assert np.array_equal(h_out.array, h_in.array)
+    assert d.ts_copy(dev, h_in.dev, 15) != 0           # not a multiple of 16 bytes
+    h_in.close()
+    h_out.close()
