@@ -37,13 +37,13 @@ import workload as wl  # noqa: E402
 METRIC = "selected KV rows/s per decode step (plan+gather+SFA); % of HBM/link roofline"
 UNIT = "rows/s"
 KERNELS = ("topk", "plan", "gather", "sfa", "refill")
-# our kernels per step: top-k (1: one CTA per request, or 2: histogram + select)
+# our kernels per step: top-k (1: one cluster per request, or 2: histogram + select)
 # + plan 1 + layers x (gather 1 + sfa 2 + refill 1)
 LAUNCHES_PLAN, LAUNCHES_PER_LAYER = 1, 4
 
 
 def topk_launches(w) -> int:
-    return 1 if (w.ctx <= 131072 and w.B >= 96) else 2
+    return 1 if w.ctx <= 131072 else 2
 
 
 def parse(argv=None):

@@ -152,7 +152,8 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(
 }
 
 // One warp per (request, miss) pair: 72 pieces, lanes stride by 32.
-__global__ void __launch_bounds__(256) refill_kernel(
+constexpr int kRefillThreads = 1024;
+__global__ void __launch_bounds__(kRefillThreads) refill_kernel(
     const int32_t* __restrict__ miss_ids, const int32_t* __restrict__ miss_pos,
     const int32_t* __restrict__ victim, const uint8_t* __restrict__ install,
     const int32_t* __restrict__ miss_count, int B, int k, const uint4* __restrict__ sel,
@@ -252,12 +253,14 @@ extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* mis
   if (update_metadata && (!pool_tags || !fifo_ptr || !ptr_next || S <= 0 || W <= 0 || S * W != P))
     return TS_ERR_INVALID_ARG;
   if (!aligned16(sel_l) || !aligned16(pool_l)) return TS_ERR_INVALID_ARG;
+  // like the gather, a quarter of the SMs: the refill is off the critical
+  // path and leaves the other SMs to the attention it runs beside
   const int64_t warps = int64_t(B) * k;
-  int64_t blocks = (warps * 32 + 255) / 256;
-  const int64_t cap = int64_t(sm_count()) * 8;
+  int64_t blocks = (warps * 32 + kRefillThreads - 1) / kRefillThreads;
+  const int64_t cap = sm_count() / 4 > 8 ? sm_count() / 4 : 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  refill_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+  refill_kernel<<<static_cast<unsigned>(blocks), kRefillThreads, 0, stream>>>(
       miss_ids, miss_pos, victim, install, miss_count, B, k, static_cast<const uint4*>(sel_l),
       static_cast<uint4*>(pool_l), P, update_metadata, pool_tags, fifo_ptr, ptr_next, S, W, err);
   return launch_status();

@@ -4,20 +4,21 @@
 // latent row of 512 latent + 64 rope values is both K and V, and decode is
 // split over the KV rows with fp32 partials merged by log-sum-exp).
 //
-// One CTA per (request b, head tile of 128 heads, chunk of 256 selected rows),
+// One CTA per (request b, head tile of 128 heads, chunk of 512 selected rows),
 // on the 5th-generation tensor cores:
-//   warp 0   : TMA producer (one thread): Q and K tiles for the score product,
-//              then V tiles for the value product, through a 3-stage ring of
-//              48 KB stages (128-byte swizzle).
+//   warp 0   : TMA producer (one thread): Q and K tiles for the score product
+//              (two 256-row halves), then V tiles for the value product,
+//              through a 2-stage ring of 48 KB stages (128-byte swizzle).
 //   warp 1   : allocates 512 TMEM columns; one thread issues tcgen05.mma.
 //   warps 2-9: softmax and epilogue; two threads per head (TMEM lane), each
 //              with half of the chunk's columns.
 // Steps inside the CTA:
-//   S[128 x 256] = Q[128 x 576] K[256 x 576]^T   -> TMEM columns 0..255
+//   S[128 x 512] = Q[128 x 576] K[512 x 576]^T   -> all 512 TMEM columns
 //   p = exp2(S*scale*log2e - max)  rounded to bf16, written to shared memory
 //       in the K-major 128-byte-swizzled layout the MMA reads
 //   O[:, 0:256]   = P V[:, 0:256]    -> TMEM columns 256..511
-//   O[:, 256:512] = P V[:, 256:512]  -> TMEM columns 0..255 (S is dead by then)
+//   O[:, 256:512] = P V[:, 256:512]  -> TMEM columns 0..255 (S is dead by then:
+//       P holds it, bf16, in shared memory)
 //   O (unnormalised), the row max and the row sum -> fp32 workspace, staged
 //       through shared memory so that every global store is a coalesced run.
 // A second kernel merges the chunks of a request: out = sum_c w_c O_c /
@@ -30,20 +31,22 @@ namespace dsakv {
 namespace {
 
 constexpr int kHeads = 128;  // MMA M
-constexpr int kChunk = 256;  // rows per CTA: N of the score product, K of the value product
+constexpr int kChunk = 512;  // rows per CTA: two score MMAs of N = 256, K of the value product
+constexpr int kHalfRows = 256;
 constexpr int kKB = 9;       // 64-wide blocks of the 576 dims
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr uint32_t kQBytes = kHeads * 128;           // 128 heads x 64 dims
-constexpr uint32_t kKBytes = kChunk * 128;           // 256 rows x 64 dims
+constexpr uint32_t kKBytes = kHalfRows * 128;        // 256 rows x 64 dims
 constexpr uint32_t kStageBytes = kQBytes + kKBytes;  // 48 KB
 constexpr uint32_t kVBox = 64 * 128;                 // 64 rows x 64 dims
 constexpr uint32_t kVBytes = 4 * kVBox;              // 64 rows x 256 dims
 constexpr uint32_t kPBlock = kHeads * 128;           // 128 heads x 64 rows
-constexpr uint32_t kPBytes = 4 * kPBlock;            // 128 heads x 256 rows
-constexpr int kLoads = kKB + 8;                      // 9 score stages + 8 value stages
+constexpr uint32_t kPBytes = 8 * kPBlock;            // 128 heads x 512 rows
+constexpr int kScoreLoads = 2 * kKB;                 // 18 score stages
+constexpr int kLoads = kScoreLoads + 16;             // + 16 value stages (8 row blocks x 2 halves)
 constexpr int kSoftmaxThreads = 256;                 // warps 2..9
 constexpr int kThreads = 64 + kSoftmaxThreads;
-constexpr uint32_t kBarBytes = 2048;
+constexpr uint32_t kBarBytes = 1536;
 constexpr int kOutStride = 256 + 4;  // floats per head row of the epilogue staging
 constexpr uint32_t kSmemBytes = 1024 + kPBytes + kStages * kStageBytes + kBarBytes;
 constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s of global timer per wait
@@ -137,12 +140,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             !mbar_wait_bounded(&bars->empty[s], ((it / kStages) - 1) & 1, abort, kWaitLimit))
           break;
         uint8_t* st = stages + s * kStageBytes;
-        if (it < kKB) {
+        if (it < kScoreLoads) {
+          const int kb = it % kKB, nh = it / kKB;
           mbar_expect_tx(&bars->full[s], kStageBytes);
-          tma_load_3d(st, &tm_q, &bars->full[s], it * 64, hg * kHeads, b);
-          tma_load_3d(st + kQBytes, &tm_k, &bars->full[s], it * 64, c * kChunk, b);
+          tma_load_3d(st, &tm_q, &bars->full[s], kb * 64, hg * kHeads, b);
+          tma_load_3d(st + kQBytes, &tm_k, &bars->full[s], kb * 64, c * kChunk + nh * kHalfRows, b);
         } else {
-          const int v = it - kKB, half = v >> 2, rb = v & 3;
+          const int v = it - kScoreLoads, half = v >> 3, rb = v & 7;
           mbar_expect_tx(&bars->full[s], kVBytes);
           for (int j = 0; j < 4; ++j)
             tma_load_3d(st + j * kVBox, &tm_v, &bars->full[s], half * 256 + j * 64,
@@ -154,20 +158,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(kHeads, kChunk, false, false);
+      const uint32_t id_s = idesc_bf16_f32(kHeads, kHalfRows, false, false);
       const uint32_t id_pv = idesc_bf16_f32(kHeads, 256, false, true);
       bool ok = true;
-      for (int it = 0; it < kKB && ok; ++it) {
+      for (int it = 0; it < kScoreLoads && ok; ++it) {
         const int s = it % kStages;
         ok = mbar_wait_bounded(&bars->full[s], (it / kStages) & 1, abort, kWaitLimit);
         if (!ok) break;
         tc_fence_after();
+        const int kb = it % kKB, nh = it / kKB;
         const uint32_t qa = smem_addr(stages + s * kStageBytes);
         const uint32_t ka = qa + kQBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma_bf16(tmem, smem_desc_sw128(qa + kk * 32, 16, 1024),
-                      smem_desc_sw128(ka + kk * 32, 16, 1024), id_s, (it | kk) != 0);
+          tc_mma_bf16(tmem + nh * kHalfRows, smem_desc_sw128(qa + kk * 32, 16, 1024),
+                      smem_desc_sw128(ka + kk * 32, 16, 1024), id_s, (kb | kk) != 0);
         tc_commit(&bars->empty[s]);
       }
       if (ok) {
@@ -175,12 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait_bounded(&bars->p_full, 0, abort, kWaitLimit);
       }
       if (ok) tc_fence_after();
-      for (int it = kKB; it < kLoads && ok; ++it) {
+      for (int it = kScoreLoads; it < kLoads && ok; ++it) {
         const int s = it % kStages;
         ok = mbar_wait_bounded(&bars->full[s], (it / kStages) & 1, abort, kWaitLimit);
         if (!ok) break;
         tc_fence_after();
-        const int v = it - kKB, half = v >> 2, rb = v & 3;
+        const int v = it - kScoreLoads, half = v >> 3, rb = v & 7;
         const uint32_t d = tmem + (half == 0 ? 256u : 0u);
         const uint32_t pa = smem_addr(p_tile) + rb * kPBlock;
         const uint32_t va = smem_addr(stages + s * kStageBytes);
@@ -432,7 +437,7 @@ extern "C" ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int
     return TS_ERR_WORKSPACE;
   const int HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
   CUtensorMap tm_q, tm_k, tm_v;
-  if (!make_map(&tm_q, q, H, B, kHeads) || !make_map(&tm_k, sel_l, k, B, kChunk) ||
+  if (!make_map(&tm_q, q, H, B, kHeads) || !make_map(&tm_k, sel_l, k, B, kHalfRows) ||
       !make_map(&tm_v, sel_l, k, B, 64))
     return TS_ERR_CUDA;
   const size_t slots = size_t(B) * HG * C * kHeads;

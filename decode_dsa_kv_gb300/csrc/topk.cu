@@ -13,11 +13,13 @@
 //            digits, then the lowest positions among exact ties), set their
 //            bits, and write the set positions of the bitmap in order: the
 //            output comes out sorted without a sort.
-// With many requests (>= 96) of up to 131,072 positions, all three run in one
-// CTA per request, with the histogram, bitmap and candidates in shared memory
-// (one launch). Otherwise hist and select spread over many CTAs per request
-// (8,192 positions each); the last select CTA of a request to finish (a
-// completion counter) runs the finish.
+// Contexts up to 131,072 positions: one launch, one thread-block cluster of
+// 1 to 4 CTAs per request, each holding the keys of 32,768 positions in shared
+// memory; the CTAs merge their histograms through distributed shared memory,
+// rank 0 resolves the exact threshold and broadcasts it, and every CTA writes
+// its own slice of the sorted output. Longer contexts: hist and select spread
+// over many CTAs per request (8,192 positions each) in two launches; the last
+// select CTA of a request to finish (a completion counter) runs the finish.
 #include <mutex>
 
 #include "common.cuh"
@@ -29,10 +31,6 @@ constexpr int kBins = 4096;    // top 12 bits of the key
 constexpr int kChunk = 8192;   // positions per CTA in the multi-CTA hist / select
 constexpr int kThreads = 512;  // multi-CTA kernels
 constexpr int kMaxK = 8192;
-constexpr int kSmallThreads = 1024;
-constexpr int kSmallMaxCtx = 131072;  // one CTA per request up to here ...
-constexpr int kSmallMinB = 96;        // ... when the requests alone fill the GPU
-constexpr int kSmallCandCap = 8192;   // candidates kept in shared memory
 constexpr int kFinishCandCap = 4096;  // ... by the multi-CTA finish
 constexpr uint32_t kAll = 0xFFFFFFFFu;
 
@@ -137,9 +135,20 @@ struct Cands {
   }
 };
 
+// A candidate list in up to four global segments (one per CTA of a cluster):
+// entry i lies in the segment s with off[s] <= i < off[s+1].
+struct SegCands {
+  const uint64_t* seg[4];
+  uint32_t off[5];
+  __device__ __forceinline__ uint64_t operator()(uint32_t i) const {
+    const int s = (i >= off[1]) + (i >= off[2]) + (i >= off[3]);
+    return __ldcg(seg[s] + (i - off[s]));
+  }
+};
+
 // Histogram of a digit of the candidates satisfying pred, then select_bin.
-template <typename Pred, typename Digit>
-__device__ void cand_digit(const Cands& cand, uint32_t c, int nbins, bool high_first, int need,
+template <typename C, typename Pred, typename Digit>
+__device__ void cand_digit(const C& cand, uint32_t c, int nbins, bool high_first, int need,
                            Pred pred, Digit digit, uint32_t* hist, int* sbuf, int* t_out,
                            int* before_out, int* count_out) {
   for (int i = threadIdx.x; i < nbins; i += blockDim.x) hist[i] = 0;
@@ -152,16 +161,14 @@ __device__ void cand_digit(const Cands& cand, uint32_t c, int nbins, bool high_f
   select_bin(hist, nbins, high_first, need, sbuf, t_out, before_out, count_out);
 }
 
-// Resolve the threshold inside the candidate list of one request, set the
-// chosen candidates' bits, and write the set positions in ascending order.
-// t1 = the 12-bit threshold bin, need1 = candidates to take. `bits` is the
-// request's bitmap (shared or global memory), n its context. hist: >= 2048
+// The exact threshold inside a request's candidate list (all candidates share
+// the 12-bit bin t1; need1 of them are taken): a candidate is taken when its
+// key > *T, or key == *T and position <= *cut. Block-wide; hist: >= 2048
 // words of shared memory.
-template <bool kSharedBits>
-__device__ void finish_request(const Cands& cand, uint32_t c, int t1, int need1, uint32_t* bits,
-                               int n, int k, int32_t* out, uint32_t* hist, int* sbuf,
-                               int32_t* err) {
-  uint32_t T = 0, cut = kAll;  // take key > T, and key == T with position <= cut
+template <typename C>
+__device__ void resolve_threshold(const C& cand, uint32_t c, int t1, int need1, uint32_t* hist,
+                                  int* sbuf, uint32_t* T_out, uint32_t* cut_out) {
+  uint32_t T = 0, cut = kAll;  // need1 >= c: every candidate
   if (need1 < static_cast<int>(c)) {
     int t2, before2, cnt2, t3, before3, cnt3;
     cand_digit(
@@ -205,22 +212,37 @@ __device__ void finish_request(const Cands& cand, uint32_t c, int t1, int need1,
             static_cast<uint32_t>(pc);
     }
   }
-  // T = 0 with cut = all takes every candidate (need1 >= c)
+  *T_out = T;
+  *cut_out = cut;
+}
+
+__device__ __forceinline__ bool taken(uint64_t e, uint32_t T, uint32_t cut) {
+  const uint32_t key = static_cast<uint32_t>(e >> 32), pos = static_cast<uint32_t>(e);
+  return key > T || (key == T && pos <= cut);
+}
+
+// Resolve the threshold, set the chosen candidates' bits in the request's
+// global bitmap, and write the set positions in ascending order.
+template <typename C>
+__device__ void finish_request(const C& cand, uint32_t c, int t1, int need1, uint32_t* bits,
+                               int n, int k, int32_t* out, uint32_t* hist, int* sbuf,
+                               int32_t* err) {
+  uint32_t T, cut;
+  resolve_threshold(cand, c, t1, need1, hist, sbuf, &T, &cut);
   for (uint32_t i = threadIdx.x; i < c; i += blockDim.x) {
     const uint64_t e = cand(i);
-    const uint32_t key = static_cast<uint32_t>(e >> 32), pos = static_cast<uint32_t>(e);
-    if (key > T || (key == T && pos <= cut)) atomicOr(bits + (pos >> 5), 1u << (pos & 31));
+    if (taken(e, T, cut)) {
+      const uint32_t pos = static_cast<uint32_t>(e);
+      atomicOr(bits + (pos >> 5), 1u << (pos & 31));
+    }
   }
   __syncthreads();
-
-  // ordered write-out of the set bits
   const int64_t nwords = (int64_t(n) + 31) / 32;
   const int64_t per = (nwords + blockDim.x - 1) / blockDim.x;
   const int64_t w0 = int64_t(threadIdx.x) * per;
   const int64_t w1 = min(w0 + per, nwords);
-  auto word = [&](int64_t w) { return kSharedBits ? bits[w] : __ldcg(bits + w); };
   int cnt = 0;
-  for (int64_t w = w0; w < w1; ++w) cnt += __popc(word(w));
+  for (int64_t w = w0; w < w1; ++w) cnt += __popc(__ldcg(bits + w));
   int total;
   int pos = block_exclusive_scan(cnt, sbuf, &total);
   if (total != k) {
@@ -229,7 +251,7 @@ __device__ void finish_request(const Cands& cand, uint32_t c, int t1, int need1,
     return;
   }
   for (int64_t w = w0; w < w1; ++w) {
-    uint32_t m = word(w);
+    uint32_t m = __ldcg(bits + w);
     while (m) {
       const int bit = __ffs(m) - 1;
       m &= m - 1;
@@ -239,97 +261,184 @@ __device__ void finish_request(const Cands& cand, uint32_t c, int t1, int need1,
 }
 
 // ---------------------------------------------------------------------------
-// one CTA per request (contexts up to kSmallMaxCtx)
+// contexts up to kClusterMaxCtx: one cluster of G = ceil(ctx / 32768) CTAs
+// per request, every CTA holding the keys of its 32,768-position slice in
+// shared memory; histograms merge through distributed shared memory.
 // ---------------------------------------------------------------------------
-struct SmallSmem {
-  uint32_t hist[kBins];
-  uint32_t bits[kSmallMaxCtx / 32];
-  uint64_t cand[kSmallCandCap];
+constexpr int kSlice = 32768;
+constexpr int kClusterMaxG = 4;
+constexpr int kClusterMaxCtx = kSlice * kClusterMaxG;
+constexpr int kClThreads = 1024;
+constexpr int kClCandCap = 4096;  // candidates kept in shared memory by rank 0
+
+struct ClSmem {
+  uint32_t keys[kSlice];         // this CTA's keys
+  uint32_t hist[kBins];          // this CTA's histogram (read by the cluster)
+  uint32_t tot[kBins];           // the merged histogram, then digit histograms
+  uint32_t bits[kSlice / 32];    // this CTA's part of the bitmap
+  uint64_t cand[kClCandCap];     // rank 0: the request's candidates
   int sbuf[64];
-  uint32_t ncand;
+  uint32_t ncand;                // candidates of this CTA (in the global list)
+  uint32_t nsel;                 // positions this CTA selected
+  uint32_t thr[2];               // (T, cut), broadcast by rank 0
 };
 
-__global__ void __launch_bounds__(kSmallThreads) topk_small_kernel(
+__global__ void __launch_bounds__(kClThreads, 1) topk_cluster_kernel(
     const float* __restrict__ scores, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
     int k, int max_ctx, TopkWs ws, int32_t* __restrict__ ids, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  SmallSmem& sm = *reinterpret_cast<SmallSmem*>(smem_raw);
-  const int b = blockIdx.x;
+  ClSmem& sm = *reinterpret_cast<ClSmem*>(smem_raw);
+  const int G = gridDim.x;
+  const uint32_t rank = cluster_ctarank();
+  const int b = blockIdx.y;
   const int n = ctx_len[b];
+  const bool ok = ctx_ok(n, k, max_ctx);  // uniform over the cluster
   int32_t* out = ids + int64_t(b) * k;
-  if (!ctx_ok(n, k, max_ctx)) {
-    for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
-    if (threadIdx.x == 0) report(err, TS_DEVERR_CTX);
-    return;
-  }
-  for (int i = threadIdx.x; i < kBins; i += blockDim.x) sm.hist[i] = 0;
-  if (threadIdx.x == 0) sm.ncand = 0;
-  __syncthreads();
-  const float* row = scores + int64_t(b) * ctx_stride;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  bool nan = false;
+  const int lo = static_cast<int>(rank) * kSlice;
+  const int hi = ok ? min(lo + kSlice, n) : lo;
+  const int len = max(hi - lo, 0);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint64_t* gcand = ws.cand + int64_t(b) * max_ctx + lo;  // this CTA's global candidate list
 
-  // pass 1: histogram; each warp walks 4 x 32 consecutive positions per step
-  for (int base = warp * 128; base < n; base += nwarps * 128) {
-    float v[4];
+  for (int i = tid; i < kBins; i += kClThreads) sm.hist[i] = 0;
+  if (tid == 0) {
+    sm.ncand = 0;
+    sm.nsel = 0;
+  }
+  __syncthreads();
+  // keys and histogram of the slice (8 loads in flight per thread)
+  bool nan = false;
+  const float* row = scores + int64_t(b) * ctx_stride + lo;
+  for (int base = warp * 256; base < len; base += (kClThreads / 32) * 256) {
+    float v[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const int i = base + u * 32 + lane;
-      v[u] = i < n ? __ldg(row + i) : 0.f;
+      v[u] = i < len ? __ldg(row + i) : 0.f;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const int i = base + u * 32 + lane;
-      const int bin = i < n ? static_cast<int>(score_key(v[u], nan) >> 20) : -1;
-      warp_hist_add(sm.hist, bin);
+      if (i < len) {
+        const uint32_t key = score_key(v[u], nan);
+        sm.keys[i] = key;
+        atomicAdd(&sm.hist[key >> 20], 1u);
+      }
     }
   }
   if (nan) report(err, TS_DEVERR_NAN);
-  __syncthreads();
-  int t1, above, cnt1;
-  select_bin(sm.hist, kBins, true, k, sm.sbuf, &t1, &above, &cnt1);
+  cluster_sync_all();
 
-  // pass 2: bitmap words of the positions above the threshold bin, and the
-  // candidate list of the threshold bin
-  uint64_t* gcand = ws.cand + int64_t(b) * max_ctx;
-  for (int base = warp * 128; base < n; base += nwarps * 128) {
-    float v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = base + u * 32 + lane;
-      v[u] = i < n ? __ldg(row + i) : 0.f;
+  // merged histogram: every CTA sums the cluster's histograms
+  for (int i4 = tid; i4 < kBins / 4; i4 += kClThreads) {
+    uint4 acc = make_uint4(0, 0, 0, 0);
+    for (int g = 0; g < G; ++g) {
+      const uint4 h = ld_dsmem_u4(dsmem_addr(&sm.hist[4 * i4], g));
+      acc.x += h.x;
+      acc.y += h.y;
+      acc.z += h.z;
+      acc.w += h.w;
     }
+    *reinterpret_cast<uint4*>(&sm.tot[4 * i4]) = acc;
+  }
+  __syncthreads();
+  int t1 = 0, above = 0, cnt1 = 0;
+  if (ok) select_bin(sm.tot, kBins, true, k, sm.sbuf, &t1, &above, &cnt1);
+  else __syncthreads();
+
+  // bitmap words above the threshold bin; the bin's candidates to the global list
+  for (int base = warp * 128; base < len; base += (kClThreads / 32) * 128) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = base + u * 32 + lane;
-      bool nan2 = false;
-      uint32_t key = 0;
-      int bin = -1;
-      if (i < n) {
-        key = score_key(v[u], nan2);
-        bin = static_cast<int>(key >> 20);
-      }
+      const uint32_t key = i < len ? sm.keys[i] : 0u;
+      const int bin = i < len ? static_cast<int>(key >> 20) : -1;
       const uint32_t above_mask = __ballot_sync(0xffffffffu, bin > t1);
       const uint32_t tie_mask = __ballot_sync(0xffffffffu, bin == t1);
-      if (lane == 0 && base + u * 32 < n) sm.bits[(base + u * 32) >> 5] = above_mask;
+      if (lane == 0 && base + u * 32 < len) sm.bits[(base + u * 32) >> 5] = above_mask;
       if (tie_mask) {
         uint32_t pos0 = 0;
         if (lane == 0) pos0 = atomicAdd(&sm.ncand, __popc(tie_mask));
         pos0 = __shfl_sync(0xffffffffu, pos0, 0);
-        if (bin == t1) {
-          const uint32_t at = pos0 + __popc(tie_mask & ((1u << lane) - 1u));
-          const uint64_t e = (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(i);
-          if (at < kSmallCandCap) sm.cand[at] = e;
-          else gcand[at] = e;
-        }
+        if (bin == t1)
+          gcand[pos0 + __popc(tie_mask & ((1u << lane) - 1u))] =
+              (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(lo + i);
       }
     }
   }
-  __threadfence_block();
+  cluster_sync_all();  // candidate lists and their counts are visible to rank 0
+
+  if (rank == 0 && ok) {
+    SegCands cl;
+    cl.off[0] = 0;
+    for (int g = 0; g < 4; ++g) {
+      const uint32_t cg = g < G ? ld_dsmem_u32(dsmem_addr(&sm.ncand, g)) : 0u;
+      cl.seg[g] = ws.cand + int64_t(b) * max_ctx + g * kSlice;
+      cl.off[g + 1] = cl.off[g] + cg;
+    }
+    const uint32_t c = cl.off[4];
+    uint32_t T, cut;
+    if (c <= kClCandCap) {
+      // the common case: the whole list in shared memory
+      for (uint32_t i = tid; i < c; i += kClThreads) sm.cand[i] = cl(i);
+      __syncthreads();
+      Cands cs{sm.cand, nullptr, kClCandCap};
+      resolve_threshold(cs, c, t1, k - above, sm.tot, sm.sbuf, &T, &cut);
+    } else {
+      resolve_threshold(cl, c, t1, k - above, sm.tot, sm.sbuf, &T, &cut);
+    }
+    if (tid < G) {
+      st_dsmem_u32(dsmem_addr(&sm.thr[0], tid), T);
+      st_dsmem_u32(dsmem_addr(&sm.thr[1], tid), cut);
+    }
+  }
+  cluster_sync_all();  // (T, cut) everywhere
+
+  // every CTA sets its own candidates' bits and counts its selected positions
+  if (ok) {
+    const uint32_t T = sm.thr[0], cut = sm.thr[1];
+    for (uint32_t i = tid; i < sm.ncand; i += kClThreads) {
+      const uint64_t e = __ldcg(gcand + i);
+      if (taken(e, T, cut)) {
+        const uint32_t p = static_cast<uint32_t>(e) - lo;
+        atomicOr(&sm.bits[p >> 5], 1u << (p & 31));
+      }
+    }
+  }
   __syncthreads();
-  const uint32_t c = sm.ncand;
-  Cands cand{sm.cand, gcand, kSmallCandCap};
-  finish_request<true>(cand, c, t1, k - above, sm.bits, n, k, out, sm.hist, sm.sbuf, err);
+  const int nwords = (len + 31) / 32;
+  const int per = (nwords + kClThreads - 1) / kClThreads;
+  const int w0 = tid * per, w1 = min(w0 + per, nwords);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(sm.bits[w]);
+  int total;
+  int pos = block_exclusive_scan(cnt, sm.sbuf, &total);
+  if (tid == 0) sm.nsel = total;
+  cluster_sync_all();  // every CTA's count is visible
+
+  int offset = 0, all = 0;
+  for (int g = 0; g < G; ++g) {
+    const int cg = static_cast<int>(ld_dsmem_u32(dsmem_addr(&sm.nsel, g)));
+    if (g < static_cast<int>(rank)) offset += cg;
+    all += cg;
+  }
+  if (!ok || all != k) {
+    if (rank == 0) {
+      for (int i = tid; i < k; i += kClThreads) out[i] = -1;
+      if (tid == 0) report(err, ok ? TS_DEVERR_COUNT : TS_DEVERR_CTX);
+    }
+  } else {
+    pos += offset;
+    for (int w = w0; w < w1; ++w) {
+      uint32_t m = sm.bits[w];
+      while (m) {
+        const int bit = __ffs(m) - 1;
+        m &= m - 1;
+        out[pos++] = lo + w * 32 + bit;
+      }
+    }
+  }
+  cluster_sync_all();  // no CTA leaves while others may read its shared memory
 }
 
 // ---------------------------------------------------------------------------
@@ -459,27 +568,40 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(
     cand_s[i] = __ldcg(cand + i);
   __syncthreads();
   Cands cl{cand_s, cand, kFinishCandCap};
-  finish_request<false>(cl, c, t1, k - above, bits, n, k, ids + int64_t(b) * k, dig, sbuf, err);
+  finish_request(cl, c, t1, k - above, bits, n, k, ids + int64_t(b) * k, dig, sbuf, err);
 }
 
-size_t small_smem_bytes() { return sizeof(SmallSmem); }
 
 // Launch the top-k on a workspace laid out by carve().
 ts_status launch_topk(const float* scores, int64_t ctx_stride, const int32_t* ctx_len, int B,
                       int max_ctx, int k, int32_t* ids, void* ws, int32_t* err,
                       cudaStream_t stream) {
   TopkWs w = carve(ws, B, max_ctx);
-  if (max_ctx <= kSmallMaxCtx && B >= kSmallMinB) {
+  if (max_ctx <= kClusterMaxCtx) {
     static bool attr = false;
     if (!attr) {
-      if (cudaFuncSetAttribute(topk_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(small_smem_bytes())) != cudaSuccess)
+      if (cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(sizeof(ClSmem))) != cudaSuccess)
         return TS_ERR_CUDA;
       attr = true;
     }
-    topk_small_kernel<<<B, kSmallThreads, small_smem_bytes(), stream>>>(
-        scores, ctx_stride, ctx_len, k, max_ctx, w, ids, err);
-    return launch_status();
+    const int G = (max_ctx + kSlice - 1) / kSlice;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G, B, 1);
+    cfg.blockDim = dim3(kClThreads, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(ClSmem);
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = G;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, ctx_stride, ctx_len, k, max_ctx, w,
+                           ids, err) != cudaSuccess)
+      return TS_ERR_CUDA;
+    return TS_OK;
   }
   // histograms, list counters and completion counters start at zero
   if (cudaMemsetAsync(ws, 0, counters_bytes(B), stream) != cudaSuccess) return TS_ERR_CUDA;

@@ -135,9 +135,11 @@ class DecodeGroup:
         self.sfa_ws = torch.empty(self.sfa_ws_bytes, dtype=torch.uint8, device=dev)
         self.err = torch.zeros((1,), **i32)
         # streams and events
-        self.main = torch.cuda.Stream(device=dev)
-        self.gstream = torch.cuda.Stream(device=dev)
-        self.side = torch.cuda.Stream(device=dev)
+        # the critical path (top-k, plan, attention) has the higher priority:
+        # when CTAs of several kernels wait for SMs, its CTAs go first
+        self.main = torch.cuda.Stream(device=dev, priority=-1)
+        self.gstream = torch.cuda.Stream(device=dev, priority=0)
+        self.side = torch.cuda.Stream(device=dev, priority=0)
         self.planned = torch.cuda.Event()
         self.gathered = [torch.cuda.Event() for _ in range(layers)]
         self.refill_done = torch.cuda.Event()
