@@ -379,9 +379,9 @@ def run_native(args, w, rank, world, local):
     peaks = measured_peaks()
     link = link_peak_gbs(torch)
 
-    def step(s, ev=None):
+    def step(s, timing=None):
         i = palindrome_index(s, T)
-        g.step(scores_d[i], q_d[i], kernel_events=ev)
+        g.step(scores_d[i], q_d[i], timing=timing)
 
     # warm-up
     for s in range(args.warmup):
@@ -398,7 +398,10 @@ def run_native(args, w, rank, world, local):
     # timed region: K steps, per-kernel events on the launching streams
     miss_log = torch.zeros((args.steps, w.B), dtype=torch.int32, device="cuda")
     inst_log = torch.zeros((args.steps,), dtype=torch.int64, device="cuda")
-    kev = None if args.no_kernel_events else {n: [] for n in KERNELS}
+    # per-launch timing events of every timed step, created before the region
+    timings = (None if args.no_kernel_events
+               else [dk.StepTiming(w.layers, g.main) for _ in range(args.steps)])
+    torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -410,7 +413,7 @@ def run_native(args, w, rank, world, local):
     e0.record(g.main)
     t_enq0 = time.perf_counter()
     for s in range(args.steps):
-        step(args.warmup + s, kev)
+        step(args.warmup + s, timings[s] if timings else None)
         with torch.cuda.stream(g.main):
             miss_log[s].copy_(g.miss_count, non_blocking=True)
     t_enq1 = time.perf_counter()
@@ -436,13 +439,16 @@ def run_native(args, w, rank, world, local):
 
     per_kernel = {}
     alg = algorithmic(w, lens, hit_frac, install_frac)
+    launch_ms = {n: [] for n in KERNELS}
+    for t in timings or []:
+        for n, v in t.ms().items():
+            launch_ms[n].extend(v)
     for n in KERNELS:
-        evs = kev[n] if kev else []
-        if not evs:
+        if not launch_ms[n]:
             continue
-        ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+        ms = sum(launch_ms[n]) / len(launch_ms[n])
         per_kernel[n] = roofline_of(n, alg[n], ms, peaks, link)
-        per_kernel[n]["launches_per_step"] = len(evs) / args.steps
+        per_kernel[n]["launches_per_step"] = len(launch_ms[n]) / args.steps
     rf_line = None
     if per_kernel:
         dom = max(per_kernel, key=lambda n: per_kernel[n]["ms_per_launch"]

@@ -13,10 +13,10 @@ import importlib
 _ABI_NAMES = {
     "ts_status_string", "ts_host_register", "ts_host_unregister", "ts_read_error", "ts_copy",
     "ts_topk_workspace_size", "ts_topk", "ts_topk_noalloc", "dsa_plan", "dsa_gather_kv", "dsa_refill_pool",
-    "sfa_workspace_size", "sfa_mla_decode", "DsaKvError", "check", "status_string", "EXPORTS",
+    "sfa_workspace_size", "sfa_mla_decode", "dsa_group_step", "DsaGroup", "DsaKvError", "check", "status_string", "EXPORTS",
     "LIB_PATH",
 }
-_RUNTIME_NAMES = {"HostKV", "DecodeGroup", "PinnedHost"}
+_RUNTIME_NAMES = {"HostKV", "DecodeGroup", "PinnedHost", "StepTiming"}
 
 
 def __getattr__(name):

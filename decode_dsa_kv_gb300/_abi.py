@@ -53,9 +53,33 @@ _SIGS = {
                              _P, _P]),
     "sfa_workspace_size": (_SZ, [_I, _I, _I]),
     "sfa_mla_decode": (_I, [_P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P, _P]),
+    "dsa_group_step": (_I, [_P, _P, _P, _P, _P]),
 }
 
 EXPORTS = tuple(_SIGS)
+
+TS_MAX_LAYERS = 16
+
+
+class DsaGroup(ctypes.Structure):
+    """The dsa_group descriptor of dsakv.h, field for field."""
+    _fields_ = [
+        ("B", _I), ("layers", _I), ("k", _I), ("S", _I), ("W", _I), ("H", _I),
+        ("max_ctx", _I),
+        ("ctx_stride", _I64),
+        ("scale", _F),
+        ("ctx_len", _P),
+        ("pool", _P), ("pool_tags", _P), ("fifo_ptr", _P),
+        ("host_kv", _P),
+        ("ids", _P), ("src_map", _P), ("miss_ids", _P), ("miss_pos", _P), ("victim", _P),
+        ("install", _P), ("miss_count", _P), ("miss_rows", _P), ("ptr_next", _P),
+        ("sel", _P), ("out", _P), ("lse", _P),
+        ("topk_ws", _P), ("topk_ws_bytes", _SZ), ("sfa_ws", _P), ("sfa_ws_bytes", _SZ),
+        ("err", _P),
+        ("main_stream", _P), ("gather_stream", _P), ("side_stream", _P),
+        ("sync", _P),
+        ("step", ctypes.c_uint32),
+    ]
 
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -178,3 +202,10 @@ def sfa_mla_decode(q, sel_l, B, H, k, scale, out, lse, ws, ws_bytes, err=None,
                    stream=None) -> int:
     return _lib.sfa_mla_decode(ptr(q), ptr(sel_l), B, H, k, float(scale), ptr(out), ptr(lse),
                                ptr(ws), ws_bytes, ptr(err), stream_handle(stream))
+
+
+def dsa_group_step(group: DsaGroup, scores, q, ids=None, timing=None) -> int:
+    """One decode step of the group; `timing` is None or a ctypes array of
+    2 * (2 + 3 * layers) event handles."""
+    return _lib.dsa_group_step(ctypes.byref(group), ptr(scores), ptr(q), ptr(ids),
+                               None if timing is None else ctypes.cast(timing, _P))

@@ -13,6 +13,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "ops.h"
 
 namespace dsakv {
 namespace {
@@ -215,17 +216,24 @@ int sm_count() {
 
 using namespace dsakv;
 
-extern "C" ts_status dsa_gather_kv(const int32_t* src_map, const int32_t* miss_ids,
-                                   const int32_t* miss_pos, const int32_t* miss_count,
-                                   const int32_t* miss_rows, int B, int k, const void* pool_l,
-                                   int P, const void* host_l, int64_t ctx_stride,
-                                   const int32_t* ctx_len, void* sel_l, int32_t* err,
-                                   cudaStream_t stream) {
+namespace dsakv {
+
+ts_status gather_check(const int32_t* src_map, const int32_t* miss_ids, const int32_t* miss_pos,
+                       const int32_t* miss_count, const int32_t* miss_rows, int B, int k,
+                       const void* pool_l, int P, const void* host_l, int64_t ctx_stride,
+                       const int32_t* ctx_len, void* sel_l) {
   if (!src_map || !miss_ids || !miss_pos || !miss_count || !miss_rows || !pool_l || !host_l ||
       !ctx_len || !sel_l)
     return TS_ERR_INVALID_ARG;
   if (B <= 0 || k <= 0 || P <= 0 || ctx_stride <= 0) return TS_ERR_INVALID_ARG;
   if (!aligned16(pool_l) || !aligned16(host_l) || !aligned16(sel_l)) return TS_ERR_INVALID_ARG;
+  return TS_OK;
+}
+
+ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const int32_t* miss_pos,
+                         const int32_t* miss_count, const int32_t* miss_rows, int B, int k,
+                         const void* pool_l, int P, const void* host_l, int64_t ctx_stride,
+                         const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream) {
   // A quarter of the SMs, one 1024-thread CTA each, keep a few MB of loads in
   // flight, which saturates the host link (measured); the other SMs stay free
   // for the attention of the previous layer, which runs beside the gather
@@ -241,18 +249,25 @@ extern "C" ts_status dsa_gather_kv(const int32_t* src_map, const int32_t* miss_i
   return launch_status();
 }
 
-extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* miss_pos,
-                                     const int32_t* victim, const uint8_t* install,
-                                     const int32_t* miss_count, int B, int k, const void* sel_l,
-                                     void* pool_l, int P, int update_metadata, int32_t* pool_tags,
-                                     int32_t* fifo_ptr, const int32_t* ptr_next, int S, int W,
-                                     int32_t* err, cudaStream_t stream) {
+ts_status refill_check(const int32_t* miss_ids, const int32_t* miss_pos, const int32_t* victim,
+                       const uint8_t* install, const int32_t* miss_count, int B, int k,
+                       const void* sel_l, void* pool_l, int P, int update_metadata,
+                       int32_t* pool_tags, int32_t* fifo_ptr, const int32_t* ptr_next, int S,
+                       int W) {
   if (!miss_ids || !miss_pos || !victim || !install || !miss_count || !sel_l || !pool_l)
     return TS_ERR_INVALID_ARG;
   if (B <= 0 || k <= 0 || P <= 0) return TS_ERR_INVALID_ARG;
   if (update_metadata && (!pool_tags || !fifo_ptr || !ptr_next || S <= 0 || W <= 0 || S * W != P))
     return TS_ERR_INVALID_ARG;
   if (!aligned16(sel_l) || !aligned16(pool_l)) return TS_ERR_INVALID_ARG;
+  return TS_OK;
+}
+
+ts_status refill_enqueue(const int32_t* miss_ids, const int32_t* miss_pos, const int32_t* victim,
+                         const uint8_t* install, const int32_t* miss_count, int B, int k,
+                         const void* sel_l, void* pool_l, int P, int update_metadata,
+                         int32_t* pool_tags, int32_t* fifo_ptr, const int32_t* ptr_next, int S,
+                         int W, int32_t* err, cudaStream_t stream) {
   // like the gather, a quarter of the SMs: the refill is off the critical
   // path and leaves the other SMs to the attention it runs beside
   const int64_t warps = int64_t(B) * k;
@@ -264,6 +279,36 @@ extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* mis
       miss_ids, miss_pos, victim, install, miss_count, B, k, static_cast<const uint4*>(sel_l),
       static_cast<uint4*>(pool_l), P, update_metadata, pool_tags, fifo_ptr, ptr_next, S, W, err);
   return launch_status();
+}
+
+}  // namespace dsakv
+
+extern "C" ts_status dsa_gather_kv(const int32_t* src_map, const int32_t* miss_ids,
+                                   const int32_t* miss_pos, const int32_t* miss_count,
+                                   const int32_t* miss_rows, int B, int k, const void* pool_l,
+                                   int P, const void* host_l, int64_t ctx_stride,
+                                   const int32_t* ctx_len, void* sel_l, int32_t* err,
+                                   cudaStream_t stream) {
+  const ts_status st = dsakv::gather_check(src_map, miss_ids, miss_pos, miss_count, miss_rows, B,
+                                           k, pool_l, P, host_l, ctx_stride, ctx_len, sel_l);
+  if (st != TS_OK) return st;
+  return dsakv::gather_enqueue(src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, pool_l,
+                               P, host_l, ctx_stride, ctx_len, sel_l, err, stream);
+}
+
+extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* miss_pos,
+                                     const int32_t* victim, const uint8_t* install,
+                                     const int32_t* miss_count, int B, int k, const void* sel_l,
+                                     void* pool_l, int P, int update_metadata, int32_t* pool_tags,
+                                     int32_t* fifo_ptr, const int32_t* ptr_next, int S, int W,
+                                     int32_t* err, cudaStream_t stream) {
+  const ts_status st = dsakv::refill_check(miss_ids, miss_pos, victim, install, miss_count, B, k,
+                                           sel_l, pool_l, P, update_metadata, pool_tags, fifo_ptr,
+                                           ptr_next, S, W);
+  if (st != TS_OK) return st;
+  return dsakv::refill_enqueue(miss_ids, miss_pos, victim, install, miss_count, B, k, sel_l,
+                               pool_l, P, update_metadata, pool_tags, fifo_ptr, ptr_next, S, W,
+                               err, stream);
 }
 
 // ---------------------------------------------------------------------------

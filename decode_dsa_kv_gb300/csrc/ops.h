@@ -1,0 +1,54 @@
+// Host-side halves of the library's operations, for callers inside the
+// library that enqueue several of them: every *_check validates arguments
+// exactly as the public call does (and enqueues nothing); every *_enqueue
+// launches on already-validated arguments. The public call is check, then
+// enqueue.
+#pragma once
+
+#include "dsakv.h"
+
+namespace dsakv {
+
+ts_status topk_check(const float* scores, int64_t ctx_stride, const int32_t* ctx_len, int B,
+                     int max_ctx, int k, int32_t* ids, const void* ws, size_t ws_bytes);
+ts_status topk_enqueue(const float* scores, int64_t ctx_stride, const int32_t* ctx_len, int B,
+                       int max_ctx, int k, int32_t* ids, void* ws, int32_t* err,
+                       cudaStream_t stream);
+
+ts_status plan_check(const int32_t* ids, const int32_t* ctx_len, int B, int k,
+                     const int32_t* pool_tags, const int32_t* fifo_ptr, int S, int W,
+                     int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos, int32_t* victim,
+                     uint8_t* install, int32_t* miss_count, int32_t* miss_rows,
+                     int32_t* ptr_next);
+ts_status plan_enqueue(const int32_t* ids, const int32_t* ctx_len, int B, int k,
+                       const int32_t* pool_tags, const int32_t* fifo_ptr, int S, int W,
+                       int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos, int32_t* victim,
+                       uint8_t* install, int32_t* miss_count, int32_t* miss_rows,
+                       int32_t* ptr_next, int32_t* err, cudaStream_t stream);
+
+ts_status gather_check(const int32_t* src_map, const int32_t* miss_ids, const int32_t* miss_pos,
+                       const int32_t* miss_count, const int32_t* miss_rows, int B, int k,
+                       const void* pool_l, int P, const void* host_l, int64_t ctx_stride,
+                       const int32_t* ctx_len, void* sel_l);
+ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const int32_t* miss_pos,
+                         const int32_t* miss_count, const int32_t* miss_rows, int B, int k,
+                         const void* pool_l, int P, const void* host_l, int64_t ctx_stride,
+                         const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream);
+
+ts_status refill_check(const int32_t* miss_ids, const int32_t* miss_pos, const int32_t* victim,
+                       const uint8_t* install, const int32_t* miss_count, int B, int k,
+                       const void* sel_l, void* pool_l, int P, int update_metadata,
+                       int32_t* pool_tags, int32_t* fifo_ptr, const int32_t* ptr_next, int S,
+                       int W);
+ts_status refill_enqueue(const int32_t* miss_ids, const int32_t* miss_pos, const int32_t* victim,
+                         const uint8_t* install, const int32_t* miss_count, int B, int k,
+                         const void* sel_l, void* pool_l, int P, int update_metadata,
+                         int32_t* pool_tags, int32_t* fifo_ptr, const int32_t* ptr_next, int S,
+                         int W, int32_t* err, cudaStream_t stream);
+
+ts_status sfa_check(const void* q, const void* sel_l, int B, int H, int k, float scale,
+                    void* out, const void* ws, size_t ws_bytes);
+ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, float scale,
+                      void* out, float* lse, void* ws, int32_t* err, cudaStream_t stream);
+
+}  // namespace dsakv

@@ -10,6 +10,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "ops.h"
 
 namespace dsakv {
 namespace {
@@ -275,20 +276,29 @@ __global__ void __launch_bounds__(kThreads) dsa_plan_kernel(
 
 using namespace dsakv;
 
-extern "C" ts_status dsa_plan(const int32_t* ids, const int32_t* ctx_len, int B, int k,
-                              const int32_t* pool_tags, const int32_t* fifo_ptr, int S, int W,
-                              int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
-                              int32_t* victim, uint8_t* install, int32_t* miss_count,
-                              int32_t* miss_rows, int32_t* ptr_next, int32_t* err,
-                              cudaStream_t stream) {
+namespace dsakv {
+
+ts_status plan_check(const int32_t* ids, const int32_t* ctx_len, int B, int k,
+                     const int32_t* pool_tags, const int32_t* fifo_ptr, int S, int W,
+                     int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos, int32_t* victim,
+                     uint8_t* install, int32_t* miss_count, int32_t* miss_rows,
+                     int32_t* ptr_next) {
   if (!ids || !ctx_len || !pool_tags || !fifo_ptr || !src_map || !miss_ids || !miss_pos ||
       !victim || !install || !miss_count || !miss_rows || !ptr_next)
     return TS_ERR_INVALID_ARG;
   if (B <= 0 || k <= 0 || S <= 0 || W <= 0) return TS_ERR_INVALID_ARG;
   if (W > 32 || k > kMaxK || B > 2147483647 / 2) return TS_ERR_UNSUPPORTED;
   if (int64_t(S) * W > (1 << 24)) return TS_ERR_UNSUPPORTED;
+  if (plan_smem_bytes(S * W, S, k) > kMaxSmem) return TS_ERR_UNSUPPORTED;
+  return TS_OK;
+}
+
+ts_status plan_enqueue(const int32_t* ids, const int32_t* ctx_len, int B, int k,
+                       const int32_t* pool_tags, const int32_t* fifo_ptr, int S, int W,
+                       int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos, int32_t* victim,
+                       uint8_t* install, int32_t* miss_count, int32_t* miss_rows,
+                       int32_t* ptr_next, int32_t* err, cudaStream_t stream) {
   const size_t smem = plan_smem_bytes(S * W, S, k);
-  if (smem > kMaxSmem) return TS_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(dsa_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(smem)) != cudaSuccess)
     return TS_ERR_CUDA;
@@ -296,4 +306,21 @@ extern "C" ts_status dsa_plan(const int32_t* ids, const int32_t* ctx_len, int B,
                                                  src_map, miss_ids, miss_pos, victim, install,
                                                  miss_count, miss_rows, ptr_next, err);
   return launch_status();
+}
+
+}  // namespace dsakv
+
+extern "C" ts_status dsa_plan(const int32_t* ids, const int32_t* ctx_len, int B, int k,
+                              const int32_t* pool_tags, const int32_t* fifo_ptr, int S, int W,
+                              int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
+                              int32_t* victim, uint8_t* install, int32_t* miss_count,
+                              int32_t* miss_rows, int32_t* ptr_next, int32_t* err,
+                              cudaStream_t stream) {
+  const ts_status st = dsakv::plan_check(ids, ctx_len, B, k, pool_tags, fifo_ptr, S, W, src_map,
+                                         miss_ids, miss_pos, victim, install, miss_count,
+                                         miss_rows, ptr_next);
+  if (st != TS_OK) return st;
+  return dsakv::plan_enqueue(ids, ctx_len, B, k, pool_tags, fifo_ptr, S, W, src_map, miss_ids,
+                             miss_pos, victim, install, miss_count, miss_rows, ptr_next, err,
+                             stream);
 }

@@ -26,6 +26,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "ops.h"
 
 namespace dsakv {
 namespace {
@@ -426,15 +427,21 @@ extern "C" size_t sfa_workspace_size(int B, int H, int k) {
   return align256(slots * DSA_DV * 4) + align256(slots * 8);
 }
 
-extern "C" ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int H, int k,
-                                    float scale, void* out, float* lse, void* ws, size_t ws_bytes,
-                                    int32_t* err, cudaStream_t stream) {
+namespace dsakv {
+
+ts_status sfa_check(const void* q, const void* sel_l, int B, int H, int k, float scale,
+                    void* out, const void* ws, size_t ws_bytes) {
   if (!q || !sel_l || !out || !ws) return TS_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || k <= 0 || !std::isfinite(scale)) return TS_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(sel_l) || !aligned16(out)) return TS_ERR_INVALID_ARG;
   if (B > 65535 || H > 65535 * kHeads || int64_t(B) * H > 2147483647) return TS_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < sfa_workspace_size(B, H, k))
     return TS_ERR_WORKSPACE;
+  return TS_OK;
+}
+
+ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, float scale,
+                      void* out, float* lse, void* ws, int32_t* err, cudaStream_t stream) {
   const int HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
   CUtensorMap tm_q, tm_k, tm_v;
   if (!make_map(&tm_q, q, H, B, kHeads) || !make_map(&tm_k, sel_l, k, B, kHalfRows) ||
@@ -456,4 +463,14 @@ extern "C" ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int
   if (cudaGetLastError() != cudaSuccess) return TS_ERR_CUDA;
   sfa_combine_kernel<<<unsigned(int64_t(B) * H), 128, 0, stream>>>(opart, ml, H, HG, C, outp, lse);
   return launch_status();
+}
+
+}  // namespace dsakv
+
+extern "C" ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int H, int k,
+                                    float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                                    int32_t* err, cudaStream_t stream) {
+  const ts_status st = sfa_check(q, sel_l, B, H, k, scale, out, ws, ws_bytes);
+  if (st != TS_OK) return st;
+  return sfa_enqueue(q, sel_l, B, H, k, scale, out, lse, ws, err, stream);
 }

@@ -1,0 +1,170 @@
+// dsa_group_step: one decode step of an IndexShare group enqueued from native
+// code (GLM-5.2 shared-Indexer KV Cache Offload, §5.1 model-side
+// orchestration and §4.4 SFA first, refill later). The order of operations,
+// the cross-stream signals and their proof of termination are the ones the
+// header states; every argument is checked before the first launch.
+//
+// Cross-stream ordering uses stream memory operations on device words: a
+// signal is a 32-bit write of the step's sequence number issued on the
+// producing stream (it lands when the stream's prior work is complete), a
+// wait blocks the consuming stream until the word, compared wrap-around, has
+// reached that number. The words live in HBM, so the front end that polls
+// them never crosses the host link.
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "ops.h"
+
+namespace dsakv {
+namespace {
+
+constexpr size_t kRowBytes = DSA_ROW_BYTES;
+enum : int { kPlanned = 0, kRefilled = 1, kGathered = 2 };
+
+template <typename T>
+T* at(T* base, int l, size_t layer_bytes) {
+  using Byte = typename std::conditional<std::is_const<T>::value, const char, char>::type;
+  return reinterpret_cast<T*>(reinterpret_cast<Byte*>(base) + size_t(l) * layer_bytes);
+}
+
+struct Layers {
+  size_t pool, host, sel, out, lse, q;
+};
+
+Layers layer_bytes(const dsa_group& g) {
+  Layers s;
+  const size_t P = size_t(g.S) * g.W;
+  s.pool = size_t(g.B) * P * kRowBytes;
+  s.host = size_t(g.B) * size_t(g.ctx_stride) * kRowBytes;
+  s.sel = size_t(g.B) * g.k * kRowBytes;
+  s.out = size_t(g.B) * g.H * DSA_DV * 2;
+  s.lse = size_t(g.B) * g.H * 4;
+  s.q = size_t(g.B) * g.H * kRowBytes;
+  return s;
+}
+
+using MemOpFn = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+struct MemOps {
+  MemOpFn wait = nullptr, write = nullptr;
+  bool ok = false;
+};
+
+const MemOps& memops() {
+  static MemOps m = [] {
+    MemOps r;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      r.wait = reinterpret_cast<MemOpFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      r.write = reinterpret_cast<MemOpFn>(p);
+    r.ok = r.wait && r.write;
+    return r;
+  }();
+  return m;
+}
+
+bool signal(cudaStream_t s, uint32_t* word, uint32_t v) {
+  return memops().write(reinterpret_cast<CUstream>(s), reinterpret_cast<CUdeviceptr>(word), v,
+                        CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS;
+}
+
+bool wait_for(cudaStream_t s, const uint32_t* word, uint32_t v) {
+  return memops().wait(reinterpret_cast<CUstream>(s), reinterpret_cast<CUdeviceptr>(word), v,
+                       CU_STREAM_WAIT_VALUE_GEQ) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace dsakv
+
+using namespace dsakv;
+
+extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const void* q,
+                                    const int32_t* ids, cudaEvent_t* timing) {
+  if (!gp || !q) return TS_ERR_INVALID_ARG;
+  dsa_group& g = *gp;
+  const int L = g.layers;
+  if (L <= 0 || L > TS_MAX_LAYERS) return TS_ERR_INVALID_ARG;
+  if (!ids && !scores) return TS_ERR_INVALID_ARG;
+  if (g.S <= 0 || g.W <= 0 || int64_t(g.S) * g.W > (1 << 24)) return TS_ERR_INVALID_ARG;
+  if (!g.sync || (reinterpret_cast<uintptr_t>(g.sync) & 3u) != 0) return TS_ERR_INVALID_ARG;
+  if (!aligned16(q)) return TS_ERR_INVALID_ARG;
+  const int P = g.S * g.W;
+  const Layers lb = layer_bytes(g);
+  const int32_t* plan_ids = ids ? ids : g.ids;
+
+  // every operation's host checks first (layer 0 stands for all layers: the
+  // layer strides are whole multiples of 16 bytes)
+  ts_status st = TS_OK;
+  if (!ids)
+    st = topk_check(scores, g.ctx_stride, g.ctx_len, g.B, g.max_ctx, g.k, g.ids, g.topk_ws,
+                    g.topk_ws_bytes);
+  if (st == TS_OK)
+    st = plan_check(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.fifo_ptr, g.S, g.W, g.src_map,
+                    g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.miss_rows,
+                    g.ptr_next);
+  if (st == TS_OK)
+    st = gather_check(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k,
+                      g.pool, P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel);
+  if (st == TS_OK)
+    st = refill_check(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k, g.sel,
+                      g.pool, P, 1, g.pool_tags, g.fifo_ptr, g.ptr_next, g.S, g.W);
+  if (st == TS_OK) st = sfa_check(q, g.sel, g.B, g.H, g.k, g.scale, g.out, g.sfa_ws, g.sfa_ws_bytes);
+  if (st != TS_OK) return st;
+  if (!memops().ok) return TS_ERR_UNSUPPORTED;
+
+  const uint32_t seq = g.step + 1;
+  g.step = seq;
+  cudaStream_t m = g.main_stream, gs = g.gather_stream, side = g.side_stream;
+  uint32_t* planned = g.sync + kPlanned;
+  uint32_t* refilled = g.sync + kRefilled;
+  uint32_t* gathered = g.sync + kGathered;
+  auto rec = [&](int slot, int end, cudaStream_t s) {
+    return timing ? cudaEventRecord(timing[2 * slot + end], s) == cudaSuccess : true;
+  };
+
+  bool ok = true;
+  if (!ids) {
+    ok = rec(0, 0, m) &&
+         topk_enqueue(scores, g.ctx_stride, g.ctx_len, g.B, g.max_ctx, g.k, g.ids, g.topk_ws,
+                      g.err, m) == TS_OK &&
+         rec(0, 1, m);
+  }
+  ok = ok && wait_for(m, refilled, seq - 1) && rec(1, 0, m) &&
+       plan_enqueue(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.fifo_ptr, g.S, g.W, g.src_map,
+                    g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.miss_rows,
+                    g.ptr_next, g.err, m) == TS_OK &&
+       rec(1, 1, m) && signal(m, planned, seq) && wait_for(gs, planned, seq);
+  for (int l = 0; ok && l < L; ++l)
+    ok = rec(2 + l, 0, gs) &&
+         gather_enqueue(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k,
+                        at(g.pool, l, lb.pool), P, at(g.host_kv, l, lb.host), g.ctx_stride,
+                        g.ctx_len, at(g.sel, l, lb.sel), g.err, gs) == TS_OK &&
+         rec(2 + l, 1, gs) && signal(gs, gathered + l, seq);
+  for (int l = 0; ok && l < L; ++l) {
+    ok = wait_for(m, gathered + l, seq) && rec(2 + L + l, 0, m) &&
+         sfa_enqueue(at(q, l, lb.q), at(g.sel, l, lb.sel), g.B, g.H, g.k, g.scale,
+                     at(g.out, l, lb.out), g.lse ? at(g.lse, l, lb.lse) : nullptr, g.sfa_ws,
+                     g.err, m) == TS_OK &&
+         rec(2 + L + l, 1, m) && wait_for(side, gathered + l, seq) && rec(2 + 2 * L + l, 0, side) &&
+         refill_enqueue(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k,
+                        at(g.sel, l, lb.sel), at(g.pool, l, lb.pool), P, l == L - 1, g.pool_tags,
+                        g.fifo_ptr, g.ptr_next, g.S, g.W, g.err, side) == TS_OK &&
+         rec(2 + 2 * L + l, 1, side);
+  }
+  ok = ok && signal(side, refilled, seq);
+  if (!ok) {
+    // give every word this step's number, so that no wait enqueued now or by
+    // the next call is left without its signal
+    for (int i = 0; i < kGathered + L; ++i) signal(side, g.sync + i, seq);
+    return TS_ERR_CUDA;
+  }
+  return TS_OK;
+}

@@ -23,6 +23,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "ops.h"
 
 namespace dsakv {
 namespace {
@@ -642,16 +643,33 @@ extern "C" size_t ts_topk_workspace_size(int B, int max_ctx, int k) {
          align256(size_t(B) * max_ctx * 8) + align256(size_t(B) * words * 4);
 }
 
-extern "C" ts_status ts_topk(const float* scores, int64_t ctx_stride, const int32_t* ctx_len, int B,
-                             int max_ctx, int k, int32_t* ids, void* ws, size_t ws_bytes,
-                             int32_t* err, cudaStream_t stream) {
+namespace dsakv {
+
+ts_status topk_check(const float* scores, int64_t ctx_stride, const int32_t* ctx_len, int B,
+                     int max_ctx, int k, int32_t* ids, const void* ws, size_t ws_bytes) {
   const ts_status st = check_topk_args(scores, ctx_stride, ctx_len, B, max_ctx, k, ids);
   if (st != TS_OK) return st;
   if (!ws) return TS_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0 ||
       ws_bytes < ts_topk_workspace_size(B, max_ctx, k))
     return TS_ERR_WORKSPACE;
+  return TS_OK;
+}
+
+ts_status topk_enqueue(const float* scores, int64_t ctx_stride, const int32_t* ctx_len, int B,
+                       int max_ctx, int k, int32_t* ids, void* ws, int32_t* err,
+                       cudaStream_t stream) {
   return launch_topk(scores, ctx_stride, ctx_len, B, max_ctx, k, ids, ws, err, stream);
+}
+
+}  // namespace dsakv
+
+extern "C" ts_status ts_topk(const float* scores, int64_t ctx_stride, const int32_t* ctx_len, int B,
+                             int max_ctx, int k, int32_t* ids, void* ws, size_t ws_bytes,
+                             int32_t* err, cudaStream_t stream) {
+  const ts_status st = topk_check(scores, ctx_stride, ctx_len, B, max_ctx, k, ids, ws, ws_bytes);
+  if (st != TS_OK) return st;
+  return topk_enqueue(scores, ctx_stride, ctx_len, B, max_ctx, k, ids, ws, err, stream);
 }
 
 // ---------------------------------------------------------------------------

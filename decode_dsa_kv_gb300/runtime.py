@@ -1,32 +1,32 @@
-"""Device state and the per-step schedule of one IndexShare group.
+"""Device state of one IndexShare group and its per-step schedule.
 
 The schedule is the one of the GLM-5.2 shared-Indexer KV Cache Offload page,
 §4.4 (SFA first, refill later) and §5.1 (one plan per group, per-layer serve,
 refill on a side stream synchronised by events, metadata update at the group's
-last layer):
+last layer). It is enqueued by the library's dsa_group_step in one native call
+per step:
 
-  main stream   : ts_topk -> [wait refill_done of the previous step] -> dsa_plan
-                  -> record planned
+  main stream   : ts_topk -> [wait refilled of the previous step] -> dsa_plan
+                  -> signal planned
                   -> for each layer l: [wait gathered[l]] -> sfa_mla_decode(l)
-  gather stream : [wait planned] -> dsa_gather_kv(0..3), recording gathered[l]
+  gather stream : [wait planned] -> dsa_gather_kv(0..3), signalling gathered[l]
                   after each layer
   side stream   : for each layer l: [wait gathered[l]] -> dsa_refill_pool(l)
                   (the last layer also updates tags and FIFO pointers)
-                  -> record refill_done
+                  -> signal refilled
+
+Signals and waits are stream memory operations on device words (the
+library's `sync` words), polled by the GPU's front end in HBM.
 
 The plan is shared by the group, so every layer's gather can start as soon as
 it exists: the host-link transfers of layer l+1 overlap the attention of
 layer l, and each layer's attention still starts the moment its own rows are
-in (SFA first). Ordering argument: refill(l) overwrites pool slots that
-gather(l) reads, so it waits for gather(l); the next step's plan reads the
-tags the last refill writes and rewrites the plan every gather and refill
-reads, so it waits for refill_done and comes after the last SFA, which waited
-for the last gather; the next step's gather(l) rewrites sel[l], which SFA(l)
-and refill(l) read, and it waits for that plan. Memory comes from PyTorch;
-the arithmetic runs in libdsakv's kernels only.
+in (SFA first). Memory and streams come from PyTorch; this module only fills
+the descriptor; the arithmetic runs in libdsakv's kernels.
 """
 from __future__ import annotations
 
+import ctypes
 import math
 
 import numpy as np
@@ -95,6 +95,50 @@ class HostKV:
             pass
 
 
+class StepTiming:
+    """CUDA timing events for the launches of one step, created (and recorded
+    once, which makes them valid) ahead of use, in the order dsa_group_step
+    fills them: top-k, plan, gather[l], sfa[l], refill[l]."""
+
+    def __init__(self, layers: int, stream=None):
+        self.layers = layers
+        n = 2 * (2 + 3 * layers)
+        st = torch.cuda.current_stream() if stream is None else stream
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in self.events:
+            e.record(st)
+        self.array = (ctypes.c_void_p * n)(*[e.cuda_event for e in self.events])
+        self.with_topk = True
+
+    def ms(self) -> dict:
+        """name -> per-launch milliseconds (after the step completed)."""
+        L = self.layers
+        ev = self.events
+
+        def pair(i):
+            return ev[2 * i].elapsed_time(ev[2 * i + 1])
+
+        out = {"topk": [pair(0)] if self.with_topk else [], "plan": [pair(1)]}
+        out["gather"] = [pair(2 + l) for l in range(L)]
+        out["sfa"] = [pair(2 + L + l) for l in range(L)]
+        out["refill"] = [pair(2 + 2 * L + l) for l in range(L)]
+        return out
+
+    def spans(self, t0) -> dict:
+        """name -> [(start, end)] in microseconds after event t0."""
+        L = self.layers
+        ev = self.events
+
+        def span(i):
+            return (t0.elapsed_time(ev[2 * i]) * 1e3, t0.elapsed_time(ev[2 * i + 1]) * 1e3)
+
+        out = {"topk": [span(0)] if self.with_topk else [], "plan": [span(1)]}
+        out["gather"] = [span(2 + l) for l in range(L)]
+        out["sfa"] = [span(2 + L + l) for l in range(L)]
+        out["refill"] = [span(2 + 2 * L + l) for l in range(L)]
+        return out
+
+
 class DecodeGroup:
     """Pool state and buffers for B requests of one IndexShare group."""
 
@@ -140,65 +184,45 @@ class DecodeGroup:
         self.main = torch.cuda.Stream(device=dev, priority=-1)
         self.gstream = torch.cuda.Stream(device=dev, priority=0)
         self.side = torch.cuda.Stream(device=dev, priority=0)
-        self.planned = torch.cuda.Event()
-        self.gathered = [torch.cuda.Event() for _ in range(layers)]
-        self.refill_done = torch.cuda.Event()
-        self.refill_done.record(self.side)
+        # cross-stream signals: device words written and waited on by the
+        # streams themselves (zero before the first step)
+        self.sync = torch.zeros((2 + layers,), **i32)
+        self.desc = self._descriptor()
+
+    def _descriptor(self):
+        d = abi.DsaGroup()
+        d.B, d.layers, d.k, d.S, d.W, d.H = self.B, self.L, self.k, self.S, self.W, self.H
+        d.max_ctx, d.ctx_stride, d.scale = self.max_ctx, self.ctx_stride, self.scale
+        d.ctx_len = self.ctx_len.data_ptr()
+        d.pool, d.pool_tags, d.fifo_ptr = (self.pool.data_ptr(), self.tags.data_ptr(),
+                                           self.fifo_ptr.data_ptr())
+        d.host_kv = self.host.dev
+        for name in ("ids", "src_map", "miss_ids", "miss_pos", "victim", "install",
+                     "miss_count", "miss_rows", "ptr_next", "sel", "out", "lse"):
+            setattr(d, name, getattr(self, name).data_ptr())
+        d.topk_ws, d.topk_ws_bytes = self.topk_ws.data_ptr(), self.topk_ws_bytes
+        d.sfa_ws, d.sfa_ws_bytes = self.sfa_ws.data_ptr(), self.sfa_ws_bytes
+        d.err = self.err.data_ptr()
+        d.main_stream = self.main.cuda_stream
+        d.gather_stream = self.gstream.cuda_stream
+        d.side_stream = self.side.cuda_stream
+        d.sync = self.sync.data_ptr()
+        d.step = 0
+        return d
 
     # -- the step --------------------------------------------------------
     def step(self, scores: torch.Tensor, q: torch.Tensor, ids: torch.Tensor | None = None,
-             kernel_events=None) -> None:
-        """Enqueue one decode step. scores: float32 [B][ctx_stride] (device);
-        q: bf16 [layers][B][H][576] (device). With `ids` given (int32 [B][k]),
-        the top-k is skipped and those ids are planned. `kernel_events`, when
-        given, is a dict name -> list of (start, end) CUDA event pairs that are
-        recorded around every launch of that kernel on its own stream."""
-        B, k, L = self.B, self.k, self.L
-        m, s = self.main, self.side
-
-        def timed(name, stream, fn):
-            if kernel_events is not None and name in kernel_events:
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                st = fn()
-                b.record(stream)
-                kernel_events[name].append((a, b))
-                return st
-            return fn()
-
-        if ids is None:
-            abi.check(timed("topk", m, lambda: abi.ts_topk(
-                scores, self.ctx_stride, self.ctx_len, B, self.max_ctx, k, self.ids,
-                self.topk_ws, self.topk_ws_bytes, self.err, m)), "ts_topk")
-            ids = self.ids
-        m.wait_event(self.refill_done)
-        abi.check(timed("plan", m, lambda: abi.dsa_plan(
-            ids, self.ctx_len, B, k, self.tags, self.fifo_ptr, self.S, self.W, self.src_map,
-            self.miss_ids, self.miss_pos, self.victim, self.install, self.miss_count,
-            self.miss_rows, self.ptr_next, self.err, m)), "dsa_plan")
-        self.planned.record(m)
-        gs = self.gstream
-        gs.wait_event(self.planned)
-        for l in range(L):
-            abi.check(timed("gather", gs, lambda: abi.dsa_gather_kv(
-                self.src_map, self.miss_ids, self.miss_pos, self.miss_count, self.miss_rows, B, k,
-                self.pool[l],
-                self.P, self.host.layer_ptr(l),
-                self.ctx_stride, self.ctx_len, self.sel[l], self.err, gs)), "dsa_gather_kv")
-            self.gathered[l].record(gs)
-        for l in range(L):
-            m.wait_event(self.gathered[l])
-            abi.check(timed("sfa", m, lambda: abi.sfa_mla_decode(
-                q[l], self.sel[l], B, self.H, k, self.scale, self.out[l], self.lse[l],
-                self.sfa_ws, self.sfa_ws_bytes, self.err, m)), "sfa_mla_decode")
-            s.wait_event(self.gathered[l])
-            last = l == L - 1
-            abi.check(timed("refill", s, lambda: abi.dsa_refill_pool(
-                self.miss_ids, self.miss_pos, self.victim, self.install, self.miss_count, B, k,
-                self.sel[l], self.pool[l], self.P, int(last), self.tags, self.fifo_ptr,
-                self.ptr_next, self.S, self.W, self.err, s)), "dsa_refill_pool")
-        self.refill_done.record(s)
+             timing: StepTiming | None = None) -> None:
+        """Enqueue one decode step (one native call). scores: float32
+        [B][ctx_stride] (device); q: bf16 bits [layers][B][H][576] (device).
+        With `ids` given (int32 [B][k]), the top-k is skipped and those ids are
+        planned. `timing`, when given, receives (start, end) events around
+        every launch."""
+        if timing is not None:
+            timing.with_topk = ids is None
+        abi.check(abi.dsa_group_step(self.desc, scores, q, ids,
+                                     None if timing is None else timing.array),
+                  "dsa_group_step")
 
     def join(self, stream=None) -> None:
         """Make `stream` (default: the current stream) wait for all step work."""

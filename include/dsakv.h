@@ -226,6 +226,96 @@ ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int H, int k,
                          float scale, void* out, float* lse, void* ws, size_t ws_bytes,
                          int32_t* err, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * dsa_group_step -- one decode step of an IndexShare group of `layers` layers,
+ * enqueued by one call ([GLM] §5.1 model-side orchestration: one plan per
+ * group, per-layer serve, refill on a side stream ordered after the serve,
+ * metadata update at the group's last layer; §4.4 SFA first, refill later).
+ * On the caller's three streams it issues:
+ *
+ *   main   : ts_topk(scores) -> wait refilled -> dsa_plan -> signal planned
+ *            -> for each layer l: wait gathered[l] -> sfa_mla_decode(l)
+ *   gather : wait planned -> for each layer l: dsa_gather_kv(l), signal
+ *            gathered[l]
+ *   side   : for each layer l: wait gathered[l] -> dsa_refill_pool(l) (the
+ *            last layer also updates tags and FIFO pointers) -> after the
+ *            last layer, signal refilled
+ *
+ * Signals and waits are stream memory operations on the caller's device
+ * words `sync` (cuStreamWriteValue32 / cuStreamWaitValue32 with the step's
+ * sequence number, compared wrap-around): the GPU's front end polls device
+ * memory, with no event round trip. Ordering: refill(l) evicts slots gather(l)
+ * reads, so it waits for gather(l); the next step's plan reads the tags the
+ * last refill writes, so it waits for `refilled`; the next step's gather(l)
+ * rewrites sel[l], which sfa(l) and refill(l) of this step read: it waits for
+ * the next plan, which follows every sfa on the main stream and the last
+ * refill. Every wait is enqueued after the signal it waits for, so every wait
+ * ends.
+ *
+ * The descriptor holds the group's buffers (the caller owns all of them):
+ *   ctx_len   int32 [B]                     k <= ctx_len[b] <= max_ctx
+ *   pool      bf16  [layers][B][S*W][576]   the device pool of every layer
+ *   pool_tags int32 [B][S*W], fifo_ptr int32 [B][S]   pool metadata
+ *   host_kv   bf16  [layers][B][ctx_stride][576]  device-accessible address
+ *                                           of pinned host memory
+ *   ids ... ptr_next                        plan buffers, as dsa_plan's
+ *   sel       bf16  [layers][B][k][576]     selection buffers
+ *   out       bf16  [layers][B][H][512], lse float [layers][B][H] (or NULL)
+ *   topk_ws / sfa_ws                        workspaces of ts_topk and
+ *                                           sfa_mla_decode (sizes as theirs)
+ *   err       int32 device error word (or NULL)
+ *   sync      uint32 [2 + layers] device words, zero before the first step
+ *             and touched by nothing else; step = 0 before the first step.
+ *             Each call uses sequence number step + 1 and stores it in
+ *             `step` (the only field the call writes).
+ * Step inputs: scores float [B][ctx_stride] (device); q bf16
+ * [layers][B][H][576] (device); ids int32 [B][k] (device) or NULL -- when
+ * given, the top-k is skipped and these ids are planned.
+ * timing: NULL, or 2 * (2 + 3 * layers) events created by the caller, filled
+ * as (start, end) pairs recorded on the launching stream around every
+ * operation, in the order top-k, plan, gather[0..layers), sfa[0..layers),
+ * refill[0..layers) (the top-k pair is left alone when ids are given).
+ * Every operation's arguments are validated before anything is enqueued;
+ * 1 <= layers <= TS_MAX_LAYERS. If a launch fails after the first one, every
+ * sync word still receives this step's number (so no later wait is left
+ * without its signal) and the error is returned.
+ * ------------------------------------------------------------------------- */
+#define TS_MAX_LAYERS 16
+
+typedef struct {
+  int B, layers, k, S, W, H, max_ctx;
+  int64_t ctx_stride;
+  float scale;
+  const int32_t* ctx_len;
+  void* pool;
+  int32_t* pool_tags;
+  int32_t* fifo_ptr;
+  const void* host_kv;
+  int32_t* ids;
+  int32_t* src_map;
+  int32_t* miss_ids;
+  int32_t* miss_pos;
+  int32_t* victim;
+  uint8_t* install;
+  int32_t* miss_count;
+  int32_t* miss_rows;
+  int32_t* ptr_next;
+  void* sel;
+  void* out;
+  float* lse;
+  void* topk_ws;
+  size_t topk_ws_bytes;
+  void* sfa_ws;
+  size_t sfa_ws_bytes;
+  int32_t* err;
+  cudaStream_t main_stream, gather_stream, side_stream;
+  uint32_t* sync;
+  uint32_t step;
+} dsa_group;
+
+ts_status dsa_group_step(dsa_group* g, const float* scores, const void* q, const int32_t* ids,
+                         cudaEvent_t* timing);
+
 #ifdef __cplusplus
 }
 #endif

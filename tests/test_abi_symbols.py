@@ -40,3 +40,24 @@ def test_host_side_validation_without_gpu():
     assert d.ts_status_string(_abi.TS_ERR_WORKSPACE).startswith("workspace")
     assert d.ts_topk_workspace_size(2, 1000, 16) > 2 * 1000 * 8
     assert d.sfa_workspace_size(1, 128, 2048) >= 4 * 128 * 512 * 4  # 4 chunks of 512 rows
+
+
+def test_group_step_validation_without_gpu():
+    """dsa_group_step refuses a bad descriptor before it enqueues anything."""
+    import decode_dsa_kv_gb300 as d
+    from decode_dsa_kv_gb300 import _abi
+    g = d.DsaGroup()
+    q = 1 << 20  # any 16-byte aligned address: nothing is read before the checks pass
+    assert d.dsa_group_step(g, None, None) == _abi.TS_ERR_INVALID_ARG       # no q
+    assert d.dsa_group_step(g, None, q) == _abi.TS_ERR_INVALID_ARG          # layers = 0
+    g.layers = _abi.TS_MAX_LAYERS + 1
+    assert d.dsa_group_step(g, q, q) == _abi.TS_ERR_INVALID_ARG
+    g.B, g.layers, g.k, g.S, g.W, g.H, g.max_ctx, g.ctx_stride = 2, 4, 16, 8, 4, 128, 64, 64
+    assert d.dsa_group_step(g, q, q) == _abi.TS_ERR_INVALID_ARG             # no sync words
+    g.sync = q + 2
+    assert d.dsa_group_step(g, q, q) == _abi.TS_ERR_INVALID_ARG             # sync misaligned
+    g.sync = q
+    assert d.dsa_group_step(g, None, q) == _abi.TS_ERR_INVALID_ARG          # no scores, no ids
+    assert d.dsa_group_step(g, q, q + 8) == _abi.TS_ERR_INVALID_ARG         # q misaligned
+    assert d.dsa_group_step(g, q, q) == _abi.TS_ERR_INVALID_ARG             # null buffers
+    assert g.step == 0                                                      # nothing enqueued
