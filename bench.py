@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -218,9 +219,37 @@ def link_peak_gbs(torch, nbytes=1 << 30, reps=5):
     return best
 
 
+def device_digest_of(source_text: str, common_text: str) -> str:
+    """Digest of the device code in a kernel source and common.cuh: every
+    __global__ / __device__ definition and every constexpr line. Host-only
+    edits leave it unchanged; any device edit changes it."""
+    text = common_text + "\n" + source_text
+    parts = []
+    for m in re.finditer(r"(__global__|__device__)[^;{]*\{", text):
+        depth, i = 0, m.end() - 1
+        while i < len(text):
+            if text[i] == "{":
+                depth += 1
+            elif text[i] == "}":
+                depth -= 1
+                if depth == 0:
+                    break
+            i += 1
+        parts.append(text[m.start():i + 1])
+    parts += re.findall(r"^\s*constexpr[^\n]*", text, flags=re.M)
+    return hashlib.sha256("\n".join(parts).encode()).hexdigest()[:16]
+
+
+def device_digest(source: str) -> str:
+    """device_digest_of for a file of the package's csrc/ (by name)."""
+    csrc = os.path.join(ROOT, "decode_dsa_kv_gb300", "csrc")
+    return device_digest_of(open(os.path.join(csrc, source)).read(),
+                            open(os.path.join(csrc, "common.cuh")).read())
+
+
 def traffic_record(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current source of that kernel (else None)."""
+    the current device code of that kernel's source file (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -230,8 +259,8 @@ def traffic_record(kernel: str, workload: str):
     src = os.path.join(ROOT, "decode_dsa_kv_gb300", "csrc", rec["source"])
     if not os.path.exists(src):
         return None
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return rec["bytes_per_launch"] if h == rec.get("source_sha256_16") else None
+    ok = device_digest(rec["source"]) == rec.get("device_digest")
+    return rec["bytes_per_launch"] if ok else None
 
 
 # ---------------------------------------------------------------------------
