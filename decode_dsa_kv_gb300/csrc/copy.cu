@@ -5,11 +5,9 @@
 // group's last layer, updates the pool metadata (§4.4 refill after SFA, §5
 // DsaInstall, §5.1 metadata update at the group's last layer).
 //
-// Both are pure 16-byte copies. The gather is flattened over every 16-byte
-// piece of the selection (72 per 1152-byte row), so consecutive threads move
-// consecutive bytes of a row whichever source it comes from: HBM for pool
-// hits, pinned host memory read in place over the host link for misses. Each
-// thread keeps several loads in flight before its stores.
+// Both are pure 16-byte copies of 1152-byte rows (72 pieces), one warp per
+// row: HBM for pool hits, pinned host memory read in place over the host link
+// for misses. Each warp keeps several rows' loads in flight before its stores.
 #include <climits>
 
 #include "common.cuh"
@@ -32,6 +30,18 @@ __device__ __forceinline__ void st_v4(uint4* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
+}
+
+// First position of token t among request b's misses, or -1: binary search of
+// the ascending miss list.
+__device__ __forceinline__ int first_pos_of(const int32_t* mids, const int32_t* mpos, int M, int t) {
+  int lo = 0, hi = M;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(mids + mid) < t) lo = mid + 1;
+    else hi = mid;
+  }
+  return (lo < M && __ldg(mids + lo) == t) ? __ldg(mpos + lo) : -1;
 }
 
 // Copy up to two 1152-byte rows with one warp: every lane moves the pieces
@@ -63,21 +73,10 @@ __device__ __forceinline__ void warp_copy_rows2(const uint4* from0, uint4* to0, 
   }
 }
 
-// First position of token t among request b's misses, or -1: binary search of
-// the ascending miss list.
-__device__ __forceinline__ int first_pos_of(const int32_t* mids, const int32_t* mpos, int M, int t) {
-  int lo = 0, hi = M;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(mids + mid) < t) lo = mid + 1;
-    else hi = mid;
-  }
-  return (lo < M && __ldg(mids + lo) == t) ? __ldg(mpos + lo) : -1;
-}
-
 // One launch, two kinds of warps (alternating), each moving two rows per step:
-//   even warps walk the compact miss list: host row miss_ids[i] ->
-//     sel[miss_pos[i]] (the host-link reads, which set the kernel's time);
+//   even warps walk the compact miss lists, concatenated over the requests
+//     and dealt out evenly: host row miss_ids[i] -> sel[miss_pos[i]] (the
+//     host-link reads, which set the kernel's time);
 //   odd warps walk the positions: pool row for a hit; for a miss, the host row
 //     only when that token repeats in the selection and this is not its first
 //     position (the even warps serve first positions). Requests without
@@ -99,23 +98,61 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(
   const int64_t nrole = miss_warp ? (nw + 1) >> 1 : nw >> 1;
   int bad = 0;
   if (miss_warp) {
-    for (int64_t r0 = w * 2; r0 < rows; r0 += nrole * 2) {
+    // The misses of all requests, concatenated: this warp takes miss indices
+    // m = w, w + nrole, ... (request b holds miss_count[b] of them), so every
+    // miss warp gets the same number of host rows whatever the spread of
+    // misses over requests. Looked up 32 at a time, one candidate per lane;
+    // `mask` holds the lanes with a row to move.
+    int64_t m1 = w, base1 = 0;
+    int b1 = 0, cnt1 = __ldg(miss_count);
+    uint32_t mask = 0;
+    const uint4* my_from = nullptr;
+    uint4* my_to = nullptr;
+    for (;;) {
+      if (mask == 0) {
+        if (b1 >= B) break;
+        const int64_t ml = m1 + int64_t(lane) * nrole;
+        int b = b1, cnt = cnt1;
+        int64_t base = base1;
+        while (b < B && ml >= base + cnt) {
+          base += cnt;
+          if (++b < B) cnt = __ldg(miss_count + b);
+        }
+        bool valid = false;
+        if (b < B) {
+          const int i = static_cast<int>(ml - base);
+          const bool in = i >= 0 && i < k;  // (a count past k is corrupt)
+          const int64_t s = int64_t(b) * k + i;
+          const int t = in ? __ldg(miss_ids + s) : -1;
+          const int j = in ? __ldg(miss_pos + s) : -1;
+          if (t < 0 || t >= __ldg(ctx_len + b) || t >= ctx_stride || j < 0 || j >= k) {
+            bad |= TS_DEVERR_ID_RANGE;
+          } else {
+            my_from = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
+            my_to = sel + (int64_t(b) * k + j) * DSA_ROW_CHUNKS;
+            valid = true;
+          }
+        }
+        mask = __ballot_sync(0xffffffffu, valid);
+        // lane 31 holds the furthest index: the walk resumes from there
+        b1 = __shfl_sync(0xffffffffu, b, 31);
+        cnt1 = __shfl_sync(0xffffffffu, cnt, 31);
+        base1 = __shfl_sync(0xffffffffu, base, 31);
+        m1 += 32 * nrole;
+        continue;
+      }
       const uint4* from[2] = {nullptr, nullptr};
       uint4* to[2] = {nullptr, nullptr};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int64_t r = r0 + e;
-        if (r >= rows) continue;
-        const int b = static_cast<int>(r / k);
-        const int i = static_cast<int>(r - int64_t(b) * k);
-        if (i >= __ldg(miss_count + b)) continue;
-        const int t = __ldg(miss_ids + r), j = __ldg(miss_pos + r);
-        if (t < 0 || t >= __ldg(ctx_len + b) || j < 0 || j >= k) {
-          bad |= TS_DEVERR_ID_RANGE;
-          continue;
+        if (mask) {
+          const int q = __ffs(mask) - 1;
+          mask &= mask - 1;
+          from[e] = reinterpret_cast<const uint4*>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_from), q));
+          to[e] = reinterpret_cast<uint4*>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_to), q));
         }
-        from[e] = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
-        to[e] = sel + (int64_t(b) * k + j) * DSA_ROW_CHUNKS;
       }
       warp_copy_rows2(from[0], to[0], from[1], to[1], lane);
     }
@@ -139,7 +176,8 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(
           const int t = -1 - src;
           const int64_t base = int64_t(b) * k;
           if (first_pos_of(miss_ids + base, miss_pos + base, M, t) == j) continue;
-          if (t < __ldg(ctx_len + b)) from[e] = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
+          if (t < __ldg(ctx_len + b) && t < ctx_stride)
+            from[e] = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
           else bad |= TS_DEVERR_ID_RANGE;
         } else {
           bad |= TS_DEVERR_ID_RANGE;
@@ -152,21 +190,24 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(
   if (bad && lane == 0) report(err, bad);
 }
 
-// One warp per (request, miss) pair: 72 pieces, lanes stride by 32.
-constexpr int kRefillThreads = 1024;
+// One warp per (request, miss) pair and every layer of the call: 72 pieces
+// per row, lanes stride by 32. Layer l's selection and pool start sel_stride
+// and pool_stride 16-byte pieces after layer l-1's.
+constexpr int kRefillThreads = 256;
 __global__ void __launch_bounds__(kRefillThreads) refill_kernel(
     const int32_t* __restrict__ miss_ids, const int32_t* __restrict__ miss_pos,
     const int32_t* __restrict__ victim, const uint8_t* __restrict__ install,
     const int32_t* __restrict__ miss_count, int B, int k, const uint4* __restrict__ sel,
-    uint4* __restrict__ pool, int P, int update_metadata, int32_t* __restrict__ pool_tags,
-    int32_t* __restrict__ fifo_ptr, const int32_t* __restrict__ ptr_next, int S, int W,
-    int32_t* err) {
+    uint4* __restrict__ pool, int P, int layers, int64_t sel_stride, int64_t pool_stride,
+    int update_metadata, int32_t* __restrict__ pool_tags, int32_t* __restrict__ fifo_ptr,
+    const int32_t* __restrict__ ptr_next, int S, int W, int32_t* err) {
   const int lane = threadIdx.x & 31;
-  const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t r = warp; r < int64_t(B) * k; r += nwarps) {
-    const int b = static_cast<int>(r / k);
-    const int i = static_cast<int>(r - int64_t(b) * k);
+  const int warp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int nwarps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
+  const int rows = B * k;  // < 2^31: B <= 65535, k <= 8192
+  for (int r = warp; r < rows; r += nwarps) {
+    const int b = r / k;
+    const int i = r - b * k;
     if (i >= __ldg(miss_count + b)) continue;
     if (!__ldg(install + r)) continue;
     const int v = __ldg(victim + r);
@@ -175,15 +216,17 @@ __global__ void __launch_bounds__(kRefillThreads) refill_kernel(
       if (lane == 0) report(err, TS_DEVERR_SLOT_RANGE);
       continue;
     }
-    const uint4* from = sel + (int64_t(b) * k + j) * DSA_ROW_CHUNKS;
-    uint4* to = pool + (int64_t(b) * P + v) * DSA_ROW_CHUNKS;
-    uint4 a = ld_nc_v4(from + lane);
-    uint4 c = ld_nc_v4(from + lane + 32);
-    uint4 d;
-    if (lane < DSA_ROW_CHUNKS - 64) d = ld_nc_v4(from + lane + 64);
-    st_v4(to + lane, a);
-    st_v4(to + lane + 32, c);
-    if (lane < DSA_ROW_CHUNKS - 64) st_v4(to + lane + 64, d);
+    const uint4* from = sel + (int64_t(b) * k + j) * DSA_ROW_CHUNKS + lane;
+    uint4* to = pool + (int64_t(b) * P + v) * DSA_ROW_CHUNKS + lane;
+    for (int l = 0; l < layers; ++l) {
+      const uint4 x0 = ld_nc_v4(from);
+      const uint4 x1 = ld_nc_v4(from + 32);
+      st_v4(to, x0);
+      st_v4(to + 32, x1);
+      if (lane < DSA_ROW_CHUNKS - 64) st_v4(to + 64, ld_nc_v4(from + 64));
+      from += sel_stride;
+      to += pool_stride;
+    }
     if (update_metadata && lane == 0) pool_tags[int64_t(b) * P + v] = __ldg(miss_ids + r);
   }
   if (update_metadata) {
@@ -236,13 +279,15 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
                          const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream) {
   // A quarter of the SMs, one 1024-thread CTA each, keep a few MB of loads in
   // flight, which saturates the host link (measured); the other SMs stay free
-  // for the attention of the previous layer, which runs beside the gather
-  // (an SM holding a gather CTA cannot also take an attention CTA).
+  // for the attention of the previous layer, which runs beside the gather.
+  // Measured alternatives that did worse: small CTAs on every SM (the zero-copy
+  // loads slow an attention CTA on the same SM by about 2x), and cp.async
+  // staging through shared memory (reads of host memory top out near half
+  // the link's rate that way).
   const int64_t rows = int64_t(B) * k;
   int64_t blocks = (rows + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
   const int64_t cap = sm_count() / 4 > 8 ? sm_count() / 4 : 8;
   if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
   gather_kernel<<<static_cast<unsigned>(blocks), kGatherThreads, 0, stream>>>(
       src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, static_cast<const uint4*>(pool_l), P,
       static_cast<const uint4*>(host_l), ctx_stride, ctx_len, static_cast<uint4*>(sel_l), err);
@@ -267,17 +312,20 @@ ts_status refill_enqueue(const int32_t* miss_ids, const int32_t* miss_pos, const
                          const uint8_t* install, const int32_t* miss_count, int B, int k,
                          const void* sel_l, void* pool_l, int P, int update_metadata,
                          int32_t* pool_tags, int32_t* fifo_ptr, const int32_t* ptr_next, int S,
-                         int W, int32_t* err, cudaStream_t stream) {
-  // like the gather, a quarter of the SMs: the refill is off the critical
-  // path and leaves the other SMs to the attention it runs beside
+                         int W, int32_t* err, cudaStream_t stream, int layers,
+                         size_t sel_layer_bytes, size_t pool_layer_bytes) {
+  // one warp per (request, miss); one small CTA per SM, which fits beside an
+  // attention CTA (measured best of 16 or 38 1024-thread CTAs and 76 or 152
+  // 256-thread ones, beside the attention and the next layer's gather)
   const int64_t warps = int64_t(B) * k;
   int64_t blocks = (warps * 32 + kRefillThreads - 1) / kRefillThreads;
-  const int64_t cap = sm_count() / 4 > 8 ? sm_count() / 4 : 8;
+  const int64_t cap = sm_count();
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   refill_kernel<<<static_cast<unsigned>(blocks), kRefillThreads, 0, stream>>>(
       miss_ids, miss_pos, victim, install, miss_count, B, k, static_cast<const uint4*>(sel_l),
-      static_cast<uint4*>(pool_l), P, update_metadata, pool_tags, fifo_ptr, ptr_next, S, W, err);
+      static_cast<uint4*>(pool_l), P, layers, int64_t(sel_layer_bytes / 16),
+      int64_t(pool_layer_bytes / 16), update_metadata, pool_tags, fifo_ptr, ptr_next, S, W, err);
   return launch_status();
 }
 
@@ -308,7 +356,7 @@ extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* mis
   if (st != TS_OK) return st;
   return dsakv::refill_enqueue(miss_ids, miss_pos, victim, install, miss_count, B, k, sel_l,
                                pool_l, P, update_metadata, pool_tags, fifo_ptr, ptr_next, S, W,
-                               err, stream);
+                               err, stream, 1, 0, 0);
 }
 
 // ---------------------------------------------------------------------------

@@ -40,11 +40,14 @@ ts_status refill_check(const int32_t* miss_ids, const int32_t* miss_pos, const i
                        const void* sel_l, void* pool_l, int P, int update_metadata,
                        int32_t* pool_tags, int32_t* fifo_ptr, const int32_t* ptr_next, int S,
                        int W);
+// `layers` consecutive layers in one launch: layer l's selection and pool
+// start l * sel_layer_bytes / l * pool_layer_bytes after sel_l / pool_l.
 ts_status refill_enqueue(const int32_t* miss_ids, const int32_t* miss_pos, const int32_t* victim,
                          const uint8_t* install, const int32_t* miss_count, int B, int k,
                          const void* sel_l, void* pool_l, int P, int update_metadata,
                          int32_t* pool_tags, int32_t* fifo_ptr, const int32_t* ptr_next, int S,
-                         int W, int32_t* err, cudaStream_t stream);
+                         int W, int32_t* err, cudaStream_t stream, int layers,
+                         size_t sel_layer_bytes, size_t pool_layer_bytes);
 
 ts_status sfa_check(const void* q, const void* sel_l, int B, int H, int k, float scale,
                     void* out, const void* ws, size_t ws_bytes);

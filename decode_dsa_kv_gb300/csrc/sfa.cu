@@ -7,8 +7,9 @@
 // One CTA per (request b, head tile of 128 heads, chunk of 512 selected rows),
 // on the 5th-generation tensor cores:
 //   warp 0   : TMA producer (one thread): Q and K tiles for the score product
-//              (two 256-row halves), then V tiles for the value product,
-//              through a 2-stage ring of 48 KB stages (128-byte swizzle).
+//              (two 256-row halves) through 4 slots of 48 KB (two of them in
+//              the P tile's space, free until the softmax), then V tiles for
+//              the value product through 3 slots of 32 KB (128-byte swizzle).
 //   warp 1   : allocates 512 TMEM columns; one thread issues tcgen05.mma.
 //   warps 2-9: softmax and epilogue; two threads per head (TMEM lane), each
 //              with half of the chunk's columns.
@@ -35,7 +36,9 @@ constexpr int kHeads = 128;  // MMA M
 constexpr int kChunk = 512;  // rows per CTA: two score MMAs of N = 256, K of the value product
 constexpr int kHalfRows = 256;
 constexpr int kKB = 9;       // 64-wide blocks of the 576 dims
-constexpr int kStages = 2;
+constexpr int kStages = 2;   // 48 KB slots of the ring region
+constexpr int kSSlots = 4;   // score-phase slots: the ring's two and two in the P region
+constexpr int kVSlots = 3;   // value-phase slots: 32 KB each in the ring region
 constexpr uint32_t kQBytes = kHeads * 128;           // 128 heads x 64 dims
 constexpr uint32_t kKBytes = kHalfRows * 128;        // 256 rows x 64 dims
 constexpr uint32_t kStageBytes = kQBytes + kKBytes;  // 48 KB
@@ -47,17 +50,26 @@ constexpr int kScoreLoads = 2 * kKB;                 // 18 score stages
 constexpr int kLoads = kScoreLoads + 16;             // + 16 value stages (8 row blocks x 2 halves)
 constexpr int kSoftmaxThreads = 256;                 // warps 2..9
 constexpr int kThreads = 64 + kSoftmaxThreads;
-constexpr uint32_t kBarBytes = 1536;
+constexpr uint32_t kBarBytes = 704;
 constexpr int kOutStride = 256 + 4;  // floats per head row of the epilogue staging
-constexpr uint32_t kSmemBytes = 1024 + kPBytes + kStages * kStageBytes + kBarBytes;
+// barriers first, then the 1024-byte aligned tiles (worst-case padding
+// included). The total leaves room on the SM for a 0-byte CTA of another
+// kernel (each CTA also holds 1 KB of reserved shared memory), so a gather or
+// refill CTA can run beside an attention CTA.
+constexpr uint32_t kTileBytes = kPBytes + kStages * kStageBytes;
+constexpr uint32_t kSmemBytes = kBarBytes + 1024 + kTileBytes;
 constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s of global timer per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-static_assert(kHeads * kOutStride * 4 <= kPBytes + kStages * kStageBytes, "epilogue staging");
+static_assert(kHeads * kOutStride * 4 <= kTileBytes, "epilogue staging");
+// 228 KB of shared memory per SM; 1 KB reserved per CTA
+static_assert(kSmemBytes + 1024 + 1024 <= 228 * 1024, "room for a second, shared-memory-free CTA");
 
 struct Bars {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kSSlots];
+  uint64_t empty[kSSlots];
+  uint64_t vfull[kVSlots];
+  uint64_t vempty[kVSlots];
   uint64_t s_full;
   uint64_t p_full;
   uint64_t o_full;
@@ -65,7 +77,7 @@ struct Bars {
   uint32_t tmem_slot;
   int abort;
   int issued;
-  float red[2][kHeads];  // the two column halves' row max, then row sum
+  float red[kHeads];  // exchange between a head's two threads: row max, then row sum
 };
 static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
 
@@ -96,21 +108,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_v, int H, int k, int HG, int C,
                      float scale_log2, float* __restrict__ opart, float2* __restrict__ ml,
                      int32_t* err) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Bars* bars = reinterpret_cast<Bars*>(smem_raw);
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + kBarBytes + 1023) & ~uintptr_t(1023));
   uint8_t* p_tile = base;
   uint8_t* stages = base + kPBytes;
-  Bars* bars = reinterpret_cast<Bars*>(stages + kStages * kStageBytes);
+  auto score_slot = [&](int s) -> uint8_t* {
+    return s < kStages ? stages + s * kStageBytes : p_tile + (s - kStages) * kStageBytes;
+  };
   volatile int* abort = &bars->abort;
 
   const int c = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSSlots; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
+    }
+    for (int s = 0; s < kVSlots; ++s) {
+      mbar_init(&bars->vfull[s], 1);
+      mbar_init(&bars->vempty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->p_full, kSoftmaxThreads);
@@ -135,25 +154,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      for (int it = 0; it < kLoads; ++it) {
-        const int s = it % kStages;
-        if (it >= kStages &&
-            !mbar_wait_bounded(&bars->empty[s], ((it / kStages) - 1) & 1, abort, kWaitLimit))
+      // score phase: kSSlots slots; slots 2 and 3 borrow the P region, which
+      // the softmax fills only after every score product has completed
+      for (int it = 0; it < kScoreLoads; ++it) {
+        const int s = it % kSSlots;
+        if (it >= kSSlots &&
+            !mbar_wait_bounded(&bars->empty[s], ((it / kSSlots) - 1) & 1, abort, kWaitLimit))
           break;
-        uint8_t* st = stages + s * kStageBytes;
-        if (it < kScoreLoads) {
-          const int kb = it % kKB, nh = it / kKB;
-          mbar_expect_tx(&bars->full[s], kStageBytes);
-          tma_load_3d(st, &tm_q, &bars->full[s], kb * 64, hg * kHeads, b);
-          tma_load_3d(st + kQBytes, &tm_k, &bars->full[s], kb * 64, c * kChunk + nh * kHalfRows, b);
-        } else {
-          const int v = it - kScoreLoads, half = v >> 3, rb = v & 7;
-          mbar_expect_tx(&bars->full[s], kVBytes);
-          for (int j = 0; j < 4; ++j)
-            tma_load_3d(st + j * kVBox, &tm_v, &bars->full[s], half * 256 + j * 64,
-                        c * kChunk + rb * 64, b);
-        }
+        uint8_t* st = score_slot(s);
+        const int kb = it % kKB, nh = it / kKB;
+        mbar_expect_tx(&bars->full[s], kStageBytes);
+        tma_load_3d(st, &tm_q, &bars->full[s], kb * 64, hg * kHeads, b);
+        tma_load_3d(st + kQBytes, &tm_k, &bars->full[s], kb * 64, c * kChunk + nh * kHalfRows, b);
         bars->issued = it + 1;
+      }
+      // value phase: kVSlots slots in the ring region, once the scores are
+      // done (their slots are free then); the first loads overlap the softmax
+      if (bars->issued == kScoreLoads &&
+          mbar_wait_bounded(&bars->s_full, 0, abort, kWaitLimit)) {
+        for (int v = 0; v < kLoads - kScoreLoads; ++v) {
+          const int s = v % kVSlots;
+          if (v >= kVSlots &&
+              !mbar_wait_bounded(&bars->vempty[s], ((v / kVSlots) - 1) & 1, abort, kWaitLimit))
+            break;
+          uint8_t* st = stages + s * kVBytes;
+          const int half = v >> 3, rb = v & 7;
+          mbar_expect_tx(&bars->vfull[s], kVBytes);
+          for (int j = 0; j < 4; ++j)
+            tma_load_3d(st + j * kVBox, &tm_v, &bars->vfull[s], half * 256 + j * 64,
+                        c * kChunk + rb * 64, b);
+          bars->issued = kScoreLoads + v + 1;
+        }
       }
     }
   } else if (warp == 1) {
@@ -163,12 +194,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_pv = idesc_bf16_f32(kHeads, 256, false, true);
       bool ok = true;
       for (int it = 0; it < kScoreLoads && ok; ++it) {
-        const int s = it % kStages;
-        ok = mbar_wait_bounded(&bars->full[s], (it / kStages) & 1, abort, kWaitLimit);
+        const int s = it % kSSlots;
+        ok = mbar_wait_bounded(&bars->full[s], (it / kSSlots) & 1, abort, kWaitLimit);
         if (!ok) break;
         tc_fence_after();
         const int kb = it % kKB, nh = it / kKB;
-        const uint32_t qa = smem_addr(stages + s * kStageBytes);
+        const uint32_t qa = smem_addr(score_slot(s));
         const uint32_t ka = qa + kQBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -181,20 +212,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait_bounded(&bars->p_full, 0, abort, kWaitLimit);
       }
       if (ok) tc_fence_after();
-      for (int it = kScoreLoads; it < kLoads && ok; ++it) {
-        const int s = it % kStages;
-        ok = mbar_wait_bounded(&bars->full[s], (it / kStages) & 1, abort, kWaitLimit);
+      for (int v = 0; v < kLoads - kScoreLoads && ok; ++v) {
+        const int s = v % kVSlots;
+        ok = mbar_wait_bounded(&bars->vfull[s], (v / kVSlots) & 1, abort, kWaitLimit);
         if (!ok) break;
         tc_fence_after();
-        const int v = it - kScoreLoads, half = v >> 3, rb = v & 7;
+        const int half = v >> 3, rb = v & 7;
         const uint32_t d = tmem + (half == 0 ? 256u : 0u);
         const uint32_t pa = smem_addr(p_tile) + rb * kPBlock;
-        const uint32_t va = smem_addr(stages + s * kStageBytes);
+        const uint32_t va = smem_addr(stages + s * kVBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_bf16(d, smem_desc_sw128(pa + kk * 32, 16, 1024),
                       smem_desc_sw128(va + kk * 2048, kVBox, 1024), id_pv, (rb | kk) != 0);
-        tc_commit(&bars->empty[s]);
+        tc_commit(&bars->vempty[s]);
       }
       if (ok) tc_commit(&bars->o_full);
     }
@@ -224,11 +255,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (col0 + cb + 32 + i < nvalid) m = fmaxf(m, __uint_as_float(r2[i]) * scale_log2);
         }
       }
-      bars->red[part][row] = m;
+      if (part == 1) bars->red[row] = m;
+    }
+    // the row max: part 1 hands its half over, part 0 combines and hands the
+    // result back (finite: column 0 is valid)
+    softmax_sync();
+    if (ok && part == 0) {
+      m = fmaxf(m, bars->red[row]);
+      bars->red[row] = m;
     }
     softmax_sync();
     if (ok) {
-      m = fmaxf(bars->red[0][row], bars->red[1][row]);  // finite: column 0 is valid
+      if (part == 1) m = bars->red[row];
       uint32_t r[32];
       for (int cb = 0; cb < kChunk / 2; cb += 32) {
         tmem_ld32(trow + col0 + cb, r);
@@ -258,11 +296,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->p_full);
     }
-    softmax_sync();  // every thread has read both halves' max
-    if (ok) bars->red[part][row] = l;
+    softmax_sync();  // part 1 has read the max
+    if (ok && part == 1) bars->red[row] = l;
     softmax_sync();
     if (ok) {
-      l = bars->red[0][row] + bars->red[1][row];
+      if (part == 0) l += bars->red[row];  // the row sum (only part 0 writes it out)
       ok = warp_wait(&bars->o_full, 0, abort);
     }
     // Epilogue: O goes through the (now idle) P tile and stage ring, 256 dims
@@ -309,10 +347,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (bars->abort) {
     if (threadIdx.x == 0) report(err, TS_DEVERR_TIMEOUT);
     if (warp == 0 && lane == 0) {
-      // let the copies already issued land before the CTA exits
+      // let the copies already issued land before the CTA exits: the last
+      // load of every slot (earlier ones completed before their slot's reuse)
       const int issued = bars->issued;
-      for (int it = issued - kStages < 0 ? 0 : issued - kStages; it < issued; ++it)
-        mbar_wait_timed(&bars->full[it % kStages], (it / kStages) & 1, kWaitLimit);
+      for (int it = issued - kSSlots < 0 ? 0 : issued - kSSlots; it < issued; ++it) {
+        if (it < kScoreLoads) {
+          mbar_wait_timed(&bars->full[it % kSSlots], (it / kSSlots) & 1, kWaitLimit);
+        } else {
+          const int v = it - kScoreLoads;
+          mbar_wait_timed(&bars->vfull[v % kVSlots], (v / kVSlots) & 1, kWaitLimit);
+        }
+      }
     }
     if (warp == 1 && lane == 0) {
       // every tcgen05 operation this thread issued completes before the free

@@ -148,17 +148,20 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
                         at(g.pool, l, lb.pool), P, at(g.host_kv, l, lb.host), g.ctx_stride,
                         g.ctx_len, at(g.sel, l, lb.sel), g.err, gs) == TS_OK &&
          rec(2 + l, 1, gs) && signal(gs, gathered + l, seq);
-  for (int l = 0; ok && l < L; ++l) {
+  // per layer: the attention on the main stream, the refill beside it on the
+  // side stream (on few SMs); the last refill also updates the metadata
+  for (int l = 0; ok && l < L; ++l)
     ok = wait_for(m, gathered + l, seq) && rec(2 + L + l, 0, m) &&
          sfa_enqueue(at(q, l, lb.q), at(g.sel, l, lb.sel), g.B, g.H, g.k, g.scale,
                      at(g.out, l, lb.out), g.lse ? at(g.lse, l, lb.lse) : nullptr, g.sfa_ws,
                      g.err, m) == TS_OK &&
-         rec(2 + L + l, 1, m) && wait_for(side, gathered + l, seq) && rec(2 + 2 * L + l, 0, side) &&
+         rec(2 + L + l, 1, m) && wait_for(side, gathered + l, seq) &&
+         rec(2 + 2 * L + l, 0, side) &&
          refill_enqueue(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k,
                         at(g.sel, l, lb.sel), at(g.pool, l, lb.pool), P, l == L - 1, g.pool_tags,
-                        g.fifo_ptr, g.ptr_next, g.S, g.W, g.err, side) == TS_OK &&
+                        g.fifo_ptr, g.ptr_next, g.S, g.W, g.err, side, 1, lb.sel,
+                        lb.pool) == TS_OK &&
          rec(2 + 2 * L + l, 1, side);
-  }
   ok = ok && signal(side, refilled, seq);
   if (!ok) {
     // give every word this step's number, so that no wait enqueued now or by

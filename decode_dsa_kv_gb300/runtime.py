@@ -21,7 +21,7 @@ library's `sync` words), polled by the GPU's front end in HBM.
 The plan is shared by the group, so every layer's gather can start as soon as
 it exists: the host-link transfers of layer l+1 overlap the attention of
 layer l, and each layer's attention still starts the moment its own rows are
-in (SFA first). Memory and streams come from PyTorch; this module only fills
+in (SFA first); each refill runs beside its layer's attention on a few SMs. Memory and streams come from PyTorch; this module only fills
 the descriptor; the arithmetic runs in libdsakv's kernels.
 """
 from __future__ import annotations

@@ -229,28 +229,28 @@ ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int H, int k,
 /* ---------------------------------------------------------------------------
  * dsa_group_step -- one decode step of an IndexShare group of `layers` layers,
  * enqueued by one call ([GLM] §5.1 model-side orchestration: one plan per
- * group, per-layer serve, refill on a side stream ordered after the serve,
- * metadata update at the group's last layer; §4.4 SFA first, refill later).
- * On the caller's three streams it issues:
+ * group, per-layer serve, refill on a side stream, metadata update at the
+ * group's last layer; §4.4 SFA first, refill later). On the caller's three
+ * streams it issues:
  *
  *   main   : ts_topk(scores) -> wait refilled -> dsa_plan -> signal planned
  *            -> for each layer l: wait gathered[l] -> sfa_mla_decode(l)
  *   gather : wait planned -> for each layer l: dsa_gather_kv(l), signal
  *            gathered[l]
  *   side   : for each layer l: wait gathered[l] -> dsa_refill_pool(l) (the
- *            last layer also updates tags and FIFO pointers) -> after the
- *            last layer, signal refilled
+ *            last layer also updates tags and FIFO pointers); then signal
+ *            refilled
  *
  * Signals and waits are stream memory operations on the caller's device
  * words `sync` (cuStreamWriteValue32 / cuStreamWaitValue32 with the step's
  * sequence number, compared wrap-around): the GPU's front end polls device
- * memory, with no event round trip. Ordering: refill(l) evicts slots gather(l)
- * reads, so it waits for gather(l); the next step's plan reads the tags the
- * last refill writes, so it waits for `refilled`; the next step's gather(l)
- * rewrites sel[l], which sfa(l) and refill(l) of this step read: it waits for
- * the next plan, which follows every sfa on the main stream and the last
- * refill. Every wait is enqueued after the signal it waits for, so every wait
- * ends.
+ * memory, with no event round trip. Ordering: refill(l) evicts slots
+ * gather(l) reads, so it waits for gather(l). The next step's plan reads the
+ * tags the last refill writes, so it waits for `refilled`; the next step's
+ * gather(l) rewrites sel[l], which sfa(l) and refill(l) of this step read: it
+ * waits for the next plan, which follows every sfa on the main stream and
+ * every refill. Every wait is enqueued after the signal it waits for, so
+ * every wait ends.
  *
  * The descriptor holds the group's buffers (the caller owns all of them):
  *   ctx_len   int32 [B]                     k <= ctx_len[b] <= max_ctx

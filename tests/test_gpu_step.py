@@ -1,6 +1,6 @@
 """Whole decode steps through the per-step schedule (top-k, one plan per group,
-per-layer gather + SFA on the main stream, refill on the side stream, metadata
-at the group's last layer), compared with the oracle run step by step on the
+per-layer gather and SFA, then the refill of every layer with the metadata
+update on the side stream), compared with the oracle run step by step on the
 same seeded inputs: bit-exact ids, plan, selection bytes and pool state; SFA
 within tolerance."""
 import math
