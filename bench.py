@@ -39,8 +39,8 @@ METRIC = "selected KV rows/s per decode step (plan+gather+SFA); % of HBM/link ro
 UNIT = "rows/s"
 KERNELS = ("topk", "plan", "gather", "sfa", "refill")
 # our kernels per step: top-k (1: one cluster per request, or 2: histogram + select)
-# + plan 1 + layers x (gather 1 + sfa 2 + refill 1)
-LAUNCHES_PLAN, LAUNCHES_PER_LAYER = 1, 4
+# + plan 1 + gather 1 (every layer) + layers x (sfa 2 + refill 1)
+LAUNCHES_PLAN, LAUNCHES_GATHER, LAUNCHES_PER_LAYER = 1, 1, 3
 
 
 def topk_launches(w) -> int:
@@ -301,8 +301,9 @@ def algorithmic(w: wl.Workload, lens, hit_frac: float, install_frac: float):
     out["topk"] = {"hbm_bytes": float(np.sum(lens)) * 4 + rows * 4, "link_bytes": 0.0}
     out["plan"] = {"hbm_bytes": rows * (4 + 4) + w.B * (w.P * 4 + 2 * w.S * 4)
                    + rows * (1 - hit_frac) * (4 * 3 + 1), "link_bytes": 0.0}
-    out["gather"] = {"hbm_bytes": rows * (hit_frac * row + row + 4),
-                     "link_bytes": rows * (1 - hit_frac) * row}
+    # one launch gathers every layer
+    out["gather"] = {"hbm_bytes": w.layers * rows * (hit_frac * row + row + 4),
+                     "link_bytes": w.layers * rows * (1 - hit_frac) * row}
     out["refill"] = {"hbm_bytes": rows * install_frac * (2 * row + 13), "link_bytes": 0.0}
     out["sfa"] = {"hbm_bytes": rows * row + w.B * w.H * (1152 + 1024),
                   "link_bytes": 0.0, "flops": 2.0 * w.B * w.H * w.k * (576 + 512)}
@@ -585,7 +586,7 @@ def run_native(args, w, rank, world, local):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * (topk_launches(w) + LAUNCHES_PLAN
-                                      + w.layers * LAUNCHES_PER_LAYER),
+                                      + LAUNCHES_GATHER + w.layers * LAUNCHES_PER_LAYER),
         "clocks": clocks,
         "hit_rate": hit_frac,
         "host_enqueue_ms_per_step": (t_enq1 - t_enq0) * 1e3 / args.steps,
@@ -635,7 +636,8 @@ def run_only(args, w, g, scores, q, peaks, link, lens, host, rank):
     if g.synchronize():
         raise RuntimeError("device error")
     ms = e0.elapsed_time(e1) / args.steps
-    alg = algorithmic(w, lens, hit, 1.0 - hit)[args.only]
+    # the per-layer entry points move one layer per launch
+    alg = algorithmic(wl.scaled(w, layers=1), lens, hit, 1.0 - hit)[args.only]
     rf = roofline_of(args.only, alg, ms, peaks, link)
     host.close()
     if rank == 0:

@@ -42,6 +42,8 @@ _SIGS = {
     "ts_status_string": (ctypes.c_char_p, [_I]),
     "ts_host_register": (_I, [_P, _SZ, ctypes.POINTER(ctypes.c_void_p)]),
     "ts_host_unregister": (_I, [_P]),
+    "ts_host_alloc": (_I, [_SZ, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p)]),
+    "ts_host_free": (_I, [_P]),
     "ts_copy": (_I, [_P, _P, _SZ, _P]),
     "ts_read_error": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "ts_topk_workspace_size": (_SZ, [_I, _I, _I]),
@@ -137,6 +139,18 @@ def ts_host_register(host_addr: int, nbytes: int) -> int:
 
 def ts_host_unregister(host_addr: int) -> int:
     return _lib.ts_host_unregister(host_addr)
+
+
+def ts_host_alloc(nbytes: int) -> tuple[int, int]:
+    """Page-locked, device-mapped host memory; returns (host, device) addresses."""
+    host = ctypes.c_void_p()
+    dev = ctypes.c_void_p()
+    check(_lib.ts_host_alloc(nbytes, ctypes.byref(host), ctypes.byref(dev)), "ts_host_alloc")
+    return int(host.value), int(dev.value)
+
+
+def ts_host_free(host_addr: int) -> int:
+    return _lib.ts_host_free(host_addr)
 
 
 def ts_copy(dst, src, nbytes: int, stream=None) -> int:

@@ -38,6 +38,33 @@ extern "C" ts_status ts_host_unregister(void* host) {
   return TS_OK;
 }
 
+extern "C" ts_status ts_host_alloc(size_t bytes, void** host, void** dev) {
+  if (!host || !dev || bytes == 0) return TS_ERR_INVALID_ARG;
+  *host = nullptr;
+  *dev = nullptr;
+  void* h = nullptr;
+  if (cudaHostAlloc(&h, bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+    cudaGetLastError();
+    return TS_ERR_CUDA;
+  }
+  if (cudaHostGetDevicePointer(dev, h, 0) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFreeHost(h);
+    return TS_ERR_CUDA;
+  }
+  *host = h;
+  return TS_OK;
+}
+
+extern "C" ts_status ts_host_free(void* host) {
+  if (!host) return TS_ERR_INVALID_ARG;
+  if (cudaFreeHost(host) != cudaSuccess) {
+    cudaGetLastError();
+    return TS_ERR_CUDA;
+  }
+  return TS_OK;
+}
+
 extern "C" ts_status ts_read_error(int32_t* err, int32_t* bits, cudaStream_t stream) {
   if (!err || !bits) return TS_ERR_INVALID_ARG;
   int32_t v = 0;

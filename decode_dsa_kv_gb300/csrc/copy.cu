@@ -73,118 +73,168 @@ __device__ __forceinline__ void warp_copy_rows2(const uint4* from0, uint4* to0, 
   }
 }
 
-// One launch, two kinds of warps (alternating), each moving two rows per step:
-//   even warps walk the compact miss lists, concatenated over the requests
-//     and dealt out evenly: host row miss_ids[i] -> sel[miss_pos[i]] (the
-//     host-link reads, which set the kernel's time);
-//   odd warps walk the positions: pool row for a hit; for a miss, the host row
-//     only when that token repeats in the selection and this is not its first
-//     position (the even warps serve first positions). Requests without
-//     repeats (miss_rows == miss_count) skip misses outright.
-// The two kinds write disjoint positions and run side by side, so the HBM
-// copies of the hits hide under the host-link time of the misses.
+// Row lists of one layer, for one warp of a role (see gather_kernel).
+struct GatherLayer {
+  const uint4* pool;
+  const uint4* host;
+  uint4* sel;
+};
+
+// The misses of all requests, concatenated: the warp takes miss indices
+// m = w, w + nrole, ... (request b holds miss_count[b] of them), so every miss
+// warp gets the same number of host rows whatever the spread of misses over
+// requests. Looked up 32 at a time, one candidate per lane; `mask` holds the
+// lanes with a row to move.
+__device__ __forceinline__ void gather_misses(const GatherLayer& L, const int32_t* miss_ids,
+                                              const int32_t* miss_pos, const int32_t* miss_count,
+                                              int B, int k, int64_t ctx_stride,
+                                              const int32_t* ctx_len, int w, int nrole, int lane,
+                                              int& bad) {
+  // indices below B * k < 2^31 (B <= 65535, k <= 8192) fit in 32 bits
+  const uint4* host = L.host;
+  uint4* sel = L.sel;
+  int m1 = w, base1 = 0;
+  int b1 = 0, cnt1 = __ldg(miss_count);
+  uint32_t mask = 0;
+  const uint4* my_from = nullptr;
+  uint4* my_to = nullptr;
+  for (;;) {
+    if (mask == 0) {
+      if (b1 >= B) break;
+      const int ml = m1 + lane * nrole;
+      int b = b1, cnt = cnt1, base = base1;
+      while (b < B && ml >= base + cnt) {
+        base += cnt;
+        if (++b < B) cnt = __ldg(miss_count + b);
+      }
+      bool valid = false;
+      if (b < B) {
+        const int i = ml - base;
+        const bool in = i >= 0 && i < k;  // (a count past k is corrupt)
+        const int64_t s = int64_t(b) * k + i;
+        const int t = in ? __ldg(miss_ids + s) : -1;
+        const int j = in ? __ldg(miss_pos + s) : -1;
+        if (t < 0 || t >= __ldg(ctx_len + b) || t >= ctx_stride || j < 0 || j >= k) {
+          bad |= TS_DEVERR_ID_RANGE;
+        } else {
+          my_from = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
+          my_to = sel + (int64_t(b) * k + j) * DSA_ROW_CHUNKS;
+          valid = true;
+        }
+      }
+      mask = __ballot_sync(0xffffffffu, valid);
+      // lane 31 holds the furthest index: the walk resumes from there
+      b1 = __shfl_sync(0xffffffffu, b, 31);
+      cnt1 = __shfl_sync(0xffffffffu, cnt, 31);
+      base1 = __shfl_sync(0xffffffffu, base, 31);
+      m1 += 32 * nrole;
+      continue;
+    }
+    const uint4* from[2] = {nullptr, nullptr};
+    uint4* to[2] = {nullptr, nullptr};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      if (mask) {
+        const int q = __ffs(mask) - 1;
+        mask &= mask - 1;
+        from[e] = reinterpret_cast<const uint4*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_from), q));
+        to[e] = reinterpret_cast<uint4*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_to), q));
+      }
+    }
+    warp_copy_rows2(from[0], to[0], from[1], to[1], lane);
+  }
+}
+
+// The positions: the pool row for a hit; for a miss, the host row only when
+// the token repeats and this is not its first position (gather_misses serves
+// first positions). Requests without repeats (miss_rows == miss_count) skip
+// misses outright.
+__device__ __forceinline__ void gather_positions(const GatherLayer& L, const int32_t* src_map,
+                                                 const int32_t* miss_ids, const int32_t* miss_pos,
+                                                 const int32_t* miss_count,
+                                                 const int32_t* miss_rows, int B, int k, int P,
+                                                 int64_t ctx_stride, const int32_t* ctx_len,
+                                                 int w, int nrole, int lane, int& bad) {
+  const uint4* pool = L.pool;
+  const uint4* host = L.host;
+  uint4* sel = L.sel;
+  const int64_t rows = int64_t(B) * k;
+  for (int64_t r0 = int64_t(w) * 2; r0 < rows; r0 += int64_t(nrole) * 2) {
+    const uint4* from[2] = {nullptr, nullptr};
+    uint4* to[2] = {nullptr, nullptr};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int64_t r = r0 + e;
+      if (r >= rows) continue;
+      const int b = static_cast<int>(r / k);
+      const int j = static_cast<int>(r - int64_t(b) * k);
+      const int src = __ldg(src_map + r);
+      if (src >= 0) {
+        if (src < P) from[e] = pool + (int64_t(b) * P + src) * DSA_ROW_CHUNKS;
+        else bad |= TS_DEVERR_SLOT_RANGE;
+      } else if (src != INT_MIN) {
+        const int M = __ldg(miss_count + b);
+        if (__ldg(miss_rows + b) == M) continue;  // no repeats: served as a miss
+        const int t = -1 - src;
+        const int64_t base = int64_t(b) * k;
+        if (first_pos_of(miss_ids + base, miss_pos + base, M, t) == j) continue;
+        if (t < __ldg(ctx_len + b) && t < ctx_stride)
+          from[e] = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
+        else bad |= TS_DEVERR_ID_RANGE;
+      } else {
+        bad |= TS_DEVERR_ID_RANGE;
+      }
+      if (from[e]) to[e] = sel + r * DSA_ROW_CHUNKS;
+    }
+    warp_copy_rows2(from[0], to[0], from[1], to[1], lane);
+  }
+}
+
+// One launch for `layers` consecutive layers (layer l's pool, host rows and
+// selection start l * pool_stride / host_stride / sel_stride pieces after
+// layer 0's), two kinds of warps (alternating), each moving two rows per step:
+//   even warps: gather_misses, the host-link reads that set the kernel's time;
+//   odd warps: gather_positions, the pool hits (HBM), beside them.
+// The two kinds write disjoint positions, so the HBM copies of the hits hide
+// under the host-link time of the misses. Every warp finishes a layer before
+// it starts the next. With `done` given, each warp counts itself out of
+// layer l in count[l] once its rows are written (after a fence), and the last
+// one resets the count and writes `seq` into done[l]: another stream's
+// stream-memory wait on done[l] then orders the layer's consumers after its
+// rows. The launch's own completion orders them for the per-layer call.
 __global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(
     const int32_t* __restrict__ src_map, const int32_t* __restrict__ miss_ids,
     const int32_t* __restrict__ miss_pos, const int32_t* __restrict__ miss_count,
     const int32_t* __restrict__ miss_rows, int B, int k, const uint4* __restrict__ pool, int P,
     const uint4* __restrict__ host, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
-    uint4* __restrict__ sel, int32_t* err) {
+    uint4* __restrict__ sel, int layers, int64_t pool_stride, int64_t host_stride,
+    int64_t sel_stride, uint32_t* __restrict__ done, uint32_t* __restrict__ count, uint32_t seq,
+    int32_t* err) {
   const int lane = threadIdx.x & 31;
-  const int64_t gw = (int64_t(blockIdx.x) * kGatherThreads + threadIdx.x) >> 5;
-  const int64_t nw = (int64_t(gridDim.x) * kGatherThreads) >> 5;
-  const int64_t rows = int64_t(B) * k;
+  const int gw = static_cast<int>((blockIdx.x * kGatherThreads + threadIdx.x) >> 5);
+  const int nw = static_cast<int>((gridDim.x * kGatherThreads) >> 5);
   const bool miss_warp = (gw & 1) == 0;
-  const int64_t w = gw >> 1;
-  const int64_t nrole = miss_warp ? (nw + 1) >> 1 : nw >> 1;
+  const int w = gw >> 1;
+  const int nrole = miss_warp ? (nw + 1) >> 1 : nw >> 1;
   int bad = 0;
-  if (miss_warp) {
-    // The misses of all requests, concatenated: this warp takes miss indices
-    // m = w, w + nrole, ... (request b holds miss_count[b] of them), so every
-    // miss warp gets the same number of host rows whatever the spread of
-    // misses over requests. Looked up 32 at a time, one candidate per lane;
-    // `mask` holds the lanes with a row to move.
-    int64_t m1 = w, base1 = 0;
-    int b1 = 0, cnt1 = __ldg(miss_count);
-    uint32_t mask = 0;
-    const uint4* my_from = nullptr;
-    uint4* my_to = nullptr;
-    for (;;) {
-      if (mask == 0) {
-        if (b1 >= B) break;
-        const int64_t ml = m1 + int64_t(lane) * nrole;
-        int b = b1, cnt = cnt1;
-        int64_t base = base1;
-        while (b < B && ml >= base + cnt) {
-          base += cnt;
-          if (++b < B) cnt = __ldg(miss_count + b);
-        }
-        bool valid = false;
-        if (b < B) {
-          const int i = static_cast<int>(ml - base);
-          const bool in = i >= 0 && i < k;  // (a count past k is corrupt)
-          const int64_t s = int64_t(b) * k + i;
-          const int t = in ? __ldg(miss_ids + s) : -1;
-          const int j = in ? __ldg(miss_pos + s) : -1;
-          if (t < 0 || t >= __ldg(ctx_len + b) || t >= ctx_stride || j < 0 || j >= k) {
-            bad |= TS_DEVERR_ID_RANGE;
-          } else {
-            my_from = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
-            my_to = sel + (int64_t(b) * k + j) * DSA_ROW_CHUNKS;
-            valid = true;
-          }
-        }
-        mask = __ballot_sync(0xffffffffu, valid);
-        // lane 31 holds the furthest index: the walk resumes from there
-        b1 = __shfl_sync(0xffffffffu, b, 31);
-        cnt1 = __shfl_sync(0xffffffffu, cnt, 31);
-        base1 = __shfl_sync(0xffffffffu, base, 31);
-        m1 += 32 * nrole;
-        continue;
+  for (int l = 0; l < layers; ++l) {
+    const GatherLayer L{pool + l * pool_stride, host + l * host_stride, sel + l * sel_stride};
+    if (miss_warp)
+      gather_misses(L, miss_ids, miss_pos, miss_count, B, k, ctx_stride, ctx_len, w, nrole, lane,
+                    bad);
+    else
+      gather_positions(L, src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, P,
+                       ctx_stride, ctx_len, w, nrole, lane, bad);
+    if (done) {
+      __threadfence();  // this lane's rows, before the warp counts itself out
+      __syncwarp();
+      if (lane == 0 && atomicAdd(count + l, 1u) == static_cast<uint32_t>(nw) - 1) {
+        __threadfence();
+        count[l] = 0;
+        atomicExch(done + l, seq);
       }
-      const uint4* from[2] = {nullptr, nullptr};
-      uint4* to[2] = {nullptr, nullptr};
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        if (mask) {
-          const int q = __ffs(mask) - 1;
-          mask &= mask - 1;
-          from[e] = reinterpret_cast<const uint4*>(
-              __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_from), q));
-          to[e] = reinterpret_cast<uint4*>(
-              __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_to), q));
-        }
-      }
-      warp_copy_rows2(from[0], to[0], from[1], to[1], lane);
-    }
-  } else {
-    for (int64_t r0 = w * 2; r0 < rows; r0 += nrole * 2) {
-      const uint4* from[2] = {nullptr, nullptr};
-      uint4* to[2] = {nullptr, nullptr};
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int64_t r = r0 + e;
-        if (r >= rows) continue;
-        const int b = static_cast<int>(r / k);
-        const int j = static_cast<int>(r - int64_t(b) * k);
-        const int src = __ldg(src_map + r);
-        if (src >= 0) {
-          if (src < P) from[e] = pool + (int64_t(b) * P + src) * DSA_ROW_CHUNKS;
-          else bad |= TS_DEVERR_SLOT_RANGE;
-        } else if (src != INT_MIN) {
-          const int M = __ldg(miss_count + b);
-          if (__ldg(miss_rows + b) == M) continue;  // no repeats: served by a miss warp
-          const int t = -1 - src;
-          const int64_t base = int64_t(b) * k;
-          if (first_pos_of(miss_ids + base, miss_pos + base, M, t) == j) continue;
-          if (t < __ldg(ctx_len + b) && t < ctx_stride)
-            from[e] = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
-          else bad |= TS_DEVERR_ID_RANGE;
-        } else {
-          bad |= TS_DEVERR_ID_RANGE;
-        }
-        if (from[e]) to[e] = sel + r * DSA_ROW_CHUNKS;
-      }
-      warp_copy_rows2(from[0], to[0], from[1], to[1], lane);
     }
   }
   if (bad && lane == 0) report(err, bad);
@@ -276,21 +326,26 @@ ts_status gather_check(const int32_t* src_map, const int32_t* miss_ids, const in
 ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const int32_t* miss_pos,
                          const int32_t* miss_count, const int32_t* miss_rows, int B, int k,
                          const void* pool_l, int P, const void* host_l, int64_t ctx_stride,
-                         const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream) {
-  // A quarter of the SMs, one 1024-thread CTA each, keep a few MB of loads in
-  // flight, which saturates the host link (measured); the other SMs stay free
-  // for the attention of the previous layer, which runs beside the gather.
-  // Measured alternatives that did worse: small CTAs on every SM (the zero-copy
-  // loads slow an attention CTA on the same SM by about 2x), and cp.async
-  // staging through shared memory (reads of host memory top out near half
-  // the link's rate that way).
+                         const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream,
+                         int layers, size_t pool_layer_bytes, size_t host_layer_bytes,
+                         size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq) {
+  // 3/8 of the SMs, one 1024-thread CTA each: with the attention and the
+  // refill running beside it the host link needs this many loads in flight
+  // (measured on decode_batch, whole step: 1/4 of the SMs 584 us, 1/3 554,
+  // 3/8 544, 1/2 561: beyond 3/8 the attention, on the other SMs, runs
+  // short). Measured alternatives that did worse: small CTAs on every SM (the
+  // zero-copy loads slow an attention CTA on the same SM by about 2x), and
+  // cp.async staging through shared memory (reads of host memory top out near
+  // half the link's rate that way).
   const int64_t rows = int64_t(B) * k;
   int64_t blocks = (rows + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
-  const int64_t cap = sm_count() / 4 > 8 ? sm_count() / 4 : 8;
+  const int64_t cap = sm_count() * 3 / 8 > 8 ? sm_count() * 3 / 8 : 8;
   if (blocks > cap) blocks = cap;
   gather_kernel<<<static_cast<unsigned>(blocks), kGatherThreads, 0, stream>>>(
       src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, static_cast<const uint4*>(pool_l), P,
-      static_cast<const uint4*>(host_l), ctx_stride, ctx_len, static_cast<uint4*>(sel_l), err);
+      static_cast<const uint4*>(host_l), ctx_stride, ctx_len, static_cast<uint4*>(sel_l), layers,
+      int64_t(pool_layer_bytes / 16), int64_t(host_layer_bytes / 16), int64_t(sel_layer_bytes / 16),
+      done, count, seq, err);
   return launch_status();
 }
 
@@ -341,7 +396,8 @@ extern "C" ts_status dsa_gather_kv(const int32_t* src_map, const int32_t* miss_i
                                            k, pool_l, P, host_l, ctx_stride, ctx_len, sel_l);
   if (st != TS_OK) return st;
   return dsakv::gather_enqueue(src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, pool_l,
-                               P, host_l, ctx_stride, ctx_len, sel_l, err, stream);
+                               P, host_l, ctx_stride, ctx_len, sel_l, err, stream, 1, 0, 0, 0,
+                               nullptr, nullptr, 0);
 }
 
 extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* miss_pos,

@@ -30,10 +30,17 @@ ts_status gather_check(const int32_t* src_map, const int32_t* miss_ids, const in
                        const int32_t* miss_count, const int32_t* miss_rows, int B, int k,
                        const void* pool_l, int P, const void* host_l, int64_t ctx_stride,
                        const int32_t* ctx_len, void* sel_l);
+// `layers` consecutive layers in one launch (layer l's pool, host rows and
+// selection start l * *_layer_bytes after pool_l / host_l / sel_l). With
+// `done` non-null the kernel writes seq into done[l] once layer l's rows are
+// all written (count: `layers` device words, zero between launches; the
+// kernel leaves them zero).
 ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const int32_t* miss_pos,
                          const int32_t* miss_count, const int32_t* miss_rows, int B, int k,
                          const void* pool_l, int P, const void* host_l, int64_t ctx_stride,
-                         const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream);
+                         const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream,
+                         int layers, size_t pool_layer_bytes, size_t host_layer_bytes,
+                         size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq);
 
 ts_status refill_check(const int32_t* miss_ids, const int32_t* miss_pos, const int32_t* victim,
                        const uint8_t* install, const int32_t* miss_count, int B, int k,

@@ -4,12 +4,13 @@
 // the cross-stream signals and their proof of termination are the ones the
 // header states; every argument is checked before the first launch.
 //
-// Cross-stream ordering uses stream memory operations on device words: a
-// signal is a 32-bit write of the step's sequence number issued on the
-// producing stream (it lands when the stream's prior work is complete), a
-// wait blocks the consuming stream until the word, compared wrap-around, has
-// reached that number. The words live in HBM, so the front end that polls
-// them never crosses the host link.
+// Cross-stream ordering uses device words holding the step's sequence number:
+// a signal is a stream memory write issued on the producing stream (it lands
+// when the stream's prior work is complete) or, for the per-layer gather
+// signals, a write by the gather kernel itself once a layer's rows are in; a
+// wait is a stream memory wait that blocks the consuming stream until the
+// word, compared wrap-around, has reached that number. No kernel waits on
+// another: only the streams' front end polls the words, in HBM.
 #include <cuda.h>
 
 #include <type_traits>
@@ -126,6 +127,7 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
   uint32_t* planned = g.sync + kPlanned;
   uint32_t* refilled = g.sync + kRefilled;
   uint32_t* gathered = g.sync + kGathered;
+  uint32_t* counts = g.sync + kGathered + L;  // the gather's per-layer warp counts
   auto rec = [&](int slot, int end, cudaStream_t s) {
     return timing ? cudaEventRecord(timing[2 * slot + end], s) == cudaSuccess : true;
   };
@@ -142,30 +144,31 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
                     g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.miss_rows,
                     g.ptr_next, g.err, m) == TS_OK &&
        rec(1, 1, m) && signal(m, planned, seq) && wait_for(gs, planned, seq);
-  for (int l = 0; ok && l < L; ++l)
-    ok = rec(2 + l, 0, gs) &&
-         gather_enqueue(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k,
-                        at(g.pool, l, lb.pool), P, at(g.host_kv, l, lb.host), g.ctx_stride,
-                        g.ctx_len, at(g.sel, l, lb.sel), g.err, gs) == TS_OK &&
-         rec(2 + l, 1, gs) && signal(gs, gathered + l, seq);
+  // one launch gathers every layer and writes seq into gathered[l] from the
+  // device as soon as layer l's rows are in (no ramp between layers)
+  ok = ok && rec(2, 0, gs) &&
+       gather_enqueue(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k,
+                      g.pool, P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel, g.err, gs, L, lb.pool,
+                      lb.host, lb.sel, gathered, counts, seq) == TS_OK &&
+       rec(2, 1, gs);
   // per layer: the attention on the main stream, the refill beside it on the
-  // side stream (on few SMs); the last refill also updates the metadata
+  // side stream; the last refill also updates the metadata
   for (int l = 0; ok && l < L; ++l)
-    ok = wait_for(m, gathered + l, seq) && rec(2 + L + l, 0, m) &&
+    ok = wait_for(m, gathered + l, seq) && rec(3 + l, 0, m) &&
          sfa_enqueue(at(q, l, lb.q), at(g.sel, l, lb.sel), g.B, g.H, g.k, g.scale,
                      at(g.out, l, lb.out), g.lse ? at(g.lse, l, lb.lse) : nullptr, g.sfa_ws,
                      g.err, m) == TS_OK &&
-         rec(2 + L + l, 1, m) && wait_for(side, gathered + l, seq) &&
-         rec(2 + 2 * L + l, 0, side) &&
+         rec(3 + l, 1, m) && wait_for(side, gathered + l, seq) &&
+         rec(3 + L + l, 0, side) &&
          refill_enqueue(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k,
                         at(g.sel, l, lb.sel), at(g.pool, l, lb.pool), P, l == L - 1, g.pool_tags,
                         g.fifo_ptr, g.ptr_next, g.S, g.W, g.err, side, 1, lb.sel,
                         lb.pool) == TS_OK &&
-         rec(2 + 2 * L + l, 1, side);
+         rec(3 + L + l, 1, side);
   ok = ok && signal(side, refilled, seq);
   if (!ok) {
-    // give every word this step's number, so that no wait enqueued now or by
-    // the next call is left without its signal
+    // give every signal word this step's number, so that no wait enqueued
+    // now or by the next call is left without its signal
     for (int i = 0; i < kGathered + L; ++i) signal(side, g.sync + i, seq);
     return TS_ERR_CUDA;
   }

@@ -9,14 +9,14 @@ per step:
   main stream   : ts_topk -> [wait refilled of the previous step] -> dsa_plan
                   -> signal planned
                   -> for each layer l: [wait gathered[l]] -> sfa_mla_decode(l)
-  gather stream : [wait planned] -> dsa_gather_kv(0..3), signalling gathered[l]
-                  after each layer
+  gather stream : [wait planned] -> one gather launch for layers 0..3; the
+                  kernel signals gathered[l] as soon as layer l's rows are in
   side stream   : for each layer l: [wait gathered[l]] -> dsa_refill_pool(l)
                   (the last layer also updates tags and FIFO pointers)
                   -> signal refilled
 
-Signals and waits are stream memory operations on device words (the
-library's `sync` words), polled by the GPU's front end in HBM.
+Waits are stream memory operations on device words (the library's `sync`
+words), polled by the GPU's front end in HBM; no kernel waits on another.
 
 The plan is shared by the group, so every layer's gather can start as soon as
 it exists: the host-link transfers of layer l+1 overlap the attention of
@@ -68,24 +68,38 @@ class PinnedHost:
 
 class HostKV:
     """Full latent KV of a group in pinned host memory, read in place by the
-    gather: uint16 (bf16 bits) [layers][B][ctx_stride][576]."""
+    gather: uint16 (bf16 bits) [layers][B][ctx_stride][576]. By default the
+    memory comes from ts_host_alloc (the gathers read it fastest); a caller's
+    own C-contiguous array is registered instead."""
 
     def __init__(self, layers: int, B: int, ctx_stride: int, array: np.ndarray | None = None):
         shape = (layers, B, ctx_stride, D)
-        self.array = np.zeros(shape, dtype=np.uint16) if array is None else array
-        assert self.array.shape == shape and self.array.dtype == np.uint16
-        assert self.array.flags["C_CONTIGUOUS"]
         self.layers, self.B, self.ctx_stride = layers, B, ctx_stride
-        self._host = self.array.ctypes.data
-        self.dev = abi.ts_host_register(self._host, self.array.nbytes)
         self.layer_bytes = B * ctx_stride * D * 2
+        nbytes = layers * self.layer_bytes
+        if array is None:
+            self._host, self.dev = abi.ts_host_alloc(nbytes)
+            self._owned = True
+            buf = (ctypes.c_uint16 * (nbytes // 2)).from_address(self._host)
+            self.array = np.frombuffer(buf, dtype=np.uint16).reshape(shape)
+        else:
+            assert array.shape == shape and array.dtype == np.uint16
+            assert array.flags["C_CONTIGUOUS"]
+            self.array = array
+            self._host = array.ctypes.data
+            self.dev = abi.ts_host_register(self._host, array.nbytes)
+            self._owned = False
 
     def layer_ptr(self, l: int) -> int:
         return self.dev + l * self.layer_bytes
 
     def close(self):
         if self._host:
-            abi.ts_host_unregister(self._host)
+            self.array = None
+            if self._owned:
+                abi.ts_host_free(self._host)
+            else:
+                abi.ts_host_unregister(self._host)
             self._host = 0
 
     def __del__(self):
@@ -98,11 +112,11 @@ class HostKV:
 class StepTiming:
     """CUDA timing events for the launches of one step, created (and recorded
     once, which makes them valid) ahead of use, in the order dsa_group_step
-    fills them: top-k, plan, gather[l], sfa[l], refill[l]."""
+    fills them: top-k, plan, gather (every layer), sfa[l], refill[l]."""
 
     def __init__(self, layers: int, stream=None):
         self.layers = layers
-        n = 2 * (2 + 3 * layers)
+        n = 2 * (3 + 2 * layers)
         st = torch.cuda.current_stream() if stream is None else stream
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         for e in self.events:
@@ -119,9 +133,9 @@ class StepTiming:
             return ev[2 * i].elapsed_time(ev[2 * i + 1])
 
         out = {"topk": [pair(0)] if self.with_topk else [], "plan": [pair(1)]}
-        out["gather"] = [pair(2 + l) for l in range(L)]
-        out["sfa"] = [pair(2 + L + l) for l in range(L)]
-        out["refill"] = [pair(2 + 2 * L + l) for l in range(L)]
+        out["gather"] = [pair(2)]
+        out["sfa"] = [pair(3 + l) for l in range(L)]
+        out["refill"] = [pair(3 + L + l) for l in range(L)]
         return out
 
     def spans(self, t0) -> dict:
@@ -133,9 +147,9 @@ class StepTiming:
             return (t0.elapsed_time(ev[2 * i]) * 1e3, t0.elapsed_time(ev[2 * i + 1]) * 1e3)
 
         out = {"topk": [span(0)] if self.with_topk else [], "plan": [span(1)]}
-        out["gather"] = [span(2 + l) for l in range(L)]
-        out["sfa"] = [span(2 + L + l) for l in range(L)]
-        out["refill"] = [span(2 + 2 * L + l) for l in range(L)]
+        out["gather"] = [span(2)]
+        out["sfa"] = [span(3 + l) for l in range(L)]
+        out["refill"] = [span(3 + L + l) for l in range(L)]
         return out
 
 
@@ -186,7 +200,7 @@ class DecodeGroup:
         self.side = torch.cuda.Stream(device=dev, priority=0)
         # cross-stream signals: device words written and waited on by the
         # streams themselves (zero before the first step)
-        self.sync = torch.zeros((2 + layers,), **i32)
+        self.sync = torch.zeros((2 + 2 * layers,), **i32)
         self.desc = self._descriptor()
 
     def _descriptor(self):
