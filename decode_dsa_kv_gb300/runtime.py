@@ -39,24 +39,42 @@ DV = 512
 
 
 class PinnedHost:
-    """A page-locked host buffer owned by numpy and registered with the CUDA
-    driver (cudaHostRegister through ts_host_register). Used instead of
-    cudaHostAlloc'd memory for every host buffer the device touches: on this
-    GB300 platform the first zero-copy read after a large DMA from
-    cudaHostAlloc'd memory stalled for about a hundred milliseconds, which
-    registered memory does not do."""
+    """A page-locked host buffer the device reads and writes in place, seen as
+    a numpy array (zero-filled). kind="alloc" (default): ts_host_alloc memory,
+    which the SMs read and write fastest (ts_copy, gathers); kind="register":
+    numpy memory registered with ts_host_register, for buffers that DMA copies
+    read (on GB300, zero-copy reads stalled for a while after a large DMA from
+    ts_host_alloc memory; not after one from registered memory)."""
 
-    def __init__(self, shape, dtype):
-        self.array = np.zeros(shape, dtype=dtype)
-        self._host = self.array.ctypes.data
-        self.dev = abi.ts_host_register(self._host, self.array.nbytes) if self.array.nbytes else 0
+    def __init__(self, shape, dtype, kind: str = "alloc"):
+        nbytes = int(np.prod(shape)) * np.dtype(dtype).itemsize
+        self.kind = kind
+        self._host = 0
+        self.dev = 0
+        if nbytes == 0:
+            self.array = np.zeros(shape, dtype=dtype)
+        elif kind == "alloc":
+            self._host, self.dev = abi.ts_host_alloc(nbytes)
+            buf = (ctypes.c_uint8 * nbytes).from_address(self._host)
+            self.array = np.frombuffer(buf, dtype=dtype).reshape(shape)
+            self.array[...] = 0
+        elif kind == "register":
+            self.array = np.zeros(shape, dtype=dtype)
+            self._host = self.array.ctypes.data
+            self.dev = abi.ts_host_register(self._host, nbytes)
+        else:
+            raise ValueError(kind)
 
     def tensor(self) -> torch.Tensor:
         return torch.from_numpy(self.array)
 
     def close(self):
-        if self._host and self.array.nbytes:
-            abi.ts_host_unregister(self._host)
+        if self._host:
+            if self.kind == "alloc":
+                self.array = None
+                abi.ts_host_free(self._host)
+            else:
+                abi.ts_host_unregister(self._host)
         self._host = 0
 
     def __del__(self):
