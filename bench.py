@@ -60,6 +60,8 @@ def parse(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--settle-s", type=float, default=6.0,
+                    help="longest settle phase before the warm-up (0: none, for profiler runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--only", choices=KERNELS, default=None,
                     help="after the warm-up steps, launch only this kernel --steps times "
@@ -450,7 +452,7 @@ def run_native(args, w, rank, world, local):
         g.step(scores_d[i], q_d[i], timing=timing)
 
     # settle, then warm-up; the score process runs on without a jump
-    base[0] = settle(torch, g, step)
+    base[0] = settle(torch, g, step, limit_s=args.settle_s) if args.settle_s > 0 else 0
     for s in range(args.warmup):
         step(s)
     g.join()
@@ -550,7 +552,8 @@ def run_native(args, w, rank, world, local):
 
         # warm-up of the end-to-end loop: settle (the first zero-copy touch of
         # each host page is slow) and at least one pass over every input slot
-        e2e_settle = settle(torch, g, e2e_step, min_steps=2 * T)
+        e2e_settle = (settle(torch, g, e2e_step, min_steps=2 * T, limit_s=args.settle_s)
+                      if args.settle_s > 0 else 0)
         e0[0] += e2e_settle
         for s in range(args.warmup):
             e2e_step(s)
