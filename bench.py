@@ -235,7 +235,7 @@ def settle(torch, g, step, chunk=20, limit_s=6.0, tol=0.03, min_steps=0):
         for _ in range(chunk):
             step(s)
             s += 1
-        g.main.wait_stream(g.side)
+        g.join(g.main)
         b.record(g.main)
         b.synchronize()
         times.append(a.elapsed_time(b))
@@ -486,7 +486,7 @@ def run_native(args, w, rank, world, local):
         with torch.cuda.stream(g.main):
             miss_log[s].copy_(g.miss_count, non_blocking=True)
     t_enq1 = time.perf_counter()
-    g.main.wait_stream(g.side)
+    g.join(g.main)
     e1.record(g.main)
     torch.cuda.synchronize()
     t_wall1 = time.time()
@@ -565,7 +565,7 @@ def run_native(args, w, rank, world, local):
         f0.record(g.main)
         for s in range(n_e2e):
             e2e_step(s)
-        g.main.wait_stream(g.side)
+        g.join(g.main)
         f1.record(g.main)
         torch.cuda.synchronize()
         if g.synchronize():

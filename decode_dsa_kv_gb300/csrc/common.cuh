@@ -17,6 +17,18 @@
 
 namespace dsakv {
 
+// SMs of the current device (looked up once per translation unit).
+inline int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
 inline ts_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }

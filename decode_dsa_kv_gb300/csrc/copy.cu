@@ -293,16 +293,6 @@ __global__ void __launch_bounds__(kRefillThreads) refill_kernel(
   }
 }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
 
 }  // namespace
 }  // namespace dsakv

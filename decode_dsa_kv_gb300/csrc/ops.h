@@ -60,5 +60,11 @@ ts_status sfa_check(const void* q, const void* sel_l, int B, int H, int k, float
                     void* out, const void* ws, size_t ws_bytes);
 ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, float scale,
                       void* out, float* lse, void* ws, int32_t* err, cudaStream_t stream);
+// The two launches of sfa_enqueue, for callers that run the merge elsewhere:
+// the chunks (partials into ws) and the merge of the chunks (ws -> out, lse).
+ts_status sfa_enqueue_chunks(const void* q, const void* sel_l, int B, int H, int k, float scale,
+                             void* ws, int32_t* err, cudaStream_t stream);
+ts_status sfa_enqueue_combine(int B, int H, int k, void* out, float* lse, const void* ws,
+                              cudaStream_t stream);
 
 }  // namespace dsakv

@@ -485,8 +485,8 @@ ts_status sfa_check(const void* q, const void* sel_l, int B, int H, int k, float
   return TS_OK;
 }
 
-ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, float scale,
-                      void* out, float* lse, void* ws, int32_t* err, cudaStream_t stream) {
+ts_status sfa_enqueue_chunks(const void* q, const void* sel_l, int B, int H, int k, float scale,
+                             void* ws, int32_t* err, cudaStream_t stream) {
   const int HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
   CUtensorMap tm_q, tm_k, tm_v;
   if (!make_map(&tm_q, q, H, B, kHeads) || !make_map(&tm_k, sel_l, k, B, kHalfRows) ||
@@ -502,12 +502,28 @@ ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, flo
       return TS_ERR_CUDA;
     attr = true;
   }
-  __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(out);
   sfa_chunk_kernel<<<dim3(C, HG, B), kThreads, kSmemBytes, stream>>>(
       tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, err);
-  if (cudaGetLastError() != cudaSuccess) return TS_ERR_CUDA;
-  sfa_combine_kernel<<<unsigned(int64_t(B) * H), 128, 0, stream>>>(opart, ml, H, HG, C, outp, lse);
   return launch_status();
+}
+
+ts_status sfa_enqueue_combine(int B, int H, int k, void* out, float* lse, const void* ws,
+                              cudaStream_t stream) {
+  const int HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
+  const size_t slots = size_t(B) * HG * C * kHeads;
+  const float* opart = static_cast<const float*>(ws);
+  const float2* ml =
+      reinterpret_cast<const float2*>(static_cast<const char*>(ws) + align256(slots * DSA_DV * 4));
+  sfa_combine_kernel<<<unsigned(int64_t(B) * H), 128, 0, stream>>>(
+      opart, ml, H, HG, C, static_cast<__nv_bfloat16*>(out), lse);
+  return launch_status();
+}
+
+ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, float scale,
+                      void* out, float* lse, void* ws, int32_t* err, cudaStream_t stream) {
+  const ts_status st = sfa_enqueue_chunks(q, sel_l, B, H, k, scale, ws, err, stream);
+  if (st != TS_OK) return st;
+  return sfa_enqueue_combine(B, H, k, out, lse, ws, stream);
 }
 
 }  // namespace dsakv

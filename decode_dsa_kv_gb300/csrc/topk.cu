@@ -286,7 +286,7 @@ struct ClSmem {
 
 __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_kernel(
     const float* __restrict__ scores, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
-    int k, int max_ctx, TopkWs ws, int32_t* __restrict__ ids, int32_t* err) {
+    int k, int max_ctx, int slice, TopkWs ws, int32_t* __restrict__ ids, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   ClSmem& sm = *reinterpret_cast<ClSmem*>(smem_raw);
   const int G = gridDim.x;
@@ -295,8 +295,8 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_kernel(
   const int n = ctx_len[b];
   const bool ok = ctx_ok(n, k, max_ctx);  // uniform over the cluster
   int32_t* out = ids + int64_t(b) * k;
-  const int lo = static_cast<int>(rank) * kSlice;
-  const int hi = ok ? min(lo + kSlice, n) : lo;
+  const int lo = static_cast<int>(rank) * slice;  // slice <= kSlice
+  const int hi = ok ? min(lo + slice, n) : lo;
   const int len = max(hi - lo, 0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint64_t* gcand = ws.cand + int64_t(b) * max_ctx + lo;  // this CTA's global candidate list
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_kernel(
     cl.off[0] = 0;
     for (int g = 0; g < 4; ++g) {
       const uint32_t cg = g < G ? ld_dsmem_u32(dsmem_addr(&sm.ncand, g)) : 0u;
-      cl.seg[g] = ws.cand + int64_t(b) * max_ctx + g * kSlice;
+      cl.seg[g] = ws.cand + int64_t(b) * max_ctx + int64_t(g) * slice;
       cl.off[g + 1] = cl.off[g] + cg;
     }
     const uint32_t c = cl.off[4];
@@ -586,7 +586,15 @@ ts_status launch_topk(const float* scores, int64_t ctx_stride, const int32_t* ct
         return TS_ERR_CUDA;
       attr = true;
     }
-    const int G = (max_ctx + kSlice - 1) / kSlice;
+    // enough CTAs per request to fill half of the SMs when the requests are
+    // few (up to kClusterMaxG; the other half stays free for the kernels of
+    // the previous step still running, which would otherwise delay this
+    // launch), each with a slice of at most kSlice positions (a multiple of
+    // 1024)
+    int G = (max_ctx + kSlice - 1) / kSlice;
+    const int fill = sm_count() / (2 * B);
+    if (fill > G) G = fill < kClusterMaxG ? fill : kClusterMaxG;
+    const int slice = ((max_ctx + G - 1) / G + 1023) / 1024 * 1024;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G, B, 1);
     cfg.blockDim = dim3(kClThreads, 1, 1);
@@ -599,8 +607,8 @@ ts_status launch_topk(const float* scores, int64_t ctx_stride, const int32_t* ct
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, ctx_stride, ctx_len, k, max_ctx, w,
-                           ids, err) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, ctx_stride, ctx_len, k, max_ctx,
+                           slice, w, ids, err) != cudaSuccess)
       return TS_ERR_CUDA;
     return TS_OK;
   }
