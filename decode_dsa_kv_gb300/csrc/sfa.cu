@@ -20,8 +20,9 @@
 //   O[:, 0:256]   = P V[:, 0:256]    -> TMEM columns 256..511
 //   O[:, 256:512] = P V[:, 256:512]  -> TMEM columns 0..255 (S is dead by then:
 //       P holds it, bf16, in shared memory)
-//   O (unnormalised), the row max and the row sum -> fp32 workspace, staged
-//       through shared memory so that every global store is a coalesced run.
+//   O (unnormalised) -> fp32 workspace straight from TMEM, as a dim-major
+//       tile [512][128 heads] (coalesced stores); the row max and the row sum
+//       beside it.
 // A second kernel merges the chunks of a request: out = sum_c w_c O_c /
 // sum_c w_c l_c with w_c = exp2(m_c - max_c m_c).
 #include <cmath>
@@ -51,7 +52,6 @@ constexpr int kLoads = kScoreLoads + 16;             // + 16 value stages (8 row
 constexpr int kSoftmaxThreads = 256;                 // warps 2..9
 constexpr int kThreads = 64 + kSoftmaxThreads;
 constexpr uint32_t kBarBytes = 704;
-constexpr int kOutStride = 256 + 4;  // floats per head row of the epilogue staging
 // barriers first, then the 1024-byte aligned tiles (worst-case padding
 // included). The total leaves room on the SM for a 0-byte CTA of another
 // kernel (each CTA also holds 1 KB of reserved shared memory), so a gather or
@@ -61,7 +61,6 @@ constexpr uint32_t kSmemBytes = kBarBytes + 1024 + kTileBytes;
 constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s of global timer per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-static_assert(kHeads * kOutStride * 4 <= kTileBytes, "epilogue staging");
 // 228 KB of shared memory per SM; 1 KB reserved per CTA
 static_assert(kSmemBytes + 1024 + 1024 <= 228 * 1024, "room for a second, shared-memory-free CTA");
 
@@ -236,7 +235,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q4 = warp & 3;            // TMEM lane quarter this warp may access
     const int part = (warp - 2) >> 2;   // which half of the chunk's columns
     const int row = q4 * 32 + lane;     // head within the tile
-    const int t = threadIdx.x - 64;     // 0..255
     const uint32_t trow = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
     const int nvalid = min(kChunk, k - c * kChunk);
     const int col0 = part * (kChunk / 2);
@@ -303,40 +301,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (part == 0) l += bars->red[row];  // the row sum (only part 0 writes it out)
       ok = warp_wait(&bars->o_full, 0, abort);
     }
-    // Epilogue: O goes through the (now idle) P tile and stage ring, 256 dims
-    // at a time, so that every store to the workspace is a coalesced run.
+    // Epilogue: O straight from TMEM to the workspace, in the chunk's
+    // dim-major tile [512 dims][128 heads]: a warp's 32 lanes are 32
+    // consecutive heads, so every store is a coalesced 128-byte run.
     const bool live = ok && !*abort;
-    float* stage_o = reinterpret_cast<float*>(base);  // [128][kOutStride]
     const size_t slot0 = ((size_t(b) * HG + hg) * C + c) * kHeads;
     const int rows_valid = min(kHeads, H - hg * kHeads);
-    if (live) tc_fence_after();
-    for (int half = 0; half < 2; ++half) {
-      if (live) {
-        uint32_t r[32];
+    if (live) {
+      tc_fence_after();
+      float* tile = opart + slot0 * DSA_DV;
+      uint32_t r[32];
+      for (int half = 0; half < 2; ++half) {
         for (int qq = 0; qq < 4; ++qq) {
           const int d = 128 * part + 32 * qq;  // dim within this half
           tmem_ld32(trow + (half == 0 ? 256u + d : uint32_t(d)), r);
           tmem_wait_ld();
-          float* dst = stage_o + row * kOutStride + d;
+          if (row < rows_valid) {
+            float* dst = tile + size_t(256 * half + d) * kHeads + row;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<float4*>(dst + 4 * j) =
-                make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            for (int i = 0; i < 32; ++i) dst[i * kHeads] = __uint_as_float(r[i]);
+          }
         }
       }
-      softmax_sync();
-      if (live) {
-        // 128 rows x 64 float4 of this half; thread t moves float4 f = t + 256 i
-        for (int i = 0; i < 32; ++i) {
-          const int f = t + kSoftmaxThreads * i;
-          const int rr = f >> 6, c4 = f & 63;
-          if (rr < rows_valid)
-            *reinterpret_cast<float4*>(opart + (slot0 + rr) * DSA_DV + 256 * half + 4 * c4) =
-                *reinterpret_cast<const float4*>(stage_o + rr * kOutStride + 4 * c4);
-        }
-      }
-      softmax_sync();
     }
     if (live && part == 0 && row < rows_valid) ml[slot0 + row] = make_float2(m, l);
   }
@@ -372,59 +358,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merge the chunks of one (request, head): out = sum_c w_c O_c / sum_c w_c l_c.
-// Loads of up to eight chunks are issued together before they are summed.
-__global__ void __launch_bounds__(128) sfa_combine_kernel(const float* __restrict__ opart,
-                                                          const float2* __restrict__ ml, int H,
-                                                          int HG, int C,
-                                                          __nv_bfloat16* __restrict__ out,
-                                                          float* __restrict__ lse) {
-  const int bh = blockIdx.x;
-  const int b = bh / H, h = bh - b * H;
-  const int hg = h / kHeads, row = h - hg * kHeads;
-  const size_t slot0 = ((size_t(b) * HG + hg) * C) * kHeads + row;
-  const int v = threadIdx.x * 4;
-  float mx = -INFINITY;
-  for (int c0 = 0; c0 < C; c0 += 8) {
-    float2 e[8];
+// Merge the chunks of a (request, head tile), kCombineDims dims per CTA, one thread per
+// head: out = sum_c w_c O_c / sum_c w_c l_c with w_c = exp2(m_c - max_c m_c).
+// The chunks' tiles are dim-major, so each load of a warp is one coalesced
+// 128-byte run; the result goes out through shared memory as 16-byte row
+// pieces.
+constexpr int kCombineDims = 16;
+__global__ void __launch_bounds__(kHeads) sfa_combine_kernel(const float* __restrict__ opart,
+                                                             const float2* __restrict__ ml, int H,
+                                                             int HG, int C,
+                                                             __nv_bfloat16* __restrict__ out,
+                                                             float* __restrict__ lse) {
+  __shared__ __align__(16) __nv_bfloat16 tile[kHeads][kCombineDims + 8];
+  const int db = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
+  const int h = threadIdx.x;
+  const int rows_valid = min(kHeads, H - hg * kHeads);
+  const size_t s0 = ((size_t(b) * HG + hg) * C) * kHeads;  // chunk 0, head 0
+  if (h < rows_valid) {
+    float mx = -INFINITY;
+    for (int c = 0; c < C; ++c) mx = fmaxf(mx, __ldg(ml + s0 + size_t(c) * kHeads + h).x);
+    float denom = 0.f;
+    float acc[kCombineDims];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      e[i] = c0 + i < C ? __ldg(ml + slot0 + size_t(c0 + i) * kHeads) : make_float2(-INFINITY, 0.f);
+    for (int i = 0; i < kCombineDims; ++i) acc[i] = 0.f;
+    for (int c = 0; c < C; ++c) {
+      const float2 e = __ldg(ml + s0 + size_t(c) * kHeads + h);
+      const float w = exp2f(e.x - mx);
+      denom += w * e.y;
+      const float* src = opart + (s0 + size_t(c) * kHeads) * DSA_DV +
+                         size_t(db) * kCombineDims * kHeads + h;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) mx = fmaxf(mx, e[i].x);
-  }
-  float denom = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = 0; c0 < C; c0 += 8) {
-    float2 e[8];
-    float4 o[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (c0 + i < C) {
-        const size_t slot = slot0 + size_t(c0 + i) * kHeads;
-        e[i] = __ldg(ml + slot);
-        o[i] = __ldcs(reinterpret_cast<const float4*>(opart + slot * DSA_DV + v));
-      }
+      for (int i = 0; i < kCombineDims; ++i) acc[i] += w * __ldcs(src + i * kHeads);
     }
+    const float inv = 1.f / denom;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (c0 + i < C) {
-        const float w = exp2f(e[i].x - mx);
-        denom += w * e[i].y;
-        acc.x += w * o[i].x;
-        acc.y += w * o[i].y;
-        acc.z += w * o[i].z;
-        acc.w += w * o[i].w;
-      }
-    }
+    for (int i = 0; i < kCombineDims; i += 2)
+      *reinterpret_cast<__nv_bfloat162*>(&tile[h][i]) =
+          __floats2bfloat162_rn(acc[i] * inv, acc[i + 1] * inv);
+    if (db == 0 && lse) lse[size_t(b) * H + hg * kHeads + h] = mx * kLn2 + logf(denom);
   }
-  const float inv = 1.f / denom;
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-  __nv_bfloat16* o = out + (size_t(b) * H + h) * DSA_DV + v;
-  *reinterpret_cast<__nv_bfloat162*>(o) = lo;
-  *reinterpret_cast<__nv_bfloat162*>(o + 2) = hi;
-  if (lse && threadIdx.x == 0) lse[size_t(b) * H + h] = mx * kLn2 + logf(denom);
+  __syncthreads();
+  // rows_valid rows of kCombineDims dims, in 16-byte pieces
+  constexpr int kPieces = kCombineDims / 8;
+  for (int j = h; j < kHeads * kPieces; j += kHeads) {
+    const int r = j / kPieces, piece = j - r * kPieces;
+    if (r < rows_valid)
+      *reinterpret_cast<uint4*>(out + (size_t(b) * H + hg * kHeads + r) * DSA_DV +
+                                db * kCombineDims + piece * 8) =
+          *reinterpret_cast<const uint4*>(&tile[r][piece * 8]);
+  }
 }
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -514,7 +496,7 @@ ts_status sfa_enqueue_combine(int B, int H, int k, void* out, float* lse, const 
   const float* opart = static_cast<const float*>(ws);
   const float2* ml =
       reinterpret_cast<const float2*>(static_cast<const char*>(ws) + align256(slots * DSA_DV * 4));
-  sfa_combine_kernel<<<unsigned(int64_t(B) * H), 128, 0, stream>>>(
+  sfa_combine_kernel<<<dim3(DSA_DV / kCombineDims, HG, B), kHeads, 0, stream>>>(
       opart, ml, H, HG, C, static_cast<__nv_bfloat16*>(out), lse);
   return launch_status();
 }
