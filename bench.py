@@ -67,6 +67,9 @@ def parse(argv=None):
                     help="after the warm-up steps, launch only this kernel --steps times "
                          "(on the state the warm-up left) and report its time per launch")
     ap.add_argument("--B", type=int, default=None, help="override the workload's request count")
+    ap.add_argument("--mtp", type=int, default=0, choices=(0, 1, 2, 3),
+                    help="MTP draft steps whose queries are folded into the heads "
+                         "(the step attends (1 + N) x H query rows over one selection)")
     ap.add_argument("--no-kernel-events", action="store_true",
                     help="time the steps without per-kernel events (no per-kernel roofline)")
     return ap.parse_args(argv)
@@ -599,6 +602,7 @@ def run_native(args, w, rank, world, local):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "layers": w.layers, "k": w.k,
                    "ctx": w.ctx, "sets": w.S, "ways": w.W, "heads": w.H,
+                   "mtp_draft_steps": args.mtp,
                    "requests_per_gpu": w.B, "distinct_input_steps": T,
                    "l2": "inputs larger than L2 (host KV, pools and per-step inputs)",
                    "parallelism": f"requests sharded over {world} GPU(s), no collective"},
@@ -671,6 +675,8 @@ def main(argv=None):
     w = wl.get(args.workload)
     if args.B:
         w = wl.scaled(w, B=args.B)
+    if args.mtp:
+        w = wl.scaled(w, H=w.H * (1 + args.mtp))
     if args.impl == "reference":
         run_reference(args, w, rank, world)
         return

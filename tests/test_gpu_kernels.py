@@ -318,6 +318,7 @@ def run_sfa(d, q_bits, rows_bits, scale):
 
 @pytest.mark.parametrize("B,H,k", [(1, 16, 256), (2, 128, 2048), (3, 128, 300), (1, 128, 1),
                                    (2, 20, 513), (1, 256, 1000), (4, 128, 4096), (2, 128, 1800),
+                                   (1, 512, 2048),
                                    (3, 64, 1279)])
 def test_sfa_parity(d, B, H, k):
     rng = np.random.default_rng(B * 1000 + H + k)
@@ -334,6 +335,25 @@ def test_sfa_parity(d, B, H, k):
         assert np.allclose(lse[b], z, rtol=0, atol=2e-3)
     assert worst_abs <= SFA_ABS_TOL, worst_abs
     assert max(rels) <= SFA_MEAN_REL_TOL, rels
+
+
+@pytest.mark.parametrize("next_n", [1, 2, 3])
+def test_sfa_mtp_folded_queries_match_separate_calls(d, next_n):
+    """MTP reuse (GLM-5.2 shared-Indexer KV Cache Offload, §5.1): the draft
+    steps reuse the first step's selection, and their queries are folded into
+    the attention's head dimension, (1 + next_n) x 128 heads in one call. Each
+    head tile is computed on its own, so the folded call equals one call per
+    draft step bit for bit."""
+    B, H, k = 3, 128, 2048
+    Hf = (1 + next_n) * H
+    q = wl.normal_bf16(B * Hf, 576, 81, 9, next_n, 0).reshape(B, Hf, 576)
+    rows = wl.normal_bf16(B * k, 576, 82, 9, next_n, 0).reshape(B, k, 576)
+    scale = 1 / math.sqrt(576)
+    out_f, lse_f = run_sfa(d, q, rows, scale)
+    for i in range(1 + next_n):
+        out_i, lse_i = run_sfa(d, np.ascontiguousarray(q[:, i * H:(i + 1) * H]), rows, scale)
+        assert np.array_equal(out_f[:, i * H:(i + 1) * H], out_i)
+        assert np.array_equal(lse_f[:, i * H:(i + 1) * H], lse_i)
 
 
 def test_sfa_constant_rows_exact(d):

@@ -99,6 +99,13 @@ def test_adversarial_scaled_overflow(d):
     run_steps(d, w, 3, sfa_layers=[2])
 
 
+def test_decode_batch_mtp_folded_queries(d):
+    # MTP reuse: two draft steps share the step's selection; their queries are
+    # folded into the heads (3 x 128), as the group step runs them
+    w = wl.scaled(wl.DECODE_BATCH, B=2, H=3 * 128)
+    run_steps(d, w, 2, sfa_layers=[1], sfa_heads=slice(0, 384, 7))
+
+
 def test_decode_batch_full_size_sampled(d):
     # the full workload (32 requests x 65,536 tokens x 4 layers) in the bench's
     # launch configuration; the oracle follows four of the requests
