@@ -67,6 +67,9 @@ def parse(argv=None):
                     help="after the warm-up steps, launch only this kernel --steps times "
                          "(on the state the warm-up left) and report its time per launch")
     ap.add_argument("--B", type=int, default=None, help="override the workload's request count")
+    ap.add_argument("--policy", choices=("fifo", "reuse"), default="fifo",
+                    help="device pool: the set-associative FIFO pool (default) or the base "
+                         "design's adjacent-step reuse of the previous selection")
     ap.add_argument("--mtp", type=int, default=0, choices=(0, 1, 2, 3),
                     help="MTP draft steps whose queries are folded into the heads "
                          "(the step attends (1 + N) x H query rows over one selection)")
@@ -444,7 +447,8 @@ def run_native(args, w, rank, world, local):
     abi.check(abi.ts_copy(scores_d, scores_pin.dev, scores_pin.array.nbytes, None), "ts_copy")
     abi.check(abi.ts_copy(q_d, q_pin.dev, q_pin.array.nbytes, None), "ts_copy")
     torch.cuda.synchronize()
-    g = dk.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host)
+    g = dk.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host,
+                       policy=args.policy)
     peaks = measured_peaks()
     link = link_peak_gbs(torch, link_buf)
 
@@ -472,7 +476,7 @@ def run_native(args, w, rank, world, local):
     inst_log = torch.zeros((args.steps,), dtype=torch.int64, device="cuda")
     # per-launch timing events of every timed step, created before the region
     timings = (None if args.no_kernel_events
-               else [dk.StepTiming(w.layers, g.main) for _ in range(args.steps)])
+               else [g.timing() for _ in range(args.steps)])
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
@@ -589,7 +593,7 @@ def run_native(args, w, rank, world, local):
     if rank != 0:
         return
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and args.policy == "fifo":
         rows, secs, nreq, L = oracle_sample(w, args.cpu_seconds)
         cpu = {"value": rows / secs, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{nreq} request(s) x {L} layers of {w.name}, one decode step each "
@@ -602,7 +606,7 @@ def run_native(args, w, rank, world, local):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "layers": w.layers, "k": w.k,
                    "ctx": w.ctx, "sets": w.S, "ways": w.W, "heads": w.H,
-                   "mtp_draft_steps": args.mtp,
+                   "mtp_draft_steps": args.mtp, "pool_policy": args.policy,
                    "requests_per_gpu": w.B, "distinct_input_steps": T,
                    "l2": "inputs larger than L2 (host KV, pools and per-step inputs)",
                    "parallelism": f"requests sharded over {world} GPU(s), no collective"},

@@ -30,6 +30,7 @@ TS_DEVERR_PTR_RANGE = 0x08
 TS_DEVERR_CTX = 0x10
 TS_DEVERR_TIMEOUT = 0x20
 TS_DEVERR_COUNT = 0x40
+TS_DEVERR_ORDER = 0x80
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -50,6 +51,7 @@ _SIGS = {
     "ts_topk": (_I, [_P, _I64, _P, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "ts_topk_noalloc": (_I, [_P, _I64, _P, _I, _I, _I, _P, _P, _P]),
     "dsa_plan": (_I, [_P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "dsa_plan_reuse": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "dsa_gather_kv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _I, _P, _I64, _P, _P, _P, _P]),
     "dsa_refill_pool": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _I, _I,
                              _P, _P]),
@@ -61,6 +63,8 @@ _SIGS = {
 EXPORTS = tuple(_SIGS)
 
 TS_MAX_LAYERS = 16
+DSA_POLICY_FIFO = 0
+DSA_POLICY_REUSE = 1
 
 
 class DsaGroup(ctypes.Structure):
@@ -81,6 +85,9 @@ class DsaGroup(ctypes.Structure):
         ("main_stream", _P), ("gather_stream", _P), ("side_stream", _P),
         ("sync", _P),
         ("step", ctypes.c_uint32),
+        ("policy", _I),
+        ("prev_ids", _P),
+        ("prev_sel", _P),
     ]
 
 for _name, (_res, _args) in _SIGS.items():
@@ -190,6 +197,13 @@ def dsa_plan(ids, ctx_len, B, k, pool_tags, fifo_ptr, S, W, src_map, miss_ids, m
                          ptr(src_map), ptr(miss_ids), ptr(miss_pos), ptr(victim), ptr(install),
                          ptr(miss_count), ptr(miss_rows), ptr(ptr_next), ptr(err),
                          stream_handle(stream))
+
+
+def dsa_plan_reuse(ids, prev_ids, ctx_len, B, k, src_map, miss_ids, miss_pos, miss_count,
+                   miss_rows, err=None, stream=None) -> int:
+    return _lib.dsa_plan_reuse(ptr(ids), ptr(prev_ids), ptr(ctx_len), B, k, ptr(src_map),
+                               ptr(miss_ids), ptr(miss_pos), ptr(miss_count), ptr(miss_rows),
+                               ptr(err), stream_handle(stream))
 
 
 def dsa_gather_kv(src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, pool_l, P, host_l,

@@ -271,6 +271,69 @@ __global__ void __launch_bounds__(kThreads) dsa_plan_kernel(
   if (tid == 0) miss_count[b] = M;
 }
 
+// ---------------------------------------------------------------------------
+// dsa_plan_reuse: the base design's adjacent-step reuse (GLM-5.2 shared-Indexer
+// KV Cache Offload, §2.1 GatherSelectionKvCache and §2.2): a token the
+// previous step also selected is served from the previous step's selection
+// buffer (its row there = its position in the previous ids), any other token
+// from host memory. One CTA per request: the previous ids in shared memory,
+// a binary search per position, the misses compacted in position order (which
+// is ascending id) by a block scan.
+// ---------------------------------------------------------------------------
+constexpr int kReuseThreads = 1024;
+
+__global__ void __launch_bounds__(kReuseThreads) dsa_plan_reuse_kernel(
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ prev_ids,
+    const int32_t* __restrict__ ctx_len, int k, int32_t* __restrict__ src_map,
+    int32_t* __restrict__ miss_ids, int32_t* __restrict__ miss_pos,
+    int32_t* __restrict__ miss_count, int32_t* __restrict__ miss_rows, int32_t* err) {
+  extern __shared__ int prev[];  // [k], then 64 ints of scan scratch
+  int* scratch = prev + k;
+  const int b = blockIdx.x;
+  const int n = ctx_len[b];
+  const int32_t* id = ids + int64_t(b) * k;
+  for (int i = threadIdx.x; i < k; i += kReuseThreads) prev[i] = prev_ids[int64_t(b) * k + i];
+  __syncthreads();
+  // each thread a contiguous run of positions, so that the scan keeps order
+  const int per = (k + kReuseThreads - 1) / kReuseThreads;
+  const int j0 = threadIdx.x * per, j1 = min(j0 + per, k);
+  int bad = 0, misses = 0;
+  for (int j = j0; j < j1; ++j) {
+    const int t = id[j];
+    if (j > 0 && id[j - 1] >= t) bad |= TS_DEVERR_ORDER;
+    if (j > 0 && prev[j] >= 0 && prev[j - 1] >= prev[j]) bad |= TS_DEVERR_ORDER;
+    if (t < 0 || t >= n) {
+      bad |= TS_DEVERR_ID_RANGE;
+      src_map[int64_t(b) * k + j] = INT_MIN;
+      continue;
+    }
+    int lo = 0, hi = k;  // first entry >= t (empty entries, -1, sort first)
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (prev[mid] < t) lo = mid + 1;
+      else hi = mid;
+    }
+    const bool hit = lo < k && prev[lo] == t;
+    src_map[int64_t(b) * k + j] = hit ? lo : -1 - t;
+    misses += hit ? 0 : 1;
+  }
+  int total;
+  int at = block_exclusive_scan(misses, scratch, &total);
+  for (int j = j0; j < j1; ++j) {
+    const int s = src_map[int64_t(b) * k + j];
+    if (s < 0 && s != INT_MIN) {
+      miss_ids[int64_t(b) * k + at] = -1 - s;
+      miss_pos[int64_t(b) * k + at] = j;
+      ++at;
+    }
+  }
+  if (threadIdx.x == 0) {
+    miss_count[b] = total;
+    miss_rows[b] = total;  // ascending ids: no token repeats
+  }
+  if (bad) report(err, bad);
+}
+
 }  // namespace
 }  // namespace dsakv
 
@@ -323,4 +386,44 @@ extern "C" ts_status dsa_plan(const int32_t* ids, const int32_t* ctx_len, int B,
   return dsakv::plan_enqueue(ids, ctx_len, B, k, pool_tags, fifo_ptr, S, W, src_map, miss_ids,
                              miss_pos, victim, install, miss_count, miss_rows, ptr_next, err,
                              stream);
+}
+
+namespace dsakv {
+
+ts_status plan_reuse_check(const int32_t* ids, const int32_t* prev_ids, const int32_t* ctx_len,
+                           int B, int k, int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
+                           int32_t* miss_count, int32_t* miss_rows) {
+  if (!ids || !prev_ids || !ctx_len || !src_map || !miss_ids || !miss_pos || !miss_count ||
+      !miss_rows)
+    return TS_ERR_INVALID_ARG;
+  if (B <= 0 || k <= 0) return TS_ERR_INVALID_ARG;
+  if (k > 16384) return TS_ERR_UNSUPPORTED;
+  return TS_OK;
+}
+
+ts_status plan_reuse_enqueue(const int32_t* ids, const int32_t* prev_ids, const int32_t* ctx_len,
+                             int B, int k, int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
+                             int32_t* miss_count, int32_t* miss_rows, int32_t* err,
+                             cudaStream_t stream) {
+  const size_t smem = size_t(k) * 4 + 64 * 4;
+  if (cudaFuncSetAttribute(dsa_plan_reuse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(smem)) != cudaSuccess)
+    return TS_ERR_CUDA;
+  dsa_plan_reuse_kernel<<<B, kReuseThreads, smem, stream>>>(ids, prev_ids, ctx_len, k, src_map,
+                                                            miss_ids, miss_pos, miss_count,
+                                                            miss_rows, err);
+  return launch_status();
+}
+
+}  // namespace dsakv
+
+extern "C" ts_status dsa_plan_reuse(const int32_t* ids, const int32_t* prev_ids,
+                                    const int32_t* ctx_len, int B, int k, int32_t* src_map,
+                                    int32_t* miss_ids, int32_t* miss_pos, int32_t* miss_count,
+                                    int32_t* miss_rows, int32_t* err, cudaStream_t stream) {
+  const ts_status st = dsakv::plan_reuse_check(ids, prev_ids, ctx_len, B, k, src_map, miss_ids,
+                                               miss_pos, miss_count, miss_rows);
+  if (st != TS_OK) return st;
+  return dsakv::plan_reuse_enqueue(ids, prev_ids, ctx_len, B, k, src_map, miss_ids, miss_pos,
+                                   miss_count, miss_rows, err, stream);
 }

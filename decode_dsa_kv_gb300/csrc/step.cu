@@ -94,11 +94,17 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
   const int L = g.layers;
   if (L <= 0 || L > TS_MAX_LAYERS) return TS_ERR_INVALID_ARG;
   if (!ids && !scores) return TS_ERR_INVALID_ARG;
+  const bool reuse = g.policy == DSA_POLICY_REUSE;
+  if (!reuse && g.policy != DSA_POLICY_FIFO) return TS_ERR_INVALID_ARG;
+  if (reuse && (ids || !g.prev_ids || !g.prev_sel)) return TS_ERR_INVALID_ARG;
   if (g.S <= 0 || g.W <= 0 || int64_t(g.S) * g.W > (1 << 24)) return TS_ERR_INVALID_ARG;
   if (!g.sync || (reinterpret_cast<uintptr_t>(g.sync) & 3u) != 0) return TS_ERR_INVALID_ARG;
   if (!aligned16(q)) return TS_ERR_INVALID_ARG;
-  const int P = g.S * g.W;
-  const Layers lb = layer_bytes(g);
+  // with reuse, the "pool" is the previous step's selection: k rows per request
+  const int P = reuse ? g.k : g.S * g.W;
+  Layers lb = layer_bytes(g);
+  if (reuse) lb.pool = lb.sel;
+  const void* pool = reuse ? static_cast<const void*>(g.prev_sel) : g.pool;
   const int32_t* plan_ids = ids ? ids : g.ids;
 
   // every operation's host checks first (layer 0 stands for all layers: the
@@ -108,13 +114,15 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
     st = topk_check(scores, g.ctx_stride, g.ctx_len, g.B, g.max_ctx, g.k, g.ids, g.topk_ws,
                     g.topk_ws_bytes);
   if (st == TS_OK)
-    st = plan_check(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.fifo_ptr, g.S, g.W, g.src_map,
-                    g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.miss_rows,
-                    g.ptr_next);
+    st = reuse ? plan_reuse_check(plan_ids, g.prev_ids, g.ctx_len, g.B, g.k, g.src_map, g.miss_ids,
+                                  g.miss_pos, g.miss_count, g.miss_rows)
+               : plan_check(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.fifo_ptr, g.S, g.W,
+                            g.src_map, g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count,
+                            g.miss_rows, g.ptr_next);
   if (st == TS_OK)
-    st = gather_check(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k,
-                      g.pool, P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel);
-  if (st == TS_OK)
+    st = gather_check(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k, pool,
+                      P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel);
+  if (st == TS_OK && !reuse)
     st = refill_check(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k, g.sel,
                       g.pool, P, 1, g.pool_tags, g.fifo_ptr, g.ptr_next, g.S, g.W);
   if (st == TS_OK) st = sfa_check(q, g.sel, g.B, g.H, g.k, g.scale, g.out, g.sfa_ws, g.sfa_ws_bytes);
@@ -140,32 +148,53 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
          rec(0, 1, m);
   }
   ok = ok && wait_for(m, refilled, seq - 1) && rec(1, 0, m) &&
-       plan_enqueue(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.fifo_ptr, g.S, g.W, g.src_map,
-                    g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.miss_rows,
-                    g.ptr_next, g.err, m) == TS_OK &&
+       (reuse ? plan_reuse_enqueue(plan_ids, g.prev_ids, g.ctx_len, g.B, g.k, g.src_map,
+                                   g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.err, m)
+              : plan_enqueue(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.fifo_ptr, g.S, g.W,
+                             g.src_map, g.miss_ids, g.miss_pos, g.victim, g.install,
+                             g.miss_count, g.miss_rows, g.ptr_next, g.err, m)) == TS_OK &&
        rec(1, 1, m) && signal(m, planned, seq) && wait_for(gs, planned, seq);
   // one launch gathers every layer and writes seq into gathered[l] from the
   // device as soon as layer l's rows are in (no ramp between layers)
   ok = ok && rec(2, 0, gs) &&
-       gather_enqueue(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k,
-                      g.pool, P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel, g.err, gs, L, lb.pool,
+       gather_enqueue(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k, pool,
+                      P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel, g.err, gs, L, lb.pool,
                       lb.host, lb.sel, gathered, counts, seq) == TS_OK &&
        rec(2, 1, gs);
   // per layer: the attention on the main stream, the refill beside it on the
   // side stream; the last refill also updates the metadata
-  for (int l = 0; ok && l < L; ++l)
+  for (int l = 0; ok && l < L; ++l) {
     ok = wait_for(m, gathered + l, seq) && rec(3 + l, 0, m) &&
          sfa_enqueue(at(q, l, lb.q), at(g.sel, l, lb.sel), g.B, g.H, g.k, g.scale,
                      at(g.out, l, lb.out), g.lse ? at(g.lse, l, lb.lse) : nullptr, g.sfa_ws,
                      g.err, m) == TS_OK &&
-         rec(3 + l, 1, m) && wait_for(side, gathered + l, seq) &&
-         rec(3 + L + l, 0, side) &&
-         refill_enqueue(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k,
-                        at(g.sel, l, lb.sel), at(g.pool, l, lb.pool), P, l == L - 1, g.pool_tags,
-                        g.fifo_ptr, g.ptr_next, g.S, g.W, g.err, side, 1, lb.sel,
-                        lb.pool) == TS_OK &&
-         rec(3 + L + l, 1, side);
-  ok = ok && signal(side, refilled, seq);
+         rec(3 + l, 1, m);
+    if (!reuse)
+      ok = ok && wait_for(side, gathered + l, seq) && rec(3 + L + l, 0, side) &&
+           refill_enqueue(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k,
+                          at(g.sel, l, lb.sel), at(g.pool, l, lb.pool), P, l == L - 1,
+                          g.pool_tags, g.fifo_ptr, g.ptr_next, g.S, g.W, g.err, side, 1, lb.sel,
+                          lb.pool) == TS_OK &&
+           rec(3 + L + l, 1, side);
+  }
+  if (reuse) {
+    // no refill: this step's selection and ids become the next step's
+    // "pool". The next step's top-k writes the old previous ids, which this
+    // step's plan read (earlier on the main stream); its gather writes the old
+    // previous selection, which this step's gather read (it waits for the
+    // next plan, after this step's attention, after this gather's last layer)
+    ok = ok && signal(m, refilled, seq);
+    if (ok) {
+      int32_t* t_ids = g.ids;
+      g.ids = g.prev_ids;
+      g.prev_ids = t_ids;
+      void* t_sel = g.sel;
+      g.sel = g.prev_sel;
+      g.prev_sel = t_sel;
+    }
+  } else {
+    ok = ok && signal(side, refilled, seq);
+  }
   if (!ok) {
     // give every signal word this step's number, so that no wait enqueued
     // now or by the next call is left without its signal

@@ -132,8 +132,9 @@ class StepTiming:
     once, which makes them valid) ahead of use, in the order dsa_group_step
     fills them: top-k, plan, gather (every layer), sfa[l], refill[l]."""
 
-    def __init__(self, layers: int, stream=None):
+    def __init__(self, layers: int, stream=None, refills: bool = True):
         self.layers = layers
+        self.refills = refills  # the reuse policy runs no refill
         n = 2 * (3 + 2 * layers)
         st = torch.cuda.current_stream() if stream is None else stream
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -153,7 +154,7 @@ class StepTiming:
         out = {"topk": [pair(0)] if self.with_topk else [], "plan": [pair(1)]}
         out["gather"] = [pair(2)]
         out["sfa"] = [pair(3 + l) for l in range(L)]
-        out["refill"] = [pair(3 + L + l) for l in range(L)]
+        out["refill"] = [pair(3 + L + l) for l in range(L)] if self.refills else []
         return out
 
     def spans(self, t0) -> dict:
@@ -167,16 +168,24 @@ class StepTiming:
         out = {"topk": [span(0)] if self.with_topk else [], "plan": [span(1)]}
         out["gather"] = [span(2)]
         out["sfa"] = [span(3 + l) for l in range(L)]
-        out["refill"] = [span(3 + L + l) for l in range(L)]
+        out["refill"] = [span(3 + L + l) for l in range(L)] if self.refills else []
         return out
 
 
 class DecodeGroup:
-    """Pool state and buffers for B requests of one IndexShare group."""
+    """Pool state and buffers for B requests of one IndexShare group.
+
+    policy "fifo": the set-associative FIFO pool of S sets x W ways;
+    policy "reuse": the base design's adjacent-step reuse, where the device
+    keeps only the previous step's selection (S and W are then unused).
+    After a step, `ids` and `sel` hold that step's ids and selection."""
 
     def __init__(self, B: int, layers: int, k: int, S: int, W: int, H: int,
                  ctx_len, ctx_stride: int, host: HostKV, scale: float | None = None,
-                 device: str = "cuda", max_ctx: int | None = None):
+                 device: str = "cuda", max_ctx: int | None = None, policy: str = "fifo"):
+        if policy not in ("fifo", "reuse"):
+            raise ValueError(policy)
+        self.policy = policy
         self.B, self.L, self.k, self.S, self.W, self.H = B, layers, k, S, W, H
         self.P = S * W
         self.ctx_stride = ctx_stride
@@ -186,10 +195,13 @@ class DecodeGroup:
         i32 = dict(dtype=torch.int32, device=dev)
         self.ctx_len = torch.as_tensor(np.asarray(ctx_len, np.int32), **i32)
         self.max_ctx = int(np.max(ctx_len)) if max_ctx is None else max_ctx
-        # pool state: data per (layer, request), metadata per request
-        self.pool = torch.zeros((layers, B, self.P, D), dtype=torch.int16, device=dev)
-        self.tags = torch.full((B, self.P), -1, **i32)
-        self.fifo_ptr = torch.zeros((B, S), **i32)
+        # pool state: data per (layer, request), metadata per request (the
+        # reuse policy keeps the previous step's ids and selection instead)
+        reuse = policy == "reuse"
+        P = 1 if reuse else self.P
+        self.pool = torch.zeros((layers, B, P, D), dtype=torch.int16, device=dev)
+        self.tags = torch.full((B, P), -1, **i32)
+        self.fifo_ptr = torch.zeros((B, 1 if reuse else S), **i32)
         # plan outputs
         self.ids = torch.empty((B, k), **i32)
         self.src_map = torch.empty((B, k), **i32)
@@ -199,9 +211,14 @@ class DecodeGroup:
         self.install = torch.empty((B, k), dtype=torch.uint8, device=dev)
         self.miss_count = torch.zeros((B,), **i32)
         self.miss_rows = torch.zeros((B,), **i32)
-        self.ptr_next = torch.empty((B, S), **i32)
+        self.ptr_next = torch.empty((B, 1 if reuse else S), **i32)
         # per-layer selection buffers and attention outputs
         self.sel = torch.empty((layers, B, k, D), dtype=torch.int16, device=dev)
+        if reuse:
+            self.prev_ids = torch.full((B, k), -1, **i32)
+            self.prev_sel = torch.zeros((layers, B, k, D), dtype=torch.int16, device=dev)
+            self._bufs = {t.data_ptr(): t for t in (self.ids, self.prev_ids, self.sel,
+                                                    self.prev_sel)}
         self.out = torch.empty((layers, B, H, DV), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((layers, B, H), dtype=torch.float32, device=dev)
         # workspaces and the device error word
@@ -221,6 +238,10 @@ class DecodeGroup:
         self.sync = torch.zeros((2 + 2 * layers,), **i32)
         self.desc = self._descriptor()
 
+    def timing(self) -> StepTiming:
+        """Timing events for one step of this group (see StepTiming)."""
+        return StepTiming(self.L, self.main, refills=self.policy == "fifo")
+
     def _descriptor(self):
         d = abi.DsaGroup()
         d.B, d.layers, d.k, d.S, d.W, d.H = self.B, self.L, self.k, self.S, self.W, self.H
@@ -235,6 +256,10 @@ class DecodeGroup:
         d.topk_ws, d.topk_ws_bytes = self.topk_ws.data_ptr(), self.topk_ws_bytes
         d.sfa_ws, d.sfa_ws_bytes = self.sfa_ws.data_ptr(), self.sfa_ws_bytes
         d.err = self.err.data_ptr()
+        if self.policy == "reuse":
+            d.policy = abi.DSA_POLICY_REUSE
+            d.prev_ids = self.prev_ids.data_ptr()
+            d.prev_sel = self.prev_sel.data_ptr()
         d.main_stream = self.main.cuda_stream
         d.gather_stream = self.gstream.cuda_stream
         d.side_stream = self.side.cuda_stream
@@ -255,6 +280,11 @@ class DecodeGroup:
         abi.check(abi.dsa_group_step(self.desc, scores, q, ids,
                                      None if timing is None else timing.array),
                   "dsa_group_step")
+        if self.policy == "reuse":
+            # the step swapped its buffers: this step's ids and selection are
+            # now the descriptor's previous ones
+            self.ids = self._bufs[self.desc.prev_ids]
+            self.sel = self._bufs[self.desc.prev_sel]
 
     def join(self, stream=None) -> None:
         """Make `stream` (default: the current stream) wait for all step work."""

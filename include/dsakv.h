@@ -62,6 +62,7 @@ typedef enum {
 #define TS_DEVERR_CTX 0x10        /* ctx_len outside [k, max_ctx] */
 #define TS_DEVERR_TIMEOUT 0x20    /* a bounded wait inside a kernel gave up */
 #define TS_DEVERR_COUNT 0x40      /* a selection did not come out at size k */
+#define TS_DEVERR_ORDER 0x80      /* ids not strictly ascending where a call needs them so */
 
 #define TS_D 576        /* values per latent row */
 #define TS_D_LATENT 512 /* latent ("nope") part, also the V part */
@@ -176,6 +177,29 @@ ts_status dsa_plan(const int32_t* ids, const int32_t* ctx_len, int B, int k,
                    int32_t* miss_rows, int32_t* ptr_next, int32_t* err, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * dsa_plan_reuse -- the base design's adjacent-step reuse ([GLM] §2.1
+ * GatherSelectionKvCache, §2.2), in the plan's form so that dsa_gather_kv
+ * serves it: the device keeps only the previous step's selection buffer
+ * (its row i holds the row of prev_ids[i]); a token the previous step also
+ * selected is a hit on that row, any other token a miss read from host.
+ *
+ *   ids       int32 [B][k]   strictly ascending per request (ts_topk's output)
+ *   prev_ids  int32 [B][k]   the previous step's ids, strictly ascending;
+ *                            -1 marks an empty entry (before the first step)
+ *   ctx_len   int32 [B]
+ * Outputs as dsa_plan's: src_map (hit: the row in the previous selection,
+ * miss of t: -1 - t, invalid: INT32_MIN), miss_ids / miss_pos (ascending),
+ * miss_count, miss_rows (= miss_count). Gather with dsa_gather_kv, the
+ * previous selection buffer as the pool (P = k). An id outside the context
+ * sets TS_DEVERR_ID_RANGE; ids not in strictly ascending order set
+ * TS_DEVERR_ORDER (the request's plan is then undefined). k <= 16384.
+ * ------------------------------------------------------------------------- */
+ts_status dsa_plan_reuse(const int32_t* ids, const int32_t* prev_ids, const int32_t* ctx_len,
+                         int B, int k, int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
+                         int32_t* miss_count, int32_t* miss_rows, int32_t* err,
+                         cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * dsa_gather_kv -- serve one layer's selected rows ([GLM] §5 DsaServe, §5.1;
  * base design §2.1 GatherSelectionKvCache). Row j of request b is copied from
  * the device pool when src_map >= 0 and read in place from pinned host memory
@@ -280,7 +304,8 @@ ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int H, int k,
  *   sync      uint32 [2 + 2 * layers] device words, zero before the first step
  *             and touched by nothing else; step = 0 before the first step.
  *             Each call uses sequence number step + 1 and stores it in
- *             `step` (the only field the call writes).
+ *             `step` (with the reuse policy it also swaps the buffers named
+ *             below; no other field is written).
  * Step inputs: scores float [B][ctx_stride] (device); q bf16
  * [layers][B][H][576] (device); ids int32 [B][k] (device) or NULL -- when
  * given, the top-k is skipped and these ids are planned.
@@ -324,7 +349,22 @@ typedef struct {
   cudaStream_t main_stream, gather_stream, side_stream;
   uint32_t* sync;
   uint32_t step;
+  /* pool policy: DSA_POLICY_FIFO, the set-associative FIFO pool above; or
+   * DSA_POLICY_REUSE, the base design's adjacent-step reuse (dsa_plan_reuse):
+   * the device keeps only the previous step's selection, prev_sel
+   * ([layers][B][k][576]) and its ids prev_ids ([B][k], -1 before the first
+   * step); pool, pool_tags, fifo_ptr, victim, install and ptr_next are not
+   * used, no refill runs, and each call then swaps ids <-> prev_ids and
+   * sel <-> prev_sel in the descriptor (so after a step prev_ids and
+   * prev_sel hold that step's ids and selection). Reuse needs the top-k
+   * inside the step (ids == NULL). */
+  int policy;
+  int32_t* prev_ids;
+  void* prev_sel;
 } dsa_group;
+
+#define DSA_POLICY_FIFO 0
+#define DSA_POLICY_REUSE 1
 
 ts_status dsa_group_step(dsa_group* g, const float* scores, const void* q, const int32_t* ids,
                          cudaEvent_t* timing);

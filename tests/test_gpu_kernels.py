@@ -381,3 +381,54 @@ def test_ts_copy_between_device_and_registered_host(d):
     assert d.ts_copy(dev, h_in.dev, 15) != 0           # not a multiple of 16 bytes
     h_in.close()
     h_out.close()
+
+
+# ---------------------------------------------------------------------------
+# adjacent-step reuse plan
+# ---------------------------------------------------------------------------
+
+def _plan_reuse(d, ids, prev, lens):
+    B, k = ids.shape
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+    out = {n: torch.zeros((B, k), dtype=torch.int32, device="cuda")
+           for n in ("src_map", "miss_ids", "miss_pos")}
+    mc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    mr = torch.zeros(B, dtype=torch.int32, device="cuda")
+    err = _err()
+    assert d.dsa_plan_reuse(t(ids), t(prev), t(lens), B, k, out["src_map"], out["miss_ids"],
+                            out["miss_pos"], mc, mr, err) == 0
+    bits = d.ts_read_error(err)
+    return {n: v.cpu().numpy() for n, v in out.items()}, mc.cpu().numpy(), mr.cpu().numpy(), bits
+
+
+@pytest.mark.parametrize("B,k,ctx,overlap", [(3, 300, 3000, 0.6), (2, 2048, 65536, 0.6),
+                                             (1, 1, 10, 1.0), (2, 513, 100000, 0.0)])
+def test_plan_reuse_matches_oracle(d, B, k, ctx, overlap):
+    rng = np.random.default_rng(k + B)
+    prev = np.stack([np.sort(rng.choice(ctx, k, replace=False)) for _ in range(B)]).astype(np.int32)
+    ids = []
+    for b in range(B):
+        keep = rng.choice(prev[b], int(round(overlap * k)), replace=False)
+        rest = rng.choice(np.setdiff1d(np.arange(ctx), prev[b]), k - keep.size, replace=False)
+        ids.append(np.sort(np.concatenate([keep, rest])))
+    ids = np.stack(ids).astype(np.int32)
+    lens = np.full(B, ctx, np.int32)
+    got, mc, mr, bits = _plan_reuse(d, ids, prev, lens)
+    assert bits == 0
+    for b in range(B):
+        p = oracle.plan_reuse(ids[b], prev[b], ctx)
+        assert np.array_equal(got["src_map"][b], p.src_map)
+        assert mc[b] == p.miss_count and mr[b] == p.miss_rows
+        assert np.array_equal(got["miss_ids"][b, :mc[b]], p.miss_ids)
+        assert np.array_equal(got["miss_pos"][b, :mc[b]], p.miss_pos)
+
+
+def test_plan_reuse_first_step_and_bad_input(d):
+    ids = np.array([[2, 5, 9]], np.int32)
+    got, mc, _, bits = _plan_reuse(d, ids, np.full((1, 3), -1, np.int32), np.array([10], np.int32))
+    assert bits == 0 and mc[0] == 3 and got["src_map"][0].tolist() == [-3, -6, -10]
+    _, _, _, bits = _plan_reuse(d, np.array([[2, 12, 9]], np.int32), np.full((1, 3), -1, np.int32),
+                                np.array([10], np.int32))
+    from decode_dsa_kv_gb300 import _abi
+    assert bits & _abi.TS_DEVERR_ID_RANGE      # 12 is past the context
+    assert bits & _abi.TS_DEVERR_ORDER         # 12 then 9: not ascending

@@ -78,6 +78,64 @@ def run_steps(d, w, steps, sample=None, sfa_layers=None, sfa_heads=None):
     return hit_rates
 
 
+def run_steps_reuse(d, w, steps, sfa_layers=(0,)):
+    """Decode steps with the adjacent-step reuse policy, against the oracle's
+    plan_reuse step by step: bit-exact ids, plan and selection bytes (which
+    must equal the host rows of the ids), SFA within tolerance. Returns the
+    per-step hit rates."""
+    lens = wl.ctx_lens(w)
+    host = d.HostKV(w.layers, w.B, w.ctx_stride)
+    wl.fill_host_kv(w, host.array)
+    g = d.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host, policy="reuse")
+    prev = {b: np.full(w.k, -1, np.int32) for b in range(w.B)}
+    scores_stream = wl.ScoreStream(w)
+    scale = 1 / math.sqrt(576)
+    rates = []
+    for step in range(steps):
+        scores = scores_stream.next()
+        q = wl.queries(w, step)
+        g.step(torch.from_numpy(scores).cuda(), torch.from_numpy(q.view(np.int16)).cuda())
+        assert g.synchronize() == 0, f"device error bits at step {step}"
+        ids = g.ids.cpu().numpy()
+        src = g.src_map.cpu().numpy()
+        rates.append(float((src >= 0).mean()))
+        for b in range(w.B):
+            ref_ids = oracle.topk_ids(scores[b], int(lens[b]), w.k)
+            assert np.array_equal(ids[b], ref_ids), (step, b)
+            p = oracle.plan_reuse(ref_ids, prev[b], int(lens[b]))
+            assert np.array_equal(src[b], p.src_map), (step, b)
+            M = p.miss_count
+            assert int(g.miss_count[b]) == M and int(g.miss_rows[b]) == M
+            assert np.array_equal(g.miss_ids[b, :M].cpu().numpy(), p.miss_ids)
+            assert np.array_equal(g.miss_pos[b, :M].cpu().numpy(), p.miss_pos)
+            for l in range(w.layers):
+                sel = g.sel[l, b].cpu().numpy().view(np.uint16)
+                assert np.array_equal(sel, host.array[l, b, ref_ids]), (step, b, l)
+            for l in sfa_layers:
+                o, _ = oracle.sfa_decode(q[l, b], host.array[l, b, ref_ids], scale)
+                got = g.out[l, b].cpu().view(torch.int16).numpy().view(np.uint16)
+                a_err, rel = sfa_errors(got, oracle.round_to_bf16_bits(o))
+                assert a_err <= SFA_ABS_TOL and rel <= SFA_MEAN_REL_TOL, (step, b, l, a_err, rel)
+            prev[b] = ref_ids
+    host.close()
+    return rates
+
+
+def test_reuse_policy_tiny(d):
+    rates = run_steps_reuse(d, wl.TINY, wl.TINY.steps)
+    assert rates[0] == 0.0 and max(rates[1:]) > 0.3
+
+
+def test_reuse_policy_decode_batch_scaled(d):
+    # the base design's reuse hits less often than the 8192-entry FIFO pool on
+    # the same score process (it keeps only the previous selection)
+    w = wl.scaled(wl.DECODE_BATCH, B=2)
+    reuse = run_steps_reuse(d, w, 5, sfa_layers=(2,))
+    fifo = run_steps(d, w, 5, sfa_layers=[])
+    assert 0.45 < np.mean(reuse[1:]) < 0.75
+    assert np.mean(fifo[1:]) > np.mean(reuse[1:])
+
+
 def test_tiny_all_steps(d):
     rates = run_steps(d, wl.TINY, wl.TINY.steps)
     assert rates[0] == 0.0 and max(rates[1:]) > 0.3
