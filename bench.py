@@ -67,6 +67,8 @@ def parse(argv=None):
                     help="after the warm-up steps, launch only this kernel --steps times "
                          "(on the state the warm-up left) and report its time per launch")
     ap.add_argument("--B", type=int, default=None, help="override the workload's request count")
+    ap.add_argument("--sets", type=int, default=None,
+                    help="override the pool's sets (16 ways each): 512 = 8K entries, 1024 = 16K")
     ap.add_argument("--policy", choices=("fifo", "reuse"), default="fifo",
                     help="device pool: the set-associative FIFO pool (default) or the base "
                          "design's adjacent-step reuse of the previous selection")
@@ -681,6 +683,8 @@ def main(argv=None):
         w = wl.scaled(w, B=args.B)
     if args.mtp:
         w = wl.scaled(w, H=w.H * (1 + args.mtp))
+    if args.sets:
+        w = wl.scaled(w, S=args.sets)
     if args.impl == "reference":
         run_reference(args, w, rank, world)
         return
