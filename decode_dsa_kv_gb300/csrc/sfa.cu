@@ -137,6 +137,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars->abort = 0;
     bars->issued = 0;
     mbar_fence_init();
+    // the first score loads go out now, while the CTA still sets itself up
+    // (the barriers are initialised; nobody reads the slots before waiting)
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    for (int it = 0; it < kSSlots && it < kScoreLoads; ++it) {
+      uint8_t* st = score_slot(it);
+      const int kb = it % kKB, nh = it / kKB;
+      mbar_expect_tx(&bars->full[it], kStageBytes);
+      tma_load_3d(st, &tm_q, &bars->full[it], kb * 64, hg * kHeads, b);
+      tma_load_3d(st + kQBytes, &tm_k, &bars->full[it], kb * 64, c * kChunk + nh * kHalfRows, b);
+      bars->issued = it + 1;
+    }
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_slot, 512);
@@ -150,12 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       // score phase: kSSlots slots; slots 2 and 3 borrow the P region, which
-      // the softmax fills only after every score product has completed
-      for (int it = 0; it < kScoreLoads; ++it) {
+      // the softmax fills only after every score product has completed (the
+      // first kSSlots loads were issued during the setup)
+      for (int it = bars->issued; it < kScoreLoads; ++it) {
         const int s = it % kSSlots;
         if (it >= kSSlots &&
             !mbar_wait_bounded(&bars->empty[s], ((it / kSSlots) - 1) & 1, abort, kWaitLimit))
