@@ -234,6 +234,6 @@ def sfa_mla_decode(q, sel_l, B, H, k, scale, out, lse, ws, ws_bytes, err=None,
 
 def dsa_group_step(group: DsaGroup, scores, q, ids=None, timing=None) -> int:
     """One decode step of the group; `timing` is None or a ctypes array of
-    2 * (2 + 3 * layers) event handles."""
+    2 * (3 + 2 * layers) event handles."""
     return _lib.dsa_group_step(ctypes.byref(group), ptr(scores), ptr(q), ptr(ids),
                                None if timing is None else ctypes.cast(timing, _P))
