@@ -5,9 +5,10 @@
 // group's last layer, updates the pool metadata (§4.4 refill after SFA, §5
 // DsaInstall, §5.1 metadata update at the group's last layer).
 //
-// Both are pure 16-byte copies of 1152-byte rows (72 pieces), one warp per
-// row: HBM for pool hits, pinned host memory read in place over the host link
-// for misses. Each warp keeps several rows' loads in flight before its stores.
+// Both are pure copies of 1152-byte rows: HBM for pool hits, pinned host
+// memory read in place over the host link for misses. The gather moves rows
+// through shared memory with bulk async copies, so a few SMs keep enough rows
+// in flight for the link and for HBM, and the attention keeps the rest.
 #include <climits>
 
 #include "common.cuh"
@@ -16,7 +17,8 @@
 namespace dsakv {
 namespace {
 
-constexpr int kGatherThreads = 1024;
+constexpr int kMissCtas = 8;  // gather CTAs reading missed rows over the host link
+constexpr int kHitCtas = 16;  // gather CTAs copying the other positions
 
 __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
   uint4 v;
@@ -44,36 +46,116 @@ __device__ __forceinline__ int first_pos_of(const int32_t* mids, const int32_t* 
   return (lo < M && __ldg(mids + lo) == t) ? __ldg(mpos + lo) : -1;
 }
 
-// Copy up to two 1152-byte rows with one warp: every lane moves the pieces
-// lane, lane+32 and lane+64 (< 72) of each row; all loads are issued before
-// any store, so a warp keeps up to 6 x 16 bytes per lane in flight.
-__device__ __forceinline__ void warp_copy_rows2(const uint4* from0, uint4* to0, const uint4* from1,
-                                                uint4* to1, int lane) {
-  uint4 a0, a1, a2, b0, b1, b2;
-  const bool third = lane < DSA_ROW_CHUNKS - 64;
-  if (from0) {
-    a0 = ld_nc_v4(from0 + lane);
-    a1 = ld_nc_v4(from0 + lane + 32);
-    if (third) a2 = ld_nc_v4(from0 + lane + 64);
-  }
-  if (from1) {
-    b0 = ld_nc_v4(from1 + lane);
-    b1 = ld_nc_v4(from1 + lane + 32);
-    if (third) b2 = ld_nc_v4(from1 + lane + 64);
-  }
-  if (from0) {
-    st_v4(to0 + lane, a0);
-    st_v4(to0 + lane + 32, a1);
-    if (third) st_v4(to0 + lane + 64, a2);
-  }
-  if (from1) {
-    st_v4(to1 + lane, b0);
-    st_v4(to1 + lane + 32, b1);
-    if (third) st_v4(to1 + lane + 64, b2);
-  }
-}
+// Rows through shared memory with bulk async copies (no registers hold the
+// rows, so a few SMs keep enough rows in flight for the host link or HBM).
+// Lane 0 of a warp issues everything: a row is loaded into one of
+// kPipeSlots ring slots and stored from there once it has arrived; a slot is
+// loaded again only after the store that read it kPipeLag stores earlier is
+// done reading. Waits are bounded; after a timeout the pipe issues nothing
+// more, still waits (bounded) for every load in flight, and reports.
+constexpr int kPipeSlots = 12;
+constexpr int kPipeLag = 2;
+constexpr int kPipeAhead = kPipeSlots - kPipeLag;  // loads in flight per warp
+constexpr int kPipeRetire = 4;  // stores after a layer's last before it counts out
+constexpr int kPipeWarps = 16;                     // warps per gather CTA
+constexpr uint64_t kBulkWaitNs = 100000000ull;     // 100 ms
+constexpr size_t kPipeWarpBytes = kPipeSlots * (DSA_ROW_BYTES + 16);  // ring, barriers, targets
+constexpr size_t kPipeSmemBytes = kPipeWarps * kPipeWarpBytes;
 
-// Row lists of one layer, for one warp of a role (see gather_kernel).
+struct RowPipe {
+  uint8_t* ring;
+  uint64_t* bars;
+  uint4** to;
+  uint32_t issued, stored;
+  bool failed;
+  // layer completion: the warp counts itself out of layer `pend` (its rows
+  // are the items below pend_end) once kPipeRetire later stores are issued,
+  // after waiting for all but those; the pipe never drains between layers
+  int pend;
+  uint32_t pend_end;
+  int nw;
+  uint32_t *count, *done, seq;
+
+  __device__ void init(uint8_t* warp_smem, int nw_, uint32_t* count_, uint32_t* done_,
+                       uint32_t seq_) {
+    ring = warp_smem;
+    bars = reinterpret_cast<uint64_t*>(warp_smem + kPipeSlots * DSA_ROW_BYTES);
+    to = reinterpret_cast<uint4**>(bars + kPipeSlots);
+    issued = stored = 0;
+    failed = false;
+    pend = -1;
+    pend_end = 0;
+    nw = nw_;
+    count = count_;
+    done = done_;
+    seq = seq_;
+    for (int s = 0; s < kPipeSlots; ++s) mbar_init(bars + s, 1);
+    mbar_fence_init();
+  }
+  // The warp's rows of layer l are written: count it out (the last warp of
+  // the launch writes seq into done[l]).
+  __device__ void signal(int l) {
+    if (!done) return;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
+    if (atomicAdd(count + l, 1u) == static_cast<uint32_t>(nw) - 1) {
+      __threadfence();
+      count[l] = 0;
+      atomicExch(done + l, seq);
+    }
+  }
+  // Store the oldest row in flight (or, after a failure, only wait for it).
+  __device__ void store_one() {
+    const uint32_t i = stored++;
+    const int s = static_cast<int>(i % kPipeSlots);
+    const bool ok = mbar_wait_timed(bars + s, (i / kPipeSlots) & 1u, kBulkWaitNs);
+    if (!ok) failed = true;
+    if (ok && !failed) {
+      bulk_store(to[s], ring + s * DSA_ROW_BYTES, DSA_ROW_BYTES);
+      bulk_commit();
+    }
+    if (pend >= 0 && stored == pend_end + kPipeRetire) {
+      // every store group but the last kPipeRetire (all after pend_end) done
+      if (failed) bulk_wait_all();
+      else bulk_wait<kPipeRetire>();
+      signal(pend);
+      pend = -1;
+    }
+  }
+  __device__ void push(const uint4* from, uint4* dst) {
+    if (failed) return;
+    while (stored + kPipeAhead <= issued) store_one();
+    if (failed) return;
+    bulk_wait_read<kPipeLag>();
+    const int s = static_cast<int>(issued % kPipeSlots);
+    to[s] = dst;
+    mbar_expect_tx(bars + s, DSA_ROW_BYTES);
+    bulk_load(ring + s * DSA_ROW_BYTES, from, DSA_ROW_BYTES, bars + s);
+    ++issued;
+  }
+  // Every row of layer l is pushed. A layer still pending from before is
+  // completed first (it had fewer than kPipeRetire stores after it).
+  __device__ void end_layer(int l) {
+    if (pend >= 0) {
+      while (stored < issued) store_one();
+      if (pend >= 0) {
+        bulk_wait_all();
+        signal(pend);
+      }
+    }
+    pend = l;
+    pend_end = issued;
+  }
+  // Every row pushed stored and written; the pending layer counted out.
+  __device__ void finish() {
+    while (stored < issued) store_one();
+    bulk_wait_all();
+    if (pend >= 0) signal(pend);
+    pend = -1;
+  }
+};
+
+// Row lists of one layer (see gather_kernel).
 struct GatherLayer {
   const uint4* pool;
   const uint4* host;
@@ -84,12 +166,12 @@ struct GatherLayer {
 // m = w, w + nrole, ... (request b holds miss_count[b] of them), so every miss
 // warp gets the same number of host rows whatever the spread of misses over
 // requests. Looked up 32 at a time, one candidate per lane; `mask` holds the
-// lanes with a row to move.
+// lanes with a row to move, which lane 0 pushes through the warp's pipe.
 __device__ __forceinline__ void gather_misses(const GatherLayer& L, const int32_t* miss_ids,
                                               const int32_t* miss_pos, const int32_t* miss_count,
                                               int B, int k, int64_t ctx_stride,
                                               const int32_t* ctx_len, int w, int nrole, int lane,
-                                              int& bad) {
+                                              RowPipe& pipe, int& bad) {
   // indices below B * k < 2^31 (B <= 65535, k <= 8192) fit in 32 bits
   const uint4* host = L.host;
   uint4* sel = L.sel;
@@ -130,113 +212,121 @@ __device__ __forceinline__ void gather_misses(const GatherLayer& L, const int32_
       m1 += 32 * nrole;
       continue;
     }
-    const uint4* from[2] = {nullptr, nullptr};
-    uint4* to[2] = {nullptr, nullptr};
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      if (mask) {
-        const int q = __ffs(mask) - 1;
-        mask &= mask - 1;
-        from[e] = reinterpret_cast<const uint4*>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_from), q));
-        to[e] = reinterpret_cast<uint4*>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_to), q));
-      }
+    while (mask) {
+      const int q = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const uint4* f = reinterpret_cast<const uint4*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_from), q));
+      uint4* t =
+          reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_to), q));
+      if (lane == 0) pipe.push(f, t);
+      __syncwarp();
     }
-    warp_copy_rows2(from[0], to[0], from[1], to[1], lane);
   }
 }
 
 // The positions: the pool row for a hit; for a miss, the host row only when
 // the token repeats and this is not its first position (gather_misses serves
-// first positions). Requests without repeats (miss_rows == miss_count) skip
-// misses outright.
-__device__ __forceinline__ void gather_positions(const GatherLayer& L, const int32_t* src_map,
-                                                 const int32_t* miss_ids, const int32_t* miss_pos,
-                                                 const int32_t* miss_count,
-                                                 const int32_t* miss_rows, int B, int k, int P,
-                                                 int64_t ctx_stride, const int32_t* ctx_len,
-                                                 int w, int nrole, int lane, int& bad) {
-  const uint4* pool = L.pool;
-  const uint4* host = L.host;
-  uint4* sel = L.sel;
+// first positions; requests without repeats, miss_rows == miss_count, skip
+// misses outright). 32 positions at a time, one lookup per lane, pushed
+// through the warp's pipe by lane 0.
+__device__ __forceinline__ void gather_positions(
+    const GatherLayer& L, const int32_t* src_map, const int32_t* miss_ids, const int32_t* miss_pos,
+    const int32_t* miss_count, const int32_t* miss_rows, int B, int k, int P, int64_t ctx_stride,
+    const int32_t* ctx_len, int w, int nrole, int lane, RowPipe& pipe, int& bad) {
   const int64_t rows = int64_t(B) * k;
-  for (int64_t r0 = int64_t(w) * 2; r0 < rows; r0 += int64_t(nrole) * 2) {
-    const uint4* from[2] = {nullptr, nullptr};
-    uint4* to[2] = {nullptr, nullptr};
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int64_t r = r0 + e;
-      if (r >= rows) continue;
+  const int64_t step = int64_t(nrole) * 32;
+  // the next batch's src_map entries are loaded before this batch's rows are
+  // pushed, so the lookup does not stall the pipe
+  int src_next = int64_t(w) * 32 + lane < rows ? __ldg(src_map + int64_t(w) * 32 + lane) : 0;
+  for (int64_t r0 = int64_t(w) * 32; r0 < rows; r0 += step) {
+    const int64_t r = r0 + lane;
+    const int src = src_next;
+    if (r + step < rows) src_next = __ldg(src_map + r + step);
+    const uint4* from = nullptr;
+    if (r < rows) {
       const int b = static_cast<int>(r / k);
       const int j = static_cast<int>(r - int64_t(b) * k);
-      const int src = __ldg(src_map + r);
       if (src >= 0) {
-        if (src < P) from[e] = pool + (int64_t(b) * P + src) * DSA_ROW_CHUNKS;
+        if (src < P) from = L.pool + (int64_t(b) * P + src) * DSA_ROW_CHUNKS;
         else bad |= TS_DEVERR_SLOT_RANGE;
       } else if (src != INT_MIN) {
         const int M = __ldg(miss_count + b);
-        if (__ldg(miss_rows + b) == M) continue;  // no repeats: served as a miss
         const int t = -1 - src;
         const int64_t base = int64_t(b) * k;
-        if (first_pos_of(miss_ids + base, miss_pos + base, M, t) == j) continue;
-        if (t < __ldg(ctx_len + b) && t < ctx_stride)
-          from[e] = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
-        else bad |= TS_DEVERR_ID_RANGE;
+        if (__ldg(miss_rows + b) != M && first_pos_of(miss_ids + base, miss_pos + base, M, t) != j) {
+          if (t < __ldg(ctx_len + b) && t < ctx_stride)
+            from = L.host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
+          else bad |= TS_DEVERR_ID_RANGE;
+        }
       } else {
         bad |= TS_DEVERR_ID_RANGE;
       }
-      if (from[e]) to[e] = sel + r * DSA_ROW_CHUNKS;
     }
-    warp_copy_rows2(from[0], to[0], from[1], to[1], lane);
+    uint4* to = L.sel + r * DSA_ROW_CHUNKS;
+    uint32_t mask = __ballot_sync(0xffffffffu, from != nullptr);
+    while (mask) {
+      const int q = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const uint4* f = reinterpret_cast<const uint4*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(from), q));
+      uint4* t = reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(to), q));
+      if (lane == 0) pipe.push(f, t);
+      __syncwarp();
+    }
   }
 }
 
 // One launch for `layers` consecutive layers (layer l's pool, host rows and
 // selection start l * pool_stride / host_stride / sel_stride pieces after
-// layer 0's), two kinds of warps (alternating), each moving two rows per step:
-//   even warps: gather_misses, the host-link reads that set the kernel's time;
-//   odd warps: gather_positions, the pool hits (HBM), beside them.
-// The two kinds write disjoint positions, so the HBM copies of the hits hide
-// under the host-link time of the misses. Every warp finishes a layer before
-// it starts the next. With `done` given, each warp counts itself out of
-// layer l in count[l] once its rows are written (after a fence), and the last
-// one resets the count and writes `seq` into done[l]: another stream's
-// stream-memory wait on done[l] then orders the layer's consumers after its
-// rows. The launch's own completion orders them for the per-layer call.
-__global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(
+// layer 0's), in two kinds of CTAs of kPipeWarps warps, every warp with its
+// own RowPipe:
+//   CTAs [0, miss_ctas): gather_misses, the host-link reads that set the
+//     kernel's time (a few SMs keep the link busy);
+//   the others: gather_positions, the pool hits (HBM), beside them.
+// The two kinds write disjoint positions. Every warp finishes pushing a layer
+// before it starts the next and keeps its pipe full across the boundary.
+// With `done` given, each warp counts itself out of layer l in count[l] once
+// its rows of the layer are written, and the last one resets the count and
+// writes `seq` into done[l]: another stream's stream-memory wait on done[l]
+// then orders the layer's consumers after its rows. The launch's own
+// completion orders them for the per-layer call.
+__global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
     const int32_t* __restrict__ src_map, const int32_t* __restrict__ miss_ids,
     const int32_t* __restrict__ miss_pos, const int32_t* __restrict__ miss_count,
     const int32_t* __restrict__ miss_rows, int B, int k, const uint4* __restrict__ pool, int P,
     const uint4* __restrict__ host, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
     uint4* __restrict__ sel, int layers, int64_t pool_stride, int64_t host_stride,
     int64_t sel_stride, uint32_t* __restrict__ done, uint32_t* __restrict__ count, uint32_t seq,
-    int32_t* err) {
+    int miss_ctas, int32_t* err) {
+  extern __shared__ __align__(128) uint8_t gather_smem[];
   const int lane = threadIdx.x & 31;
-  const int gw = static_cast<int>((blockIdx.x * kGatherThreads + threadIdx.x) >> 5);
-  const int nw = static_cast<int>((gridDim.x * kGatherThreads) >> 5);
-  const bool miss_warp = (gw & 1) == 0;
-  const int w = gw >> 1;
-  const int nrole = miss_warp ? (nw + 1) >> 1 : nw >> 1;
+  const int wc = threadIdx.x >> 5;  // warp in the CTA
+  const int nw = static_cast<int>(gridDim.x) * kPipeWarps;
+  const bool miss_cta = static_cast<int>(blockIdx.x) < miss_ctas;
+  const int cta = miss_cta ? blockIdx.x : blockIdx.x - miss_ctas;
+  const int w = cta * kPipeWarps + wc;
+  const int nrole = (miss_cta ? miss_ctas : static_cast<int>(gridDim.x) - miss_ctas) * kPipeWarps;
   int bad = 0;
+  RowPipe pipe;
+  if (lane == 0) pipe.init(gather_smem + wc * kPipeWarpBytes, nw, count, done, seq);
+  __syncwarp();
   for (int l = 0; l < layers; ++l) {
     const GatherLayer L{pool + l * pool_stride, host + l * host_stride, sel + l * sel_stride};
-    if (miss_warp)
+    if (miss_cta)
       gather_misses(L, miss_ids, miss_pos, miss_count, B, k, ctx_stride, ctx_len, w, nrole, lane,
-                    bad);
+                    pipe, bad);
     else
       gather_positions(L, src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, P,
-                       ctx_stride, ctx_len, w, nrole, lane, bad);
-    if (done) {
-      __threadfence();  // this lane's rows, before the warp counts itself out
-      __syncwarp();
-      if (lane == 0 && atomicAdd(count + l, 1u) == static_cast<uint32_t>(nw) - 1) {
-        __threadfence();
-        count[l] = 0;
-        atomicExch(done + l, seq);
-      }
-    }
+                       ctx_stride, ctx_len, w, nrole, lane, pipe, bad);
+    if (lane == 0) pipe.end_layer(l);
+    __syncwarp();
   }
+  if (lane == 0) {
+    pipe.finish();
+    if (pipe.failed) bad |= TS_DEVERR_TIMEOUT;
+  }
+  bad = __reduce_or_sync(0xffffffffu, bad);  // lookups are per lane
   if (bad && lane == 0) report(err, bad);
 }
 
@@ -319,23 +409,23 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
                          const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream,
                          int layers, size_t pool_layer_bytes, size_t host_layer_bytes,
                          size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq) {
-  // 3/8 of the SMs, one 1024-thread CTA each: with the attention and the
-  // refill running beside it the host link needs this many loads in flight
-  // (measured on decode_batch, whole step: 1/4 of the SMs 584 us, 1/3 554,
-  // 3/8 544, 1/2 561: beyond 3/8 the attention, on the other SMs, runs
-  // short). Measured alternatives that did worse: small CTAs on every SM (the
-  // zero-copy loads slow an attention CTA on the same SM by about 2x), and
-  // cp.async staging through shared memory (reads of host memory top out near
-  // half the link's rate that way).
-  const int64_t rows = int64_t(B) * k;
-  int64_t blocks = (rows + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
-  const int64_t cap = sm_count() * 3 / 8 > 8 ? sm_count() * 3 / 8 : 8;
-  if (blocks > cap) blocks = cap;
-  gather_kernel<<<static_cast<unsigned>(blocks), kGatherThreads, 0, stream>>>(
+  // kMissCtas + kHitCtas CTAs (24 SMs): the misses' share of them reads at
+  // the host link's rate (measured alone: 8 SMs of bulk copies reach the
+  // same ~205 GB/s as plain loads on 16-57 SMs), the rest copy the hits at
+  // HBM speed, and each layer's attention fits in one wave on the SMs left
+  // (decode_batch: 128 CTAs; with the gather on 57 SMs it took two).
+  // Measured alternatives that did worse: plain loads on 3/8 of the SMs
+  // (the earlier design, 0.549 vs 0.540 ms a step), other splits (9 + 15,
+  // 10 + 14, 12 + 12, 6 + 18, 4 + 20 CTAs), 8 or 32 warps per CTA.
+  static const bool attr =
+      cudaFuncSetAttribute(gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kPipeSmemBytes)) == cudaSuccess;
+  if (!attr) return TS_ERR_CUDA;
+  gather_kernel<<<kMissCtas + kHitCtas, kPipeWarps * 32, kPipeSmemBytes, stream>>>(
       src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, static_cast<const uint4*>(pool_l), P,
       static_cast<const uint4*>(host_l), ctx_stride, ctx_len, static_cast<uint4*>(sel_l), layers,
       int64_t(pool_layer_bytes / 16), int64_t(host_layer_bytes / 16), int64_t(sel_layer_bytes / 16),
-      done, count, seq, err);
+      done, count, seq, kMissCtas, err);
   return launch_status();
 }
 
