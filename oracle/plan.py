@@ -41,6 +41,17 @@ class Plan:
         return int(self.miss_ids.size)
 
     @property
+    def install_code(self) -> np.ndarray:
+        """uint8 [M], when each miss may be written into its victim slot:
+        0 not installed; 1 the slot is read by no position of this step, so
+        the row may go in as soon as it arrives; 2 the slot is read as a hit
+        in this step, so the row goes in only after the layer's hits are read
+        ([GLM] §4.4: each layer reads its rows before its own refill)."""
+        hit_slots = {int(s) for s in self.src_map if s >= 0}
+        return np.asarray([0 if not keep else 2 if int(v) in hit_slots else 1
+                           for v, keep in zip(self.victim, self.install)], dtype=np.uint8)
+
+    @property
     def miss_rows(self) -> int:
         """Positions that miss, a repeated missed id counted at each position."""
         return int(np.sum((self.src_map < 0) & (self.src_map != np.iinfo(np.int32).min)))

@@ -146,3 +146,45 @@ def test_rejects_bad_input():
         dsa_plan([3, 40], 20, [-1] * 4, [0, 0], 2, 2)      # id past the context
     with pytest.raises(ValueError):
         dsa_plan([3], 20, [-1] * 4, [0, 2], 2, 2)          # pointer >= W
+
+
+def test_install_code_orders_installs_around_hit_reads():
+    """install_code splits the installs into those that may land before the
+    step's hits are read (1) and those that must wait for the reads (2):
+    writing the 1s first, then reading every hit, then writing the 2s serves
+    every hit its own token and leaves the simulator's final cache. Writing
+    all installs before the reads breaks a hit in some of these steps, so the
+    split is needed (the page: each layer reads its rows before its own refill,
+    §4.4)."""
+    rng = np.random.default_rng(23)
+    needed = 0
+    for trial in range(60):
+        S = int(rng.choice([1, 2, 4]))
+        W = int(rng.choice([1, 2, 4]))
+        ctx = int(rng.integers(8, 48))
+        tags = [-1] * (S * W)
+        ptr = [0] * S
+        for step in range(6):
+            k = int(rng.integers(1, ctx + 1))
+            ids = sorted(rng.choice(ctx, size=k, replace=False).tolist())
+            plan = dsa_plan(ids, ctx, tags, ptr, S, W)
+            code = plan.install_code
+            assert code.tolist() == [0 if not keep else code[i] for i, keep in enumerate(plan.install)]
+            _, _, tags_end, ptr_end = fifo_simulate(ids, tags, ptr, S, W)
+            for order in ("split", "all_first"):
+                pool = list(tags)               # a slot's row is its token
+                for t, v, c in zip(plan.miss_ids, plan.victim, code):
+                    if c == 1 or (order == "all_first" and c == 2):
+                        pool[v] = int(t)
+                served = [pool[s] == t for s, t in zip(plan.src_map, ids) if s >= 0]
+                if order == "split":
+                    assert all(served), (trial, step)
+                    for t, v, c in zip(plan.miss_ids, plan.victim, code):
+                        if c == 2:
+                            pool[v] = int(t)
+                    assert pool == tags_end
+                elif not all(served):
+                    needed += 1
+                    assert any(c == 2 for c in code)
+            tags, ptr = tags_end, ptr_end
+    assert needed > 0
