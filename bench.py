@@ -302,9 +302,14 @@ def traffic_record(kernel: str, workload: str):
 # algorithmic bytes / flops per launch
 # ---------------------------------------------------------------------------
 
-def algorithmic(w: wl.Workload, lens, hit_frac: float, install_frac: float):
+def algorithmic(w: wl.Workload, lens, hit_frac: float, install_frac: float,
+                deferred_frac: float = None):
     """Per-launch algorithmic work of every kernel, with the measured hit and
-    install fractions (per selected row)."""
+    install fractions (per selected row). The gather writes the installs
+    whose victim slots no hit of the step reads; the refill copies the rest
+    (`deferred_frac`; all installs when None, as in the per-layer calls)."""
+    direct = 0.0 if deferred_frac is None else install_frac - deferred_frac
+    deferred = install_frac if deferred_frac is None else deferred_frac
     rows = w.B * w.k
     row = 1152
     out = {}
@@ -312,9 +317,10 @@ def algorithmic(w: wl.Workload, lens, hit_frac: float, install_frac: float):
     out["plan"] = {"hbm_bytes": rows * (4 + 4) + w.B * (w.P * 4 + 2 * w.S * 4)
                    + rows * (1 - hit_frac) * (4 * 3 + 1), "link_bytes": 0.0}
     # one launch gathers every layer
-    out["gather"] = {"hbm_bytes": w.layers * rows * (hit_frac * row + row + 4),
+    out["gather"] = {"hbm_bytes": w.layers * rows * (hit_frac * row + row + direct * row + 4),
                      "link_bytes": w.layers * rows * (1 - hit_frac) * row}
-    out["refill"] = {"hbm_bytes": rows * install_frac * (2 * row + 13), "link_bytes": 0.0}
+    out["refill"] = {"hbm_bytes": rows * (deferred * 2 * row + install_frac * 13),
+                     "link_bytes": 0.0}
     out["sfa"] = {"hbm_bytes": rows * row + w.B * w.H * (1152 + 1024),
                   "link_bytes": 0.0, "flops": 2.0 * w.B * w.H * w.k * (576 + 512)}
     return out
@@ -514,9 +520,14 @@ def run_native(args, w, rank, world, local):
     misses = miss_log.double().sum().item()
     hit_frac = 1.0 - misses / (args.steps * w.B * w.k)
     install_frac = (1.0 - hit_frac)   # installs ~ misses (overflow sets install fewer)
+    deferred_frac = None
+    if args.policy == "fifo":
+        # installs into slots read as hits in the same step (the last step's plan)
+        valid = torch.arange(w.k, device="cuda")[None, :] < g.miss_count[:, None]
+        deferred_frac = float(((g.install == 2) & valid).sum().item()) / (w.B * w.k)
 
     per_kernel = {}
-    alg = algorithmic(w, lens, hit_frac, install_frac)
+    alg = algorithmic(w, lens, hit_frac, install_frac, deferred_frac)
     launch_ms = {n: [] for n in KERNELS}
     for t in timings or []:
         for n, v in t.ms().items():
@@ -619,6 +630,7 @@ def run_native(args, w, rank, world, local):
                                       + LAUNCHES_GATHER + w.layers * LAUNCHES_PER_LAYER),
         "clocks": clocks,
         "hit_rate": hit_frac,
+        "deferred_install_frac": deferred_frac,
         "host_enqueue_ms_per_step": (t_enq1 - t_enq0) * 1e3 / args.steps,
         "settle_steps": base[0],
         "link_peak_gbs": link,

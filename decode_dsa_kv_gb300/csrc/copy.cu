@@ -59,13 +59,14 @@ constexpr int kPipeAhead = kPipeSlots - kPipeLag;  // loads in flight per warp
 constexpr int kPipeRetire = 4;  // stores after a layer's last before it counts out
 constexpr int kPipeWarps = 16;                     // warps per gather CTA
 constexpr uint64_t kBulkWaitNs = 100000000ull;     // 100 ms
-constexpr size_t kPipeWarpBytes = kPipeSlots * (DSA_ROW_BYTES + 16);  // ring, barriers, targets
+constexpr size_t kPipeWarpBytes = kPipeSlots * (DSA_ROW_BYTES + 24);  // ring, barriers, targets
 constexpr size_t kPipeSmemBytes = kPipeWarps * kPipeWarpBytes;
 
 struct RowPipe {
   uint8_t* ring;
   uint64_t* bars;
   uint4** to;
+  uint4** to2;  // a second target of the row, or null
   uint32_t issued, stored;
   bool failed;
   // layer completion: the warp counts itself out of layer `pend` (its rows
@@ -81,6 +82,7 @@ struct RowPipe {
     ring = warp_smem;
     bars = reinterpret_cast<uint64_t*>(warp_smem + kPipeSlots * DSA_ROW_BYTES);
     to = reinterpret_cast<uint4**>(bars + kPipeSlots);
+    to2 = to + kPipeSlots;
     issued = stored = 0;
     failed = false;
     pend = -1;
@@ -112,6 +114,7 @@ struct RowPipe {
     if (!ok) failed = true;
     if (ok && !failed) {
       bulk_store(to[s], ring + s * DSA_ROW_BYTES, DSA_ROW_BYTES);
+      if (to2[s]) bulk_store(to2[s], ring + s * DSA_ROW_BYTES, DSA_ROW_BYTES);
       bulk_commit();
     }
     if (pend >= 0 && stored == pend_end + kPipeRetire) {
@@ -122,13 +125,14 @@ struct RowPipe {
       pend = -1;
     }
   }
-  __device__ void push(const uint4* from, uint4* dst) {
+  __device__ void push(const uint4* from, uint4* dst, uint4* dst2 = nullptr) {
     if (failed) return;
     while (stored + kPipeAhead <= issued) store_one();
     if (failed) return;
     bulk_wait_read<kPipeLag>();
     const int s = static_cast<int>(issued % kPipeSlots);
     to[s] = dst;
+    to2[s] = dst2;
     mbar_expect_tx(bars + s, DSA_ROW_BYTES);
     bulk_load(ring + s * DSA_ROW_BYTES, from, DSA_ROW_BYTES, bars + s);
     ++issued;
@@ -157,7 +161,7 @@ struct RowPipe {
 
 // Row lists of one layer (see gather_kernel).
 struct GatherLayer {
-  const uint4* pool;
+  uint4* pool;  // read for hits; written for installs on arrival
   const uint4* host;
   uint4* sel;
 };
@@ -167,9 +171,13 @@ struct GatherLayer {
 // warp gets the same number of host rows whatever the spread of misses over
 // requests. Looked up 32 at a time, one candidate per lane; `mask` holds the
 // lanes with a row to move, which lane 0 pushes through the warp's pipe.
+// With `victim` given, a miss with install code 1 (its victim slot is read by
+// no position of this step) is also written into that slot of the pool as it
+// arrives, which leaves the refill only the code-2 installs.
 __device__ __forceinline__ void gather_misses(const GatherLayer& L, const int32_t* miss_ids,
                                               const int32_t* miss_pos, const int32_t* miss_count,
-                                              int B, int k, int64_t ctx_stride,
+                                              const int32_t* victim, const uint8_t* install,
+                                              int B, int k, int P, int64_t ctx_stride,
                                               const int32_t* ctx_len, int w, int nrole, int lane,
                                               RowPipe& pipe, int& bad) {
   // indices below B * k < 2^31 (B <= 65535, k <= 8192) fit in 32 bits
@@ -180,6 +188,7 @@ __device__ __forceinline__ void gather_misses(const GatherLayer& L, const int32_
   uint32_t mask = 0;
   const uint4* my_from = nullptr;
   uint4* my_to = nullptr;
+  uint4* my_to2 = nullptr;
   for (;;) {
     if (mask == 0) {
       if (b1 >= B) break;
@@ -201,6 +210,12 @@ __device__ __forceinline__ void gather_misses(const GatherLayer& L, const int32_
         } else {
           my_from = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
           my_to = sel + (int64_t(b) * k + j) * DSA_ROW_CHUNKS;
+          my_to2 = nullptr;
+          if (victim && __ldg(install + s) == 1) {
+            const int v = __ldg(victim + s);
+            if (v >= 0 && v < P) my_to2 = L.pool + (int64_t(b) * P + v) * DSA_ROW_CHUNKS;
+            else bad |= TS_DEVERR_SLOT_RANGE;
+          }
           valid = true;
         }
       }
@@ -219,7 +234,9 @@ __device__ __forceinline__ void gather_misses(const GatherLayer& L, const int32_
           __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_from), q));
       uint4* t =
           reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_to), q));
-      if (lane == 0) pipe.push(f, t);
+      uint4* t2 = reinterpret_cast<uint4*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_to2), q));
+      if (lane == 0) pipe.push(f, t, t2);
       __syncwarp();
     }
   }
@@ -284,7 +301,9 @@ __device__ __forceinline__ void gather_positions(
 //   CTAs [0, miss_ctas): gather_misses, the host-link reads that set the
 //     kernel's time (a few SMs keep the link busy);
 //   the others: gather_positions, the pool hits (HBM), beside them.
-// The two kinds write disjoint positions. Every warp finishes pushing a layer
+// The two kinds write disjoint positions; with `victim` given the miss CTAs
+// also install the code-1 misses into the pool (slots no hit of the step
+// reads). Every warp finishes pushing a layer
 // before it starts the next and keeps its pipe full across the boundary.
 // With `done` given, each warp counts itself out of layer l in count[l] once
 // its rows of the layer are written, and the last one resets the count and
@@ -294,7 +313,8 @@ __device__ __forceinline__ void gather_positions(
 __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
     const int32_t* __restrict__ src_map, const int32_t* __restrict__ miss_ids,
     const int32_t* __restrict__ miss_pos, const int32_t* __restrict__ miss_count,
-    const int32_t* __restrict__ miss_rows, int B, int k, const uint4* __restrict__ pool, int P,
+    const int32_t* __restrict__ miss_rows, const int32_t* __restrict__ victim,
+    const uint8_t* __restrict__ install, int B, int k, uint4* pool, int P,
     const uint4* __restrict__ host, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
     uint4* __restrict__ sel, int layers, int64_t pool_stride, int64_t host_stride,
     int64_t sel_stride, uint32_t* __restrict__ done, uint32_t* __restrict__ count, uint32_t seq,
@@ -314,8 +334,8 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
   for (int l = 0; l < layers; ++l) {
     const GatherLayer L{pool + l * pool_stride, host + l * host_stride, sel + l * sel_stride};
     if (miss_cta)
-      gather_misses(L, miss_ids, miss_pos, miss_count, B, k, ctx_stride, ctx_len, w, nrole, lane,
-                    pipe, bad);
+      gather_misses(L, miss_ids, miss_pos, miss_count, victim, install, B, k, P, ctx_stride,
+                    ctx_len, w, nrole, lane, pipe, bad);
     else
       gather_positions(L, src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, P,
                        ctx_stride, ctx_len, w, nrole, lane, pipe, bad);
@@ -330,9 +350,10 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
   if (bad && lane == 0) report(err, bad);
 }
 
-// One warp per (request, miss) pair and every layer of the call: 72 pieces
-// per row, lanes stride by 32. Layer l's selection and pool start sel_stride
-// and pool_stride 16-byte pieces after layer l-1's.
+// The installs of every layer of the call: 32 (request, miss) entries per
+// warp at a time, then one row after the other with the whole warp (72
+// pieces per row, lanes stride by 32). Layer l's selection and pool start
+// sel_stride and pool_stride 16-byte pieces after layer l-1's.
 constexpr int kRefillThreads = 256;
 __global__ void __launch_bounds__(kRefillThreads) refill_kernel(
     const int32_t* __restrict__ miss_ids, const int32_t* __restrict__ miss_pos,
@@ -340,34 +361,51 @@ __global__ void __launch_bounds__(kRefillThreads) refill_kernel(
     const int32_t* __restrict__ miss_count, int B, int k, const uint4* __restrict__ sel,
     uint4* __restrict__ pool, int P, int layers, int64_t sel_stride, int64_t pool_stride,
     int update_metadata, int32_t* __restrict__ pool_tags, int32_t* __restrict__ fifo_ptr,
-    const int32_t* __restrict__ ptr_next, int S, int W, int32_t* err) {
+    const int32_t* __restrict__ ptr_next, int S, int W, int min_install, int32_t* err) {
   const int lane = threadIdx.x & 31;
   const int warp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int nwarps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
   const int rows = B * k;  // < 2^31: B <= 65535, k <= 8192
-  for (int r = warp; r < rows; r += nwarps) {
-    const int b = r / k;
-    const int i = r - b * k;
-    if (i >= __ldg(miss_count + b)) continue;
-    if (!__ldg(install + r)) continue;
-    const int v = __ldg(victim + r);
-    const int j = __ldg(miss_pos + r);
-    if (v < 0 || v >= P || j < 0 || j >= k) {
-      if (lane == 0) report(err, TS_DEVERR_SLOT_RANGE);
-      continue;
+  // 32 entries at a time, one per lane; then the warp copies the rows that
+  // need it, one after the other
+  for (int r0 = warp * 32; r0 < rows; r0 += nwarps * 32) {
+    const int r = r0 + lane;
+    bool need = false;
+    int64_t from_row = 0, to_row = 0;
+    if (r < rows) {
+      const int b = r / k;
+      const int i = r - b * k;
+      const int code = i < __ldg(miss_count + b) ? __ldg(install + r) : 0;
+      if (code) {
+        const int v = __ldg(victim + r);
+        const int j = __ldg(miss_pos + r);
+        if (v < 0 || v >= P || j < 0 || j >= k) {
+          report(err, TS_DEVERR_SLOT_RANGE);
+        } else {
+          if (update_metadata) pool_tags[int64_t(b) * P + v] = __ldg(miss_ids + r);
+          // (rows with a lower code went in with the gather)
+          need = code >= min_install;
+          from_row = int64_t(b) * k + j;
+          to_row = int64_t(b) * P + v;
+        }
+      }
     }
-    const uint4* from = sel + (int64_t(b) * k + j) * DSA_ROW_CHUNKS + lane;
-    uint4* to = pool + (int64_t(b) * P + v) * DSA_ROW_CHUNKS + lane;
-    for (int l = 0; l < layers; ++l) {
-      const uint4 x0 = ld_nc_v4(from);
-      const uint4 x1 = ld_nc_v4(from + 32);
-      st_v4(to, x0);
-      st_v4(to + 32, x1);
-      if (lane < DSA_ROW_CHUNKS - 64) st_v4(to + 64, ld_nc_v4(from + 64));
-      from += sel_stride;
-      to += pool_stride;
+    uint32_t mask = __ballot_sync(0xffffffffu, need);
+    while (mask) {
+      const int q = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const uint4* from = sel + __shfl_sync(0xffffffffu, from_row, q) * DSA_ROW_CHUNKS + lane;
+      uint4* to = pool + __shfl_sync(0xffffffffu, to_row, q) * DSA_ROW_CHUNKS + lane;
+      for (int l = 0; l < layers; ++l) {
+        const uint4 x0 = ld_nc_v4(from);
+        const uint4 x1 = ld_nc_v4(from + 32);
+        st_v4(to, x0);
+        st_v4(to + 32, x1);
+        if (lane < DSA_ROW_CHUNKS - 64) st_v4(to + 64, ld_nc_v4(from + 64));
+        from += sel_stride;
+        to += pool_stride;
+      }
     }
-    if (update_metadata && lane == 0) pool_tags[int64_t(b) * P + v] = __ldg(miss_ids + r);
   }
   if (update_metadata) {
     const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -408,7 +446,8 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
                          const void* pool_l, int P, const void* host_l, int64_t ctx_stride,
                          const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream,
                          int layers, size_t pool_layer_bytes, size_t host_layer_bytes,
-                         size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq) {
+                         size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq,
+                         const int32_t* victim, const uint8_t* install) {
   // kMissCtas + kHitCtas CTAs (24 SMs): the misses' share of them reads at
   // the host link's rate (measured alone: 8 SMs of bulk copies reach the
   // same ~205 GB/s as plain loads on 16-57 SMs), the rest copy the hits at
@@ -422,10 +461,11 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
                            static_cast<int>(kPipeSmemBytes)) == cudaSuccess;
   if (!attr) return TS_ERR_CUDA;
   gather_kernel<<<kMissCtas + kHitCtas, kPipeWarps * 32, kPipeSmemBytes, stream>>>(
-      src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, static_cast<const uint4*>(pool_l), P,
-      static_cast<const uint4*>(host_l), ctx_stride, ctx_len, static_cast<uint4*>(sel_l), layers,
-      int64_t(pool_layer_bytes / 16), int64_t(host_layer_bytes / 16), int64_t(sel_layer_bytes / 16),
-      done, count, seq, kMissCtas, err);
+      src_map, miss_ids, miss_pos, miss_count, miss_rows, victim, install, B, k,
+      static_cast<uint4*>(const_cast<void*>(pool_l)), P, static_cast<const uint4*>(host_l),
+      ctx_stride, ctx_len, static_cast<uint4*>(sel_l), layers, int64_t(pool_layer_bytes / 16),
+      int64_t(host_layer_bytes / 16), int64_t(sel_layer_bytes / 16), done, count, seq, kMissCtas,
+      err);
   return launch_status();
 }
 
@@ -448,7 +488,7 @@ ts_status refill_enqueue(const int32_t* miss_ids, const int32_t* miss_pos, const
                          const void* sel_l, void* pool_l, int P, int update_metadata,
                          int32_t* pool_tags, int32_t* fifo_ptr, const int32_t* ptr_next, int S,
                          int W, int32_t* err, cudaStream_t stream, int layers,
-                         size_t sel_layer_bytes, size_t pool_layer_bytes) {
+                         size_t sel_layer_bytes, size_t pool_layer_bytes, int min_install) {
   // one warp per (request, miss); one small CTA per SM, which fits beside an
   // attention CTA (measured best of 16 or 38 1024-thread CTAs and 76 or 152
   // 256-thread ones, beside the attention and the next layer's gather)
@@ -460,7 +500,8 @@ ts_status refill_enqueue(const int32_t* miss_ids, const int32_t* miss_pos, const
   refill_kernel<<<static_cast<unsigned>(blocks), kRefillThreads, 0, stream>>>(
       miss_ids, miss_pos, victim, install, miss_count, B, k, static_cast<const uint4*>(sel_l),
       static_cast<uint4*>(pool_l), P, layers, int64_t(sel_layer_bytes / 16),
-      int64_t(pool_layer_bytes / 16), update_metadata, pool_tags, fifo_ptr, ptr_next, S, W, err);
+      int64_t(pool_layer_bytes / 16), update_metadata, pool_tags, fifo_ptr, ptr_next, S, W,
+      min_install, err);
   return launch_status();
 }
 
@@ -477,7 +518,7 @@ extern "C" ts_status dsa_gather_kv(const int32_t* src_map, const int32_t* miss_i
   if (st != TS_OK) return st;
   return dsakv::gather_enqueue(src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, pool_l,
                                P, host_l, ctx_stride, ctx_len, sel_l, err, stream, 1, 0, 0, 0,
-                               nullptr, nullptr, 0);
+                               nullptr, nullptr, 0, nullptr, nullptr);
 }
 
 extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* miss_pos,
@@ -492,7 +533,7 @@ extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* mis
   if (st != TS_OK) return st;
   return dsakv::refill_enqueue(miss_ids, miss_pos, victim, install, miss_count, B, k, sel_l,
                                pool_l, P, update_metadata, pool_tags, fifo_ptr, ptr_next, S, W,
-                               err, stream, 1, 0, 0);
+                               err, stream, 1, 0, 0, 1);
 }
 
 // ---------------------------------------------------------------------------

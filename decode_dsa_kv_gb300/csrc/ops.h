@@ -42,13 +42,16 @@ ts_status gather_check(const int32_t* src_map, const int32_t* miss_ids, const in
 // selection start l * *_layer_bytes after pool_l / host_l / sel_l). With
 // `done` non-null the kernel writes seq into done[l] once layer l's rows are
 // all written (count: `layers` device words, zero between launches; the
-// kernel leaves them zero).
+// kernel leaves them zero). With `victim` and `install` (dsa_plan's) given,
+// the misses with install code 1 are also written into their victim slots
+// of the pool as they arrive (the refill then needs only min_install = 2).
 ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const int32_t* miss_pos,
                          const int32_t* miss_count, const int32_t* miss_rows, int B, int k,
                          const void* pool_l, int P, const void* host_l, int64_t ctx_stride,
                          const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream,
                          int layers, size_t pool_layer_bytes, size_t host_layer_bytes,
-                         size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq);
+                         size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq,
+                         const int32_t* victim, const uint8_t* install);
 
 ts_status refill_check(const int32_t* miss_ids, const int32_t* miss_pos, const int32_t* victim,
                        const uint8_t* install, const int32_t* miss_count, int B, int k,
@@ -57,12 +60,14 @@ ts_status refill_check(const int32_t* miss_ids, const int32_t* miss_pos, const i
                        int W);
 // `layers` consecutive layers in one launch: layer l's selection and pool
 // start l * sel_layer_bytes / l * pool_layer_bytes after sel_l / pool_l.
+// Only installs with install >= min_install are written (1: all; 2: those the
+// gather did not write on arrival).
 ts_status refill_enqueue(const int32_t* miss_ids, const int32_t* miss_pos, const int32_t* victim,
                          const uint8_t* install, const int32_t* miss_count, int B, int k,
                          const void* sel_l, void* pool_l, int P, int update_metadata,
                          int32_t* pool_tags, int32_t* fifo_ptr, const int32_t* ptr_next, int S,
                          int W, int32_t* err, cudaStream_t stream, int layers,
-                         size_t sel_layer_bytes, size_t pool_layer_bytes);
+                         size_t sel_layer_bytes, size_t pool_layer_bytes, int min_install);
 
 ts_status sfa_check(const void* q, const void* sel_l, int B, int H, int k, float scale,
                     void* out, const void* ws, size_t ws_bytes);

@@ -31,6 +31,7 @@ struct PlanSmem {
   uint64_t* key;  // [pow2(k)] sort keys (general path)
   int* scratch;   // [64]
   int* flags;     // [4]
+  uint32_t* hit;  // [ceil(P / 32)] slots read as hits in this step
 };
 
 __host__ __device__ inline int pow2_at_least(int x) {
@@ -46,7 +47,8 @@ __host__ __device__ inline size_t key_bytes(int k) {
 }
 
 __host__ __device__ inline size_t plan_smem_bytes(int P, int S, int k) {
-  return key_bytes(k) + size_t(P) * 4 + size_t(S) * 12 + size_t(k) * 16 + 64 * 4 + 4 * 4 + 64;
+  return key_bytes(k) + size_t(P) * 4 + size_t(S) * 12 + size_t(k) * 16 + 64 * 4 + 4 * 4 +
+         size_t((P + 31) / 32) * 4 + 64;
 }
 
 __device__ PlanSmem carve(char* base, int P, int S, int k) {
@@ -73,6 +75,8 @@ __device__ PlanSmem carve(char* base, int P, int S, int k) {
   s.scratch = p;
   p += 64;
   s.flags = p;
+  p += 4;
+  s.hit = reinterpret_cast<uint32_t*>(p);
   return s;
 }
 
@@ -123,6 +127,7 @@ __global__ void __launch_bounds__(kThreads) dsa_plan_kernel(
     const int p = ptr_row[s];
     if (p < 0 || p >= W) report(err, TS_DEVERR_PTR_RANGE);
   }
+  for (int i = tid; i < (P + 31) / 32; i += kThreads) sm.hit[i] = 0;
   __syncthreads();
 
   // classify, and check whether the ids are strictly ascending
@@ -139,6 +144,7 @@ __global__ void __launch_bounds__(kThreads) dsa_plan_kernel(
       const int set = t % S;
       const int way = lookup(sm.tags, set, W, t);
       src = way >= 0 ? set * W + way : -1 - t;
+      if (way >= 0) atomicOr(sm.hit + (src >> 5), 1u << (src & 31));
     }
     src_map[int64_t(b) * k + j] = src;
     sm.src[j] = src;
@@ -261,7 +267,11 @@ __global__ void __launch_bounds__(kThreads) dsa_plan_kernel(
     miss_ids[g] = t;
     miss_pos[g] = sm.mpos[i];
     victim[g] = set * W + (pp + r) % W;
-    install[g] = r >= c - W ? 1 : 0;
+    // 1: the victim slot is read by no position of this step, the row may
+    // go in on arrival; 2: it is read as a hit, the row goes in after the
+    // layer's reads ([GLM] §4.4)
+    const int v = set * W + (pp + r) % W;
+    install[g] = r >= c - W ? ((sm.hit[v >> 5] >> (v & 31)) & 1u ? 2 : 1) : 0;
   }
   for (int s = tid; s < S; s += kThreads) {
     const int p = ptr_row[s];

@@ -155,11 +155,14 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
                              g.miss_count, g.miss_rows, g.ptr_next, g.err, m)) == TS_OK &&
        rec(1, 1, m) && signal(m, planned, seq) && wait_for(gs, planned, seq);
   // one launch gathers every layer and writes seq into gathered[l] from the
-  // device as soon as layer l's rows are in (no ramp between layers)
+  // device as soon as layer l's rows are in (no ramp between layers); it also
+  // installs the misses whose victim slots no hit of the step reads (install
+  // code 1), so each layer's refill copies only the code-2 rows
   ok = ok && rec(2, 0, gs) &&
        gather_enqueue(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k, pool,
                       P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel, g.err, gs, L, lb.pool,
-                      lb.host, lb.sel, gathered, counts, seq) == TS_OK &&
+                      lb.host, lb.sel, gathered, counts, seq, reuse ? nullptr : g.victim,
+                      reuse ? nullptr : g.install) == TS_OK &&
        rec(2, 1, gs);
   // per layer: the attention on the main stream, the refill beside it on the
   // side stream; the last refill also updates the metadata
@@ -174,7 +177,7 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
            refill_enqueue(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k,
                           at(g.sel, l, lb.sel), at(g.pool, l, lb.pool), P, l == L - 1,
                           g.pool_tags, g.fifo_ptr, g.ptr_next, g.S, g.W, g.err, side, 1, lb.sel,
-                          lb.pool) == TS_OK &&
+                          lb.pool, 2) == TS_OK &&
            rec(3 + L + l, 1, side);
   }
   if (reuse) {

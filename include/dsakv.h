@@ -158,9 +158,13 @@ ts_status ts_topk_noalloc(const float* scores, int64_t ctx_stride, const int32_t
  *   miss_pos   int32 [B][k]   first position of each missed token in ids
  *   victim     int32 [B][k]   slot the miss replaces: set*W + (ptr + rank) mod W,
  *                             rank = order of the miss among its set's misses
- *   install    uint8 [B][k]   1 when the miss survives the step (the last W
- *                             misses of a set); 0 when a later miss of the same
- *                             set in the same step replaces it
+ *   install    uint8 [B][k]   non-zero when the miss survives the step (the
+ *                             last W misses of a set); 0 when a later miss of
+ *                             the same set in the same step replaces it.
+ *                             1: no position of this step reads the victim
+ *                             slot (the row may go in as soon as it arrives);
+ *                             2: the slot is read as a hit in this step (the
+ *                             row goes in only after the layer's reads)
  *   miss_count int32 [B]      distinct missed tokens
  *   miss_rows  int32 [B]      positions that miss (a repeated missed token counts
  *                             at every position; equals miss_count when no
@@ -225,7 +229,7 @@ ts_status dsa_gather_kv(const int32_t* src_map, const int32_t* miss_ids,
 
 /* ---------------------------------------------------------------------------
  * dsa_refill_pool -- the deferred refill of one layer's pool ([GLM] §4.4, §5
- * DsaInstall, §5.1). For every installed miss i of request b:
+ * DsaInstall, §5.1). For every installed miss i of request b (install != 0):
  *   pool_l[b][victim[i]] = sel_l[b][miss_pos[i]]   (the missed row's bytes)
  * and, when update_metadata != 0 (the group's last layer):
  *   pool_tags[b][victim[i]] = miss_ids[i];  fifo_ptr[b][:] = ptr_next[b][:].

@@ -149,7 +149,7 @@ def _check_plan(d, ids, lens, tags, ptr, S, W):
         assert np.array_equal(got["miss_ids"][b, :M], want.miss_ids)
         assert np.array_equal(got["miss_pos"][b, :M], want.miss_pos)
         assert np.array_equal(got["victim"][b, :M], want.victim)
-        assert np.array_equal(got["install"][b, :M].astype(bool), want.install)
+        assert np.array_equal(got["install"][b, :M], want.install_code)
         assert np.array_equal(got["ptr_next"][b], want.ptr_next)
     return got
 

@@ -29,7 +29,10 @@ def d():
 def run_steps(d, w, steps, sample=None, sfa_layers=None, sfa_heads=None):
     """Run `steps` decode steps of workload `w` on the GPU and, for the
     requests in `sample` (default: all), on the oracle; compare after each
-    step. Returns per-step hit rates of the GPU plan."""
+    step. Returns per-step hit rates of the GPU plan and the number of
+    installs whose victim slot was read as a hit in the same step (install
+    code 2: the refill writes them after the layer's reads; the gather writes
+    the others on arrival)."""
     lens = wl.ctx_lens(w)
     host = d.HostKV(w.layers, w.B, w.ctx_stride)
     wl.fill_host_kv(w, host.array)
@@ -40,6 +43,7 @@ def run_steps(d, w, steps, sample=None, sfa_layers=None, sfa_heads=None):
     scores_stream = wl.ScoreStream(w)
     scale = 1 / math.sqrt(576)
     hit_rates = []
+    deferred = 0
     for step in range(steps):
         scores = scores_stream.next()
         q = wl.queries(w, step)
@@ -60,7 +64,8 @@ def run_steps(d, w, steps, sample=None, sfa_layers=None, sfa_heads=None):
             assert int(g.miss_rows[b]) == plan.miss_rows
             assert np.array_equal(g.miss_ids[b, :M].cpu().numpy(), plan.miss_ids)
             assert np.array_equal(g.victim[b, :M].cpu().numpy(), plan.victim)
-            assert np.array_equal(g.install[b, :M].cpu().numpy().astype(bool), plan.install)
+            assert np.array_equal(g.install[b, :M].cpu().numpy(), plan.install_code)
+            deferred += int(np.sum(plan.install_code == 2))
             assert np.array_equal(g.tags[b].cpu().numpy(), states[b].tags), (step, b)
             assert np.array_equal(g.fifo_ptr[b].cpu().numpy(), states[b].fifo_ptr)
             for l in range(w.layers):
@@ -75,7 +80,7 @@ def run_steps(d, w, steps, sample=None, sfa_layers=None, sfa_heads=None):
                 a, rel = sfa_errors(got, oracle.round_to_bf16_bits(o))
                 assert a <= SFA_ABS_TOL and rel <= SFA_MEAN_REL_TOL, (step, b, l, a, rel)
     host.close()
-    return hit_rates
+    return hit_rates, deferred
 
 
 def run_steps_reuse(d, w, steps, sfa_layers=(0,)):
@@ -131,20 +136,21 @@ def test_reuse_policy_decode_batch_scaled(d):
     # the same score process (it keeps only the previous selection)
     w = wl.scaled(wl.DECODE_BATCH, B=2)
     reuse = run_steps_reuse(d, w, 5, sfa_layers=(2,))
-    fifo = run_steps(d, w, 5, sfa_layers=[])
+    fifo, _ = run_steps(d, w, 5, sfa_layers=[])
     assert 0.45 < np.mean(reuse[1:]) < 0.75
     assert np.mean(fifo[1:]) > np.mean(reuse[1:])
 
 
 def test_tiny_all_steps(d):
-    rates = run_steps(d, wl.TINY, wl.TINY.steps)
+    rates, _ = run_steps(d, wl.TINY, wl.TINY.steps)
     assert rates[0] == 0.0 and max(rates[1:]) > 0.3
 
 
 def test_decode_batch_scaled(d):
     w = wl.scaled(wl.DECODE_BATCH, B=3)
-    rates = run_steps(d, w, 5, sfa_layers=[0, 3])
+    rates, deferred = run_steps(d, w, 5, sfa_layers=[0, 3])
     assert rates[-1] > 0.5
+    assert deferred > 0  # both install paths ran
 
 
 def test_long_context_scaled(d):
