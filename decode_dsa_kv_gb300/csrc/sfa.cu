@@ -69,8 +69,10 @@ struct Bars {
   uint64_t empty[kSSlots];
   uint64_t vfull[kVSlots];
   uint64_t vempty[kVSlots];
+  uint64_t s_half;  // score product of the first 256 rows complete
   uint64_t s_full;
   uint64_t p_full;
+  uint64_t o_half;  // value product of dims 0..255 complete
   uint64_t o_full;
   uint64_t drain;
   uint32_t tmem_slot;
@@ -130,8 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->vfull[s], 1);
       mbar_init(&bars->vempty[s], 1);
     }
+    mbar_init(&bars->s_half, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->p_full, kSoftmaxThreads);
+    mbar_init(&bars->o_half, 1);
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -216,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_mma_bf16(tmem + nh * kHalfRows, smem_desc_sw128(qa + kk * 32, 16, 1024),
                       smem_desc_sw128(ka + kk * 32, 16, 1024), id_s, (kb | kk) != 0);
         tc_commit(&bars->empty[s]);
+        if (it == kKB - 1) tc_commit(&bars->s_half);
       }
       if (ok) {
         tc_commit(&bars->s_full);
@@ -236,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_mma_bf16(d, smem_desc_sw128(pa + kk * 32, 16, 1024),
                       smem_desc_sw128(va + kk * 2048, kVBox, 1024), id_pv, (rb | kk) != 0);
         tc_commit(&bars->vempty[s]);
+        if (v == 7) tc_commit(&bars->o_half);
       }
       if (ok) tc_commit(&bars->o_full);
     }
@@ -250,20 +256,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nvalid = min(kChunk, k - c * kChunk);
     const int col0 = part * (kChunk / 2);
     float m = -INFINITY, l = 0.f;
-    bool ok = warp_wait(&bars->s_full, 0, abort);
-    if (ok) {
+    // Row max in two passes of 128 columns per thread: the first 256 rows'
+    // scores are read while the tensor core computes the other 256.
+    bool ok = true;
+    for (int h = 0; h < 2 && ok; ++h) {
+      ok = warp_wait(h == 0 ? &bars->s_half : &bars->s_full, 0, abort);
+      if (!ok) break;
       tc_fence_after();
+      const int cm = h * kHalfRows + part * (kHalfRows / 2);
       uint32_t r[32], r2[32];
-      for (int cb = 0; cb < kChunk / 2; cb += 64) {
-        tmem_ld32(trow + col0 + cb, r);
-        tmem_ld32(trow + col0 + cb + 32, r2);
+      for (int cb = 0; cb < kHalfRows / 2; cb += 64) {
+        tmem_ld32(trow + cm + cb, r);
+        tmem_ld32(trow + cm + cb + 32, r2);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          if (col0 + cb + i < nvalid) m = fmaxf(m, __uint_as_float(r[i]) * scale_log2);
-          if (col0 + cb + 32 + i < nvalid) m = fmaxf(m, __uint_as_float(r2[i]) * scale_log2);
+          if (cm + cb + i < nvalid) m = fmaxf(m, __uint_as_float(r[i]) * scale_log2);
+          if (cm + cb + 32 + i < nvalid) m = fmaxf(m, __uint_as_float(r2[i]) * scale_log2);
         }
       }
+    }
+    if (ok) {
       if (part == 1) bars->red[row] = m;
     }
     // the row max: part 1 hands its half over, part 0 combines and hands the
@@ -310,28 +323,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     softmax_sync();
     if (ok) {
       if (part == 0) l += bars->red[row];  // the row sum (only part 0 writes it out)
-      ok = warp_wait(&bars->o_full, 0, abort);
+      ok = warp_wait(&bars->o_half, 0, abort);
     }
     // Epilogue: O straight from TMEM to the workspace, in the chunk's
     // dim-major tile [512 dims][128 heads]: a warp's 32 lanes are 32
-    // consecutive heads, so every store is a coalesced 128-byte run.
-    const bool live = ok && !*abort;
+    // consecutive heads, so every store is a coalesced 128-byte run. Dims
+    // 0..255 (TMEM columns 256..511) go out while the tensor core still
+    // computes dims 256..511 (columns 0..255).
     const size_t slot0 = ((size_t(b) * HG + hg) * C + c) * kHeads;
     const int rows_valid = min(kHeads, H - hg * kHeads);
-    if (live) {
+    float* tile = opart + slot0 * DSA_DV;
+    bool live = ok && !*abort;
+    for (int half = 0; half < 2 && live; ++half) {
+      if (half == 1) {
+        live = warp_wait(&bars->o_full, 0, abort) && !*abort;
+        if (!live) break;
+      }
       tc_fence_after();
-      float* tile = opart + slot0 * DSA_DV;
       uint32_t r[32];
-      for (int half = 0; half < 2; ++half) {
-        for (int qq = 0; qq < 4; ++qq) {
-          const int d = 128 * part + 32 * qq;  // dim within this half
-          tmem_ld32(trow + (half == 0 ? 256u + d : uint32_t(d)), r);
-          tmem_wait_ld();
-          if (row < rows_valid) {
-            float* dst = tile + size_t(256 * half + d) * kHeads + row;
+      for (int qq = 0; qq < 4; ++qq) {
+        const int d = 128 * part + 32 * qq;  // dim within this half
+        tmem_ld32(trow + (half == 0 ? 256u + d : uint32_t(d)), r);
+        tmem_wait_ld();
+        if (row < rows_valid) {
+          float* dst = tile + size_t(256 * half + d) * kHeads + row;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) dst[i * kHeads] = __uint_as_float(r[i]);
-          }
+          for (int i = 0; i < 32; ++i) dst[i * kHeads] = __uint_as_float(r[i]);
         }
       }
     }

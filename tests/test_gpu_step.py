@@ -175,3 +175,14 @@ def test_decode_batch_full_size_sampled(d):
     # launch configuration; the oracle follows four of the requests
     w = wl.DECODE_BATCH
     run_steps(d, w, 3, sample=[0, 13, 31], sfa_layers=[0, 3], sfa_heads=slice(0, 128, 9))
+
+
+def test_large_batch_scaled(d):
+    # the large-batch shape (128 requests, 8192-entry pools, 128 heads: the
+    # plan, gather and attention grids at their widest) with contexts cut to
+    # 16,384 positions (32 tokens per set, so sets fill and evict); the oracle
+    # follows four requests
+    w = wl.scaled(wl.LARGE_BATCH, ctx=16384)
+    rates, _ = run_steps(d, w, 4, sample=[0, 57, 100, 127], sfa_layers=[2],
+                         sfa_heads=slice(0, 128, 5))
+    assert rates[0] == 0.0 and rates[-1] > 0.4
