@@ -9,6 +9,7 @@
 // memory read in place over the host link for misses. The gather moves rows
 // through shared memory with bulk async copies, so a few SMs keep enough rows
 // in flight for the link and for HBM, and the attention keeps the rest.
+#include <algorithm>
 #include <climits>
 
 #include "common.cuh"
@@ -441,6 +442,31 @@ ts_status gather_check(const int32_t* src_map, const int32_t* miss_ids, const in
   return TS_OK;
 }
 
+// The launch's CTAs of the two kinds. The hit CTAs grow with the rows a layer
+// moves (kHitCtas per kRowsPerHitUnit rows, at most kMaxUnits units). The miss
+// CTAs: kMissCtas keep the host link busy while the host rows the launch reads
+// span at most kWideHostBytes; over a wider span each zero-copy read waits
+// longer (measured on GB300: random 1152-byte reads over 19 GB of page-locked
+// memory from 8 SMs ran at 92 GB/s, from 24 at 126, where over 9.6 GB they ran
+// at 124 and 207), so three units go to the misses, and never fewer units than
+// the hits get. Measured per step: 4 x 4 x 1,048,576-row host KV (19 GB, 95 %
+// misses) 0.81 ms with 8 + 16 CTAs, 0.47 with 24 + 16; 128 requests x 32,768
+// rows (19 GB, 79 % hits) 4.44 ms with 8 + 16, 1.76 with 32 + 64.
+struct GatherGrid {
+  int miss, hit;  // multiples of kMissCtas and kHitCtas
+};
+const int64_t kRowsPerHitUnit = 65536;  // rows a layer moves per kHitCtas
+const int kMaxUnits = 4;
+const double kWideHostBytes = 12e9;  // host rows spanning more: 3 units of miss CTAs
+GatherGrid gather_grid(int B, int k, double host_bytes) {
+  const int64_t rows = int64_t(B) * k;
+  const int h = static_cast<int>(
+      std::min<int64_t>(kMaxUnits, std::max<int64_t>(1, (rows + kRowsPerHitUnit - 1) /
+                                                            kRowsPerHitUnit)));
+  const int m = std::max(h, host_bytes > kWideHostBytes ? 3 : 1);
+  return {kMissCtas * m, kHitCtas * h};
+}
+
 ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const int32_t* miss_pos,
                          const int32_t* miss_count, const int32_t* miss_rows, int B, int k,
                          const void* pool_l, int P, const void* host_l, int64_t ctx_stride,
@@ -448,6 +474,7 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
                          int layers, size_t pool_layer_bytes, size_t host_layer_bytes,
                          size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq,
                          const int32_t* victim, const uint8_t* install) {
+  // At the decode_batch shape (32 x 2048 rows a layer, 9.7 GB of host KV):
   // kMissCtas + kHitCtas CTAs (24 SMs): the misses' share of them reads at
   // the host link's rate (measured alone: 8 SMs of bulk copies reach the
   // same ~205 GB/s as plain loads on 16-57 SMs), the rest copy the hits at
@@ -460,11 +487,15 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
       cudaFuncSetAttribute(gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kPipeSmemBytes)) == cudaSuccess;
   if (!attr) return TS_ERR_CUDA;
-  gather_kernel<<<kMissCtas + kHitCtas, kPipeWarps * 32, kPipeSmemBytes, stream>>>(
+  const double host_bytes =
+      double(host_layer_bytes ? host_layer_bytes : size_t(B) * size_t(ctx_stride) * DSA_ROW_BYTES) *
+      layers;
+  const GatherGrid grid = gather_grid(B, k, host_bytes);
+  gather_kernel<<<grid.miss + grid.hit, kPipeWarps * 32, kPipeSmemBytes, stream>>>(
       src_map, miss_ids, miss_pos, miss_count, miss_rows, victim, install, B, k,
       static_cast<uint4*>(const_cast<void*>(pool_l)), P, static_cast<const uint4*>(host_l),
       ctx_stride, ctx_len, static_cast<uint4*>(sel_l), layers, int64_t(pool_layer_bytes / 16),
-      int64_t(host_layer_bytes / 16), int64_t(sel_layer_bytes / 16), done, count, seq, kMissCtas,
+      int64_t(host_layer_bytes / 16), int64_t(sel_layer_bytes / 16), done, count, seq, grid.miss,
       err);
   return launch_status();
 }
