@@ -208,7 +208,7 @@ def measured_peaks():
 
 
 def link_peak_gbs(torch, buf, reps=5):
-    """Host-to-device bandwidth of this machine's host link: DMA copy of pinned
+    """Host-to-device bandwidth of the machine's host link: DMA copy of pinned
     (registered) host memory `buf` (a PinnedHost; best of `reps`, CUDA
     events)."""
     buf.array[:] = 1
@@ -344,6 +344,17 @@ def roofline_of(name, alg, ms, peaks, link_gbs):
             "link_gbs": alg["link_bytes"] / t / 1e9 if alg["link_bytes"] else 0.0}
 
 
+def config_of(args, w: wl.Workload, world: int) -> dict:
+    """The workload a line reports on; the same dict for both arms."""
+    return {"workload": w.name, "B": w.B, "layers": w.layers, "k": w.k,
+            "ctx": w.ctx, "sets": w.S, "ways": w.W, "heads": w.H,
+            "mtp_draft_steps": args.mtp, "pool_policy": args.policy,
+            "requests_per_gpu": w.B,
+            "distinct_input_steps": max(1, min(args.period, args.warmup + args.steps)),
+            "l2": "inputs larger than L2 (host KV, pools and per-step inputs)",
+            "parallelism": f"requests sharded over {world} GPU(s), no collective"}
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline and the reference arm)
 # ---------------------------------------------------------------------------
@@ -413,8 +424,7 @@ def run_reference(args, w, rank, world):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": min(args.warmup, 3),
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "layers": w.layers, "k": w.k,
-                       "sets": w.S, "ways": w.W, "heads": w.H, "ctx": w.ctx},
+            "config": config_of(args, w, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -617,12 +627,7 @@ def run_native(args, w, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "layers": w.layers, "k": w.k,
-                   "ctx": w.ctx, "sets": w.S, "ways": w.W, "heads": w.H,
-                   "mtp_draft_steps": args.mtp, "pool_policy": args.policy,
-                   "requests_per_gpu": w.B, "distinct_input_steps": T,
-                   "l2": "inputs larger than L2 (host KV, pools and per-step inputs)",
-                   "parallelism": f"requests sharded over {world} GPU(s), no collective"},
+        "config": config_of(args, w, world),
         "roofline": rf_line,
         "cpu_baseline": cpu,
         "e2e": e2e,
