@@ -39,8 +39,9 @@ METRIC = "selected KV rows/s per decode step (plan+gather+SFA); % of HBM/link ro
 UNIT = "rows/s"
 KERNELS = ("topk", "plan", "gather", "sfa", "refill")
 # our kernels per step: top-k (1: one cluster per request, or 2: histogram + select)
-# + plan 1 + gather 1 (every layer) + layers x (sfa 2 + refill 1)
-LAUNCHES_PLAN, LAUNCHES_GATHER, LAUNCHES_PER_LAYER = 1, 1, 3
+# + plan 1 + gather 1 (every layer) + layers x (sfa 2 + refill 1; the reuse
+# policy has no refill)
+LAUNCHES_PLAN, LAUNCHES_GATHER, LAUNCHES_SFA = 1, 1, 2
 
 
 def topk_launches(w) -> int:
@@ -631,8 +632,9 @@ def run_native(args, w, rank, world, local):
         "roofline": rf_line,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * (topk_launches(w) + LAUNCHES_PLAN
-                                      + LAUNCHES_GATHER + w.layers * LAUNCHES_PER_LAYER),
+        "gpu_launches": args.steps * (topk_launches(w) + LAUNCHES_PLAN + LAUNCHES_GATHER
+                                      + w.layers * (LAUNCHES_SFA
+                                                    + (1 if args.policy == "fifo" else 0))),
         "clocks": clocks,
         "hit_rate": hit_frac,
         "deferred_install_frac": deferred_frac,
