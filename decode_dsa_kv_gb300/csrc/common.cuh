@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "dsakv.h"
 
 #define DSA_D 576
@@ -17,16 +19,46 @@
 
 namespace dsakv {
 
-// SMs of the current device (looked up once per translation unit).
+// SMs of the current device (looked up once per device).
 inline int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
+  static std::atomic<int> cached[64];  // static storage: starts at zero
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 148;
   }
+  const bool slot = dev >= 0 && dev < 64;
+  if (slot) {
+    const int n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = 148;
+  }
+  if (slot) cached[dev].store(n, std::memory_order_relaxed);
   return n;
+}
+
+// A kernel's dynamic shared-memory limit is an attribute per device: raise it
+// on the current device the first time a launch there needs it (`done` holds
+// one bit per device; devices past 63 raise it on every launch).
+inline bool raise_smem_limit(const void* kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  const uint64_t bit = dev >= 0 && dev < 64 ? uint64_t(1) << dev : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return true;
 }
 
 inline ts_status launch_status() {

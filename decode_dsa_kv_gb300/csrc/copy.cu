@@ -483,10 +483,10 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
   // Measured alternatives that did worse: plain loads on 3/8 of the SMs
   // (the earlier design, 0.549 vs 0.540 ms a step), other splits (9 + 15,
   // 10 + 14, 12 + 12, 6 + 18, 4 + 20 CTAs), 8 or 32 warps per CTA.
-  static const bool attr =
-      cudaFuncSetAttribute(gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kPipeSmemBytes)) == cudaSuccess;
-  if (!attr) return TS_ERR_CUDA;
+  static std::atomic<uint64_t> smem_set{0};
+  if (!raise_smem_limit(reinterpret_cast<const void*>(gather_kernel),
+                        static_cast<int>(kPipeSmemBytes), smem_set))
+    return TS_ERR_CUDA;
   const double host_bytes =
       double(host_layer_bytes ? host_layer_bytes : size_t(B) * size_t(ctx_stride) * DSA_ROW_BYTES) *
       layers;

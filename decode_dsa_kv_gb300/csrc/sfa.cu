@@ -505,13 +505,10 @@ ts_status sfa_enqueue_chunks(const void* q, const void* sel_l, int B, int H, int
   const size_t slots = size_t(B) * HG * C * kHeads;
   float* opart = static_cast<float*>(ws);
   float2* ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + align256(slots * DSA_DV * 4));
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(sfa_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-      return TS_ERR_CUDA;
-    attr = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel),
+                        static_cast<int>(kSmemBytes), smem_set))
+    return TS_ERR_CUDA;
   sfa_chunk_kernel<<<dim3(C, HG, B), kThreads, kSmemBytes, stream>>>(
       tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, err);
   return launch_status();

@@ -579,13 +579,10 @@ ts_status launch_topk(const float* scores, int64_t ctx_stride, const int32_t* ct
                       cudaStream_t stream) {
   TopkWs w = carve(ws, B, max_ctx);
   if (max_ctx <= kClusterMaxCtx) {
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(sizeof(ClSmem))) != cudaSuccess)
-        return TS_ERR_CUDA;
-      attr = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (!raise_smem_limit(reinterpret_cast<const void*>(topk_cluster_kernel),
+                          int(sizeof(ClSmem)), smem_set))
+      return TS_ERR_CUDA;
     // enough CTAs per request to fill half of the SMs when the requests are
     // few (up to kClusterMaxG; the other half stays free for the kernels of
     // the previous step still running, which would otherwise delay this
@@ -615,13 +612,10 @@ ts_status launch_topk(const float* scores, int64_t ctx_stride, const int32_t* ct
   // histograms, list counters and completion counters start at zero
   if (cudaMemsetAsync(ws, 0, counters_bytes(B), stream) != cudaSuccess) return TS_ERR_CUDA;
   const dim3 grid((max_ctx + kChunk - 1) / kChunk, B);
-  static bool hist_attr = false;
-  if (!hist_attr) {
-    if (cudaFuncSetAttribute(topk_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kHistCopies * kBins * 4) != cudaSuccess)
-      return TS_ERR_CUDA;
-    hist_attr = true;
-  }
+  static std::atomic<uint64_t> hist_smem_set{0};
+  if (!raise_smem_limit(reinterpret_cast<const void*>(topk_hist_kernel), kHistCopies * kBins * 4,
+                        hist_smem_set))
+    return TS_ERR_CUDA;
   topk_hist_kernel<<<grid, kThreads, kHistCopies * kBins * 4, stream>>>(scores, ctx_stride,
                                                                         ctx_len, k, max_ctx, w, err);
   topk_select_kernel<<<grid, kThreads, 0, stream>>>(scores, ctx_stride, ctx_len, k, max_ctx, w,
