@@ -200,8 +200,21 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
   }
   if (!ok) {
     // give every signal word this step's number, so that no wait enqueued
-    // now or by the next call is left without its signal
+    // now or by the next call is left without its signal. The side stream
+    // first waits for everything already enqueued on the other two streams
+    // (every wait enqueued there has its signal: a per-layer wait is
+    // enqueued only after the gather launch that writes it), so no signal
+    // lands while a kernel of this step still reads or writes the pool
+    cudaEvent_t ev[2] = {nullptr, nullptr};
+    const cudaStream_t others[2] = {m, gs};
+    for (int i = 0; i < 2; ++i)
+      if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess &&
+          cudaEventRecord(ev[i], others[i]) == cudaSuccess)
+        cudaStreamWaitEvent(side, ev[i], 0);
     for (int i = 0; i < kGathered + L; ++i) signal(side, g.sync + i, seq);
+    for (int i = 0; i < 2; ++i)
+      if (ev[i]) cudaEventDestroy(ev[i]);
+    cudaGetLastError();
     return TS_ERR_CUDA;
   }
   return TS_OK;

@@ -319,8 +319,11 @@ ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int H, int k,
  * refill[0..layers) (the top-k pair is left alone when ids are given).
  * Every operation's arguments are validated before anything is enqueued;
  * 1 <= layers <= TS_MAX_LAYERS. If a launch fails after the first one, every
- * sync word still receives this step's number (so no later wait is left
- * without its signal) and the error is returned.
+ * sync word still receives this step's number, written on the side stream
+ * after the work already enqueued on all three streams (so no later wait is
+ * left without its signal, and none passes early), and TS_ERR_CUDA is
+ * returned; synchronize the three streams before trusting any buffer of the
+ * group again.
  * ------------------------------------------------------------------------- */
 #define TS_MAX_LAYERS 16
 

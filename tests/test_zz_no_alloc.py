@@ -4,10 +4,12 @@ Some callers cannot call cudaMalloc: a plugin running inside a host engine
 that owns every device allocation, or a process whose device memory was all
 reserved before it started. For them the library offers a top-k whose scratch
 is a fixed device array inside the library. This test calls it through the C
-ABI and checks it against ts_topk with a caller workspace on two calls in a
-row (different shapes, so the second call must not see the first call's
-leftovers), and checks that sizes past its limit are refused up front. It sits
-in a file of its own that pytest collects last."""
+ABI and checks it against ts_topk with a caller workspace, and a few requests
+against the CPU oracle, on calls in a row: the one-launch path, then the
+long-context path twice with different shapes (that path's histograms and
+counters live in the shared array, so the second call must clear what the
+first left there). It also checks that sizes past its limit are refused up
+front. It sits in a file of its own that pytest collects last."""
 import numpy as np
 import pytest
 
@@ -34,9 +36,12 @@ def _inputs(rng, B, ctx, ties):
     return s
 
 
-def test_noalloc_matches_workspace_topk_on_two_calls(d):
+def test_noalloc_matches_workspace_topk_on_calls_in_a_row(d):
+    import oracle
     rng = np.random.default_rng(2024)
-    cases = [(32, 65536, 2048, False), (4, 1 << 20, 2048, True)]   # the second is at the limit
+    # one-launch path, then the long-context path at the limit (2 x 2^21) and
+    # again at another shape (4 x 2^20)
+    cases = [(32, 65536, 2048, False), (2, 1 << 21, 2048, True), (4, 1 << 20, 2048, True)]
     for B, ctx, k, ties in cases:
         scores = torch.from_numpy(_inputs(rng, B, ctx, ties)).cuda()
         lens = torch.full((B,), ctx, dtype=torch.int32, device="cuda")
@@ -49,6 +54,10 @@ def test_noalloc_matches_workspace_topk_on_two_calls(d):
         assert d.ts_topk_noalloc(scores, ctx, lens, B, ctx, k, got, err) == 0
         assert d.ts_read_error(err) == 0
         assert torch.equal(got, ref), (B, ctx, k)
+        host_scores = scores.cpu().numpy()
+        for b in (0, B - 1):
+            assert np.array_equal(got[b].cpu().numpy(), oracle.topk_ids(host_scores[b], ctx, k)), \
+                (B, ctx, b)
 
 
 def test_noalloc_refuses_sizes_past_its_limit(d):
