@@ -51,19 +51,21 @@ def topk_launches(w) -> int:
 def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
-    ap.add_argument("--workload", default="decode_batch", choices=sorted(wl.BY_NAME))
-    ap.add_argument("--period", type=int, default=64,
-                    help="distinct input steps generated; steps cycle through them forward "
-                         "and back, so the score process has no jump")
-    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--workload", default="large_batch", choices=sorted(wl.BY_NAME))
+    ap.add_argument("--settle-steps", type=int, default=64,
+                    help="most untimed steps before the warm-up, run in chunks of 16 until "
+                         "two chunks agree (0: none, for profiler runs)")
+    ap.add_argument("--query-slots", type=int, default=4,
+                    help="distinct query tensors, cycled (queries do not change the work)")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-settle-steps", type=int, default=16)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--settle-s", type=float, default=6.0,
-                    help="longest settle phase before the warm-up (0: none, for profiler runs)")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=6.0,
+                    help="CPU seconds of oracle work per leg of the CPU baseline")
     ap.add_argument("--only", choices=KERNELS, default=None,
                     help="after the warm-up steps, launch only this kernel --steps times "
                          "(on the state the warm-up left) and report its time per launch")
@@ -78,6 +80,7 @@ def parse(argv=None):
                          "(the step attends (1 + N) x H query rows over one selection)")
     ap.add_argument("--no-kernel-events", action="store_true",
                     help="time the steps without per-kernel events (no per-kernel roofline)")
+    ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
 
@@ -119,15 +122,6 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
 def first_request(rank: int, w: wl.Workload) -> int:
     """Rank r serves requests r*B .. r*B+B-1 of the workload's request stream."""
     return rank * w.B
-
-
-def palindrome_index(s: int, period: int) -> int:
-    """Step s -> input slot, walking 0..T-1 then T-2..1 and again (no jump)."""
-    if period <= 1:
-        return 0
-    cyc = 2 * period - 2
-    r = s % cyc
-    return r if r < period else cyc - r
 
 
 # ---------------------------------------------------------------------------
@@ -229,30 +223,30 @@ def link_peak_gbs(torch, buf, reps=5):
     return best
 
 
-def settle(torch, g, step, chunk=20, limit_s=6.0, tol=0.03, min_steps=0):
-    """Run steps until the step time is steady: on this platform, zero-copy
-    reads of host memory run slow for a second or two after host memory is
-    registered, copied by DMA or freed. Untimed (extra warm-up); returns the
-    steps run. Stops when two consecutive chunks agree within `tol` and are
-    within `tol` of the fastest chunk seen, or after `limit_s` seconds."""
-    t_end = time.time() + limit_s
-    times, s = [], 0
-    while time.time() < t_end:
+def settle(torch, g, step, max_steps, chunk=16, tol=0.03):
+    """Run untimed steps in chunks until the step time is steady: on this
+    platform, zero-copy reads of host memory run slow for a while after host
+    memory is registered, copied by DMA or first touched. Stops when two
+    consecutive chunks agree within `tol` and are within `tol` of the fastest
+    chunk seen, or before more than `max_steps` steps; returns the steps run.
+    `step()` takes the next step of the forward input stream."""
+    times, n = [], 0
+    while n + chunk <= max_steps:
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(g.main)
         for _ in range(chunk):
-            step(s)
-            s += 1
+            step()
+        n += chunk
         g.join(g.main)
         b.record(g.main)
         b.synchronize()
         times.append(a.elapsed_time(b))
-        if len(times) >= 2 and s >= min_steps:
+        if len(times) >= 2:
             lo = min(times)
             if abs(times[-1] - times[-2]) <= tol * lo and times[-1] <= (1 + tol) * lo:
                 break
-    return s
+    return n
 
 
 def device_digest_of(source_text: str, common_text: str) -> str:
@@ -351,7 +345,8 @@ def config_of(args, w: wl.Workload, world: int) -> dict:
             "ctx": w.ctx, "sets": w.S, "ways": w.W, "heads": w.H,
             "mtp_draft_steps": args.mtp, "pool_policy": args.policy,
             "requests_per_gpu": w.B,
-            "distinct_input_steps": max(1, min(args.period, args.warmup + args.steps)),
+            "score_stream": "forward only: every step run (settle, warm-up, timed, end to end) "
+                            "is the next step of the workload's score process; none is replayed",
             "l2": "inputs larger than L2 (host KV, pools and per-step inputs)",
             "parallelism": f"requests sharded over {world} GPU(s), no collective"}
 
@@ -360,74 +355,162 @@ def config_of(args, w: wl.Workload, world: int) -> dict:
 # CPU oracle (baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w: wl.Workload, budget_s: float, layers_per_request: int | None = None,
-                  first: int = 0):
-    """Run the oracle's decode step on requests of the workload (full
-    contexts), one request at a time, for about `budget_s` seconds of CPU work.
-    Returns (rows served, seconds, requests, layers)."""
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model Name", "CPU part"):
+        m = re.search(rf"^{key}\s*:\s*(.+)$", text, flags=re.M)
+        if m:
+            return m.group(1).strip()
+    return "unknown"
+
+
+def oracle_worker(spec: dict) -> dict:
+    """One worker of the CPU baseline (run in its own process): the oracle's
+    whole decode step (top-k, plan, and per layer gather, float64 SFA over all
+    heads, refill; metadata update) for requests spec["requests"] of the
+    workload, one at a time on a cold pool, until spec["budget_s"] seconds of
+    oracle work have run. Every context is full size; on a cold pool the step
+    reads only the selected rows, so only those are generated (the rest of
+    each host array is untouched zero pages). Only the decode step is timed."""
     import oracle
-    L = w.layers if layers_per_request is None else layers_per_request
-    lens = wl.ctx_lens(w, first)
-    stream = wl.ScoreStream(w, first)
-    scores = stream.next()
-    q = wl.queries(w, 0, first_request=first)
+    import workload.gen as gen
+    gen._threads = lambda: 1
+    w = wl.scaled(wl.get(spec["workload"]), **spec.get("overrides", {}))
+    L = w.layers
+    lens = wl.ctx_lens(w)
+    scale = 1 / math.sqrt(576)
     rows = secs = 0.0
     n = 0
-    for b in range(w.B):
-        host = np.zeros((L, 1, w.ctx_stride, 576), np.uint16)
+    for b in spec["requests"]:
+        scores = wl.ScoreStream(wl.scaled(w, B=1), b).next()[0]
+        n_ctx = int(lens[b])
+        ids = oracle.topk_ids(scores, n_ctx, w.k)
+        host = np.zeros((L, w.ctx_stride, 576), np.uint16)
         for l in range(L):
-            n_ctx = int(lens[b])
-            wl.normal_bf16(n_ctx, 576, w.seed, 1, l, first + b, 0, host[l, 0, :n_ctx])
+            for t in ids:
+                wl.normal_bf16(1, 576, w.seed, wl.gen.DOMAIN_KV, l, b, int(t), host[l, t:t + 1])
+        q = np.empty((L, w.H, 576), np.uint16)
+        for l in range(L):
+            wl.normal_bf16(w.H, 576, w.seed, wl.gen.DOMAIN_Q, 0, (l << 32) | b, 0, q[l])
         st = oracle.init_state(L, w.S, w.W)
         t0 = time.perf_counter()
-        oracle.decode_step(st, scores[b], int(lens[b]), w.k, w.S, w.W, host[:, 0], q[:L, b],
-                           1 / math.sqrt(576))
+        oracle.decode_step(st, scores, n_ctx, w.k, w.S, w.W, host, q, scale)
         secs += time.perf_counter() - t0
         rows += L * w.k
         n += 1
-        if secs >= budget_s:
+        if secs >= spec["budget_s"]:
             break
-    return rows, secs, n, L
+    return {"rows": rows, "secs": secs, "requests": n}
+
+
+def _spawn_workers(specs, threads_env):
+    env = dict(os.environ, **threads_env)
+    procs = [subprocess.Popen([sys.executable, os.path.abspath(__file__), "--oracle-worker",
+                               json.dumps(sp)], stdout=subprocess.PIPE, text=True, env=env,
+                              cwd=ROOT) for sp in specs]
+    out = []
+    for p in procs:
+        o, _ = p.communicate()
+        if p.returncode != 0:
+            raise RuntimeError("oracle worker failed")
+        out.append(json.loads(o.strip().splitlines()[-1]))
+    return out
+
+
+def cpu_baseline_leg(args, w: wl.Workload, overrides: dict) -> dict:
+    """The oracle as it stands, on the host cores, on a bounded sample of the
+    workload (cold-pool decode steps of whole requests, all layers): once on
+    one core (BLAS and OpenMP held to one thread) and once on every core (one
+    single-threaded worker process per core, each on its own requests, all at
+    once; the value is the sum of the workers' rates)."""
+    one = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+    cores = os.cpu_count() or 1
+    nw = max(1, min(cores, w.B))
+    single = _spawn_workers([{"workload": w.name, "overrides": overrides,
+                              "requests": list(range(w.B)), "budget_s": args.cpu_seconds}], one)[0]
+    per = max(args.cpu_seconds / 2, 1.0)
+    par = _spawn_workers([{"workload": w.name, "overrides": overrides,
+                           "requests": list(range(i, w.B, nw)), "budget_s": per}
+                          for i in range(nw)], one)
+    single_rate = single["rows"] / single["secs"]
+    par_rate = sum(r["rows"] / r["secs"] for r in par)
+    return {"value": par_rate, "unit": UNIT, "cores": nw, "kind": "oracle",
+            "single_core_value": single_rate, "cpu_model": cpu_model(),
+            "host_cores": cores,
+            "sample": (f"cold-pool decode steps of whole {w.name} requests ({w.layers} layers, "
+                       f"top-k, plan, gather, float64 SFA over {w.H} heads, refill), full "
+                       f"contexts; one core: {single['requests']} request(s) in "
+                       f"{single['secs']:.1f} s; all cores: {nw} single-threaded processes, "
+                       f"{sum(r['requests'] for r in par)} request(s) in total")}
+
+
+def oracle_hit_check(w: wl.Workload, scores_steps, lens, first_timed: int, timed: int,
+                     gpu_miss_log, requests) -> dict:
+    """The oracle's plan followed step by step over every step the device ran
+    up to the end of the timed region, for a few requests: its hit rate over
+    the timed steps beside the device's for the same requests and steps (the
+    plans are bit-exact, so the two must be equal)."""
+    import oracle
+    ora_hits = gpu_hits = 0
+    for b in requests:
+        st = oracle.init_state(1, w.S, w.W)
+        for t in range(first_timed + timed):
+            ids = oracle.topk_ids(scores_steps[t, b], int(lens[b]), w.k)
+            plan = oracle.dsa_plan(ids, int(lens[b]), st.tags, st.fifo_ptr, w.S, w.W)
+            oracle.metadata_update(st.tags, st.fifo_ptr, plan)
+            if t >= first_timed:
+                ora_hits += w.k - plan.miss_rows
+                gpu_hits += w.k - int(gpu_miss_log[t - first_timed, b])
+    n = len(requests) * timed * w.k
+    return {"requests": list(requests), "steps": timed, "oracle_hit_rate": ora_hits / n,
+            "device_hit_rate": gpu_hits / n}
 
 
 def run_reference(args, w, rank, world):
     """`--impl reference`: the CPU oracle, on the host cores, timed step by
-    step on a bounded sample of the workload (rank 0 only)."""
+    step: each step is the next step of request 0's score process through one
+    layer of the group (top-k, plan, gather, float64 SFA over all heads,
+    refill), on a pool that carries over from step to step (rank 0 only)."""
     if rank != 0:
         return
     import oracle
     lens = wl.ctx_lens(w)
-    stream = wl.ScoreStream(w)
-    scores = stream.next()
-    q = wl.queries(w, 0)
+    stream = wl.ScoreStream(wl.scaled(w, B=1))   # request 0's scores
     b = 0
     host = np.zeros((1, w.ctx_stride, 576), np.uint16)
     n_ctx = int(lens[b])
     wl.normal_bf16(n_ctx, 576, w.seed, 1, 0, b, 0, host[0, :n_ctx])
     st = oracle.init_state(1, w.S, w.W)
     scale = 1 / math.sqrt(576)
+    step_no = [0]
 
     def one():
-        oracle.decode_step(st, scores[b], n_ctx, w.k, w.S, w.W, host, q[:1, b], scale)
+        q = wl.queries(wl.scaled(w, B=1, layers=1), step_no[0])
+        oracle.decode_step(st, stream.next()[0], n_ctx, w.k, w.S, w.W, host, q[:1, 0], scale)
+        step_no[0] += 1
 
-    # each step: one request, one layer of the group (top-k, plan, gather,
-    # SFA over all heads, refill); the first timed probe sizes the run
-    for _ in range(min(args.warmup, 3)):
+    for _ in range(args.warmup):
         one()
-    t0 = time.perf_counter()
+    dt = 0.0
     for _ in range(args.steps):
+        t0 = time.perf_counter()
         one()
-    dt = time.perf_counter() - t0
+        dt += time.perf_counter() - t0
     value = args.steps * w.k / dt
-    sample = (f"each step: 1 request x 1 layer of {w.name} (ctx {n_ctx}, k {w.k}, "
-              f"{w.H} heads): top-k, plan, gather, fp64 SFA, refill")
+    sample = (f"each step: the next step of request 0 of {w.name} (ctx {n_ctx}, k {w.k}, "
+              f"{w.H} heads) through 1 layer: top-k, plan, gather, float64 SFA, refill; the pool "
+              f"carries over ({args.warmup} warm-up steps first); numpy with its default threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": min(args.warmup, 3),
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(args, w, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -437,62 +520,75 @@ def run_reference(args, w, rank, world):
 # native arm
 # ---------------------------------------------------------------------------
 
-def run_native(args, w, rank, world, local):
+def run_native(args, w, rank, world, local, overrides):
     import torch
     torch.cuda.set_device(local)
     init_dist(world, "nccl")
     import decode_dsa_kv_gb300 as dk
+    from decode_dsa_kv_gb300 import _abi as abi
 
     first = first_request(rank, w)
     lens = wl.ctx_lens(w, first)
     host = dk.HostKV(w.layers, w.B, w.ctx_stride)
     wl.fill_host_kv(w, host.array, first_request=first)
-    T = max(1, min(args.period, args.warmup + args.steps))
+    # the input stream runs forward only: settle, warm-up, timed and
+    # end-to-end steps each take the next step of the score process
+    n_e2e = 0 if args.no_e2e else min(args.e2e_steps, args.steps)
+    e2e_steps = (args.e2e_settle_steps + args.warmup + n_e2e) if n_e2e else 0
+    T = args.settle_steps + args.warmup + args.steps + e2e_steps
+    QS = max(1, min(args.query_slots, T))
     stream = wl.ScoreStream(w, first)
     # every registered host buffer of the run is made here, before any timing
     # (registering host memory slows zero-copy reads for a while afterwards)
     scores_pin = dk.PinnedHost((T, w.B, w.ctx_stride), np.float32)
-    q_pin = dk.PinnedHost((T, w.layers, w.B, w.H, 576), np.int16)
+    q_pin = dk.PinnedHost((QS, w.layers, w.B, w.H, 576), np.int16)
     out_pin = dk.PinnedHost((w.layers, w.B, w.H, 512), np.int16)
     link_buf = dk.PinnedHost((1 << 30,), np.uint8, kind="register")  # a DMA source
     for t in range(T):
         scores_pin.array[t] = stream.next()
+    for t in range(QS):
         wl.queries(w, t, out=q_pin.array[t].view(np.uint16), first_request=first)
-    # device-resident copies of every input slot, moved by the SMs (no DMA
-    # from these buffers)
-    from decode_dsa_kv_gb300 import _abi as abi
+    # device-resident copies of every input step, moved by the SMs (no DMA
+    # from these buffers); then one read of every host KV page by the SMs
+    # (the first zero-copy access of a host page is slow)
     scores_d = torch.empty(scores_pin.array.shape, dtype=torch.float32, device="cuda")
     q_d = torch.empty(q_pin.array.shape, dtype=torch.int16, device="cuda")
     abi.check(abi.ts_copy(scores_d, scores_pin.dev, scores_pin.array.nbytes, None), "ts_copy")
     abi.check(abi.ts_copy(q_d, q_pin.dev, q_pin.array.nbytes, None), "ts_copy")
+    touch = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    host_bytes = host.array.nbytes
+    for off in range(0, host_bytes, 1 << 30):
+        abi.check(abi.ts_copy(touch, host.dev + off, min(1 << 30, host_bytes - off), None),
+                  "ts_copy")
     torch.cuda.synchronize()
+    del touch
     g = dk.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host,
                        policy=args.policy)
     peaks = measured_peaks()
     link = link_peak_gbs(torch, link_buf)
 
-    base = [0]  # steps run before warm-up step 0 (the settle phase)
+    cursor = [0]  # the next step of the input stream
 
-    def step(s, timing=None):
-        i = palindrome_index(base[0] + s, T)
-        g.step(scores_d[i], q_d[i], timing=timing)
+    def step(timing=None):
+        i = cursor[0]
+        cursor[0] += 1
+        g.step(scores_d[i], q_d[i % QS], timing=timing)
 
-    # settle, then warm-up; the score process runs on without a jump
-    base[0] = settle(torch, g, step, limit_s=args.settle_s) if args.settle_s > 0 else 0
-    for s in range(args.warmup):
-        step(s)
+    settled = settle(torch, g, step, args.settle_steps) if args.settle_steps > 0 else 0
+    for _ in range(args.warmup):
+        step()
     g.join()
     torch.cuda.synchronize()
     if g.synchronize():
         raise RuntimeError("device error during warm-up")
 
     if args.only:
-        i = palindrome_index(base[0] + args.warmup, T)
-        return run_only(args, w, g, scores_d[i], q_d[i], peaks, link, lens, host, rank)
+        i = cursor[0]
+        return run_only(args, w, g, scores_d[i], q_d[i % QS], peaks, link, lens, host, rank)
 
     # timed region: K steps, per-kernel events on the launching streams
+    first_timed = cursor[0]
     miss_log = torch.zeros((args.steps, w.B), dtype=torch.int32, device="cuda")
-    inst_log = torch.zeros((args.steps,), dtype=torch.int64, device="cuda")
     # per-launch timing events of every timed step, created before the region
     timings = (None if args.no_kernel_events
                else [g.timing() for _ in range(args.steps)])
@@ -508,7 +604,7 @@ def run_native(args, w, rank, world, local):
     e0.record(g.main)
     t_enq0 = time.perf_counter()
     for s in range(args.steps):
-        step(args.warmup + s, timings[s] if timings else None)
+        step(timings[s] if timings else None)
         with torch.cuda.stream(g.main):
             miss_log[s].copy_(g.miss_count, non_blocking=True)
     t_enq1 = time.perf_counter()
@@ -528,7 +624,8 @@ def run_native(args, w, rank, world, local):
     value = rows_step / (ms_step * 1e-3)
 
     # hit and install fractions over the timed region (plan outputs)
-    misses = miss_log.double().sum().item()
+    miss_host = miss_log.cpu().numpy()
+    misses = float(miss_host.astype(np.float64).sum())
     hit_frac = 1.0 - misses / (args.steps * w.B * w.k)
     install_frac = (1.0 - hit_frac)   # installs ~ misses (overflow sets install fewer)
     deferred_frac = None
@@ -562,40 +659,36 @@ def run_native(args, w, rank, world, local):
 
     # end to end through the same schedule with host buffers: per step the
     # scores and queries are copied in from pinned host memory and the
-    # attention output copied back
+    # attention output copied back; the input stream keeps running forward
     e2e = None
-    if not args.no_e2e:
-        from decode_dsa_kv_gb300 import _abi as abi
+    if n_e2e:
         ins_s = torch.empty((w.B, w.ctx_stride), dtype=torch.float32, device="cuda")
         ins_q = torch.empty((w.layers, w.B, w.H, 576), dtype=torch.int16, device="cuda")
         s_bytes, q_bytes = ins_s.numel() * 4, ins_q.numel() * 2
         o_bytes = g.out.numel() * 2
-        n_e2e = min(args.e2e_steps, args.steps)
-        e0 = [base[0] + args.warmup + args.steps]
 
-        def e2e_step(s):
-            i = palindrome_index(e0[0] + s, T)
+        def e2e_step():
+            i = cursor[0]
+            cursor[0] += 1
             # the step's inputs in and its attention output out, through the SMs
-            abi.check(abi.ts_copy(ins_s, scores_pin.dev + i * s_bytes, s_bytes, g.main), "ts_copy")
-            abi.check(abi.ts_copy(ins_q, q_pin.dev + i * q_bytes, q_bytes, g.main), "ts_copy")
+            abi.check(abi.ts_copy(ins_s, scores_pin.dev + i * s_bytes, s_bytes, g.main),
+                      "ts_copy")
+            abi.check(abi.ts_copy(ins_q, q_pin.dev + (i % QS) * q_bytes, q_bytes, g.main),
+                      "ts_copy")
             g.step(ins_s, ins_q)
             abi.check(abi.ts_copy(out_pin.dev, g.out, o_bytes, g.main), "ts_copy")
 
-        # warm-up of the end-to-end loop: settle (the first zero-copy touch of
-        # each host page is slow) and at least one pass over every input slot
-        e2e_settle = (settle(torch, g, e2e_step, min_steps=2 * T, limit_s=args.settle_s)
-                      if args.settle_s > 0 else 0)
-        e0[0] += e2e_settle
-        for s in range(args.warmup):
-            e2e_step(s)
-        e0[0] += args.warmup
+        e2e_settle = (settle(torch, g, e2e_step, args.e2e_settle_steps)
+                      if args.e2e_settle_steps > 0 else 0)
+        for _ in range(args.warmup):
+            e2e_step()
         torch.cuda.synchronize()
         barrier(world)
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(g.main)
-        for s in range(n_e2e):
-            e2e_step(s)
+        for _ in range(n_e2e):
+            e2e_step()
         g.join(g.main)
         f1.record(g.main)
         torch.cuda.synchronize()
@@ -608,6 +701,7 @@ def run_native(args, w, rank, world, local):
                "copies": "ts_copy (SM copies) from / to page-locked host memory (ts_host_alloc)"}
 
     clocks = sampler.summary(t_wall0, t_wall1)
+    scores_steps = scores_pin.array[:first_timed + args.steps].copy() if rank == 0 else None
     host.close()
     scores_pin.close()
     q_pin.close()
@@ -618,11 +712,10 @@ def run_native(args, w, rank, world, local):
         return
     cpu = None
     if not args.no_cpu_baseline and args.policy == "fifo":
-        rows, secs, nreq, L = oracle_sample(w, args.cpu_seconds)
-        cpu = {"value": rows / secs, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{nreq} request(s) x {L} layers of {w.name}, one decode step each "
-                         f"(cold pool), full contexts; numpy with its default threads",
-               "seconds": secs}
+        cpu = cpu_baseline_leg(args, w, overrides)
+        reqs = [0] if w.ctx > 131072 else sorted({0, w.B // 2, w.B - 1})
+        cpu["plan_check"] = oracle_hit_check(w, scores_steps, lens, first_timed, args.steps,
+                                             miss_host, reqs)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -639,7 +732,8 @@ def run_native(args, w, rank, world, local):
         "hit_rate": hit_frac,
         "deferred_install_frac": deferred_frac,
         "host_enqueue_ms_per_step": (t_enq1 - t_enq0) * 1e3 / args.steps,
-        "settle_steps": base[0],
+        "settle_steps": settled,
+        "distinct_input_steps": cursor[0],
         "link_peak_gbs": link,
         "kernels": {n: {k2: (round(v, 4) if isinstance(v, float) else v)
                         for k2, v in per_kernel[n].items()} for n in per_kernel},
@@ -696,18 +790,24 @@ def run_only(args, w, g, scores, q, peaks, link, lens, host, rank):
 
 def main(argv=None):
     args = parse(argv)
+    if args.oracle_worker:
+        print(json.dumps(oracle_worker(json.loads(args.oracle_worker))), flush=True)
+        return
     rank, world, local = dist_env()
     w = wl.get(args.workload)
+    overrides = {}
     if args.B:
-        w = wl.scaled(w, B=args.B)
+        overrides["B"] = args.B
     if args.mtp:
-        w = wl.scaled(w, H=w.H * (1 + args.mtp))
+        overrides["H"] = w.H * (1 + args.mtp)
     if args.sets:
-        w = wl.scaled(w, S=args.sets)
+        overrides["S"] = args.sets
+    if overrides:
+        w = wl.scaled(w, **overrides)
     if args.impl == "reference":
         run_reference(args, w, rank, world)
         return
-    run_native(args, w, rank, world, local)
+    run_native(args, w, rank, world, local, overrides)
 
 
 if __name__ == "__main__":

@@ -51,11 +51,3 @@ def test_two_ranks_shard_requests_and_take_the_max_time():
     # the ranks' requests are the first 2B requests of one stream
     both = wl.ctx_lens(wl.scaled(w, B=2 * w.B))
     assert lens0 + lens1 == both.tolist()
-
-
-def test_palindrome_cycle_has_no_jump():
-    T = 5
-    seq = [bench.palindrome_index(s, T) for s in range(20)]
-    assert seq[:9] == [0, 1, 2, 3, 4, 3, 2, 1, 0]
-    assert all(abs(a - b) == 1 for a, b in zip(seq, seq[1:]))
-    assert bench.palindrome_index(7, 1) == 0
