@@ -39,13 +39,19 @@ METRIC = "selected KV rows/s per decode step (plan+gather+SFA); % of HBM/link ro
 UNIT = "rows/s"
 KERNELS = ("topk", "plan", "gather", "sfa", "refill")
 # our kernels per step: top-k (1: one cluster per request, or 2: histogram + select)
-# + plan 1 + gather 1 (every layer) + layers x (sfa 2 + refill 1; the reuse
-# policy has no refill)
-LAUNCHES_PLAN, LAUNCHES_GATHER, LAUNCHES_SFA = 1, 1, 2
+# + plan 1 + gather 1 (every layer) + layers x (sfa 1 or 2 + refill 1; the
+# reuse policy has no refill)
+LAUNCHES_PLAN, LAUNCHES_GATHER = 1, 1
 
 
 def topk_launches(w) -> int:
     return 1 if w.ctx <= 131072 else 2
+
+
+def sfa_launches(w) -> int:
+    """1 when the chunks of a head tile (ceil(k / 512) of them) merge inside
+    one cluster (1, 2 or 4 chunks), else chunk kernel + merge kernel."""
+    return 1 if -(-w.k // 512) in (1, 2, 4) else 2
 
 
 def parse(argv=None):
@@ -726,7 +732,7 @@ def run_native(args, w, rank, world, local, overrides):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * (topk_launches(w) + LAUNCHES_PLAN + LAUNCHES_GATHER
-                                      + w.layers * (LAUNCHES_SFA
+                                      + w.layers * (sfa_launches(w)
                                                     + (1 if args.policy == "fifo" else 0))),
         "clocks": clocks,
         "hit_rate": hit_frac,

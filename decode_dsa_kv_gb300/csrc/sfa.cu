@@ -20,11 +20,14 @@
 //   O[:, 0:256]   = P V[:, 0:256]    -> TMEM columns 256..511
 //   O[:, 256:512] = P V[:, 256:512]  -> TMEM columns 0..255 (S is dead by then:
 //       P holds it, bf16, in shared memory)
-//   O (unnormalised) -> fp32 workspace straight from TMEM, as a dim-major
-//       tile [512][128 heads] (coalesced stores); the row max and the row sum
-//       beside it.
-// A second kernel merges the chunks of a request: out = sum_c w_c O_c /
+// Merging the chunks of a (request, head tile): out = sum_c w_c O_c /
 // sum_c w_c l_c with w_c = exp2(m_c - max_c m_c).
+//   k <= 512, <= 1024 or in (1536, 2048] (1, 2 or 4 chunks): the chunk CTAs
+//       form one thread-block cluster and merge through distributed shared
+//       memory (merge_in_cluster); one launch, no workspace traffic.
+//   otherwise: O (unnormalised) -> fp32 workspace straight from TMEM, as a
+//       dim-major tile [512][128 heads] (coalesced stores), the row max and
+//       the row sum beside it, and a second kernel merges the chunks.
 #include <cmath>
 
 #include "common.cuh"
@@ -104,11 +107,141 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// ---- merge of a cluster's chunks through distributed shared memory ----
+// The output row (512 dims) is cut into 16 units of 32 dims; CTA r of a
+// cluster of C owns units [r * 16 / C, (r + 1) * 16 / C). Every other CTA
+// sends its weighted O of those units into one of the owner's C - 1 receive
+// slots (the tile region, free once the value product is done); a slot is
+// [unit][head][32 fp32], the 16-byte pieces of a head's 128 bytes rotated by
+// head & 7 so that 8 consecutive heads hit different banks.
+constexpr int kUnits = DSA_DV / 32;
+constexpr uint32_t kUnitBytes = kHeads * 128;  // one unit of every head
+constexpr uint32_t kMlOffset = kTileBytes - kHeads * sizeof(float2);  // published (m, l)
+static_assert(3 * (kUnits / 4) * kUnitBytes <= kMlOffset, "slots of a 4-CTA cluster");
+static_assert(1 * (kUnits / 2) * kUnitBytes <= kMlOffset, "slot of a 2-CTA cluster");
+
+// TMEM column of dims [32u, 32u + 32): dims 0..255 sit in columns 256..511.
+__device__ __forceinline__ uint32_t o_col(int u) {
+  return u < kUnits / 2 ? 256u + 32u * static_cast<uint32_t>(u)
+                        : 32u * static_cast<uint32_t>(u - kUnits / 2);
+}
+
+__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+// Softmax warps, after the row max m and (part 0) the row sum l of this
+// chunk are known: out = sum_c w_c O_c / sum_c w_c l_c, w_c = 2^(m_c - max m).
+// Two threads per head; `part` takes the units of its parity. Every thread
+// passes both cluster barriers whatever happened before (a failed wait only
+// skips work), so no CTA of the cluster waits for ever.
+__device__ __forceinline__ void merge_in_cluster(Bars* bars, uint8_t* base, uint32_t trow, int row,
+                                                 int part, float m, float l, bool ok,
+                                                 volatile int* abort, int H, int C, int hg, int b,
+                                                 __nv_bfloat16* __restrict__ out,
+                                                 float* __restrict__ lse) {
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int upo = kUnits / C;  // units each CTA owns
+  const int rows_valid = min(kHeads, H - hg * kHeads);
+  const bool live = ok && warp_wait(&bars->o_full, 0, abort) && !*abort;
+  float2* ml_pub = reinterpret_cast<float2*>(base + kMlOffset);
+  if (part == 0) ml_pub[row] = live ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
+  tc_fence_before();
+  cluster_sync_all();  // 1: every CTA's value product is done (tiles free), (m, l) published
+  tc_fence_after();
+  float M = -INFINITY, L = 0.f;
+  float2 e[4];
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    e[cc] = cc < C ? ld_dsmem_f2(dsmem_addr(ml_pub + row, cc)) : make_float2(-INFINITY, 0.f);
+    M = fmaxf(M, e[cc].x);
+  }
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc)
+    if (cc < C) L += exp2f(e[cc].x - M) * e[cc].y;
+  const float w = live ? exp2f(m - M) : 0.f;
+  if (live) {
+    for (int u = part; u < kUnits; u += 2) {
+      const int o = u / upo;
+      if (o == rank) continue;
+      uint32_t r[32];
+      tmem_ld32(trow + o_col(u), r);
+      tmem_wait_ld();
+      if (row < rows_valid) {
+        const int slot = (rank - o - 1 + C) % C;
+        const uint32_t dst = dsmem_addr(
+            base + slot * upo * kUnitBytes + ((u % upo) * kHeads + row) * 128, o);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_dsmem_f4(dst + ((j ^ (row & 7)) << 4), w * __uint_as_float(r[4 * j]),
+                      w * __uint_as_float(r[4 * j + 1]), w * __uint_as_float(r[4 * j + 2]),
+                      w * __uint_as_float(r[4 * j + 3]));
+      }
+    }
+  }
+  cluster_sync_all();  // 2: every contribution has landed; no remote access after this
+  if (live) {
+    const float inv = 1.f / L;
+    for (int u = part; u < kUnits; u += 2) {
+      if (u / upo != rank) continue;
+      uint32_t r[32];
+      tmem_ld32(trow + o_col(u), r);
+      tmem_wait_ld();
+      if (row < rows_valid) {
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = w * __uint_as_float(r[i]);
+        for (int sl = 0; sl < C - 1; ++sl) {
+          const uint8_t* src = base + sl * upo * kUnitBytes + ((u % upo) * kHeads + row) * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 v = *reinterpret_cast<const float4*>(src + ((j ^ (row & 7)) << 4));
+            acc[4 * j] += v.x;
+            acc[4 * j + 1] += v.y;
+            acc[4 * j + 2] += v.z;
+            acc[4 * j + 3] += v.w;
+          }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(out + (size_t(b) * H + hg * kHeads + row) * DSA_DV +
+                                              32 * u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t p[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 h2 =
+                __floats2bfloat162_rn(acc[8 * j + 2 * i] * inv, acc[8 * j + 2 * i + 1] * inv);
+            p[i] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          dst[j] = make_uint4(p[0], p[1], p[2], p[3]);
+        }
+      }
+    }
+    if (rank == 0 && part == 0 && row < rows_valid && lse)
+      lse[size_t(b) * H + hg * kHeads + row] = M * kLn2 + logf(L);
+  }
+}
+
+// kMerge = false: O, the row max and the row sum of the chunk go to the
+// workspace for sfa_combine_kernel. kMerge = true: the C chunk CTAs of a
+// (request, head tile) form one thread-block cluster and merge their O
+// through distributed shared memory; CTA r of the cluster writes dims
+// [r * 512 / C, (r + 1) * 512 / C) of the bf16 output (C = 1, 2 or 4).
+template <bool kMerge>
 __global__ void __launch_bounds__(kThreads, 1)
     sfa_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, int H, int k, int HG, int C,
                      float scale_log2, float* __restrict__ opart, float2* __restrict__ ml,
-                     int32_t* err) {
+                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Bars* bars = reinterpret_cast<Bars*>(smem_raw);
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -321,38 +454,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     softmax_sync();  // part 1 has read the max
     if (ok && part == 1) bars->red[row] = l;
     softmax_sync();
-    if (ok) {
-      if (part == 0) l += bars->red[row];  // the row sum (only part 0 writes it out)
-      ok = warp_wait(&bars->o_half, 0, abort);
-    }
-    // Epilogue: O straight from TMEM to the workspace, in the chunk's
-    // dim-major tile [512 dims][128 heads]: a warp's 32 lanes are 32
-    // consecutive heads, so every store is a coalesced 128-byte run. Dims
-    // 0..255 (TMEM columns 256..511) go out while the tensor core still
-    // computes dims 256..511 (columns 0..255).
-    const size_t slot0 = ((size_t(b) * HG + hg) * C + c) * kHeads;
-    const int rows_valid = min(kHeads, H - hg * kHeads);
-    float* tile = opart + slot0 * DSA_DV;
-    bool live = ok && !*abort;
-    for (int half = 0; half < 2 && live; ++half) {
-      if (half == 1) {
-        live = warp_wait(&bars->o_full, 0, abort) && !*abort;
-        if (!live) break;
-      }
-      tc_fence_after();
-      uint32_t r[32];
-      for (int qq = 0; qq < 4; ++qq) {
-        const int d = 128 * part + 32 * qq;  // dim within this half
-        tmem_ld32(trow + (half == 0 ? 256u + d : uint32_t(d)), r);
-        tmem_wait_ld();
-        if (row < rows_valid) {
-          float* dst = tile + size_t(256 * half + d) * kHeads + row;
+    if (ok && part == 0) l += bars->red[row];  // the row sum (only part 0 holds it)
+    if constexpr (!kMerge) {
+      if (ok) ok = warp_wait(&bars->o_half, 0, abort);
+      // Epilogue: O straight from TMEM to the workspace, in the chunk's
+      // dim-major tile [512 dims][128 heads]: a warp's 32 lanes are 32
+      // consecutive heads, so every store is a coalesced 128-byte run. Dims
+      // 0..255 (TMEM columns 256..511) go out while the tensor core still
+      // computes dims 256..511 (columns 0..255).
+      const size_t slot0 = ((size_t(b) * HG + hg) * C + c) * kHeads;
+      const int rows_valid = min(kHeads, H - hg * kHeads);
+      float* tile = opart + slot0 * DSA_DV;
+      bool live = ok && !*abort;
+      for (int half = 0; half < 2 && live; ++half) {
+        if (half == 1) {
+          live = warp_wait(&bars->o_full, 0, abort) && !*abort;
+          if (!live) break;
+        }
+        tc_fence_after();
+        uint32_t r[32];
+        for (int qq = 0; qq < 4; ++qq) {
+          const int d = 128 * part + 32 * qq;  // dim within this half
+          tmem_ld32(trow + (half == 0 ? 256u + d : uint32_t(d)), r);
+          tmem_wait_ld();
+          if (row < rows_valid) {
+            float* dst = tile + size_t(256 * half + d) * kHeads + row;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) dst[i * kHeads] = __uint_as_float(r[i]);
+            for (int i = 0; i < 32; ++i) dst[i * kHeads] = __uint_as_float(r[i]);
+          }
         }
       }
+      if (live && part == 0 && row < rows_valid) ml[slot0 + row] = make_float2(m, l);
+    } else {
+      merge_in_cluster(bars, base, trow, row, part, m, l, ok, abort, H, C, hg, b, out, lse);
     }
-    if (live && part == 0 && row < rows_valid) ml[slot0 + row] = make_float2(m, l);
+  }
+  if constexpr (kMerge) {
+    // the TMA and MMA warps take part in the merge's two cluster barriers
+    if (warp < 2) {
+      __syncwarp();
+      cluster_sync_all();
+      cluster_sync_all();
+    }
   }
 
   // ---------------- teardown ----------------
@@ -506,12 +649,53 @@ ts_status sfa_enqueue_chunks(const void* q, const void* sel_l, int B, int H, int
   float* opart = static_cast<float*>(ws);
   float2* ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + align256(slots * DSA_DV * 4));
   static std::atomic<uint64_t> smem_set{0};
-  if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel),
+  if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<false>),
                         static_cast<int>(kSmemBytes), smem_set))
     return TS_ERR_CUDA;
-  sfa_chunk_kernel<<<dim3(C, HG, B), kThreads, kSmemBytes, stream>>>(
-      tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, err);
+  sfa_chunk_kernel<false><<<dim3(C, HG, B), kThreads, kSmemBytes, stream>>>(
+      tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, nullptr, nullptr, err);
   return launch_status();
+}
+
+// One launch: the chunks of a (request, head tile) as one cluster that merges
+// them in distributed shared memory (C = ceil(k / 512) of 1, 2 or 4).
+bool sfa_merges_in_cluster(int k) {
+  const int C = (k + kChunk - 1) / kChunk;
+  return C == 1 || C == 2 || C == 4;
+}
+
+ts_status sfa_enqueue_merged(const void* q, const void* sel_l, int B, int H, int k, float scale,
+                             void* out, float* lse, int32_t* err, cudaStream_t stream) {
+  const int HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!make_map(&tm_q, q, H, B, kHeads) || !make_map(&tm_k, sel_l, k, B, kHalfRows) ||
+      !make_map(&tm_v, sel_l, k, B, 64))
+    return TS_ERR_CUDA;
+  static std::atomic<uint64_t> smem_set{0};
+  if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<true>),
+                        static_cast<int>(kSmemBytes), smem_set))
+    return TS_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, HG, B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  float* no_part = nullptr;
+  float2* no_ml = nullptr;
+  if (cudaLaunchKernelEx(&cfg, sfa_chunk_kernel<true>, tm_q, tm_k, tm_v, H, k, HG, C,
+                         scale * kLog2e, no_part, no_ml, static_cast<__nv_bfloat16*>(out), lse,
+                         err) != cudaSuccess) {
+    cudaGetLastError();
+    return TS_ERR_CUDA;
+  }
+  return TS_OK;
 }
 
 ts_status sfa_enqueue_combine(int B, int H, int k, void* out, float* lse, const void* ws,
@@ -528,6 +712,8 @@ ts_status sfa_enqueue_combine(int B, int H, int k, void* out, float* lse, const 
 
 ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, float scale,
                       void* out, float* lse, void* ws, int32_t* err, cudaStream_t stream) {
+  if (sfa_merges_in_cluster(k))
+    return sfa_enqueue_merged(q, sel_l, B, H, k, scale, out, lse, err, stream);
   const ts_status st = sfa_enqueue_chunks(q, sel_l, B, H, k, scale, ws, err, stream);
   if (st != TS_OK) return st;
   return sfa_enqueue_combine(B, H, k, out, lse, ws, stream);
