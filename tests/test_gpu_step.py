@@ -186,3 +186,13 @@ def test_large_batch_scaled(d):
     rates, _ = run_steps(d, w, 4, sample=[0, 57, 100, 127], sfa_layers=[2],
                          sfa_heads=slice(0, 128, 5))
     assert rates[0] == 0.0 and rates[-1] > 0.4
+
+
+def test_adversarial_full_size_sampled(d):
+    # the full adversarial workload (4 requests x 1,048,576 positions, 19 GB of
+    # host KV): the bench's launch configuration, including the gather's grid
+    # for host KV over 12 GB; the oracle follows requests 0 and 3 (the
+    # overflowing one)
+    w = wl.ADVERSARIAL
+    rates, _ = run_steps(d, w, 2, sample=[0, 3], sfa_layers=[3], sfa_heads=slice(0, 128, 11))
+    assert max(rates) < 0.2
