@@ -47,6 +47,7 @@ _SIGS = {
     "ts_host_free": (_I, [_P]),
     "ts_copy": (_I, [_P, _P, _SZ, _P]),
     "ts_read_error": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+    "ts_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "ts_topk_workspace_size": (_SZ, [_I, _I, _I]),
     "ts_topk": (_I, [_P, _I64, _P, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "ts_topk_noalloc": (_I, [_P, _I64, _P, _I, _I, _I, _P, _P, _P]),
@@ -172,6 +173,12 @@ def ts_read_error(err, stream=None) -> int:
         raise DsaKvError(st, "ts_read_error")
     return int(bits.value)
 
+
+
+def ts_set_wait_limit_ns(ns: int) -> None:
+    """Limit of every bounded wait inside the attention kernels launched from
+    now on (nanoseconds of the GPU's global timer); 0 restores their own."""
+    _lib.ts_set_wait_limit_ns(int(ns))
 
 def ts_topk_workspace_size(B: int, max_ctx: int, k: int) -> int:
     return int(_lib.ts_topk_workspace_size(B, max_ctx, k))

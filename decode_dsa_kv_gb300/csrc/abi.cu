@@ -1,6 +1,22 @@
 // Host-side parts of the C ABI that launch nothing: status text, host-memory
-// registration for zero-copy reads, and the error-word read-back.
+// registration for zero-copy reads, the error-word read-back, and the wait
+// limit of the attention kernels.
 #include "common.cuh"
+
+namespace dsakv {
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{0};
+}  // namespace
+
+uint64_t wait_limit_ns(uint64_t default_ns) {
+  const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return v ? v : default_ns;
+}
+}  // namespace dsakv
+
+extern "C" void ts_set_wait_limit_ns(uint64_t ns) {
+  dsakv::g_wait_limit_ns.store(ns, std::memory_order_relaxed);
+}
 
 extern "C" const char* ts_status_string(ts_status s) {
   switch (s) {

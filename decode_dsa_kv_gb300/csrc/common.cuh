@@ -61,6 +61,10 @@ inline bool raise_smem_limit(const void* kernel, int bytes, std::atomic<uint64_t
   return true;
 }
 
+// Limit of the bounded waits inside the attention kernels, in nanoseconds of
+// the global timer: `default_ns` unless ts_set_wait_limit_ns set another.
+uint64_t wait_limit_ns(uint64_t default_ns);
+
 inline ts_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }

@@ -87,9 +87,10 @@ static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
 
 // Wait by lane 0 of the warp, result shared by the whole warp (which is then
 // converged for the .sync.aligned tcgen05 instructions that follow).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort, kWaitLimit) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort, limit_ns) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   return ok != 0;
 }
@@ -146,13 +147,14 @@ __device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float a, float b, flo
 // skips work), so no CTA of the cluster waits for ever.
 __device__ __forceinline__ void merge_in_cluster(Bars* bars, uint8_t* base, uint32_t trow, int row,
                                                  int part, float m, float l, bool ok,
-                                                 volatile int* abort, int H, int C, int hg, int b,
+                                                 volatile int* abort, uint64_t wait_ns, int H,
+                                                 int C, int hg, int b,
                                                  __nv_bfloat16* __restrict__ out,
                                                  float* __restrict__ lse) {
   const int rank = static_cast<int>(cluster_ctarank());
   const int upo = kUnits / C;  // units each CTA owns
   const int rows_valid = min(kHeads, H - hg * kHeads);
-  const bool live = ok && warp_wait(&bars->o_full, 0, abort) && !*abort;
+  const bool live = ok && warp_wait(&bars->o_full, 0, abort, wait_ns) && !*abort;
   float2* ml_pub = reinterpret_cast<float2*>(base + kMlOffset);
   if (part == 0) ml_pub[row] = live ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
   tc_fence_before();
@@ -241,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     sfa_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, int H, int k, int HG, int C,
                      float scale_log2, float* __restrict__ opart, float2* __restrict__ ml,
-                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int32_t* err) {
+                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint64_t wait_ns,
+                     int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Bars* bars = reinterpret_cast<Bars*>(smem_raw);
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = bars->issued; it < kScoreLoads; ++it) {
         const int s = it % kSSlots;
         if (it >= kSSlots &&
-            !mbar_wait_bounded(&bars->empty[s], ((it / kSSlots) - 1) & 1, abort, kWaitLimit))
+            !mbar_wait_bounded(&bars->empty[s], ((it / kSSlots) - 1) & 1, abort, wait_ns))
           break;
         uint8_t* st = score_slot(s);
         const int kb = it % kKB, nh = it / kKB;
@@ -318,11 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // value phase: kVSlots slots in the ring region, once the scores are
       // done (their slots are free then); the first loads overlap the softmax
       if (bars->issued == kScoreLoads &&
-          mbar_wait_bounded(&bars->s_full, 0, abort, kWaitLimit)) {
+          mbar_wait_bounded(&bars->s_full, 0, abort, wait_ns)) {
         for (int v = 0; v < kLoads - kScoreLoads; ++v) {
           const int s = v % kVSlots;
           if (v >= kVSlots &&
-              !mbar_wait_bounded(&bars->vempty[s], ((v / kVSlots) - 1) & 1, abort, kWaitLimit))
+              !mbar_wait_bounded(&bars->vempty[s], ((v / kVSlots) - 1) & 1, abort, wait_ns))
             break;
           uint8_t* st = stages + s * kVBytes;
           const int half = v >> 3, rb = v & 7;
@@ -342,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int it = 0; it < kScoreLoads && ok; ++it) {
         const int s = it % kSSlots;
-        ok = mbar_wait_bounded(&bars->full[s], (it / kSSlots) & 1, abort, kWaitLimit);
+        ok = mbar_wait_bounded(&bars->full[s], (it / kSSlots) & 1, abort, wait_ns);
         if (!ok) break;
         tc_fence_after();
         const int kb = it % kKB, nh = it / kKB;
@@ -357,12 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) {
         tc_commit(&bars->s_full);
-        ok = mbar_wait_bounded(&bars->p_full, 0, abort, kWaitLimit);
+        ok = mbar_wait_bounded(&bars->p_full, 0, abort, wait_ns);
       }
       if (ok) tc_fence_after();
       for (int v = 0; v < kLoads - kScoreLoads && ok; ++v) {
         const int s = v % kVSlots;
-        ok = mbar_wait_bounded(&bars->vfull[s], (v / kVSlots) & 1, abort, kWaitLimit);
+        ok = mbar_wait_bounded(&bars->vfull[s], (v / kVSlots) & 1, abort, wait_ns);
         if (!ok) break;
         tc_fence_after();
         const int half = v >> 3, rb = v & 7;
@@ -393,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // scores are read while the tensor core computes the other 256.
     bool ok = true;
     for (int h = 0; h < 2 && ok; ++h) {
-      ok = warp_wait(h == 0 ? &bars->s_half : &bars->s_full, 0, abort);
+      ok = warp_wait(h == 0 ? &bars->s_half : &bars->s_full, 0, abort, wait_ns);
       if (!ok) break;
       tc_fence_after();
       const int cm = h * kHalfRows + part * (kHalfRows / 2);
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     softmax_sync();
     if (ok && part == 0) l += bars->red[row];  // the row sum (only part 0 holds it)
     if constexpr (!kMerge) {
-      if (ok) ok = warp_wait(&bars->o_half, 0, abort);
+      if (ok) ok = warp_wait(&bars->o_half, 0, abort, wait_ns);
       // Epilogue: O straight from TMEM to the workspace, in the chunk's
       // dim-major tile [512 dims][128 heads]: a warp's 32 lanes are 32
       // consecutive heads, so every store is a coalesced 128-byte run. Dims
@@ -468,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool live = ok && !*abort;
       for (int half = 0; half < 2 && live; ++half) {
         if (half == 1) {
-          live = warp_wait(&bars->o_full, 0, abort) && !*abort;
+          live = warp_wait(&bars->o_full, 0, abort, wait_ns) && !*abort;
           if (!live) break;
         }
         tc_fence_after();
@@ -486,7 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (live && part == 0 && row < rows_valid) ml[slot0 + row] = make_float2(m, l);
     } else {
-      merge_in_cluster(bars, base, trow, row, part, m, l, ok, abort, H, C, hg, b, out, lse);
+      merge_in_cluster(bars, base, trow, row, part, m, l, ok, abort, wait_ns, H, C, hg, b, out,
+                       lse);
     }
   }
   if constexpr (kMerge) {
@@ -653,7 +657,8 @@ ts_status sfa_enqueue_chunks(const void* q, const void* sel_l, int B, int H, int
                         static_cast<int>(kSmemBytes), smem_set))
     return TS_ERR_CUDA;
   sfa_chunk_kernel<false><<<dim3(C, HG, B), kThreads, kSmemBytes, stream>>>(
-      tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, nullptr, nullptr, err);
+      tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, nullptr, nullptr,
+      wait_limit_ns(kWaitLimit), err);
   return launch_status();
 }
 
@@ -691,7 +696,7 @@ ts_status sfa_enqueue_merged(const void* q, const void* sel_l, int B, int H, int
   float2* no_ml = nullptr;
   if (cudaLaunchKernelEx(&cfg, sfa_chunk_kernel<true>, tm_q, tm_k, tm_v, H, k, HG, C,
                          scale * kLog2e, no_part, no_ml, static_cast<__nv_bfloat16*>(out), lse,
-                         err) != cudaSuccess) {
+                         wait_limit_ns(kWaitLimit), err) != cudaSuccess) {
     cudaGetLastError();
     return TS_ERR_CUDA;
   }

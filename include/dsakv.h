@@ -99,6 +99,15 @@ ts_status ts_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream)
  * device. Returns TS_ERR_DEVICE_CHECK when any bit was set. */
 ts_status ts_read_error(int32_t* err, int32_t* bits, cudaStream_t stream);
 
+/* Limit, in nanoseconds of the GPU's global timer, of each bounded wait inside
+ * the attention kernels launched after this call (their own limit is 2 s);
+ * 0 restores it. Process-wide, the library's one setting. For tests of the
+ * error path: with a limit shorter than a tile load the attention gives up
+ * (TS_DEVERR_TIMEOUT; its output is then undefined), lets every copy it issued
+ * land, frees its tensor memory and returns, and the next call with the
+ * default limit computes normally. Host only. */
+void ts_set_wait_limit_ns(uint64_t ns);
+
 /* ---------------------------------------------------------------------------
  * ts_topk -- top-k of the Lightning-Indexer scores ([GLM] §2.1: the indexer
  * picks the history positions most relevant to the current query; SFA runs on

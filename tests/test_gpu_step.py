@@ -196,3 +196,12 @@ def test_adversarial_full_size_sampled(d):
     w = wl.ADVERSARIAL
     rates, _ = run_steps(d, w, 2, sample=[0, 3], sfa_layers=[3], sfa_heads=slice(0, 128, 11))
     assert max(rates) < 0.2
+
+
+def test_large_batch_full_size_sampled(d):
+    # the full large-batch workload (128 requests x 32,768 positions x 4 layers,
+    # 19 GB of host KV), the bench's default configuration and launch grid; the
+    # oracle follows the first and the last request
+    w = wl.LARGE_BATCH
+    rates, _ = run_steps(d, w, 5, sample=[0, 127], sfa_layers=[1], sfa_heads=slice(0, 128, 13))
+    assert rates[0] == 0.0 and rates[-1] > 0.3
