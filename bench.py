@@ -652,6 +652,14 @@ def run_native(args, w, rank, world, local, overrides):
         ms = sum(launch_ms[n]) / len(launch_ms[n])
         per_kernel[n] = roofline_of(n, alg[n], ms, peaks, link)
         per_kernel[n]["launches_per_step"] = len(launch_ms[n]) / args.steps
+    # where the launches of the last timed step sat, in microseconds after its
+    # first launch began
+    last_spans = None
+    if timings:
+        t_last = timings[-1]
+        first = t_last.events[0] if t_last.with_topk else t_last.events[2]
+        last_spans = {n: [(round(a, 1), round(b, 1)) for a, b in v]
+                      for n, v in t_last.spans(first).items()}
     rf_line = None
     if per_kernel:
         dom = max(per_kernel, key=lambda n: per_kernel[n]["ms_per_launch"]
@@ -741,6 +749,7 @@ def run_native(args, w, rank, world, local, overrides):
         "settle_steps": settled,
         "distinct_input_steps": cursor[0],
         "link_peak_gbs": link,
+        "last_step_spans_us": last_spans,
         "kernels": {n: {k2: (round(v, 4) if isinstance(v, float) else v)
                         for k2, v in per_kernel[n].items()} for n in per_kernel},
     }
