@@ -81,6 +81,10 @@ def parse(argv=None):
     ap.add_argument("--policy", choices=("fifo", "reuse"), default="fifo",
                     help="device pool: the set-associative FIFO pool (default) or the base "
                          "design's adjacent-step reuse of the previous selection")
+    ap.add_argument("--layout", choices=("staged", "selection"), default="staged",
+                    help="staged: the attention reads its rows straight from the pool (only "
+                         "the misses are staged in HBM); selection: every row is gathered "
+                         "into a selection buffer first")
     ap.add_argument("--mtp", type=int, default=0, choices=(0, 1, 2, 3),
                     help="MTP draft steps whose queries are folded into the heads "
                          "(the step attends (1 + N) x H query rows over one selection)")
@@ -304,22 +308,29 @@ def traffic_record(kernel: str, workload: str):
 # ---------------------------------------------------------------------------
 
 def algorithmic(w: wl.Workload, lens, hit_frac: float, install_frac: float,
-                deferred_frac: float = None):
+                deferred_frac: float = None, staged: bool = False):
     """Per-launch algorithmic work of every kernel, with the measured hit and
     install fractions (per selected row). The gather writes the installs
     whose victim slots no hit of the step reads; the refill copies the rest
-    (`deferred_frac`; all installs when None, as in the per-layer calls)."""
+    (`deferred_frac`; all installs when None, as in the per-layer calls).
+    Staged layout: the gather moves only the misses (staged in HBM, plus the
+    installs on arrival); the attention reads every row where it lies."""
     direct = 0.0 if deferred_frac is None else install_frac - deferred_frac
     deferred = install_frac if deferred_frac is None else deferred_frac
     rows = w.B * w.k
     row = 1152
+    miss = 1 - hit_frac
     out = {}
     out["topk"] = {"hbm_bytes": float(np.sum(lens)) * 4 + rows * 4, "link_bytes": 0.0}
     out["plan"] = {"hbm_bytes": rows * (4 + 4) + w.B * (w.P * 4 + 2 * w.S * 4)
-                   + rows * (1 - hit_frac) * (4 * 3 + 1), "link_bytes": 0.0}
+                   + rows * miss * (4 * 3 + 1), "link_bytes": 0.0}
     # one launch gathers every layer
-    out["gather"] = {"hbm_bytes": w.layers * rows * (hit_frac * row + row + direct * row + 4),
-                     "link_bytes": w.layers * rows * (1 - hit_frac) * row}
+    if staged:
+        out["gather"] = {"hbm_bytes": w.layers * rows * (miss * (row + 13) + direct * row),
+                         "link_bytes": w.layers * rows * miss * row}
+    else:
+        out["gather"] = {"hbm_bytes": w.layers * rows * (hit_frac * row + row + direct * row + 4),
+                         "link_bytes": w.layers * rows * miss * row}
     out["refill"] = {"hbm_bytes": rows * (deferred * 2 * row + install_frac * 13),
                      "link_bytes": 0.0}
     out["sfa"] = {"hbm_bytes": rows * row + w.B * w.H * (1152 + 1024),
@@ -350,6 +361,7 @@ def config_of(args, w: wl.Workload, world: int) -> dict:
     return {"workload": w.name, "B": w.B, "layers": w.layers, "k": w.k,
             "ctx": w.ctx, "sets": w.S, "ways": w.W, "heads": w.H,
             "mtp_draft_steps": args.mtp, "pool_policy": args.policy,
+            "layout": args.layout,
             "requests_per_gpu": w.B,
             "score_stream": "forward only: every step run (settle, warm-up, timed, end to end) "
                             "is the next step of the workload's score process; none is replayed",
@@ -568,8 +580,9 @@ def run_native(args, w, rank, world, local, overrides):
                   "ts_copy")
     torch.cuda.synchronize()
     del touch
+    staged = args.layout == "staged" and args.policy == "fifo"
     g = dk.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host,
-                       policy=args.policy)
+                       policy=args.policy, layout="staged" if staged else "selection")
     peaks = measured_peaks()
     link = link_peak_gbs(torch, link_buf)
 
@@ -641,7 +654,7 @@ def run_native(args, w, rank, world, local, overrides):
         deferred_frac = float(((g.install == 2) & valid).sum().item()) / (w.B * w.k)
 
     per_kernel = {}
-    alg = algorithmic(w, lens, hit_frac, install_frac, deferred_frac)
+    alg = algorithmic(w, lens, hit_frac, install_frac, deferred_frac, staged)
     launch_ms = {n: [] for n in KERNELS}
     for t in timings or []:
         for n, v in t.ms().items():
@@ -764,21 +777,33 @@ def run_only(args, w, g, scores, q, peaks, link, lens, host, rank):
     from decode_dsa_kv_gb300 import _abi as abi
     B, k = w.B, w.k
     m = g.main
+    staged = g.layout == "staged"
     launch = {
         "topk": lambda: abi.ts_topk(scores, g.ctx_stride, g.ctx_len, B, g.max_ctx, k, g.ids,
                                     g.topk_ws, g.topk_ws_bytes, g.err, m),
         "plan": lambda: abi.dsa_plan(g.ids, g.ctx_len, B, k, g.tags, g.fifo_ptr, g.S, g.W,
                                      g.src_map, g.miss_ids, g.miss_pos, g.victim, g.install,
                                      g.miss_count, g.miss_rows, g.ptr_next, g.err, m),
-        "gather": lambda: abi.dsa_gather_kv(g.src_map, g.miss_ids, g.miss_pos, g.miss_count,
-                                            g.miss_rows, B, k, g.pool[0], g.P, host.layer_ptr(0),
-                                            g.ctx_stride, g.ctx_len, g.sel[0], g.err, m),
-        "sfa": lambda: abi.sfa_mla_decode(q[0], g.sel[0], B, g.H, k, g.scale, g.out[0],
-                                          g.lse[0], g.sfa_ws, g.sfa_ws_bytes, g.err, m),
-        "refill": lambda: abi.dsa_refill_pool(g.miss_ids, g.miss_pos, g.victim, g.install,
-                                              g.miss_count, B, k, g.sel[0], g.pool[0], g.P, 0,
-                                              g.tags, g.fifo_ptr, g.ptr_next, g.S, g.W, g.err,
-                                              m),
+        "gather": (lambda: abi.dsa_stage_misses(g.miss_ids, g.miss_pos, g.miss_count, None, None,
+                                                B, k, g.pool[0], g.P, host.layer_ptr(0),
+                                                g.ctx_stride, g.ctx_len, g.err, m)) if staged
+        else (lambda: abi.dsa_gather_kv(g.src_map, g.miss_ids, g.miss_pos, g.miss_count,
+                                        g.miss_rows, B, k, g.pool[0], g.P, host.layer_ptr(0),
+                                        g.ctx_stride, g.ctx_len, g.sel[0], g.err, m)),
+        "sfa": (lambda: abi.sfa_mla_decode_pool(q[0], g.pool[0], g.P, g.src_map, g.miss_ids,
+                                                g.miss_pos, g.miss_count, g.miss_rows, B, g.H, k,
+                                                g.scale, g.out[0], g.lse[0], g.sfa_ws,
+                                                g.sfa_ws_bytes, g.err, m)) if staged
+        else (lambda: abi.sfa_mla_decode(q[0], g.sel[0], B, g.H, k, g.scale, g.out[0],
+                                         g.lse[0], g.sfa_ws, g.sfa_ws_bytes, g.err, m)),
+        # (no metadata update: every launch leaves the same pool state)
+        "refill": (lambda: abi.dsa_refill_pool_staged(g.miss_ids, g.miss_pos, g.victim,
+                                                      g.install, g.miss_count, B, k, g.pool[0],
+                                                      g.P, 0, g.tags, g.fifo_ptr, g.ptr_next,
+                                                      g.S, g.W, g.err, m)) if staged
+        else (lambda: abi.dsa_refill_pool(g.miss_ids, g.miss_pos, g.victim, g.install,
+                                          g.miss_count, B, k, g.sel[0], g.pool[0], g.P, 0,
+                                          g.tags, g.fifo_ptr, g.ptr_next, g.S, g.W, g.err, m)),
     }[args.only]
     abi.check(launch(), args.only)
     torch.cuda.synchronize()
@@ -795,7 +820,7 @@ def run_only(args, w, g, scores, q, peaks, link, lens, host, rank):
         raise RuntimeError("device error")
     ms = e0.elapsed_time(e1) / args.steps
     # the per-layer entry points move one layer per launch
-    alg = algorithmic(wl.scaled(w, layers=1), lens, hit, 1.0 - hit)[args.only]
+    alg = algorithmic(wl.scaled(w, layers=1), lens, hit, 1.0 - hit, staged=staged)[args.only]
     rf = roofline_of(args.only, alg, ms, peaks, link)
     host.close()
     if rank == 0:

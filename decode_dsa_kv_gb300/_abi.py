@@ -54,10 +54,15 @@ _SIGS = {
     "dsa_plan": (_I, [_P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dsa_plan_reuse": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "dsa_gather_kv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _I, _P, _I64, _P, _P, _P, _P]),
+    "dsa_stage_misses": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _I, _P, _I64, _P, _P, _P]),
     "dsa_refill_pool": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _I, _I,
                              _P, _P]),
+    "dsa_refill_pool_staged": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _I, _I,
+                                    _P, _P]),
     "sfa_workspace_size": (_SZ, [_I, _I, _I]),
     "sfa_mla_decode": (_I, [_P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P, _P]),
+    "sfa_mla_decode_pool": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ,
+                                 _P, _P]),
     "dsa_group_step": (_I, [_P, _P, _P, _P, _P]),
 }
 
@@ -66,6 +71,8 @@ EXPORTS = tuple(_SIGS)
 TS_MAX_LAYERS = 16
 DSA_POLICY_FIFO = 0
 DSA_POLICY_REUSE = 1
+DSA_LAYOUT_SELECTION = 0
+DSA_LAYOUT_STAGED = 1
 
 
 class DsaGroup(ctypes.Structure):
@@ -89,6 +96,7 @@ class DsaGroup(ctypes.Structure):
         ("policy", _I),
         ("prev_ids", _P),
         ("prev_sel", _P),
+        ("layout", _I),
     ]
 
 for _name, (_res, _args) in _SIGS.items():
@@ -229,6 +237,22 @@ def dsa_refill_pool(miss_ids, miss_pos, victim, install, miss_count, B, k, sel_l
                                 ptr(ptr_next), S, W, ptr(err), stream_handle(stream))
 
 
+def dsa_stage_misses(miss_ids, miss_pos, miss_count, victim, install, B, k, pool_l, P, host_l,
+                     ctx_stride, ctx_len, err=None, stream=None) -> int:
+    return _lib.dsa_stage_misses(ptr(miss_ids), ptr(miss_pos), ptr(miss_count), ptr(victim),
+                                 ptr(install), B, k, ptr(pool_l), P, ptr(host_l), ctx_stride,
+                                 ptr(ctx_len), ptr(err), stream_handle(stream))
+
+
+def dsa_refill_pool_staged(miss_ids, miss_pos, victim, install, miss_count, B, k, pool_l, P,
+                           update_metadata, pool_tags, fifo_ptr, ptr_next, S, W, err=None,
+                           stream=None) -> int:
+    return _lib.dsa_refill_pool_staged(ptr(miss_ids), ptr(miss_pos), ptr(victim), ptr(install),
+                                       ptr(miss_count), B, k, ptr(pool_l), P,
+                                       int(update_metadata), ptr(pool_tags), ptr(fifo_ptr),
+                                       ptr(ptr_next), S, W, ptr(err), stream_handle(stream))
+
+
 def sfa_workspace_size(B: int, H: int, k: int) -> int:
     return int(_lib.sfa_workspace_size(B, H, k))
 
@@ -237,6 +261,14 @@ def sfa_mla_decode(q, sel_l, B, H, k, scale, out, lse, ws, ws_bytes, err=None,
                    stream=None) -> int:
     return _lib.sfa_mla_decode(ptr(q), ptr(sel_l), B, H, k, float(scale), ptr(out), ptr(lse),
                                ptr(ws), ws_bytes, ptr(err), stream_handle(stream))
+
+
+def sfa_mla_decode_pool(q, pool_l, P, src_map, miss_ids, miss_pos, miss_count, miss_rows, B, H,
+                        k, scale, out, lse, ws, ws_bytes, err=None, stream=None) -> int:
+    return _lib.sfa_mla_decode_pool(ptr(q), ptr(pool_l), P, ptr(src_map), ptr(miss_ids),
+                                    ptr(miss_pos), ptr(miss_count), ptr(miss_rows), B, H, k,
+                                    float(scale), ptr(out), ptr(lse), ptr(ws), ws_bytes, ptr(err),
+                                    stream_handle(stream))
 
 
 def dsa_group_step(group: DsaGroup, scores, q, ids=None, timing=None) -> int:

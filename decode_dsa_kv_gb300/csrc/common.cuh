@@ -109,6 +109,19 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* to
   return ex;
 }
 
+// First position of token t among a request's misses (the plan's ascending
+// miss list mids[0..M) and first positions mpos), or -1: binary search.
+__device__ __forceinline__ int miss_first_pos(const int32_t* mids, const int32_t* mpos, int M,
+                                              int t) {
+  int lo = 0, hi = M;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(mids + mid) < t) lo = mid + 1;
+    else hi = mid;
+  }
+  return (lo < M && __ldg(mids + lo) == t) ? __ldg(mpos + lo) : -1;
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses, mbarriers, TMA
 // ---------------------------------------------------------------------------

@@ -35,18 +35,6 @@ __device__ __forceinline__ void st_v4(uint4* p, uint4 v) {
                : "memory");
 }
 
-// First position of token t among request b's misses, or -1: binary search of
-// the ascending miss list.
-__device__ __forceinline__ int first_pos_of(const int32_t* mids, const int32_t* mpos, int M, int t) {
-  int lo = 0, hi = M;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(mids + mid) < t) lo = mid + 1;
-    else hi = mid;
-  }
-  return (lo < M && __ldg(mids + lo) == t) ? __ldg(mpos + lo) : -1;
-}
-
 // Rows through shared memory with bulk async copies (no registers hold the
 // rows, so a few SMs keep enough rows in flight for the host link or HBM).
 // Lane 0 of a warp issues everything: a row is loaded into one of
@@ -178,9 +166,9 @@ struct GatherLayer {
 __device__ __forceinline__ void gather_misses(const GatherLayer& L, const int32_t* miss_ids,
                                               const int32_t* miss_pos, const int32_t* miss_count,
                                               const int32_t* victim, const uint8_t* install,
-                                              int B, int k, int P, int64_t ctx_stride,
-                                              const int32_t* ctx_len, int w, int nrole, int lane,
-                                              RowPipe& pipe, int& bad) {
+                                              int B, int k, int P, int sel_rows, int pool_rows,
+                                              int64_t ctx_stride, const int32_t* ctx_len, int w,
+                                              int nrole, int lane, RowPipe& pipe, int& bad) {
   // indices below B * k < 2^31 (B <= 65535, k <= 8192) fit in 32 bits
   const uint4* host = L.host;
   uint4* sel = L.sel;
@@ -210,11 +198,11 @@ __device__ __forceinline__ void gather_misses(const GatherLayer& L, const int32_
           bad |= TS_DEVERR_ID_RANGE;
         } else {
           my_from = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
-          my_to = sel + (int64_t(b) * k + j) * DSA_ROW_CHUNKS;
+          my_to = sel + (int64_t(b) * sel_rows + j) * DSA_ROW_CHUNKS;
           my_to2 = nullptr;
           if (victim && __ldg(install + s) == 1) {
             const int v = __ldg(victim + s);
-            if (v >= 0 && v < P) my_to2 = L.pool + (int64_t(b) * P + v) * DSA_ROW_CHUNKS;
+            if (v >= 0 && v < P) my_to2 = L.pool + (int64_t(b) * pool_rows + v) * DSA_ROW_CHUNKS;
             else bad |= TS_DEVERR_SLOT_RANGE;
           }
           valid = true;
@@ -272,7 +260,7 @@ __device__ __forceinline__ void gather_positions(
         const int M = __ldg(miss_count + b);
         const int t = -1 - src;
         const int64_t base = int64_t(b) * k;
-        if (__ldg(miss_rows + b) != M && first_pos_of(miss_ids + base, miss_pos + base, M, t) != j) {
+        if (__ldg(miss_rows + b) != M && miss_first_pos(miss_ids + base, miss_pos + base, M, t) != j) {
           if (t < __ldg(ctx_len + b) && t < ctx_stride)
             from = L.host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
           else bad |= TS_DEVERR_ID_RANGE;
@@ -297,8 +285,10 @@ __device__ __forceinline__ void gather_positions(
 
 // One launch for `layers` consecutive layers (layer l's pool, host rows and
 // selection start l * pool_stride / host_stride / sel_stride pieces after
-// layer 0's), in two kinds of CTAs of kPipeWarps warps, every warp with its
-// own RowPipe:
+// layer 0's; a request's rows start sel_rows / pool_rows rows apart in the
+// selection / pool: k and P, or P + k each for the staged layout, whose
+// "selection" is the staging rows after the pool's slots), in two kinds of
+// CTAs of kPipeWarps warps, every warp with its own RowPipe:
 //   CTAs [0, miss_ctas): gather_misses, the host-link reads that set the
 //     kernel's time (a few SMs keep the link busy);
 //   the others: gather_positions, the pool hits (HBM), beside them.
@@ -319,7 +309,7 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
     const uint4* __restrict__ host, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
     uint4* __restrict__ sel, int layers, int64_t pool_stride, int64_t host_stride,
     int64_t sel_stride, uint32_t* __restrict__ done, uint32_t* __restrict__ count, uint32_t seq,
-    int miss_ctas, int32_t* err) {
+    int miss_ctas, int sel_rows, int pool_rows, int32_t* err) {
   extern __shared__ __align__(128) uint8_t gather_smem[];
   const int lane = threadIdx.x & 31;
   const int wc = threadIdx.x >> 5;  // warp in the CTA
@@ -335,8 +325,8 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
   for (int l = 0; l < layers; ++l) {
     const GatherLayer L{pool + l * pool_stride, host + l * host_stride, sel + l * sel_stride};
     if (miss_cta)
-      gather_misses(L, miss_ids, miss_pos, miss_count, victim, install, B, k, P, ctx_stride,
-                    ctx_len, w, nrole, lane, pipe, bad);
+      gather_misses(L, miss_ids, miss_pos, miss_count, victim, install, B, k, P, sel_rows,
+                    pool_rows, ctx_stride, ctx_len, w, nrole, lane, pipe, bad);
     else
       gather_positions(L, src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, P,
                        ctx_stride, ctx_len, w, nrole, lane, pipe, bad);
@@ -362,7 +352,8 @@ __global__ void __launch_bounds__(kRefillThreads) refill_kernel(
     const int32_t* __restrict__ miss_count, int B, int k, const uint4* __restrict__ sel,
     uint4* __restrict__ pool, int P, int layers, int64_t sel_stride, int64_t pool_stride,
     int update_metadata, int32_t* __restrict__ pool_tags, int32_t* __restrict__ fifo_ptr,
-    const int32_t* __restrict__ ptr_next, int S, int W, int min_install, int32_t* err) {
+    const int32_t* __restrict__ ptr_next, int S, int W, int min_install, int sel_rows,
+    int pool_rows, int32_t* err) {
   const int lane = threadIdx.x & 31;
   const int warp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int nwarps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
@@ -386,8 +377,8 @@ __global__ void __launch_bounds__(kRefillThreads) refill_kernel(
           if (update_metadata) pool_tags[int64_t(b) * P + v] = __ldg(miss_ids + r);
           // (rows with a lower code went in with the gather)
           need = code >= min_install;
-          from_row = int64_t(b) * k + j;
-          to_row = int64_t(b) * P + v;
+          from_row = int64_t(b) * sel_rows + j;
+          to_row = int64_t(b) * pool_rows + v;
         }
       }
     }
@@ -473,7 +464,7 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
                          const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream,
                          int layers, size_t pool_layer_bytes, size_t host_layer_bytes,
                          size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq,
-                         const int32_t* victim, const uint8_t* install) {
+                         const int32_t* victim, const uint8_t* install, bool staged) {
   // At the decode_batch shape (32 x 2048 rows a layer, 9.7 GB of host KV):
   // kMissCtas + kHitCtas CTAs (24 SMs): the misses' share of them reads at
   // the host link's rate (measured alone: 8 SMs of bulk copies reach the
@@ -483,6 +474,8 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
   // Measured alternatives that did worse: plain loads on 3/8 of the SMs
   // (the earlier design, 0.549 vs 0.540 ms a step), other splits (9 + 15,
   // 10 + 14, 12 + 12, 6 + 18, 4 + 20 CTAs), 8 or 32 warps per CTA.
+  // The staged layout moves only the misses (the attention reads the hits
+  // from the pool itself): the miss CTAs alone, into the staging rows.
   static std::atomic<uint64_t> smem_set{0};
   if (!raise_smem_limit(reinterpret_cast<const void*>(gather_kernel),
                         static_cast<int>(kPipeSmemBytes), smem_set))
@@ -491,13 +484,29 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
       double(host_layer_bytes ? host_layer_bytes : size_t(B) * size_t(ctx_stride) * DSA_ROW_BYTES) *
       layers;
   const GatherGrid grid = gather_grid(B, k, host_bytes);
-  gather_kernel<<<grid.miss + grid.hit, kPipeWarps * 32, kPipeSmemBytes, stream>>>(
-      src_map, miss_ids, miss_pos, miss_count, miss_rows, victim, install, B, k,
-      static_cast<uint4*>(const_cast<void*>(pool_l)), P, static_cast<const uint4*>(host_l),
-      ctx_stride, ctx_len, static_cast<uint4*>(sel_l), layers, int64_t(pool_layer_bytes / 16),
-      int64_t(host_layer_bytes / 16), int64_t(sel_layer_bytes / 16), done, count, seq, grid.miss,
-      err);
+  const int hit = staged ? 0 : grid.hit;
+  const int pool_rows = staged ? P + k : P;
+  const int sel_rows = staged ? P + k : k;
+  uint4* pool = static_cast<uint4*>(const_cast<void*>(pool_l));
+  uint4* sel = staged ? pool + size_t(P) * DSA_ROW_CHUNKS : static_cast<uint4*>(sel_l);
+  if (staged) sel_layer_bytes = pool_layer_bytes;
+  gather_kernel<<<grid.miss + hit, kPipeWarps * 32, kPipeSmemBytes, stream>>>(
+      src_map, miss_ids, miss_pos, miss_count, miss_rows, victim, install, B, k, pool, P,
+      static_cast<const uint4*>(host_l), ctx_stride, ctx_len, sel, layers,
+      int64_t(pool_layer_bytes / 16), int64_t(host_layer_bytes / 16),
+      int64_t(sel_layer_bytes / 16), done, count, seq, grid.miss, sel_rows, pool_rows, err);
   return launch_status();
+}
+
+ts_status stage_check(const int32_t* miss_ids, const int32_t* miss_pos, const int32_t* miss_count,
+                      int B, int k, const void* pool_l, int P, const void* host_l,
+                      int64_t ctx_stride, const int32_t* ctx_len) {
+  if (!miss_ids || !miss_pos || !miss_count || !pool_l || !host_l || !ctx_len)
+    return TS_ERR_INVALID_ARG;
+  if (B <= 0 || k <= 0 || P <= 0 || ctx_stride <= 0) return TS_ERR_INVALID_ARG;
+  if (int64_t(B) * (int64_t(P) + k) >= (int64_t(1) << 31)) return TS_ERR_UNSUPPORTED;
+  if (!aligned16(pool_l) || !aligned16(host_l)) return TS_ERR_INVALID_ARG;
+  return TS_OK;
 }
 
 ts_status refill_check(const int32_t* miss_ids, const int32_t* miss_pos, const int32_t* victim,
@@ -519,20 +528,26 @@ ts_status refill_enqueue(const int32_t* miss_ids, const int32_t* miss_pos, const
                          const void* sel_l, void* pool_l, int P, int update_metadata,
                          int32_t* pool_tags, int32_t* fifo_ptr, const int32_t* ptr_next, int S,
                          int W, int32_t* err, cudaStream_t stream, int layers,
-                         size_t sel_layer_bytes, size_t pool_layer_bytes, int min_install) {
+                         size_t sel_layer_bytes, size_t pool_layer_bytes, int min_install,
+                         bool staged) {
   // one warp per (request, miss); one small CTA per SM, which fits beside an
   // attention CTA (measured best of 16 or 38 1024-thread CTAs and 76 or 152
-  // 256-thread ones, beside the attention and the next layer's gather)
+  // 256-thread ones, beside the attention and the next layer's gather). The
+  // staged layout refills from the pool's own staging rows.
   const int64_t warps = int64_t(B) * k;
   int64_t blocks = (warps * 32 + kRefillThreads - 1) / kRefillThreads;
   const int64_t cap = sm_count();
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  const int pool_rows = staged ? P + k : P;
+  const int sel_rows = staged ? P + k : k;
+  const uint4* sel = staged ? static_cast<const uint4*>(pool_l) + size_t(P) * DSA_ROW_CHUNKS
+                            : static_cast<const uint4*>(sel_l);
+  if (staged) sel_layer_bytes = pool_layer_bytes;
   refill_kernel<<<static_cast<unsigned>(blocks), kRefillThreads, 0, stream>>>(
-      miss_ids, miss_pos, victim, install, miss_count, B, k, static_cast<const uint4*>(sel_l),
-      static_cast<uint4*>(pool_l), P, layers, int64_t(sel_layer_bytes / 16),
-      int64_t(pool_layer_bytes / 16), update_metadata, pool_tags, fifo_ptr, ptr_next, S, W,
-      min_install, err);
+      miss_ids, miss_pos, victim, install, miss_count, B, k, sel, static_cast<uint4*>(pool_l), P,
+      layers, int64_t(sel_layer_bytes / 16), int64_t(pool_layer_bytes / 16), update_metadata,
+      pool_tags, fifo_ptr, ptr_next, S, W, min_install, sel_rows, pool_rows, err);
   return launch_status();
 }
 
@@ -549,7 +564,21 @@ extern "C" ts_status dsa_gather_kv(const int32_t* src_map, const int32_t* miss_i
   if (st != TS_OK) return st;
   return dsakv::gather_enqueue(src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, pool_l,
                                P, host_l, ctx_stride, ctx_len, sel_l, err, stream, 1, 0, 0, 0,
-                               nullptr, nullptr, 0, nullptr, nullptr);
+                               nullptr, nullptr, 0, nullptr, nullptr, false);
+}
+
+extern "C" ts_status dsa_stage_misses(const int32_t* miss_ids, const int32_t* miss_pos,
+                                      const int32_t* miss_count, const int32_t* victim,
+                                      const uint8_t* install, int B, int k, void* pool_l, int P,
+                                      const void* host_l, int64_t ctx_stride,
+                                      const int32_t* ctx_len, int32_t* err, cudaStream_t stream) {
+  const ts_status st = dsakv::stage_check(miss_ids, miss_pos, miss_count, B, k, pool_l, P, host_l,
+                                          ctx_stride, ctx_len);
+  if (st != TS_OK) return st;
+  if ((victim == nullptr) != (install == nullptr)) return TS_ERR_INVALID_ARG;
+  return dsakv::gather_enqueue(nullptr, miss_ids, miss_pos, miss_count, nullptr, B, k, pool_l, P,
+                               host_l, ctx_stride, ctx_len, nullptr, err, stream, 1, 0, 0, 0,
+                               nullptr, nullptr, 0, victim, install, true);
 }
 
 extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* miss_pos,
@@ -564,7 +593,23 @@ extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* mis
   if (st != TS_OK) return st;
   return dsakv::refill_enqueue(miss_ids, miss_pos, victim, install, miss_count, B, k, sel_l,
                                pool_l, P, update_metadata, pool_tags, fifo_ptr, ptr_next, S, W,
-                               err, stream, 1, 0, 0, 1);
+                               err, stream, 1, 0, 0, 1, false);
+}
+
+extern "C" ts_status dsa_refill_pool_staged(const int32_t* miss_ids, const int32_t* miss_pos,
+                                            const int32_t* victim, const uint8_t* install,
+                                            const int32_t* miss_count, int B, int k, void* pool_l,
+                                            int P, int update_metadata, int32_t* pool_tags,
+                                            int32_t* fifo_ptr, const int32_t* ptr_next, int S,
+                                            int W, int32_t* err, cudaStream_t stream) {
+  if (int64_t(B) * (int64_t(P) + k) >= (int64_t(1) << 31)) return TS_ERR_UNSUPPORTED;
+  const ts_status st = dsakv::refill_check(miss_ids, miss_pos, victim, install, miss_count, B, k,
+                                           pool_l, pool_l, P, update_metadata, pool_tags,
+                                           fifo_ptr, ptr_next, S, W);
+  if (st != TS_OK) return st;
+  return dsakv::refill_enqueue(miss_ids, miss_pos, victim, install, miss_count, B, k, nullptr,
+                               pool_l, P, update_metadata, pool_tags, fifo_ptr, ptr_next, S, W,
+                               err, stream, 1, 0, 0, 1, true);
 }
 
 // ---------------------------------------------------------------------------

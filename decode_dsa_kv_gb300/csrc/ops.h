@@ -51,7 +51,16 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
                          const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream,
                          int layers, size_t pool_layer_bytes, size_t host_layer_bytes,
                          size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq,
-                         const int32_t* victim, const uint8_t* install);
+                         const int32_t* victim, const uint8_t* install, bool staged);
+
+// The staged layout: a layer's pool tensor is [B][P + k][576]; rows P .. P+k-1
+// of a request hold the step's missed rows at their first positions, so the
+// attention reads every row straight from the pool (sfa_pool_*). gather_enqueue
+// with staged = true moves only the misses (src_map, miss_rows and sel_l
+// unused) into those rows; refill_enqueue with staged = true copies from them.
+ts_status stage_check(const int32_t* miss_ids, const int32_t* miss_pos, const int32_t* miss_count,
+                      int B, int k, const void* pool_l, int P, const void* host_l,
+                      int64_t ctx_stride, const int32_t* ctx_len);
 
 ts_status refill_check(const int32_t* miss_ids, const int32_t* miss_pos, const int32_t* victim,
                        const uint8_t* install, const int32_t* miss_count, int B, int k,
@@ -67,17 +76,23 @@ ts_status refill_enqueue(const int32_t* miss_ids, const int32_t* miss_pos, const
                          const void* sel_l, void* pool_l, int P, int update_metadata,
                          int32_t* pool_tags, int32_t* fifo_ptr, const int32_t* ptr_next, int S,
                          int W, int32_t* err, cudaStream_t stream, int layers,
-                         size_t sel_layer_bytes, size_t pool_layer_bytes, int min_install);
+                         size_t sel_layer_bytes, size_t pool_layer_bytes, int min_install,
+                         bool staged);
 
 ts_status sfa_check(const void* q, const void* sel_l, int B, int H, int k, float scale,
                     void* out, const void* ws, size_t ws_bytes);
 ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, float scale,
                       void* out, float* lse, void* ws, int32_t* err, cudaStream_t stream);
-// The two launches of sfa_enqueue, for callers that run the merge elsewhere:
-// the chunks (partials into ws) and the merge of the chunks (ws -> out, lse).
-ts_status sfa_enqueue_chunks(const void* q, const void* sel_l, int B, int H, int k, float scale,
-                             void* ws, int32_t* err, cudaStream_t stream);
-ts_status sfa_enqueue_combine(int B, int H, int k, void* out, float* lse, const void* ws,
-                              cudaStream_t stream);
+// The attention reading its rows straight from a staged-layout pool by the
+// plan (hits: the slot; misses: the staged row at P + first position).
+ts_status sfa_pool_check(const void* q, const void* pool_l, int P, const int32_t* src_map,
+                         const int32_t* miss_ids, const int32_t* miss_pos,
+                         const int32_t* miss_count, const int32_t* miss_rows, int B, int H, int k,
+                         float scale, void* out, const void* ws, size_t ws_bytes);
+ts_status sfa_pool_enqueue(const void* q, const void* pool_l, int P, const int32_t* src_map,
+                           const int32_t* miss_ids, const int32_t* miss_pos,
+                           const int32_t* miss_count, const int32_t* miss_rows, int B, int H,
+                           int k, float scale, void* out, float* lse, void* ws, int32_t* err,
+                           cudaStream_t stream);
 
 }  // namespace dsakv

@@ -28,6 +28,7 @@
 //   otherwise: O (unnormalised) -> fp32 workspace straight from TMEM, as a
 //       dim-major tile [512][128 heads] (coalesced stores), the row max and
 //       the row sum beside it, and a second kernel merges the chunks.
+#include <climits>
 #include <cmath>
 
 #include "common.cuh"
@@ -233,18 +234,58 @@ __device__ __forceinline__ void merge_in_cluster(Bars* bars, uint8_t* base, uint
   }
 }
 
+// Where the variant that reads straight from the pool finds a selected row:
+// the plan's source map over a staged-layout pool tensor, `prow` = P + k rows
+// per request (the P slots, then the step's missed rows staged at P + their
+// first position).
+struct PoolSrc {
+  const int32_t* src_map;
+  const int32_t* miss_ids;
+  const int32_t* miss_pos;
+  const int32_t* miss_count;
+  const int32_t* miss_rows;
+  int P, prow;
+};
+
+// Row of the pool tensor (counted over all requests) that position j of
+// request b reads: a hit's slot, a miss's staged row (its first position's,
+// when the request repeats tokens). A bad entry sets bits of `bad` and reads
+// the position's own staged row instead (in bounds; the result is undefined).
+__device__ __forceinline__ int pool_row(const PoolSrc& ps, int b, int k, int j, int M,
+                                        bool repeats, int& bad) {
+  const int src = __ldg(ps.src_map + int64_t(b) * k + j);
+  int rel = ps.P + j;
+  if (src >= 0) {
+    if (src < ps.P) rel = src;
+    else bad |= TS_DEVERR_SLOT_RANGE;
+  } else if (src == INT_MIN) {
+    bad |= TS_DEVERR_ID_RANGE;
+  } else if (repeats) {
+    const int f = miss_first_pos(ps.miss_ids + int64_t(b) * k, ps.miss_pos + int64_t(b) * k, M,
+                                 -1 - src);
+    if (f >= 0 && f < k) rel = ps.P + f;
+    else bad |= TS_DEVERR_ID_RANGE;
+  }
+  return static_cast<int>(int64_t(b) * ps.prow + rel);
+}
+
 // kMerge = false: O, the row max and the row sum of the chunk go to the
 // workspace for sfa_combine_kernel. kMerge = true: the C chunk CTAs of a
 // (request, head tile) form one thread-block cluster and merge their O
 // through distributed shared memory; CTA r of the cluster writes dims
 // [r * 512 / C, (r + 1) * 512 / C) of the bf16 output (C = 1, 2 or 4).
-template <bool kMerge>
+// kPool = false: the rows are the selection buffer's, loaded as tiles (tm_k,
+// tm_v: 3-D maps over [B][k][576]). kPool = true: the rows are read straight
+// from a staged-layout pool by the plan (`ps`), four rows per TMA gather
+// (tm_k = tm_v: a 2-D map over all B * prow pool rows, one row high), issued
+// by the 32 lanes of the producer warp.
+template <bool kMerge, bool kPool>
 __global__ void __launch_bounds__(kThreads, 1)
     sfa_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, int H, int k, int HG, int C,
                      float scale_log2, float* __restrict__ opart, float2* __restrict__ ml,
                      __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint64_t wait_ns,
-                     int32_t* err) {
+                     const PoolSrc ps, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Bars* bars = reinterpret_cast<Bars*>(smem_raw);
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -282,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    for (int it = 0; it < kSSlots && it < kScoreLoads; ++it) {
+    for (int it = 0; !kPool && it < kSSlots && it < kScoreLoads; ++it) {
       uint8_t* st = score_slot(it);
       const int kb = it % kKB, nh = it / kKB;
       mbar_expect_tx(&bars->full[it], kStageBytes);
@@ -300,7 +341,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 0 && kPool) {
+    // ---------------- TMA producer, rows gathered from the pool ----------------
+    // Lane 0 waits for a slot and loads the Q tile; then every lane issues two
+    // 4-row gathers: score stages take rows 4*lane.. and 128 + 4*lane.. of the
+    // 256-row half, value stages rows 4*(lane & 15).. of the 64-row block for
+    // dim boxes (lane >> 4) and (lane >> 4) + 2. Positions past k read row k-1
+    // (their weights are zero).
+    const int M = min(max(__ldg(ps.miss_count + b), 0), k);
+    const bool repeats = __ldg(ps.miss_rows + b) != __ldg(ps.miss_count + b);
+    const int j0 = c * kChunk;
+    int bad = 0;
+    bool ok = true;
+    int kr[8];
+    for (int it = 0; it < kScoreLoads && ok; ++it) {
+      const int s = it % kSSlots;
+      if (it >= kSSlots) ok = warp_wait(&bars->empty[s], ((it / kSSlots) - 1) & 1, abort, wait_ns);
+      if (!ok) break;
+      const int kb = it % kKB, nh = it / kKB;
+      if (kb == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          kr[i] = pool_row(ps, b, k, min(j0 + nh * kHalfRows + 4 * lane + i, k - 1), M, repeats,
+                           bad);
+          kr[4 + i] = pool_row(ps, b, k, min(j0 + nh * kHalfRows + 128 + 4 * lane + i, k - 1), M,
+                               repeats, bad);
+        }
+      }
+      uint8_t* st = score_slot(s);
+      if (lane == 0) {
+        mbar_expect_tx(&bars->full[s], kStageBytes);
+        tma_load_3d(st, &tm_q, &bars->full[s], kb * 64, hg * kHeads, b);
+      }
+      __syncwarp();
+      uint8_t* kt = st + kQBytes;
+      tma_gather4(kt + lane * 512, &tm_k, &bars->full[s], kb * 64, kr[0], kr[1], kr[2], kr[3]);
+      tma_gather4(kt + (lane + 32) * 512, &tm_k, &bars->full[s], kb * 64, kr[4], kr[5], kr[6],
+                  kr[7]);
+      if (lane == 0) bars->issued = it + 1;
+    }
+    // value phase, once the scores are done (their slots are free then)
+    if (ok) ok = warp_wait(&bars->s_full, 0, abort, wait_ns);
+    for (int v = 0; v < kLoads - kScoreLoads && ok; ++v) {
+      const int s = v % kVSlots;
+      if (v >= kVSlots) ok = warp_wait(&bars->vempty[s], ((v / kVSlots) - 1) & 1, abort, wait_ns);
+      if (!ok) break;
+      const int half = v >> 3, rb = v & 7;
+      const int g = lane & 15, jb = lane >> 4;
+      int vr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        vr[i] = pool_row(ps, b, k, min(j0 + rb * 64 + 4 * g + i, k - 1), M, repeats, bad);
+      uint8_t* st = stages + s * kVBytes;
+      if (lane == 0) mbar_expect_tx(&bars->vfull[s], kVBytes);
+      __syncwarp();
+      tma_gather4(st + jb * kVBox + g * 512, &tm_v, &bars->vfull[s], half * 256 + jb * 64, vr[0],
+                  vr[1], vr[2], vr[3]);
+      tma_gather4(st + (jb + 2) * kVBox + g * 512, &tm_v, &bars->vfull[s],
+                  half * 256 + (jb + 2) * 64, vr[0], vr[1], vr[2], vr[3]);
+      if (lane == 0) bars->issued = kScoreLoads + v + 1;
+    }
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    if (bad && lane == 0) report(err, bad);
+  } else if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       // score phase: kSSlots slots; slots 2 and 3 borrow the P region, which
@@ -617,6 +720,87 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t batch, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over `rows` rows of 576 bf16, box 64 values x 1 row (the form the
+// 4-row gathers take).
+bool make_rows_map(CUtensorMap* map, const void* ptr, uint64_t rows) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {DSA_D, rows};
+  const cuuint64_t strides[1] = {DSA_ROW_BYTES};
+  const cuuint32_t box[2] = {64, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The chunks of a (request, head tile) merge inside one cluster when they are
+// 1, 2 or 4 (C = ceil(k / 512)); otherwise through the workspace and a second
+// kernel.
+bool sfa_merges_in_cluster(int k) {
+  const int C = (k + kChunk - 1) / kChunk;
+  return C == 1 || C == 2 || C == 4;
+}
+
+// The attention's launches, from a selection buffer (sel_l, ps unused) or
+// straight from a staged-layout pool (kPool: pool_l with ps).
+template <bool kPool>
+ts_status launch_attention(const void* q, const void* rows, uint64_t total_rows, const PoolSrc& ps,
+                           int B, int H, int k, float scale, void* out, float* lse, void* ws,
+                           int32_t* err, cudaStream_t stream) {
+  const int HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!make_map(&tm_q, q, H, B, kHeads)) return TS_ERR_CUDA;
+  if (kPool) {
+    if (!make_rows_map(&tm_k, rows, total_rows)) return TS_ERR_CUDA;
+    tm_v = tm_k;
+  } else if (!make_map(&tm_k, rows, k, B, kHalfRows) || !make_map(&tm_v, rows, k, B, 64)) {
+    return TS_ERR_CUDA;
+  }
+  const uint64_t wait_ns = wait_limit_ns(kWaitLimit);
+  if (sfa_merges_in_cluster(k)) {
+    static std::atomic<uint64_t> smem_set{0};
+    if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<true, kPool>),
+                          static_cast<int>(kSmemBytes), smem_set))
+      return TS_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C, HG, B);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    float* no_part = nullptr;
+    float2* no_ml = nullptr;
+    if (cudaLaunchKernelEx(&cfg, sfa_chunk_kernel<true, kPool>, tm_q, tm_k, tm_v, H, k, HG, C,
+                           scale * kLog2e, no_part, no_ml, static_cast<__nv_bfloat16*>(out), lse,
+                           wait_ns, ps, err) != cudaSuccess) {
+      cudaGetLastError();
+      return TS_ERR_CUDA;
+    }
+    return TS_OK;
+  }
+  const size_t slots = size_t(B) * HG * C * kHeads;
+  float* opart = static_cast<float*>(ws);
+  float2* ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + align256(slots * DSA_DV * 4));
+  static std::atomic<uint64_t> smem_set{0};
+  if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<false, kPool>),
+                        static_cast<int>(kSmemBytes), smem_set))
+    return TS_ERR_CUDA;
+  sfa_chunk_kernel<false, kPool><<<dim3(C, HG, B), kThreads, kSmemBytes, stream>>>(
+      tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, nullptr, nullptr, wait_ns, ps,
+      err);
+  if (launch_status() != TS_OK) return TS_ERR_CUDA;
+  sfa_combine_kernel<<<dim3(DSA_DV / kCombineDims, HG, B), kHeads, 0, stream>>>(
+      opart, ml, H, HG, C, static_cast<__nv_bfloat16*>(out), lse);
+  return launch_status();
+}
+
 }  // namespace
 }  // namespace dsakv
 
@@ -642,86 +826,32 @@ ts_status sfa_check(const void* q, const void* sel_l, int B, int H, int k, float
   return TS_OK;
 }
 
-ts_status sfa_enqueue_chunks(const void* q, const void* sel_l, int B, int H, int k, float scale,
-                             void* ws, int32_t* err, cudaStream_t stream) {
-  const int HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
-  CUtensorMap tm_q, tm_k, tm_v;
-  if (!make_map(&tm_q, q, H, B, kHeads) || !make_map(&tm_k, sel_l, k, B, kHalfRows) ||
-      !make_map(&tm_v, sel_l, k, B, 64))
-    return TS_ERR_CUDA;
-  const size_t slots = size_t(B) * HG * C * kHeads;
-  float* opart = static_cast<float*>(ws);
-  float2* ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + align256(slots * DSA_DV * 4));
-  static std::atomic<uint64_t> smem_set{0};
-  if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<false>),
-                        static_cast<int>(kSmemBytes), smem_set))
-    return TS_ERR_CUDA;
-  sfa_chunk_kernel<false><<<dim3(C, HG, B), kThreads, kSmemBytes, stream>>>(
-      tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, nullptr, nullptr,
-      wait_limit_ns(kWaitLimit), err);
-  return launch_status();
+ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, float scale,
+                      void* out, float* lse, void* ws, int32_t* err, cudaStream_t stream) {
+  return launch_attention<false>(q, sel_l, 0, PoolSrc{}, B, H, k, scale, out, lse, ws, err,
+                                 stream);
 }
 
-// One launch: the chunks of a (request, head tile) as one cluster that merges
-// them in distributed shared memory (C = ceil(k / 512) of 1, 2 or 4).
-bool sfa_merges_in_cluster(int k) {
-  const int C = (k + kChunk - 1) / kChunk;
-  return C == 1 || C == 2 || C == 4;
-}
-
-ts_status sfa_enqueue_merged(const void* q, const void* sel_l, int B, int H, int k, float scale,
-                             void* out, float* lse, int32_t* err, cudaStream_t stream) {
-  const int HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
-  CUtensorMap tm_q, tm_k, tm_v;
-  if (!make_map(&tm_q, q, H, B, kHeads) || !make_map(&tm_k, sel_l, k, B, kHalfRows) ||
-      !make_map(&tm_v, sel_l, k, B, 64))
-    return TS_ERR_CUDA;
-  static std::atomic<uint64_t> smem_set{0};
-  if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<true>),
-                        static_cast<int>(kSmemBytes), smem_set))
-    return TS_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, HG, B);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = C;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  float* no_part = nullptr;
-  float2* no_ml = nullptr;
-  if (cudaLaunchKernelEx(&cfg, sfa_chunk_kernel<true>, tm_q, tm_k, tm_v, H, k, HG, C,
-                         scale * kLog2e, no_part, no_ml, static_cast<__nv_bfloat16*>(out), lse,
-                         wait_limit_ns(kWaitLimit), err) != cudaSuccess) {
-    cudaGetLastError();
-    return TS_ERR_CUDA;
-  }
+ts_status sfa_pool_check(const void* q, const void* pool_l, int P, const int32_t* src_map,
+                         const int32_t* miss_ids, const int32_t* miss_pos,
+                         const int32_t* miss_count, const int32_t* miss_rows, int B, int H, int k,
+                         float scale, void* out, const void* ws, size_t ws_bytes) {
+  const ts_status st = sfa_check(q, pool_l, B, H, k, scale, out, ws, ws_bytes);
+  if (st != TS_OK) return st;
+  if (!src_map || !miss_ids || !miss_pos || !miss_count || !miss_rows || P <= 0)
+    return TS_ERR_INVALID_ARG;
+  if (int64_t(B) * (int64_t(P) + k) >= (int64_t(1) << 31)) return TS_ERR_UNSUPPORTED;
   return TS_OK;
 }
 
-ts_status sfa_enqueue_combine(int B, int H, int k, void* out, float* lse, const void* ws,
-                              cudaStream_t stream) {
-  const int HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
-  const size_t slots = size_t(B) * HG * C * kHeads;
-  const float* opart = static_cast<const float*>(ws);
-  const float2* ml =
-      reinterpret_cast<const float2*>(static_cast<const char*>(ws) + align256(slots * DSA_DV * 4));
-  sfa_combine_kernel<<<dim3(DSA_DV / kCombineDims, HG, B), kHeads, 0, stream>>>(
-      opart, ml, H, HG, C, static_cast<__nv_bfloat16*>(out), lse);
-  return launch_status();
-}
-
-ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, float scale,
-                      void* out, float* lse, void* ws, int32_t* err, cudaStream_t stream) {
-  if (sfa_merges_in_cluster(k))
-    return sfa_enqueue_merged(q, sel_l, B, H, k, scale, out, lse, err, stream);
-  const ts_status st = sfa_enqueue_chunks(q, sel_l, B, H, k, scale, ws, err, stream);
-  if (st != TS_OK) return st;
-  return sfa_enqueue_combine(B, H, k, out, lse, ws, stream);
+ts_status sfa_pool_enqueue(const void* q, const void* pool_l, int P, const int32_t* src_map,
+                           const int32_t* miss_ids, const int32_t* miss_pos,
+                           const int32_t* miss_count, const int32_t* miss_rows, int B, int H,
+                           int k, float scale, void* out, float* lse, void* ws, int32_t* err,
+                           cudaStream_t stream) {
+  const PoolSrc ps{src_map, miss_ids, miss_pos, miss_count, miss_rows, P, P + k};
+  return launch_attention<true>(q, pool_l, uint64_t(B) * uint64_t(P + k), ps, B, H, k, scale, out,
+                                lse, ws, err, stream);
 }
 
 }  // namespace dsakv
@@ -732,4 +862,17 @@ extern "C" ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int
   const ts_status st = sfa_check(q, sel_l, B, H, k, scale, out, ws, ws_bytes);
   if (st != TS_OK) return st;
   return sfa_enqueue(q, sel_l, B, H, k, scale, out, lse, ws, err, stream);
+}
+
+extern "C" ts_status sfa_mla_decode_pool(const void* q, const void* pool_l, int P,
+                                         const int32_t* src_map, const int32_t* miss_ids,
+                                         const int32_t* miss_pos, const int32_t* miss_count,
+                                         const int32_t* miss_rows, int B, int H, int k,
+                                         float scale, void* out, float* lse, void* ws,
+                                         size_t ws_bytes, int32_t* err, cudaStream_t stream) {
+  const ts_status st = sfa_pool_check(q, pool_l, P, src_map, miss_ids, miss_pos, miss_count,
+                                      miss_rows, B, H, k, scale, out, ws, ws_bytes);
+  if (st != TS_OK) return st;
+  return sfa_pool_enqueue(q, pool_l, P, src_map, miss_ids, miss_pos, miss_count, miss_rows, B, H,
+                          k, scale, out, lse, ws, err, stream);
 }

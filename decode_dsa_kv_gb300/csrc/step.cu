@@ -96,6 +96,9 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
   if (!ids && !scores) return TS_ERR_INVALID_ARG;
   const bool reuse = g.policy == DSA_POLICY_REUSE;
   if (!reuse && g.policy != DSA_POLICY_FIFO) return TS_ERR_INVALID_ARG;
+  const bool staged = g.layout == DSA_LAYOUT_STAGED;
+  if (!staged && g.layout != DSA_LAYOUT_SELECTION) return TS_ERR_INVALID_ARG;
+  if (staged && reuse) return TS_ERR_UNSUPPORTED;
   if (reuse && (ids || !g.prev_ids || !g.prev_sel)) return TS_ERR_INVALID_ARG;
   if (g.S <= 0 || g.W <= 0 || int64_t(g.S) * g.W > (1 << 24)) return TS_ERR_INVALID_ARG;
   if (!g.sync || (reinterpret_cast<uintptr_t>(g.sync) & 3u) != 0) return TS_ERR_INVALID_ARG;
@@ -104,6 +107,7 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
   const int P = reuse ? g.k : g.S * g.W;
   Layers lb = layer_bytes(g);
   if (reuse) lb.pool = lb.sel;
+  if (staged) lb.pool = size_t(g.B) * (size_t(P) + g.k) * kRowBytes;
   const void* pool = reuse ? static_cast<const void*>(g.prev_sel) : g.pool;
   const int32_t* plan_ids = ids ? ids : g.ids;
 
@@ -120,12 +124,19 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
                             g.src_map, g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count,
                             g.miss_rows, g.ptr_next);
   if (st == TS_OK)
-    st = gather_check(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k, pool,
-                      P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel);
+    st = staged ? stage_check(g.miss_ids, g.miss_pos, g.miss_count, g.B, g.k, g.pool, P, g.host_kv,
+                              g.ctx_stride, g.ctx_len)
+                : gather_check(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B,
+                               g.k, pool, P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel);
   if (st == TS_OK && !reuse)
-    st = refill_check(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k, g.sel,
-                      g.pool, P, 1, g.pool_tags, g.fifo_ptr, g.ptr_next, g.S, g.W);
-  if (st == TS_OK) st = sfa_check(q, g.sel, g.B, g.H, g.k, g.scale, g.out, g.sfa_ws, g.sfa_ws_bytes);
+    st = refill_check(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k,
+                      staged ? g.pool : g.sel, g.pool, P, 1, g.pool_tags, g.fifo_ptr, g.ptr_next,
+                      g.S, g.W);
+  if (st == TS_OK)
+    st = staged ? sfa_pool_check(q, g.pool, P, g.src_map, g.miss_ids, g.miss_pos, g.miss_count,
+                                 g.miss_rows, g.B, g.H, g.k, g.scale, g.out, g.sfa_ws,
+                                 g.sfa_ws_bytes)
+                : sfa_check(q, g.sel, g.B, g.H, g.k, g.scale, g.out, g.sfa_ws, g.sfa_ws_bytes);
   if (st != TS_OK) return st;
   if (!memops().ok) return TS_ERR_UNSUPPORTED;
 
@@ -136,6 +147,7 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
   uint32_t* refilled = g.sync + kRefilled;
   uint32_t* gathered = g.sync + kGathered;
   uint32_t* counts = g.sync + kGathered + L;  // the gather's per-layer warp counts
+  uint32_t* attended = g.sync + kGathered + 2 * L;  // staged layout: a layer's attention is done
   auto rec = [&](int slot, int end, cudaStream_t s) {
     return timing ? cudaEventRecord(timing[2 * slot + end], s) == cudaSuccess : true;
   };
@@ -162,22 +174,28 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
        gather_enqueue(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k, pool,
                       P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel, g.err, gs, L, lb.pool,
                       lb.host, lb.sel, gathered, counts, seq, reuse ? nullptr : g.victim,
-                      reuse ? nullptr : g.install) == TS_OK &&
+                      reuse ? nullptr : g.install, staged) == TS_OK &&
        rec(2, 1, gs);
   // per layer: the attention on the main stream, the refill beside it on the
-  // side stream; the last refill also updates the metadata
+  // side stream; the last refill also updates the metadata. The staged
+  // attention reads hit rows from the pool itself, so the layer's refill
+  // (which overwrites slots read as hits) waits for that attention
   for (int l = 0; ok && l < L; ++l) {
+    float* lse_l = g.lse ? at(g.lse, l, lb.lse) : nullptr;
     ok = wait_for(m, gathered + l, seq) && rec(3 + l, 0, m) &&
-         sfa_enqueue(at(q, l, lb.q), at(g.sel, l, lb.sel), g.B, g.H, g.k, g.scale,
-                     at(g.out, l, lb.out), g.lse ? at(g.lse, l, lb.lse) : nullptr, g.sfa_ws,
-                     g.err, m) == TS_OK &&
-         rec(3 + l, 1, m);
+         (staged ? sfa_pool_enqueue(at(q, l, lb.q), at(g.pool, l, lb.pool), P, g.src_map,
+                                    g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.H,
+                                    g.k, g.scale, at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m)
+                 : sfa_enqueue(at(q, l, lb.q), at(g.sel, l, lb.sel), g.B, g.H, g.k, g.scale,
+                               at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m)) == TS_OK &&
+         rec(3 + l, 1, m) && (!staged || signal(m, attended + l, seq));
     if (!reuse)
-      ok = ok && wait_for(side, gathered + l, seq) && rec(3 + L + l, 0, side) &&
+      ok = ok && wait_for(side, (staged ? attended : gathered) + l, seq) &&
+           rec(3 + L + l, 0, side) &&
            refill_enqueue(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k,
-                          at(g.sel, l, lb.sel), at(g.pool, l, lb.pool), P, l == L - 1,
-                          g.pool_tags, g.fifo_ptr, g.ptr_next, g.S, g.W, g.err, side, 1, lb.sel,
-                          lb.pool, 2) == TS_OK &&
+                          staged ? nullptr : at(g.sel, l, lb.sel), at(g.pool, l, lb.pool), P,
+                          l == L - 1, g.pool_tags, g.fifo_ptr, g.ptr_next, g.S, g.W, g.err, side,
+                          1, lb.sel, lb.pool, 2, staged) == TS_OK &&
            rec(3 + L + l, 1, side);
   }
   if (reuse) {
@@ -212,6 +230,7 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
           cudaEventRecord(ev[i], others[i]) == cudaSuccess)
         cudaStreamWaitEvent(side, ev[i], 0);
     for (int i = 0; i < kGathered + L; ++i) signal(side, g.sync + i, seq);
+    for (int i = 0; staged && i < L; ++i) signal(side, attended + i, seq);
     for (int i = 0; i < 2; ++i)
       if (ev[i]) cudaEventDestroy(ev[i]);
     cudaGetLastError();

@@ -178,14 +178,23 @@ class DecodeGroup:
     policy "fifo": the set-associative FIFO pool of S sets x W ways;
     policy "reuse": the base design's adjacent-step reuse, where the device
     keeps only the previous step's selection (S and W are then unused).
-    After a step, `ids` and `sel` hold that step's ids and selection."""
+    After a step, `ids` and `sel` hold that step's ids and selection.
+
+    layout "selection": every layer's rows are gathered into `sel`, which the
+    attention reads; layout "staged" (FIFO only): the attention reads its rows
+    straight from the pool, which then holds P + k rows per request (rows P..
+    stage the step's misses at their first positions) and `sel` is None."""
 
     def __init__(self, B: int, layers: int, k: int, S: int, W: int, H: int,
                  ctx_len, ctx_stride: int, host: HostKV, scale: float | None = None,
-                 device: str = "cuda", max_ctx: int | None = None, policy: str = "fifo"):
+                 device: str = "cuda", max_ctx: int | None = None, policy: str = "fifo",
+                 layout: str = "selection"):
         if policy not in ("fifo", "reuse"):
             raise ValueError(policy)
+        if layout not in ("selection", "staged") or (layout == "staged" and policy != "fifo"):
+            raise ValueError(layout)
         self.policy = policy
+        self.layout = layout
         self.B, self.L, self.k, self.S, self.W, self.H = B, layers, k, S, W, H
         self.P = S * W
         self.ctx_stride = ctx_stride
@@ -199,7 +208,8 @@ class DecodeGroup:
         # reuse policy keeps the previous step's ids and selection instead)
         reuse = policy == "reuse"
         P = 1 if reuse else self.P
-        self.pool = torch.zeros((layers, B, P, D), dtype=torch.int16, device=dev)
+        rows = P + k if layout == "staged" else P
+        self.pool = torch.zeros((layers, B, rows, D), dtype=torch.int16, device=dev)
         self.tags = torch.full((B, P), -1, **i32)
         self.fifo_ptr = torch.zeros((B, 1 if reuse else S), **i32)
         # plan outputs
@@ -213,7 +223,8 @@ class DecodeGroup:
         self.miss_rows = torch.zeros((B,), **i32)
         self.ptr_next = torch.empty((B, 1 if reuse else S), **i32)
         # per-layer selection buffers and attention outputs
-        self.sel = torch.empty((layers, B, k, D), dtype=torch.int16, device=dev)
+        self.sel = (None if layout == "staged"
+                    else torch.empty((layers, B, k, D), dtype=torch.int16, device=dev))
         if reuse:
             self.prev_ids = torch.full((B, k), -1, **i32)
             self.prev_sel = torch.zeros((layers, B, k, D), dtype=torch.int16, device=dev)
@@ -235,8 +246,14 @@ class DecodeGroup:
         self.side = torch.cuda.Stream(device=dev, priority=0)
         # cross-stream signals: device words written and waited on by the
         # streams themselves (zero before the first step)
-        self.sync = torch.zeros((2 + 2 * layers,), **i32)
+        self.sync = torch.zeros((2 + 3 * layers,), **i32)
         self.desc = self._descriptor()
+
+    def staged_rows(self, l: int, b: int):
+        """Staged layout: the rows the step staged for request b of layer l
+        (int16 [k][576]; row j holds the host row of a miss first selected at
+        position j, the other rows are stale)."""
+        return self.pool[l, b, self.P:]
 
     def timing(self) -> StepTiming:
         """Timing events for one step of this group (see StepTiming)."""
@@ -252,7 +269,9 @@ class DecodeGroup:
         d.host_kv = self.host.dev
         for name in ("ids", "src_map", "miss_ids", "miss_pos", "victim", "install",
                      "miss_count", "miss_rows", "ptr_next", "sel", "out", "lse"):
-            setattr(d, name, getattr(self, name).data_ptr())
+            t = getattr(self, name)
+            setattr(d, name, 0 if t is None else t.data_ptr())
+        d.layout = abi.DSA_LAYOUT_STAGED if self.layout == "staged" else abi.DSA_LAYOUT_SELECTION
         d.topk_ws, d.topk_ws_bytes = self.topk_ws.data_ptr(), self.topk_ws_bytes
         d.sfa_ws, d.sfa_ws_bytes = self.sfa_ws.data_ptr(), self.sfa_ws_bytes
         d.err = self.err.data_ptr()

@@ -237,6 +237,32 @@ ts_status dsa_gather_kv(const int32_t* src_map, const int32_t* miss_ids,
                         cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * dsa_stage_misses -- serve one layer's missed rows into a staged-layout pool
+ * ([GLM] §5 DsaServe, §5.1; the hit half of the serve needs no copy here, see
+ * sfa_mla_decode_pool). Only the host-link part of the gather: each distinct
+ * missed token t of request b, first at position j (dsa_plan's miss_ids /
+ * miss_pos / miss_count), is read in place from pinned host memory into
+ *   pool_l[b][P + j]
+ * and, with victim / install given (both or neither), an install with code 1
+ * (no position of the step reads its victim slot) also goes straight into
+ *   pool_l[b][victim]
+ * as it arrives, leaving the refill only the code-2 installs.
+ *
+ *   pool_l  bf16 [B][P + k][576]       device, the staged layout: rows 0..P-1
+ *                                      of a request are its pool slots, rows
+ *                                      P..P+k-1 stage the step's misses
+ *   host_l  bf16 [B][ctx_stride][576]  device-accessible address of pinned
+ *                                      host memory, this layer's latent KV
+ * Both 16-byte aligned; B * (P + k) < 2^31. A bad id or victim sets
+ * TS_DEVERR_ID_RANGE / TS_DEVERR_SLOT_RANGE and skips that row.
+ * ------------------------------------------------------------------------- */
+ts_status dsa_stage_misses(const int32_t* miss_ids, const int32_t* miss_pos,
+                           const int32_t* miss_count, const int32_t* victim,
+                           const uint8_t* install, int B, int k, void* pool_l, int P,
+                           const void* host_l, int64_t ctx_stride, const int32_t* ctx_len,
+                           int32_t* err, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * dsa_refill_pool -- the deferred refill of one layer's pool ([GLM] §4.4, §5
  * DsaInstall, §5.1). For every installed miss i of request b (install != 0):
  *   pool_l[b][victim[i]] = sel_l[b][miss_pos[i]]   (the missed row's bytes)
@@ -251,6 +277,18 @@ ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* miss_pos,
                           void* pool_l, int P, int update_metadata, int32_t* pool_tags,
                           int32_t* fifo_ptr, const int32_t* ptr_next, int S, int W,
                           int32_t* err, cudaStream_t stream);
+
+/* dsa_refill_pool_staged -- dsa_refill_pool for the staged layout: the rows
+ * come from the pool's own staging rows, pool_l[b][victim[i]] =
+ * pool_l[b][P + miss_pos[i]] (pool_l [B][P + k][576]; tags and pointers as
+ * dsa_refill_pool's). Must run after this layer's sfa_mla_decode_pool, which
+ * reads the slots read as hits in place. */
+ts_status dsa_refill_pool_staged(const int32_t* miss_ids, const int32_t* miss_pos,
+                                 const int32_t* victim, const uint8_t* install,
+                                 const int32_t* miss_count, int B, int k, void* pool_l, int P,
+                                 int update_metadata, int32_t* pool_tags, int32_t* fifo_ptr,
+                                 const int32_t* ptr_next, int S, int W, int32_t* err,
+                                 cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * sfa_mla_decode -- sparse absorbed-MLA decode attention over the selection
@@ -272,6 +310,32 @@ size_t sfa_workspace_size(int B, int H, int k);
 ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int H, int k,
                          float scale, void* out, float* lse, void* ws, size_t ws_bytes,
                          int32_t* err, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * sfa_mla_decode_pool -- sfa_mla_decode whose rows come straight from a
+ * staged-layout pool by the plan, with no selection buffer in between: the
+ * gather fused into the attention ([GLM] §5 DsaServe's selection, consumed
+ * where it lies; §2.1 SFA). Row j of request b is
+ *   pool_l[b][src_map[b][j]]          for a hit (src_map >= 0),
+ *   pool_l[b][P + first position of t] for a miss of t (src_map = -1 - t),
+ * staged there by dsa_stage_misses. The tensor cores get the rows by TMA
+ * gathers of four rows at a time. Same arithmetic, tile order and results
+ * as sfa_mla_decode over the selection those rows make (bit for bit).
+ *
+ *   q        bf16 [B][H][576]
+ *   pool_l   bf16 [B][P + k][576]     16-byte aligned; B * (P + k) < 2^31
+ *   src_map, miss_ids, miss_pos, miss_count, miss_rows   dsa_plan's
+ *   out, lse, ws, ws_bytes            as sfa_mla_decode's
+ * An out-of-range slot or a miss that is not in the miss list sets
+ * TS_DEVERR_SLOT_RANGE / TS_DEVERR_ID_RANGE (that row then reads its own
+ * staging row; the result is undefined). Must run after this layer's
+ * dsa_stage_misses and before its dsa_refill_pool_staged.
+ * ------------------------------------------------------------------------- */
+ts_status sfa_mla_decode_pool(const void* q, const void* pool_l, int P, const int32_t* src_map,
+                              const int32_t* miss_ids, const int32_t* miss_pos,
+                              const int32_t* miss_count, const int32_t* miss_rows, int B, int H,
+                              int k, float scale, void* out, float* lse, void* ws,
+                              size_t ws_bytes, int32_t* err, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * dsa_group_step -- one decode step of an IndexShare group of `layers` layers,
@@ -302,6 +366,12 @@ ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int H, int k,
  * every refill. Every wait is enqueued after the signal it waits for, so
  * every wait ends.
  *
+ * With layout = DSA_LAYOUT_STAGED the gather launch moves only the misses
+ * (as dsa_stage_misses per layer), the attention is sfa_mla_decode_pool(l),
+ * the main stream writes attended[l] after it, and refill(l) waits for
+ * attended[l] instead of gathered[l] (the attention reads the hit slots in
+ * place; the refill overwrites some of them).
+ *
  * The descriptor holds the group's buffers (the caller owns all of them):
  *   ctx_len   int32 [B]                     k <= ctx_len[b] <= max_ctx
  *   pool      bf16  [layers][B][S*W][576]   the device pool of every layer
@@ -314,7 +384,8 @@ ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int H, int k,
  *   topk_ws / sfa_ws                        workspaces of ts_topk and
  *                                           sfa_mla_decode (sizes as theirs)
  *   err       int32 device error word (or NULL)
- *   sync      uint32 [2 + 2 * layers] device words, zero before the first step
+ *   sync      uint32 [2 + 2 * layers] device words (2 + 3 * layers with the
+ *             staged layout), zero before the first step
  *             and touched by nothing else; step = 0 before the first step.
  *             Each call uses sequence number step + 1 and stores it in
  *             `step` (with the reuse policy it also swaps the buffers named
@@ -377,10 +448,22 @@ typedef struct {
   int policy;
   int32_t* prev_ids;
   void* prev_sel;
+  /* where the attention reads its rows: DSA_LAYOUT_SELECTION, the selection
+   * buffers above (gathered there by dsa_gather_kv's kernel); or
+   * DSA_LAYOUT_STAGED, straight from the pool: `pool` is then
+   * [layers][B][S*W + k][576], each request's rows S*W .. S*W+k-1 staging the
+   * step's missed rows at their first positions; only the misses cross into
+   * HBM (dsa_stage_misses' kernel), the attention is sfa_mla_decode_pool's,
+   * each layer's refill waits for that layer's attention (the hits it read
+   * stay in place until then), and `sel` is not used. Needs the FIFO policy
+   * and 2 + 3 * layers sync words. */
+  int layout;
 } dsa_group;
 
 #define DSA_POLICY_FIFO 0
 #define DSA_POLICY_REUSE 1
+#define DSA_LAYOUT_SELECTION 0
+#define DSA_LAYOUT_STAGED 1
 
 ts_status dsa_group_step(dsa_group* g, const float* scores, const void* q, const int32_t* ids,
                          cudaEvent_t* timing);

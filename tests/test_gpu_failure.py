@@ -72,24 +72,28 @@ def test_attention_wait_that_runs_out_reports_and_recovers(d, k):
             assert a <= SFA_ABS_TOL and rel <= SFA_MEAN_REL_TOL, (b, a, rel)
 
 
-def test_group_step_orders_streams_under_delays(d):
+@pytest.mark.parametrize("layout", ["selection", "staged"])
+def test_group_step_orders_streams_under_delays(d, layout):
     # small pools (256 sets x 16 ways) over 16,384-position contexts, so sets
     # evict from the second step on and code-2 installs (victim slots read as
     # hits in the same step) are common
     w = wl.scaled(wl.DECODE_BATCH, B=2, ctx=16384, S=256)
     T = 7
+    staged = layout == "staged"
     lens = wl.ctx_lens(w)
     host = d.HostKV(w.layers, w.B, w.ctx_stride)
     wl.fill_host_kv(w, host.array)
-    g = d.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host)
+    g = d.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host, layout=layout)
     stream = wl.ScoreStream(w)
     scores = np.stack([stream.next() for _ in range(T)])
     qs = np.stack([wl.queries(w, t) for t in range(T)])
     scores_d = torch.from_numpy(scores).cuda()
     q_d = torch.from_numpy(qs.view(np.int16)).cuda()
+    # what each step's attention read: the selection buffers, or the staged rows
+    rows = g.pool[:, :, w.P:] if staged else g.sel
     snap = {"ids": torch.empty((T, w.B, w.k), dtype=torch.int32, device="cuda"),
             "src": torch.empty((T, w.B, w.k), dtype=torch.int32, device="cuda"),
-            "sel": torch.empty((T,) + tuple(g.sel.shape), dtype=torch.int16, device="cuda"),
+            "rows": torch.empty((T,) + tuple(rows.shape), dtype=torch.int16, device="cuda"),
             "out": torch.empty((T,) + tuple(g.out.shape), dtype=torch.bfloat16, device="cuda"),
             "install": torch.empty((T, w.B, w.k), dtype=torch.uint8, device="cuda"),
             "mc": torch.empty((T, w.B), dtype=torch.int32, device="cuda")}
@@ -98,21 +102,25 @@ def test_group_step_orders_streams_under_delays(d):
     for t in range(T):
         # about 2 ms of spinning ahead of this step's work on one stream:
         # the refill (then the next plan must wait for it), the gather (the
-        # attention and the refill must wait), or the top-k and plan (the
-        # gather must wait)
+        # attention and the refill must wait), or the top-k, plan and
+        # attention (the gather must wait for the plan; with the staged layout
+        # the refill must wait for the attention)
         with torch.cuda.stream(delayed[t % 3]):
             torch.cuda._sleep(4_000_000)
         g.step(scores_d[t], q_d[t])
         with torch.cuda.stream(g.main):   # after the step's last attention
             snap["ids"][t].copy_(g.ids)
             snap["src"][t].copy_(g.src_map)
-            snap["sel"][t].copy_(g.sel)
+            snap["rows"][t].copy_(rows)
             snap["out"][t].copy_(g.out)
             snap["install"][t].copy_(g.install)
             snap["mc"][t].copy_(g.miss_count)
     assert g.synchronize() == 0
     snap = {k: v.cpu() for k, v in snap.items()}
     scale = 1 / math.sqrt(576)
+    ws_bytes = d.sfa_workspace_size(1, w.H, w.k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
     deferred = 0
     for b in range(w.B):
         st = oracle.init_state(w.layers, w.S, w.W)
@@ -127,8 +135,21 @@ def test_group_step_orders_streams_under_delays(d):
             assert np.array_equal(snap["install"][t, b, :M].numpy(), plan.install_code)
             deferred += int(np.sum(plan.install_code == 2))
             for l in range(w.layers):
-                sel = snap["sel"][t, l, b].numpy().view(np.uint16)
-                assert np.array_equal(sel, r["sel"][l]), (t, b, l)
+                got_rows = snap["rows"][t, l, b].numpy().view(np.uint16)
+                if staged:
+                    assert np.array_equal(got_rows[plan.miss_pos], host.array[l, b][plan.miss_ids])
+                else:
+                    assert np.array_equal(got_rows, r["sel"][l]), (t, b, l)
+            # the attention read exactly the oracle's rows: bit-exact against
+            # the selection kernel over them, and within tolerance
+            out = torch.empty((1, w.H, 512), dtype=torch.bfloat16, device="cuda")
+            qb = torch.from_numpy(np.ascontiguousarray(qs[t, 3, b:b + 1]).view(np.int16)).cuda()
+            selb = torch.from_numpy(np.ascontiguousarray(r["sel"][3][None]).view(np.int16)).cuda()
+            assert d.sfa_mla_decode(qb, selb, 1, w.H, w.k, scale, out, None, ws, ws_bytes,
+                                    err) == 0
+            assert d.ts_read_error(err) == 0
+            assert torch.equal(snap["out"][t, 3, b].view(torch.int16),
+                               out[0].cpu().view(torch.int16)), (t, b)
             o, _ = oracle.sfa_decode(qs[t, 3, b], r["sel"][3], scale)
             got = snap["out"][t, 3, b].view(torch.int16).numpy().view(np.uint16)
             a, rel = sfa_errors(got, oracle.round_to_bf16_bits(o))
@@ -137,6 +158,7 @@ def test_group_step_orders_streams_under_delays(d):
         assert np.array_equal(g.tags[b].cpu().numpy(), st.tags)
         assert np.array_equal(g.fifo_ptr[b].cpu().numpy(), st.fifo_ptr)
         for l in range(w.layers):
-            assert np.array_equal(g.pool[l, b].cpu().numpy().view(np.uint16), st.pool[l]), (b, l)
+            assert np.array_equal(g.pool[l, b, :w.P].cpu().numpy().view(np.uint16), st.pool[l]), \
+                (b, l)
     assert deferred > 0   # installs that had to wait for the layer's reads occurred
     host.close()
