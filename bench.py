@@ -78,9 +78,10 @@ def parse(argv=None):
     ap.add_argument("--B", type=int, default=None, help="override the workload's request count")
     ap.add_argument("--sets", type=int, default=None,
                     help="override the pool's sets (16 ways each): 512 = 8K entries, 1024 = 16K")
-    ap.add_argument("--policy", choices=("fifo", "reuse"), default="fifo",
-                    help="device pool: the set-associative FIFO pool (default) or the base "
-                         "design's adjacent-step reuse of the previous selection")
+    ap.add_argument("--policy", choices=("fifo", "lru", "reuse"), default="fifo",
+                    help="device pool: the set-associative FIFO pool (default), a fully "
+                         "associative LRU pool of the same size, or the base design's "
+                         "adjacent-step reuse of the previous selection")
     ap.add_argument("--layout", choices=("staged", "selection"), default="staged",
                     help="staged: the attention reads its rows straight from the pool (only "
                          "the misses are staged in HBM); selection: every row is gathered "
@@ -467,19 +468,24 @@ def cpu_baseline_leg(args, w: wl.Workload, overrides: dict) -> dict:
 
 
 def oracle_hit_check(w: wl.Workload, scores_steps, lens, first_timed: int, timed: int,
-                     gpu_miss_log, requests) -> dict:
-    """The oracle's plan followed step by step over every step the device ran
-    up to the end of the timed region, for a few requests: its hit rate over
-    the timed steps beside the device's for the same requests and steps (the
-    plans are bit-exact, so the two must be equal)."""
+                     gpu_miss_log, requests, policy: str = "fifo") -> dict:
+    """The oracle's plan (the FIFO pool, or the LRU pool) followed step by step
+    over every step the device ran up to the end of the timed region, for a
+    few requests: its hit rate over the timed steps beside the device's for
+    the same requests and steps (the plans are bit-exact, so the two must be
+    equal)."""
     import oracle
     ora_hits = gpu_hits = 0
     for b in requests:
         st = oracle.init_state(1, w.S, w.W)
+        lru = oracle.LruSlots(w.P)
         for t in range(first_timed + timed):
             ids = oracle.topk_ids(scores_steps[t, b], int(lens[b]), w.k)
-            plan = oracle.dsa_plan(ids, int(lens[b]), st.tags, st.fifo_ptr, w.S, w.W)
-            oracle.metadata_update(st.tags, st.fifo_ptr, plan)
+            if policy == "lru":
+                plan = lru.plan(ids, int(lens[b]))
+            else:
+                plan = oracle.dsa_plan(ids, int(lens[b]), st.tags, st.fifo_ptr, w.S, w.W)
+                oracle.metadata_update(st.tags, st.fifo_ptr, plan)
             if t >= first_timed:
                 ora_hits += w.k - plan.miss_rows
                 gpu_hits += w.k - int(gpu_miss_log[t - first_timed, b])
@@ -580,7 +586,7 @@ def run_native(args, w, rank, world, local, overrides):
                   "ts_copy")
     torch.cuda.synchronize()
     del touch
-    staged = args.layout == "staged" and args.policy == "fifo"
+    staged = args.layout == "staged" and args.policy != "reuse"
     g = dk.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host,
                        policy=args.policy, layout="staged" if staged else "selection")
     peaks = measured_peaks()
@@ -738,11 +744,11 @@ def run_native(args, w, rank, world, local, overrides):
     if rank != 0:
         return
     cpu = None
-    if not args.no_cpu_baseline and args.policy == "fifo":
+    if not args.no_cpu_baseline and args.policy != "reuse":
         cpu = cpu_baseline_leg(args, w, overrides)
         reqs = [0] if w.ctx > 131072 else sorted({0, w.B // 2, w.B - 1})
         cpu["plan_check"] = oracle_hit_check(w, scores_steps, lens, first_timed, args.steps,
-                                             miss_host, reqs)
+                                             miss_host, reqs, args.policy)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,

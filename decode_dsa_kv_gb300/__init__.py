@@ -13,7 +13,7 @@ import importlib
 _ABI_NAMES = {
     "ts_status_string", "ts_host_register", "ts_host_unregister", "ts_host_alloc", "ts_host_free",
     "ts_read_error", "ts_copy", "ts_set_wait_limit_ns",
-    "ts_topk_workspace_size", "ts_topk", "ts_topk_noalloc", "dsa_plan", "dsa_plan_reuse",
+    "ts_topk_workspace_size", "ts_topk", "ts_topk_noalloc", "dsa_plan", "dsa_plan_reuse", "dsa_plan_lru",
     "dsa_gather_kv", "dsa_stage_misses", "dsa_refill_pool", "dsa_refill_pool_staged",
     "sfa_mla_decode_pool",
     "sfa_workspace_size", "sfa_mla_decode", "dsa_group_step", "DsaGroup", "DsaKvError", "check", "status_string", "EXPORTS",

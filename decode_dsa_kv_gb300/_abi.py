@@ -53,6 +53,7 @@ _SIGS = {
     "ts_topk_noalloc": (_I, [_P, _I64, _P, _I, _I, _I, _P, _P, _P]),
     "dsa_plan": (_I, [_P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dsa_plan_reuse": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "dsa_plan_lru": (_I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dsa_gather_kv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _I, _P, _I64, _P, _P, _P, _P]),
     "dsa_stage_misses": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _I, _P, _I64, _P, _P, _P]),
     "dsa_refill_pool": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _I, _I,
@@ -71,6 +72,7 @@ EXPORTS = tuple(_SIGS)
 TS_MAX_LAYERS = 16
 DSA_POLICY_FIFO = 0
 DSA_POLICY_REUSE = 1
+DSA_POLICY_LRU = 2
 DSA_LAYOUT_SELECTION = 0
 DSA_LAYOUT_STAGED = 1
 
@@ -97,6 +99,8 @@ class DsaGroup(ctypes.Structure):
         ("prev_ids", _P),
         ("prev_sel", _P),
         ("layout", _I),
+        ("lru_stamp", _P),
+        ("lru_clock", _P),
     ]
 
 for _name, (_res, _args) in _SIGS.items():
@@ -219,6 +223,14 @@ def dsa_plan_reuse(ids, prev_ids, ctx_len, B, k, src_map, miss_ids, miss_pos, mi
     return _lib.dsa_plan_reuse(ptr(ids), ptr(prev_ids), ptr(ctx_len), B, k, ptr(src_map),
                                ptr(miss_ids), ptr(miss_pos), ptr(miss_count), ptr(miss_rows),
                                ptr(err), stream_handle(stream))
+
+
+def dsa_plan_lru(ids, ctx_len, B, k, pool_tags, lru_stamp, lru_clock, P, src_map, miss_ids,
+                 miss_pos, victim, install, miss_count, miss_rows, err=None, stream=None) -> int:
+    return _lib.dsa_plan_lru(ptr(ids), ptr(ctx_len), B, k, ptr(pool_tags), ptr(lru_stamp),
+                             ptr(lru_clock), P, ptr(src_map), ptr(miss_ids), ptr(miss_pos),
+                             ptr(victim), ptr(install), ptr(miss_count), ptr(miss_rows), ptr(err),
+                             stream_handle(stream))
 
 
 def dsa_gather_kv(src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, pool_l, P, host_l,

@@ -62,6 +62,12 @@ constexpr uint32_t kBarBytes = 704;
 // refill CTA can run beside an attention CTA.
 constexpr uint32_t kTileBytes = kPBytes + kStages * kStageBytes;
 constexpr uint32_t kSmemBytes = kBarBytes + 1024 + kTileBytes;
+// The variant that reads from the pool also keeps the chunk's 512 pool rows
+// (relative to the request, so P + k <= 65536) after the barrier block; it
+// then fills the SM's shared memory, with no room left for another CTA.
+constexpr uint32_t kRowIdxBytes = kChunk * 2;
+constexpr uint32_t kPoolSmemBytes = kSmemBytes + kRowIdxBytes;
+static_assert(kPoolSmemBytes <= 227 * 1024, "dynamic shared memory of one CTA");
 constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s of global timer per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -247,10 +253,10 @@ struct PoolSrc {
   int P, prow;
 };
 
-// Row of the pool tensor (counted over all requests) that position j of
-// request b reads: a hit's slot, a miss's staged row (its first position's,
-// when the request repeats tokens). A bad entry sets bits of `bad` and reads
-// the position's own staged row instead (in bounds; the result is undefined).
+// Row of request b's part of the pool tensor that position j reads: a hit's
+// slot, a miss's staged row (its first position's, when the request repeats
+// tokens). A bad entry sets bits of `bad` and reads the position's own staged
+// row instead (in bounds; the result is undefined).
 __device__ __forceinline__ int pool_row(const PoolSrc& ps, int b, int k, int j, int M,
                                         bool repeats, int& bad) {
   const int src = __ldg(ps.src_map + int64_t(b) * k + j);
@@ -266,7 +272,7 @@ __device__ __forceinline__ int pool_row(const PoolSrc& ps, int b, int k, int j, 
     if (f >= 0 && f < k) rel = ps.P + f;
     else bad |= TS_DEVERR_ID_RANGE;
   }
-  return static_cast<int>(int64_t(b) * ps.prow + rel);
+  return rel;
 }
 
 // kMerge = false: O, the row max and the row sum of the chunk go to the
@@ -288,8 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const PoolSrc ps, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Bars* bars = reinterpret_cast<Bars*>(smem_raw);
+  uint16_t* ridx = reinterpret_cast<uint16_t*>(smem_raw + kBarBytes);  // kPool only
   uint8_t* base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + kBarBytes + 1023) & ~uintptr_t(1023));
+      (reinterpret_cast<uintptr_t>(smem_raw) + kBarBytes + (kPool ? kRowIdxBytes : 0u) + 1023) &
+      ~uintptr_t(1023));
   uint8_t* p_tile = base;
   uint8_t* stages = base + kPBytes;
   auto score_slot = [&](int s) -> uint8_t* {
@@ -343,31 +351,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && kPool) {
     // ---------------- TMA producer, rows gathered from the pool ----------------
-    // Lane 0 waits for a slot and loads the Q tile; then every lane issues two
-    // 4-row gathers: score stages take rows 4*lane.. and 128 + 4*lane.. of the
-    // 256-row half, value stages rows 4*(lane & 15).. of the 64-row block for
-    // dim boxes (lane >> 4) and (lane >> 4) + 2. Positions past k read row k-1
-    // (their weights are zero).
+    // The chunk's 512 pool rows first (16 per lane, into shared memory); then
+    // per stage lane 0 waits for the slot and loads the Q tile, and every
+    // lane issues two 4-row gathers: score stages take rows 4*lane.. and
+    // 128 + 4*lane.. of the 256-row half, value stages rows 4*(lane & 15).. of
+    // the 64-row block for dim boxes (lane >> 4) and (lane >> 4) + 2.
+    // Positions past k read row k-1 (their weights are zero).
     const int M = min(max(__ldg(ps.miss_count + b), 0), k);
     const bool repeats = __ldg(ps.miss_rows + b) != __ldg(ps.miss_count + b);
     const int j0 = c * kChunk;
+    const int rbase = b * ps.prow;  // B * prow < 2^31 (host check)
     int bad = 0;
+#pragma unroll 4
+    for (int p = lane; p < kChunk; p += 32)
+      ridx[p] = static_cast<uint16_t>(pool_row(ps, b, k, min(j0 + p, k - 1), M, repeats, bad));
+    __syncwarp();
+    auto row = [&](int p) { return rbase + static_cast<int>(ridx[p]); };
     bool ok = true;
-    int kr[8];
     for (int it = 0; it < kScoreLoads && ok; ++it) {
       const int s = it % kSSlots;
       if (it >= kSSlots) ok = warp_wait(&bars->empty[s], ((it / kSSlots) - 1) & 1, abort, wait_ns);
       if (!ok) break;
       const int kb = it % kKB, nh = it / kKB;
-      if (kb == 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          kr[i] = pool_row(ps, b, k, min(j0 + nh * kHalfRows + 4 * lane + i, k - 1), M, repeats,
-                           bad);
-          kr[4 + i] = pool_row(ps, b, k, min(j0 + nh * kHalfRows + 128 + 4 * lane + i, k - 1), M,
-                               repeats, bad);
-        }
-      }
       uint8_t* st = score_slot(s);
       if (lane == 0) {
         mbar_expect_tx(&bars->full[s], kStageBytes);
@@ -375,9 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       uint8_t* kt = st + kQBytes;
-      tma_gather4(kt + lane * 512, &tm_k, &bars->full[s], kb * 64, kr[0], kr[1], kr[2], kr[3]);
-      tma_gather4(kt + (lane + 32) * 512, &tm_k, &bars->full[s], kb * 64, kr[4], kr[5], kr[6],
-                  kr[7]);
+      const int p0 = nh * kHalfRows + 4 * lane, p1 = p0 + 128;
+      tma_gather4(kt + lane * 512, &tm_k, &bars->full[s], kb * 64, row(p0), row(p0 + 1),
+                  row(p0 + 2), row(p0 + 3));
+      tma_gather4(kt + (lane + 32) * 512, &tm_k, &bars->full[s], kb * 64, row(p1), row(p1 + 1),
+                  row(p1 + 2), row(p1 + 3));
       if (lane == 0) bars->issued = it + 1;
     }
     // value phase, once the scores are done (their slots are free then)
@@ -388,17 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const int half = v >> 3, rb = v & 7;
       const int g = lane & 15, jb = lane >> 4;
-      int vr[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        vr[i] = pool_row(ps, b, k, min(j0 + rb * 64 + 4 * g + i, k - 1), M, repeats, bad);
+      const int p = rb * 64 + 4 * g;
       uint8_t* st = stages + s * kVBytes;
       if (lane == 0) mbar_expect_tx(&bars->vfull[s], kVBytes);
       __syncwarp();
-      tma_gather4(st + jb * kVBox + g * 512, &tm_v, &bars->vfull[s], half * 256 + jb * 64, vr[0],
-                  vr[1], vr[2], vr[3]);
+      tma_gather4(st + jb * kVBox + g * 512, &tm_v, &bars->vfull[s], half * 256 + jb * 64, row(p),
+                  row(p + 1), row(p + 2), row(p + 3));
       tma_gather4(st + (jb + 2) * kVBox + g * 512, &tm_v, &bars->vfull[s],
-                  half * 256 + (jb + 2) * 64, vr[0], vr[1], vr[2], vr[3]);
+                  half * 256 + (jb + 2) * 64, row(p), row(p + 1), row(p + 2), row(p + 3));
       if (lane == 0) bars->issued = kScoreLoads + v + 1;
     }
     bad = __reduce_or_sync(0xffffffffu, bad);
@@ -758,15 +762,16 @@ ts_status launch_attention(const void* q, const void* rows, uint64_t total_rows,
     return TS_ERR_CUDA;
   }
   const uint64_t wait_ns = wait_limit_ns(kWaitLimit);
+  const uint32_t smem = kPool ? kPoolSmemBytes : kSmemBytes;
   if (sfa_merges_in_cluster(k)) {
     static std::atomic<uint64_t> smem_set{0};
     if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<true, kPool>),
-                          static_cast<int>(kSmemBytes), smem_set))
+                          static_cast<int>(smem), smem_set))
       return TS_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C, HG, B);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -790,9 +795,9 @@ ts_status launch_attention(const void* q, const void* rows, uint64_t total_rows,
   float2* ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + align256(slots * DSA_DV * 4));
   static std::atomic<uint64_t> smem_set{0};
   if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<false, kPool>),
-                        static_cast<int>(kSmemBytes), smem_set))
+                        static_cast<int>(smem), smem_set))
     return TS_ERR_CUDA;
-  sfa_chunk_kernel<false, kPool><<<dim3(C, HG, B), kThreads, kSmemBytes, stream>>>(
+  sfa_chunk_kernel<false, kPool><<<dim3(C, HG, B), kThreads, smem, stream>>>(
       tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, nullptr, nullptr, wait_ns, ps,
       err);
   if (launch_status() != TS_OK) return TS_ERR_CUDA;
@@ -840,7 +845,8 @@ ts_status sfa_pool_check(const void* q, const void* pool_l, int P, const int32_t
   if (st != TS_OK) return st;
   if (!src_map || !miss_ids || !miss_pos || !miss_count || !miss_rows || P <= 0)
     return TS_ERR_INVALID_ARG;
-  if (int64_t(B) * (int64_t(P) + k) >= (int64_t(1) << 31)) return TS_ERR_UNSUPPORTED;
+  if (int64_t(B) * (int64_t(P) + k) >= (int64_t(1) << 31) || int64_t(P) + k > 65536)
+    return TS_ERR_UNSUPPORTED;
   return TS_OK;
 }
 

@@ -95,7 +95,9 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
   if (L <= 0 || L > TS_MAX_LAYERS) return TS_ERR_INVALID_ARG;
   if (!ids && !scores) return TS_ERR_INVALID_ARG;
   const bool reuse = g.policy == DSA_POLICY_REUSE;
-  if (!reuse && g.policy != DSA_POLICY_FIFO) return TS_ERR_INVALID_ARG;
+  const bool lru = g.policy == DSA_POLICY_LRU;
+  if (!reuse && !lru && g.policy != DSA_POLICY_FIFO) return TS_ERR_INVALID_ARG;
+  const bool refills = !reuse && !lru;  // only the FIFO pool defers installs
   const bool staged = g.layout == DSA_LAYOUT_STAGED;
   if (!staged && g.layout != DSA_LAYOUT_SELECTION) return TS_ERR_INVALID_ARG;
   if (staged && reuse) return TS_ERR_UNSUPPORTED;
@@ -120,6 +122,9 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
   if (st == TS_OK)
     st = reuse ? plan_reuse_check(plan_ids, g.prev_ids, g.ctx_len, g.B, g.k, g.src_map, g.miss_ids,
                                   g.miss_pos, g.miss_count, g.miss_rows)
+         : lru ? plan_lru_check(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.lru_stamp,
+                                g.lru_clock, P, g.src_map, g.miss_ids, g.miss_pos, g.victim,
+                                g.install, g.miss_count, g.miss_rows)
                : plan_check(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.fifo_ptr, g.S, g.W,
                             g.src_map, g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count,
                             g.miss_rows, g.ptr_next);
@@ -128,7 +133,7 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
                               g.ctx_stride, g.ctx_len)
                 : gather_check(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B,
                                g.k, pool, P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel);
-  if (st == TS_OK && !reuse)
+  if (st == TS_OK && refills)
     st = refill_check(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k,
                       staged ? g.pool : g.sel, g.pool, P, 1, g.pool_tags, g.fifo_ptr, g.ptr_next,
                       g.S, g.W);
@@ -162,6 +167,9 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
   ok = ok && wait_for(m, refilled, seq - 1) && rec(1, 0, m) &&
        (reuse ? plan_reuse_enqueue(plan_ids, g.prev_ids, g.ctx_len, g.B, g.k, g.src_map,
                                    g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.err, m)
+        : lru ? plan_lru_enqueue(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.lru_stamp,
+                                 g.lru_clock, P, g.src_map, g.miss_ids, g.miss_pos, g.victim,
+                                 g.install, g.miss_count, g.miss_rows, g.err, m)
               : plan_enqueue(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.fifo_ptr, g.S, g.W,
                              g.src_map, g.miss_ids, g.miss_pos, g.victim, g.install,
                              g.miss_count, g.miss_rows, g.ptr_next, g.err, m)) == TS_OK &&
@@ -189,7 +197,7 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
                  : sfa_enqueue(at(q, l, lb.q), at(g.sel, l, lb.sel), g.B, g.H, g.k, g.scale,
                                at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m)) == TS_OK &&
          rec(3 + l, 1, m) && (!staged || signal(m, attended + l, seq));
-    if (!reuse)
+    if (refills)
       ok = ok && wait_for(side, (staged ? attended : gathered) + l, seq) &&
            rec(3 + L + l, 0, side) &&
            refill_enqueue(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k,
@@ -198,7 +206,14 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
                           1, lb.sel, lb.pool, 2, staged) == TS_OK &&
            rec(3 + L + l, 1, side);
   }
-  if (reuse) {
+  if (lru) {
+    // no refill: the plan updated the pool's metadata and the gather wrote
+    // every install as its row arrived. The next plan only has to follow
+    // this step's (it does, on the main stream); the next gather, which
+    // installs into slots this step's attention may read (staged layout),
+    // waits for the next plan, after this step's last attention
+    ok = ok && signal(m, refilled, seq);
+  } else if (reuse) {
     // no refill: this step's selection and ids become the next step's
     // "pool". The next step's top-k writes the old previous ids, which this
     // step's plan read (earlier on the main stream); its gather writes the old

@@ -176,6 +176,8 @@ class DecodeGroup:
     """Pool state and buffers for B requests of one IndexShare group.
 
     policy "fifo": the set-associative FIFO pool of S sets x W ways;
+    policy "lru": a fully associative pool of S x W entries, least recently
+    used first (tags, last-use stamps and a clock per request);
     policy "reuse": the base design's adjacent-step reuse, where the device
     keeps only the previous step's selection (S and W are then unused).
     After a step, `ids` and `sel` hold that step's ids and selection.
@@ -189,9 +191,9 @@ class DecodeGroup:
                  ctx_len, ctx_stride: int, host: HostKV, scale: float | None = None,
                  device: str = "cuda", max_ctx: int | None = None, policy: str = "fifo",
                  layout: str = "selection"):
-        if policy not in ("fifo", "reuse"):
+        if policy not in ("fifo", "reuse", "lru"):
             raise ValueError(policy)
-        if layout not in ("selection", "staged") or (layout == "staged" and policy != "fifo"):
+        if layout not in ("selection", "staged") or (layout == "staged" and policy == "reuse"):
             raise ValueError(layout)
         self.policy = policy
         self.layout = layout
@@ -211,7 +213,10 @@ class DecodeGroup:
         rows = P + k if layout == "staged" else P
         self.pool = torch.zeros((layers, B, rows, D), dtype=torch.int16, device=dev)
         self.tags = torch.full((B, P), -1, **i32)
-        self.fifo_ptr = torch.zeros((B, 1 if reuse else S), **i32)
+        self.fifo_ptr = torch.zeros((B, S if policy == "fifo" else 1), **i32)
+        # LRU pool: each slot's last-use tick and each request's clock (uint32)
+        self.lru_stamp = torch.zeros((B, P) if policy == "lru" else (1,), **i32)
+        self.lru_clock = torch.zeros((B,) if policy == "lru" else (1,), **i32)
         # plan outputs
         self.ids = torch.empty((B, k), **i32)
         self.src_map = torch.empty((B, k), **i32)
@@ -221,7 +226,7 @@ class DecodeGroup:
         self.install = torch.empty((B, k), dtype=torch.uint8, device=dev)
         self.miss_count = torch.zeros((B,), **i32)
         self.miss_rows = torch.zeros((B,), **i32)
-        self.ptr_next = torch.empty((B, 1 if reuse else S), **i32)
+        self.ptr_next = torch.empty((B, S if policy == "fifo" else 1), **i32)
         # per-layer selection buffers and attention outputs
         self.sel = (None if layout == "staged"
                     else torch.empty((layers, B, k, D), dtype=torch.int16, device=dev))
@@ -275,6 +280,10 @@ class DecodeGroup:
         d.topk_ws, d.topk_ws_bytes = self.topk_ws.data_ptr(), self.topk_ws_bytes
         d.sfa_ws, d.sfa_ws_bytes = self.sfa_ws.data_ptr(), self.sfa_ws_bytes
         d.err = self.err.data_ptr()
+        if self.policy == "lru":
+            d.policy = abi.DSA_POLICY_LRU
+            d.lru_stamp = self.lru_stamp.data_ptr()
+            d.lru_clock = self.lru_clock.data_ptr()
         if self.policy == "reuse":
             d.policy = abi.DSA_POLICY_REUSE
             d.prev_ids = self.prev_ids.data_ptr()

@@ -213,6 +213,36 @@ ts_status dsa_plan_reuse(const int32_t* ids, const int32_t* prev_ids, const int3
                          cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * dsa_plan_lru -- dsa_plan for a fully associative pool of P entries managed
+ * least recently used first ([GLM] §3: the 8192-entry device pool the pages
+ * measured before adopting the set-associative FIFO of §4.3). A token may sit
+ * in any slot. Per step: every selected token already resident is a hit (its
+ * slot); the hits are touched in position order, then the distinct misses are
+ * installed in ascending id, each into the least recently used slot (empty
+ * slots first, lowest index first). Each touch and each install takes the
+ * next tick of the request's clock.
+ *
+ *   ids        int32 [B][k]   strictly ascending per request (ts_topk's output)
+ *   pool_tags  int32 [B][P]   token held by each slot, -1 = empty (in/out)
+ *   lru_stamp  uint32 [B][P]  tick of each slot's last use (in/out)
+ *   lru_clock  uint32 [B]     tick of each request's latest use (in/out; 0 with
+ *                             a cold pool; wraps after 2^32 ticks, about two
+ *                             million steps of k = 2048)
+ * Outputs as dsa_plan's; every install has code 1 (with k <= P a victim is
+ * never a slot the step reads, so the gather may write it on arrival) and no
+ * refill is needed. Unlike dsa_plan, the pool's tags, stamps and clock are
+ * updated here, at plan time: nothing else reads them, and the next plan runs
+ * after this one. Requires k <= P, k <= 4096, 8 * pow2(P) + 12 * k bytes <=
+ * 200 KiB (P <= 16384 at k = 2048). Ids not strictly ascending set
+ * TS_DEVERR_ORDER (the plan is then undefined).
+ * ------------------------------------------------------------------------- */
+ts_status dsa_plan_lru(const int32_t* ids, const int32_t* ctx_len, int B, int k,
+                       int32_t* pool_tags, uint32_t* lru_stamp, uint32_t* lru_clock, int P,
+                       int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos, int32_t* victim,
+                       uint8_t* install, int32_t* miss_count, int32_t* miss_rows, int32_t* err,
+                       cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * dsa_gather_kv -- serve one layer's selected rows ([GLM] §5 DsaServe, §5.1;
  * base design §2.1 GatherSelectionKvCache). Row j of request b is copied from
  * the device pool when src_map >= 0 and read in place from pinned host memory
@@ -323,7 +353,8 @@ ts_status sfa_mla_decode(const void* q, const void* sel_l, int B, int H, int k,
  * as sfa_mla_decode over the selection those rows make (bit for bit).
  *
  *   q        bf16 [B][H][576]
- *   pool_l   bf16 [B][P + k][576]     16-byte aligned; B * (P + k) < 2^31
+ *   pool_l   bf16 [B][P + k][576]     16-byte aligned; P + k <= 65536,
+ *                                     B * (P + k) < 2^31
  *   src_map, miss_ids, miss_pos, miss_count, miss_rows   dsa_plan's
  *   out, lse, ws, ws_bytes            as sfa_mla_decode's
  * An out-of-range slot or a miss that is not in the miss list sets
@@ -458,10 +489,17 @@ typedef struct {
    * stay in place until then), and `sel` is not used. Needs the FIFO policy
    * and 2 + 3 * layers sync words. */
   int layout;
+  /* DSA_POLICY_LRU: the fully associative LRU pool of P = S*W entries per
+   * request (dsa_plan_lru): lru_stamp uint32 [B][P] and lru_clock uint32 [B],
+   * zero for a cold pool; fifo_ptr, ptr_next are not used and no refill runs
+   * (every install is written by the gather as its row arrives). */
+  uint32_t* lru_stamp;
+  uint32_t* lru_clock;
 } dsa_group;
 
 #define DSA_POLICY_FIFO 0
 #define DSA_POLICY_REUSE 1
+#define DSA_POLICY_LRU 2
 #define DSA_LAYOUT_SELECTION 0
 #define DSA_LAYOUT_STAGED 1
 

@@ -22,7 +22,7 @@ invariants); no function here is "parity unpinned".
 from .topk import topk_ids
 from .plan import Plan, dsa_plan
 from .reuse import ReusePlan, plan_reuse
-from .lru import LruPool
+from .lru import LruPool, LruSlots
 from .serve import dsa_serve
 from .install import dsa_install, metadata_update
 from .sfa import bf16_bits_to_f64, round_to_bf16_bits, sfa_decode

@@ -80,3 +80,62 @@ def test_policy_ordering_on_the_decode_batch_score_process():
     assert r["reuse"] < r["fifo_8k"] < r["lru_8k"]
     assert r["fifo_8k"] < r["fifo_16k"]
     assert 0.55 < r["reuse"] < 0.65
+
+
+def lru_slots_brute(steps, P, ctx):
+    """Slot-level LRU, one use at a time: every hit touched, every miss into
+    the slot with the smallest last-use time (empty slots first, lowest
+    index). Returns per step (src_map, victims, installs, tags, last_use)."""
+    tags, last, clock, out = [-1] * P, [0] * P, 0, []
+    for ids in steps:
+        ids = [int(t) for t in ids]
+        where = {t: s for s, t in enumerate(tags) if t >= 0}
+        src = [where[t] if t in where else -1 - t for t in ids]
+        for s in src:
+            if s >= 0:
+                clock += 1
+                last[s] = clock
+        misses = sorted({t for t in ids if t not in where})
+        vict, latest = [], {}
+        for i, t in enumerate(misses):
+            empty = [s for s in range(P) if tags[s] < 0]
+            v = empty[0] if empty else min(range(P), key=lambda s: last[s])
+            vict.append(v)
+            latest[v] = i
+            tags[v] = t
+            clock += 1
+            last[v] = clock
+        inst = [latest[v] == i for i, v in enumerate(vict)]
+        out.append((src, vict, inst, list(tags), list(last)))
+    return out
+
+
+@pytest.mark.parametrize("P,k,n", [(20, 12, 60), (16, 12, 40), (8, 12, 30), (64, 16, 200)])
+def test_lru_slots_against_brute_force(P, k, n):
+    # includes steps missing more tokens than there are free slots (P = 8 and
+    # 16 with 12 selected), so same-step installs evict each other
+    rng = np.random.default_rng(P * 100 + k)
+    steps = [np.sort(rng.choice(n, k, replace=False)) for _ in range(40)]
+    pool, counter = oracle.LruSlots(P), oracle.LruPool(P)
+    for ids, (src, vict, inst, tags, last) in zip(steps, lru_slots_brute(steps, P, n)):
+        plan = pool.plan(ids, n)
+        assert plan.src_map.tolist() == src
+        assert plan.victim.tolist() == vict and plan.install.tolist() == inst
+        assert pool.tags == tags and pool.last_use == last
+        assert int(np.sum(plan.src_map >= 0)) == counter.step(ids)
+        # invariants: a token sits in one slot; every installed miss is resident
+        resident = [t for t in pool.tags if t >= 0]
+        assert len(resident) == len(set(resident))
+        for t, keep in zip(plan.miss_ids, plan.install):
+            assert (int(t) in resident) == bool(keep) or not keep
+
+
+def test_lru_slots_hand_worked():
+    pool = oracle.LruSlots(3)
+    p = pool.plan([5, 9], 20)                 # cold: empty slots 0, 1
+    assert p.victim.tolist() == [0, 1] and pool.tags == [5, 9, -1]
+    p = pool.plan([1, 9], 20)                 # 9 hits (touched), 1 takes empty slot 2
+    assert p.src_map.tolist() == [-2, 1] and p.victim.tolist() == [2]
+    p = pool.plan([3], 20)                    # LRU is slot 0 (token 5, time 1)
+    assert p.victim.tolist() == [0] and pool.tags == [3, 9, 1]
+    assert pool.clock == 5 and pool.last_use == [5, 3, 4]
