@@ -29,7 +29,8 @@ namespace dsakv {
 namespace {
 
 constexpr int kBins = 4096;    // top 12 bits of the key
-constexpr int kChunk = 8192;   // positions per CTA in the multi-CTA hist / select
+constexpr int kChunk = 8192;   // positions per CTA in the multi-CTA select
+constexpr int kHistChunk = 32768;  // positions per CTA in the multi-CTA hist (one wave at 4 x 1M)
 constexpr int kThreads = 512;  // multi-CTA kernels
 constexpr int kMaxK = 8192;
 constexpr int kFinishCandCap = 4096;  // ... by the multi-CTA finish
@@ -238,12 +239,21 @@ __device__ void finish_request(const C& cand, uint32_t c, int t1, int need1, uin
     }
   }
   __syncthreads();
+  // each thread owns a run of consecutive words; kRun of them are loaded
+  // before any is used, so the loads of a long bitmap overlap
+  constexpr int kRun = 16;
   const int64_t nwords = (int64_t(n) + 31) / 32;
   const int64_t per = (nwords + blockDim.x - 1) / blockDim.x;
   const int64_t w0 = int64_t(threadIdx.x) * per;
   const int64_t w1 = min(w0 + per, nwords);
   int cnt = 0;
-  for (int64_t w = w0; w < w1; ++w) cnt += __popc(__ldcg(bits + w));
+  for (int64_t w = w0; w < w1; w += kRun) {
+    uint32_t m[kRun];
+#pragma unroll
+    for (int u = 0; u < kRun; ++u) m[u] = w + u < w1 ? __ldcg(bits + w + u) : 0u;
+#pragma unroll
+    for (int u = 0; u < kRun; ++u) cnt += __popc(m[u]);
+  }
   int total;
   int pos = block_exclusive_scan(cnt, sbuf, &total);
   if (total != k) {
@@ -251,12 +261,17 @@ __device__ void finish_request(const C& cand, uint32_t c, int t1, int need1, uin
     for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
     return;
   }
-  for (int64_t w = w0; w < w1; ++w) {
-    uint32_t m = __ldcg(bits + w);
-    while (m) {
-      const int bit = __ffs(m) - 1;
-      m &= m - 1;
-      out[pos++] = static_cast<int32_t>(w * 32 + bit);
+  for (int64_t w = w0; w < w1; w += kRun) {
+    uint32_t m[kRun];
+#pragma unroll
+    for (int u = 0; u < kRun; ++u) m[u] = w + u < w1 ? __ldcg(bits + w + u) : 0u;
+#pragma unroll
+    for (int u = 0; u < kRun; ++u) {
+      while (m[u]) {
+        const int bit = __ffs(m[u]) - 1;
+        m[u] &= m[u] - 1;
+        out[pos++] = static_cast<int32_t>((w + u) * 32 + bit);
+      }
     }
   }
 }
@@ -459,9 +474,9 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
   const int b = blockIdx.y;
   const int n = ctx_len[b];
   if (!ctx_ok(n, k, max_ctx)) return;
-  const int64_t start = int64_t(blockIdx.x) * kChunk;
+  const int64_t start = int64_t(blockIdx.x) * kHistChunk;
   if (start >= n) return;
-  const int64_t end = min(start + int64_t(kChunk), int64_t(n));
+  const int64_t end = min(start + int64_t(kHistChunk), int64_t(n));
   for (int i = threadIdx.x; i < kHistCopies * kBins; i += kThreads) hcopies[i] = 0;
   __syncthreads();
   const float* row = scores + int64_t(b) * ctx_stride;
@@ -616,8 +631,10 @@ ts_status launch_topk(const float* scores, int64_t ctx_stride, const int32_t* ct
   if (!raise_smem_limit(reinterpret_cast<const void*>(topk_hist_kernel), kHistCopies * kBins * 4,
                         hist_smem_set))
     return TS_ERR_CUDA;
-  topk_hist_kernel<<<grid, kThreads, kHistCopies * kBins * 4, stream>>>(scores, ctx_stride,
-                                                                        ctx_len, k, max_ctx, w, err);
+  const dim3 hgrid((max_ctx + kHistChunk - 1) / kHistChunk, B);
+  topk_hist_kernel<<<hgrid, kThreads, kHistCopies * kBins * 4, stream>>>(scores, ctx_stride,
+                                                                         ctx_len, k, max_ctx, w,
+                                                                         err);
   topk_select_kernel<<<grid, kThreads, 0, stream>>>(scores, ctx_stride, ctx_len, k, max_ctx, w,
                                                     ids, err);
   return launch_status();
