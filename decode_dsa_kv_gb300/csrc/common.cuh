@@ -225,19 +225,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Four rows of a 2-D tensor map (box: `col`.. one row high) -> shared memory,
-// the rows one after the other at `dst` (the map's swizzle applied), completion
-// counted on `bar`.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int col, int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(smem_addr(bar))
-      : "memory");
-}
-
 // Untiled bulk copies (both addresses 16-byte aligned, size a multiple of 16).
 // global -> shared, completion counted on `bar`:
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,

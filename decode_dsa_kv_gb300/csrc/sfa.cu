@@ -55,6 +55,10 @@ constexpr int kScoreLoads = 2 * kKB;                 // 18 score stages
 constexpr int kLoads = kScoreLoads + 16;             // + 16 value stages (8 row blocks x 2 halves)
 constexpr int kSoftmaxThreads = 256;                 // warps 2..9
 constexpr int kThreads = 64 + kSoftmaxThreads;
+// The pool variant loads its tiles with 16-byte cp.async copies from four
+// loader warps (warp 0 and warps 10..12): 128 threads.
+constexpr int kLoaderThreads = 128;
+constexpr int kPoolThreads = kThreads + 96;
 constexpr uint32_t kBarBytes = 704;
 // barriers first, then the 1024-byte aligned tiles (worst-case padding
 // included). The total leaves room on the SM for a 0-byte CTA of another
@@ -250,8 +254,29 @@ struct PoolSrc {
   const int32_t* miss_pos;
   const int32_t* miss_count;
   const int32_t* miss_rows;
+  const uint8_t* rows;  // the pool tensor, [B][prow][576] bf16
+  const uint8_t* q;     // the queries, [B][H][576] bf16
   int P, prow;
 };
+
+// 16-byte copies global -> shared that write shared memory as they land
+// (cp.async, cached in L2 only), committed and waited for in groups.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Barrier among the pool variant's four loader warps (named barrier 2).
+__device__ __forceinline__ void loader_sync() {
+  asm volatile("bar.sync 2, 128;" ::: "memory");
+}
 
 // Row of request b's part of the pool tensor that position j reads: a hit's
 // slot, a miss's staged row (its first position's, when the request repeats
@@ -280,13 +305,15 @@ __device__ __forceinline__ int pool_row(const PoolSrc& ps, int b, int k, int j, 
 // (request, head tile) form one thread-block cluster and merge their O
 // through distributed shared memory; CTA r of the cluster writes dims
 // [r * 512 / C, (r + 1) * 512 / C) of the bf16 output (C = 1, 2 or 4).
-// kPool = false: the rows are the selection buffer's, loaded as tiles (tm_k,
-// tm_v: 3-D maps over [B][k][576]). kPool = true: the rows are read straight
-// from a staged-layout pool by the plan (`ps`), four rows per TMA gather
-// (tm_k = tm_v: a 2-D map over all B * prow pool rows, one row high), issued
-// by the 32 lanes of the producer warp.
+// kPool = false: the rows are the selection buffer's, loaded as TMA tiles
+// (tm_q, tm_k, tm_v). kPool = true: the rows are read straight from a
+// staged-layout pool by the plan (`ps`), by four loader warps with 16-byte
+// cp.async copies (the maps are unused). Measured on GB300: TMA 4-row gathers
+// (one instruction per 4 rows x 64 dims) kept the attention at 117 us a layer
+// at the decode_batch shape against 46 us for tile loads; the TMA unit's
+// instruction rate, not the memory, bounded it.
 template <bool kMerge, bool kPool>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
     sfa_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, int H, int k, int HG, int C,
                      float scale_log2, float* __restrict__ opart, float2* __restrict__ ml,
@@ -310,11 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSSlots; ++s) {
-      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->full[s], kPool ? kLoaderThreads : 1);
       mbar_init(&bars->empty[s], 1);
     }
     for (int s = 0; s < kVSlots; ++s) {
-      mbar_init(&bars->vfull[s], 1);
+      mbar_init(&bars->vfull[s], kPool ? kLoaderThreads : 1);
       mbar_init(&bars->vempty[s], 1);
     }
     mbar_init(&bars->s_half, 1);
@@ -328,9 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_fence_init();
     // the first score loads go out now, while the CTA still sets itself up
     // (the barriers are initialised; nobody reads the slots before waiting)
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
+    if (!kPool) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
     for (int it = 0; !kPool && it < kSSlots && it < kScoreLoads; ++it) {
       uint8_t* st = score_slot(it);
       const int kb = it % kKB, nh = it / kKB;
@@ -349,24 +378,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
-  if (warp == 0 && kPool) {
-    // ---------------- TMA producer, rows gathered from the pool ----------------
-    // The chunk's 512 pool rows first (16 per lane, into shared memory); then
-    // per stage lane 0 waits for the slot and loads the Q tile, and every
-    // lane issues two 4-row gathers: score stages take rows 4*lane.. and
-    // 128 + 4*lane.. of the 256-row half, value stages rows 4*(lane & 15).. of
-    // the 64-row block for dim boxes (lane >> 4) and (lane >> 4) + 2.
-    // Positions past k read row k-1 (their weights are zero).
+  if (kPool && (warp == 0 || warp >= 10)) {
+    // ---------------- loaders: rows straight from the pool ----------------
+    // The chunk's 512 pool rows first (relative to the request, into shared
+    // memory); then per stage every loader thread copies its 16-byte pieces
+    // into the tile's 128-byte-swizzled layout (a piece c of a stage is row
+    // c >> 3, 16-byte column c & 7; 8 consecutive threads read one 128-byte
+    // run). A stage is signalled two stages later: after cp.async.wait_group
+    // the thread makes its copies visible to the tensor cores' async proxy
+    // and arrives on the stage's barrier (count: all 128 loaders). Positions
+    // past k read row k-1 (their weights are zero); heads past H read head
+    // H-1 (their outputs are not stored).
+    const int lt = warp == 0 ? lane : (warp - 9) * 32 + lane;  // 0..127
     const int M = min(max(__ldg(ps.miss_count + b), 0), k);
     const bool repeats = __ldg(ps.miss_rows + b) != __ldg(ps.miss_count + b);
     const int j0 = c * kChunk;
-    const int rbase = b * ps.prow;  // B * prow < 2^31 (host check)
     int bad = 0;
-#pragma unroll 4
-    for (int p = lane; p < kChunk; p += 32)
+    for (int p = lt; p < kChunk; p += kLoaderThreads)
       ridx[p] = static_cast<uint16_t>(pool_row(ps, b, k, min(j0 + p, k - 1), M, repeats, bad));
-    __syncwarp();
-    auto row = [&](int p) { return rbase + static_cast<int>(ridx[p]); };
+    loader_sync();
+    const uint8_t* prow0 = ps.rows + int64_t(b) * ps.prow * DSA_ROW_BYTES;
+    auto row_src = [&](int p) { return prow0 + int64_t(ridx[p]) * DSA_ROW_BYTES; };
+    uint64_t* lag0 = nullptr;  // the last stage issued, not yet signalled
+    uint64_t* lag1 = nullptr;  // the one before it
+    auto issued_stage = [&](uint64_t* bar) {
+      cp_async_commit();
+      if (lag1) {
+        cp_async_wait<2>();
+        fence_proxy_async_smem();
+        mbar_arrive(lag1);
+      }
+      lag1 = lag0;
+      lag0 = bar;
+    };
+    auto signal_all = [&]() {
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      if (lag1) mbar_arrive(lag1);
+      if (lag0) mbar_arrive(lag0);
+      lag0 = lag1 = nullptr;
+    };
     bool ok = true;
     for (int it = 0; it < kScoreLoads && ok; ++it) {
       const int s = it % kSSlots;
@@ -374,40 +425,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const int kb = it % kKB, nh = it / kKB;
       uint8_t* st = score_slot(s);
-      if (lane == 0) {
-        mbar_expect_tx(&bars->full[s], kStageBytes);
-        tma_load_3d(st, &tm_q, &bars->full[s], kb * 64, hg * kHeads, b);
+#pragma unroll
+      for (int i = 0; i < kHeads * 8 / kLoaderThreads; ++i) {
+        const int pc = lt + kLoaderThreads * i, h = pc >> 3, col = pc & 7;
+        const int hh = min(hg * kHeads + h, H - 1);
+        cp_async16(st + h * 128 + ((col ^ (h & 7)) << 4),
+                   ps.q + (int64_t(b) * H + hh) * DSA_ROW_BYTES + kb * 128 + col * 16);
       }
-      __syncwarp();
-      uint8_t* kt = st + kQBytes;
-      const int p0 = nh * kHalfRows + 4 * lane, p1 = p0 + 128;
-      tma_gather4(kt + lane * 512, &tm_k, &bars->full[s], kb * 64, row(p0), row(p0 + 1),
-                  row(p0 + 2), row(p0 + 3));
-      tma_gather4(kt + (lane + 32) * 512, &tm_k, &bars->full[s], kb * 64, row(p1), row(p1 + 1),
-                  row(p1 + 2), row(p1 + 3));
-      if (lane == 0) bars->issued = it + 1;
+#pragma unroll
+      for (int i = 0; i < kHalfRows * 8 / kLoaderThreads; ++i) {
+        const int pc = lt + kLoaderThreads * i, r = pc >> 3, col = pc & 7;
+        cp_async16(st + kQBytes + r * 128 + ((col ^ (r & 7)) << 4),
+                   row_src(nh * kHalfRows + r) + kb * 128 + col * 16);
+      }
+      issued_stage(&bars->full[s]);
     }
-    // value phase, once the scores are done (their slots are free then)
+    signal_all();
+    // value phase, once the scores are done (their slots are free then):
+    // piece c of a stage is row c >> 5 of the 64-row block, dim box
+    // (c >> 3) & 3, 16-byte column c & 7
     if (ok) ok = warp_wait(&bars->s_full, 0, abort, wait_ns);
     for (int v = 0; v < kLoads - kScoreLoads && ok; ++v) {
       const int s = v % kVSlots;
       if (v >= kVSlots) ok = warp_wait(&bars->vempty[s], ((v / kVSlots) - 1) & 1, abort, wait_ns);
       if (!ok) break;
       const int half = v >> 3, rb = v & 7;
-      const int g = lane & 15, jb = lane >> 4;
-      const int p = rb * 64 + 4 * g;
       uint8_t* st = stages + s * kVBytes;
-      if (lane == 0) mbar_expect_tx(&bars->vfull[s], kVBytes);
-      __syncwarp();
-      tma_gather4(st + jb * kVBox + g * 512, &tm_v, &bars->vfull[s], half * 256 + jb * 64, row(p),
-                  row(p + 1), row(p + 2), row(p + 3));
-      tma_gather4(st + (jb + 2) * kVBox + g * 512, &tm_v, &bars->vfull[s],
-                  half * 256 + (jb + 2) * 64, row(p), row(p + 1), row(p + 2), row(p + 3));
-      if (lane == 0) bars->issued = kScoreLoads + v + 1;
+#pragma unroll
+      for (int i = 0; i < 64 * 32 / kLoaderThreads; ++i) {
+        const int pc = lt + kLoaderThreads * i, r = pc >> 5, j = (pc >> 3) & 3, col = pc & 7;
+        cp_async16(st + j * kVBox + r * 128 + ((col ^ (r & 7)) << 4),
+                   row_src(rb * 64 + r) + (half * 256 + j * 64) * 2 + col * 16);
+      }
+      issued_stage(&bars->vfull[s]);
     }
-    bad = __reduce_or_sync(0xffffffffu, bad);
-    if (bad && lane == 0) report(err, bad);
-  } else if (warp == 0) {
+    signal_all();
+  } else if (!kPool && warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       // score phase: kSSlots slots; slots 2 and 3 borrow the P region, which
@@ -488,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) tc_commit(&bars->o_full);
     }
-  } else {
+  } else if (warp < 10) {
     // ---------------- softmax and epilogue: two threads per head ----------------
     // Every softmax_sync below is reached by all 256 softmax threads whatever
     // happened before it (a wait that gave up only skips work).
@@ -602,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if constexpr (kMerge) {
     // the TMA and MMA warps take part in the merge's two cluster barriers
-    if (warp < 2) {
+    if (warp < 2 || warp >= 10) {
       __syncwarp();
       cluster_sync_all();
       cluster_sync_all();
@@ -614,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (bars->abort) {
     if (threadIdx.x == 0) report(err, TS_DEVERR_TIMEOUT);
-    if (warp == 0 && lane == 0) {
+    if (!kPool && warp == 0 && lane == 0) {
       // let the copies already issued land before the CTA exits: the last
       // load of every slot (earlier ones completed before their slot's reuse)
       const int issued = bars->issued;
@@ -724,20 +777,6 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t batch, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D map over `rows` rows of 576 bf16, box 64 values x 1 row (the form the
-// 4-row gathers take).
-bool make_rows_map(CUtensorMap* map, const void* ptr, uint64_t rows) {
-  EncodeTiled enc = encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {DSA_D, rows};
-  const cuuint64_t strides[1] = {DSA_ROW_BYTES};
-  const cuuint32_t box[2] = {64, 1};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // The chunks of a (request, head tile) merge inside one cluster when they are
 // 1, 2 or 4 (C = ceil(k / 512)); otherwise through the workspace and a second
 // kernel.
@@ -749,20 +788,19 @@ bool sfa_merges_in_cluster(int k) {
 // The attention's launches, from a selection buffer (sel_l, ps unused) or
 // straight from a staged-layout pool (kPool: pool_l with ps).
 template <bool kPool>
-ts_status launch_attention(const void* q, const void* rows, uint64_t total_rows, const PoolSrc& ps,
+ts_status launch_attention(const void* q, const void* rows, const PoolSrc& ps,
                            int B, int H, int k, float scale, void* out, float* lse, void* ws,
                            int32_t* err, cudaStream_t stream) {
   const int HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
-  CUtensorMap tm_q, tm_k, tm_v;
-  if (!make_map(&tm_q, q, H, B, kHeads)) return TS_ERR_CUDA;
-  if (kPool) {
-    if (!make_rows_map(&tm_k, rows, total_rows)) return TS_ERR_CUDA;
-    tm_v = tm_k;
-  } else if (!make_map(&tm_k, rows, k, B, kHalfRows) || !make_map(&tm_v, rows, k, B, 64)) {
+  // the tile variant loads through tensor maps; the pool variant's loader
+  // warps copy with plain addresses (its maps stay unused)
+  CUtensorMap tm_q = {}, tm_k = {}, tm_v = {};
+  if (!kPool && (!make_map(&tm_q, q, H, B, kHeads) || !make_map(&tm_k, rows, k, B, kHalfRows) ||
+                 !make_map(&tm_v, rows, k, B, 64)))
     return TS_ERR_CUDA;
-  }
   const uint64_t wait_ns = wait_limit_ns(kWaitLimit);
   const uint32_t smem = kPool ? kPoolSmemBytes : kSmemBytes;
+  const int threads = kPool ? kPoolThreads : kThreads;
   if (sfa_merges_in_cluster(k)) {
     static std::atomic<uint64_t> smem_set{0};
     if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<true, kPool>),
@@ -770,7 +808,7 @@ ts_status launch_attention(const void* q, const void* rows, uint64_t total_rows,
       return TS_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C, HG, B);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
@@ -797,7 +835,7 @@ ts_status launch_attention(const void* q, const void* rows, uint64_t total_rows,
   if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<false, kPool>),
                         static_cast<int>(smem), smem_set))
     return TS_ERR_CUDA;
-  sfa_chunk_kernel<false, kPool><<<dim3(C, HG, B), kThreads, smem, stream>>>(
+  sfa_chunk_kernel<false, kPool><<<dim3(C, HG, B), threads, smem, stream>>>(
       tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, nullptr, nullptr, wait_ns, ps,
       err);
   if (launch_status() != TS_OK) return TS_ERR_CUDA;
@@ -833,8 +871,7 @@ ts_status sfa_check(const void* q, const void* sel_l, int B, int H, int k, float
 
 ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, float scale,
                       void* out, float* lse, void* ws, int32_t* err, cudaStream_t stream) {
-  return launch_attention<false>(q, sel_l, 0, PoolSrc{}, B, H, k, scale, out, lse, ws, err,
-                                 stream);
+  return launch_attention<false>(q, sel_l, PoolSrc{}, B, H, k, scale, out, lse, ws, err, stream);
 }
 
 ts_status sfa_pool_check(const void* q, const void* pool_l, int P, const int32_t* src_map,
@@ -855,9 +892,9 @@ ts_status sfa_pool_enqueue(const void* q, const void* pool_l, int P, const int32
                            const int32_t* miss_count, const int32_t* miss_rows, int B, int H,
                            int k, float scale, void* out, float* lse, void* ws, int32_t* err,
                            cudaStream_t stream) {
-  const PoolSrc ps{src_map, miss_ids, miss_pos, miss_count, miss_rows, P, P + k};
-  return launch_attention<true>(q, pool_l, uint64_t(B) * uint64_t(P + k), ps, B, H, k, scale, out,
-                                lse, ws, err, stream);
+  const PoolSrc ps{src_map, miss_ids, miss_pos, miss_count, miss_rows,
+                   static_cast<const uint8_t*>(pool_l), static_cast<const uint8_t*>(q), P, P + k};
+  return launch_attention<true>(q, pool_l, ps, B, H, k, scale, out, lse, ws, err, stream);
 }
 
 }  // namespace dsakv

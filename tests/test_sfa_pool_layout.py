@@ -1,9 +1,10 @@
 """Index arithmetic of the attention variant that reads its rows straight from
-the pool (csrc/sfa.cu, the kPool producer), restated on the CPU: over every
-score and value stage, the 4-row gathers of the 32 producer lanes land inside
-their stage's tile, cover every 128-byte row block of it exactly once, and put
-selection position p at tile row p (so the tile equals the one a plain tile
-load of the selection gives); and the pool row each position reads stays inside
+the pool (csrc/sfa.cu, the kPool loader warps), restated on the CPU: over every
+score and value stage, the 16-byte copies of the 128 loader threads land inside
+their stage's tile, cover it exactly once, and put 16-byte column c of
+selection row p where a 128-byte-swizzled tile load of the selection would
+(row p at p * 128, column c at (c ^ (p & 7)) * 16); every source piece lies
+inside its 1152-byte row; and the pool row each position reads stays inside
 the pool tensor, for hits, misses and bad entries alike."""
 import numpy as np
 
@@ -12,38 +13,56 @@ kQBytes = kHeads * 128
 kKBytes = kHalf * 128
 kVBox = 64 * 128
 kVBytes = 4 * kVBox
+kLoaders = 128
 INT_MIN = -(1 << 31)
 
 
-def test_score_and_value_gathers_cover_their_tiles_once():
+def _swz(row, col):
+    return row * 128 + ((col ^ (row & 7)) << 4)
+
+
+def test_score_stage_copies_cover_q_and_k_tiles_once():
     for nh in range(2):
-        seen = {}
-        for lane in range(32):
-            for g, first in ((lane, nh * kHalf + 4 * lane), (lane + 32, nh * kHalf + 128 + 4 * lane)):
-                dst = g * 512
-                assert 0 <= dst and dst + 512 <= kKBytes
-                for i in range(4):
-                    row_block = (dst + i * 128) // 128
-                    assert row_block not in seen
-                    seen[row_block] = first + i
-        # tile row r (128-byte block r of the K area) holds position nh*256 + r
-        assert seen == {r: nh * kHalf + r for r in range(kHalf)}
-    for rb in range(8):
-        for half in range(2):
+        for kb in range(kKB):
+            q_seen, k_seen = {}, {}
+            for lt in range(kLoaders):
+                for i in range(kHeads * 8 // kLoaders):
+                    pc = lt + kLoaders * i
+                    h, col = pc >> 3, pc & 7
+                    dst = _swz(h, col)
+                    assert 0 <= dst and dst + 16 <= kQBytes and dst not in q_seen
+                    src = kb * 128 + col * 16        # inside the head's row
+                    assert 0 <= src and src + 16 <= 1152
+                    q_seen[dst] = (h, kb * 64 + col * 8)
+                for i in range(kHalf * 8 // kLoaders):
+                    pc = lt + kLoaders * i
+                    r, col = pc >> 3, pc & 7
+                    dst = kQBytes + _swz(r, col)
+                    assert kQBytes <= dst and dst + 16 <= kQBytes + kKBytes and dst not in k_seen
+                    src = kb * 128 + col * 16
+                    assert 0 <= src and src + 16 <= 1152
+                    k_seen[dst] = (nh * kHalf + r, kb * 64 + col * 8)
+            assert len(q_seen) == kQBytes // 16 and len(k_seen) == kKBytes // 16
+            # what a swizzled tile load puts there: position / dims per 16 bytes
+            assert k_seen == {kQBytes + _swz(r, c): (nh * kHalf + r, kb * 64 + c * 8)
+                              for r in range(kHalf) for c in range(8)}
+
+
+def test_value_stage_copies_cover_the_tile_once():
+    for half in range(2):
+        for rb in range(8):
             seen = {}
-            for lane in range(32):
-                g, jb = lane & 15, lane >> 4
-                for box in (jb, jb + 2):
-                    dst = box * kVBox + g * 512
-                    assert 0 <= dst and dst + 512 <= kVBytes
-                    col = half * 256 + box * 64
-                    assert 0 <= col and col + 64 <= 512
-                    for i in range(4):
-                        key = (box, (g * 512 + i * 128) // 128)
-                        assert key not in seen
-                        seen[key] = (rb * 64 + 4 * g + i, col)
-            assert seen == {(box, r): (rb * 64 + r, half * 256 + box * 64)
-                            for box in range(4) for r in range(64)}
+            for lt in range(kLoaders):
+                for i in range(64 * 32 // kLoaders):
+                    pc = lt + kLoaders * i
+                    r, j, col = pc >> 5, (pc >> 3) & 3, pc & 7
+                    dst = j * kVBox + _swz(r, col)
+                    assert 0 <= dst and dst + 16 <= kVBytes and dst not in seen
+                    src = (half * 256 + j * 64) * 2 + col * 16
+                    assert 0 <= src and src + 16 <= 1024      # inside the 512 value dims
+                    seen[dst] = (rb * 64 + r, half * 256 + j * 64 + col * 8)
+            assert seen == {j * kVBox + _swz(r, c): (rb * 64 + r, half * 256 + j * 64 + c * 8)
+                            for j in range(4) for r in range(64) for c in range(8)}
 
 
 def _pool_row(src_map, miss_ids, miss_pos, M, repeats, b, k, j, P, prow):
