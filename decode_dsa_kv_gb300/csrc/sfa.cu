@@ -20,14 +20,14 @@
 //   O[:, 0:256]   = P V[:, 0:256]    -> TMEM columns 256..511
 //   O[:, 256:512] = P V[:, 256:512]  -> TMEM columns 0..255 (S is dead by then:
 //       P holds it, bf16, in shared memory)
-// Merging the chunks of a (request, head tile): out = sum_c w_c O_c /
-// sum_c w_c l_c with w_c = exp2(m_c - max_c m_c).
-//   k <= 512, <= 1024 or in (1536, 2048] (1, 2 or 4 chunks): the chunk CTAs
-//       form one thread-block cluster and merge through distributed shared
-//       memory (merge_in_cluster); one launch, no workspace traffic.
-//   otherwise: O (unnormalised) -> fp32 workspace straight from TMEM, as a
-//       dim-major tile [512][128 heads] (coalesced stores), the row max and
-//       the row sum beside it, and a second kernel merges the chunks.
+//   O (unnormalised) -> fp32 workspace straight from TMEM, as a dim-major
+//       tile [512][128 heads] (coalesced stores); the row max and the row sum
+//       beside it.
+// A second kernel merges the chunks of a request: out = sum_c w_c O_c /
+// sum_c w_c l_c with w_c = exp2(m_c - max_c m_c). (Merging inside a cluster
+// of the chunk CTAs through distributed shared memory instead measured
+// slower on GB300: 45 vs 37 us a layer at the decode_batch shape alone, and
+// slower in the step; the cluster waits for its slowest chunk.)
 #include <climits>
 #include <cmath>
 
@@ -119,131 +119,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// ---- merge of a cluster's chunks through distributed shared memory ----
-// The output row (512 dims) is cut into 16 units of 32 dims; CTA r of a
-// cluster of C owns units [r * 16 / C, (r + 1) * 16 / C). Every other CTA
-// sends its weighted O of those units into one of the owner's C - 1 receive
-// slots (the tile region, free once the value product is done); a slot is
-// [unit][head][32 fp32], the 16-byte pieces of a head's 128 bytes rotated by
-// head & 7 so that 8 consecutive heads hit different banks.
-constexpr int kUnits = DSA_DV / 32;
-constexpr uint32_t kUnitBytes = kHeads * 128;  // one unit of every head
-constexpr uint32_t kMlOffset = kTileBytes - kHeads * sizeof(float2);  // published (m, l)
-static_assert(3 * (kUnits / 4) * kUnitBytes <= kMlOffset, "slots of a 4-CTA cluster");
-static_assert(1 * (kUnits / 2) * kUnitBytes <= kMlOffset, "slot of a 2-CTA cluster");
-
-// TMEM column of dims [32u, 32u + 32): dims 0..255 sit in columns 256..511.
-__device__ __forceinline__ uint32_t o_col(int u) {
-  return u < kUnits / 2 ? 256u + 32u * static_cast<uint32_t>(u)
-                        : 32u * static_cast<uint32_t>(u - kUnits / 2);
-}
-
-__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr)
-               : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
-
-// Softmax warps, after the row max m and (part 0) the row sum l of this
-// chunk are known: out = sum_c w_c O_c / sum_c w_c l_c, w_c = 2^(m_c - max m).
-// Two threads per head; `part` takes the units of its parity. Every thread
-// passes both cluster barriers whatever happened before (a failed wait only
-// skips work), so no CTA of the cluster waits for ever.
-__device__ __forceinline__ void merge_in_cluster(Bars* bars, uint8_t* base, uint32_t trow, int row,
-                                                 int part, float m, float l, bool ok,
-                                                 volatile int* abort, uint64_t wait_ns, int H,
-                                                 int C, int hg, int b,
-                                                 __nv_bfloat16* __restrict__ out,
-                                                 float* __restrict__ lse) {
-  const int rank = static_cast<int>(cluster_ctarank());
-  const int upo = kUnits / C;  // units each CTA owns
-  const int rows_valid = min(kHeads, H - hg * kHeads);
-  const bool live = ok && warp_wait(&bars->o_full, 0, abort, wait_ns) && !*abort;
-  float2* ml_pub = reinterpret_cast<float2*>(base + kMlOffset);
-  if (part == 0) ml_pub[row] = live ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
-  tc_fence_before();
-  cluster_sync_all();  // 1: every CTA's value product is done (tiles free), (m, l) published
-  tc_fence_after();
-  float M = -INFINITY, L = 0.f;
-  float2 e[4];
-#pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    e[cc] = cc < C ? ld_dsmem_f2(dsmem_addr(ml_pub + row, cc)) : make_float2(-INFINITY, 0.f);
-    M = fmaxf(M, e[cc].x);
-  }
-#pragma unroll
-  for (int cc = 0; cc < 4; ++cc)
-    if (cc < C) L += exp2f(e[cc].x - M) * e[cc].y;
-  const float w = live ? exp2f(m - M) : 0.f;
-  if (live) {
-    for (int u = part; u < kUnits; u += 2) {
-      const int o = u / upo;
-      if (o == rank) continue;
-      uint32_t r[32];
-      tmem_ld32(trow + o_col(u), r);
-      tmem_wait_ld();
-      if (row < rows_valid) {
-        const int slot = (rank - o - 1 + C) % C;
-        const uint32_t dst = dsmem_addr(
-            base + slot * upo * kUnitBytes + ((u % upo) * kHeads + row) * 128, o);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          st_dsmem_f4(dst + ((j ^ (row & 7)) << 4), w * __uint_as_float(r[4 * j]),
-                      w * __uint_as_float(r[4 * j + 1]), w * __uint_as_float(r[4 * j + 2]),
-                      w * __uint_as_float(r[4 * j + 3]));
-      }
-    }
-  }
-  cluster_sync_all();  // 2: every contribution has landed; no remote access after this
-  if (live) {
-    const float inv = 1.f / L;
-    for (int u = part; u < kUnits; u += 2) {
-      if (u / upo != rank) continue;
-      uint32_t r[32];
-      tmem_ld32(trow + o_col(u), r);
-      tmem_wait_ld();
-      if (row < rows_valid) {
-        float acc[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = w * __uint_as_float(r[i]);
-        for (int sl = 0; sl < C - 1; ++sl) {
-          const uint8_t* src = base + sl * upo * kUnitBytes + ((u % upo) * kHeads + row) * 128;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 v = *reinterpret_cast<const float4*>(src + ((j ^ (row & 7)) << 4));
-            acc[4 * j] += v.x;
-            acc[4 * j + 1] += v.y;
-            acc[4 * j + 2] += v.z;
-            acc[4 * j + 3] += v.w;
-          }
-        }
-        uint4* dst = reinterpret_cast<uint4*>(out + (size_t(b) * H + hg * kHeads + row) * DSA_DV +
-                                              32 * u);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t p[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 h2 =
-                __floats2bfloat162_rn(acc[8 * j + 2 * i] * inv, acc[8 * j + 2 * i + 1] * inv);
-            p[i] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          dst[j] = make_uint4(p[0], p[1], p[2], p[3]);
-        }
-      }
-    }
-    if (rank == 0 && part == 0 && row < rows_valid && lse)
-      lse[size_t(b) * H + hg * kHeads + row] = M * kLn2 + logf(L);
-  }
-}
-
 // Where the variant that reads straight from the pool finds a selected row:
 // the plan's source map over a staged-layout pool tensor, `prow` = P + k rows
 // per request (the P slots, then the step's missed rows staged at P + their
@@ -300,25 +175,20 @@ __device__ __forceinline__ int pool_row(const PoolSrc& ps, int b, int k, int j, 
   return rel;
 }
 
-// kMerge = false: O, the row max and the row sum of the chunk go to the
-// workspace for sfa_combine_kernel. kMerge = true: the C chunk CTAs of a
-// (request, head tile) form one thread-block cluster and merge their O
-// through distributed shared memory; CTA r of the cluster writes dims
-// [r * 512 / C, (r + 1) * 512 / C) of the bf16 output (C = 1, 2 or 4).
-// kPool = false: the rows are the selection buffer's, loaded as TMA tiles
+// O, the row max and the row sum of the chunk go to the workspace for
+// sfa_combine_kernel. kPool = false: the rows are the selection buffer's, loaded as TMA tiles
 // (tm_q, tm_k, tm_v). kPool = true: the rows are read straight from a
 // staged-layout pool by the plan (`ps`), by four loader warps with 16-byte
 // cp.async copies (the maps are unused). Measured on GB300: TMA 4-row gathers
 // (one instruction per 4 rows x 64 dims) kept the attention at 117 us a layer
 // at the decode_batch shape against 46 us for tile loads; the TMA unit's
 // instruction rate, not the memory, bounded it.
-template <bool kMerge, bool kPool>
+template <bool kPool>
 __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
     sfa_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, int H, int k, int HG, int C,
                      float scale_log2, float* __restrict__ opart, float2* __restrict__ ml,
-                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint64_t wait_ns,
-                     const PoolSrc ps, int32_t* err) {
+                     uint64_t wait_ns, const PoolSrc ps, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Bars* bars = reinterpret_cast<Bars*>(smem_raw);
   uint16_t* ridx = reinterpret_cast<uint16_t*>(smem_raw + kBarBytes);  // kPool only
@@ -396,6 +266,8 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
     int bad = 0;
     for (int p = lt; p < kChunk; p += kLoaderThreads)
       ridx[p] = static_cast<uint16_t>(pool_row(ps, b, k, min(j0 + p, k - 1), M, repeats, bad));
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    if (bad && lane == 0) report(err, bad);
     loader_sync();
     const uint8_t* prow0 = ps.rows + int64_t(b) * ps.prow * DSA_ROW_BYTES;
     auto row_src = [&](int p) { return prow0 + int64_t(ridx[p]) * DSA_ROW_BYTES; };
@@ -618,48 +490,35 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
     if (ok && part == 1) bars->red[row] = l;
     softmax_sync();
     if (ok && part == 0) l += bars->red[row];  // the row sum (only part 0 holds it)
-    if constexpr (!kMerge) {
-      if (ok) ok = warp_wait(&bars->o_half, 0, abort, wait_ns);
-      // Epilogue: O straight from TMEM to the workspace, in the chunk's
-      // dim-major tile [512 dims][128 heads]: a warp's 32 lanes are 32
-      // consecutive heads, so every store is a coalesced 128-byte run. Dims
-      // 0..255 (TMEM columns 256..511) go out while the tensor core still
-      // computes dims 256..511 (columns 0..255).
-      const size_t slot0 = ((size_t(b) * HG + hg) * C + c) * kHeads;
-      const int rows_valid = min(kHeads, H - hg * kHeads);
-      float* tile = opart + slot0 * DSA_DV;
-      bool live = ok && !*abort;
-      for (int half = 0; half < 2 && live; ++half) {
-        if (half == 1) {
-          live = warp_wait(&bars->o_full, 0, abort, wait_ns) && !*abort;
-          if (!live) break;
-        }
-        tc_fence_after();
-        uint32_t r[32];
-        for (int qq = 0; qq < 4; ++qq) {
-          const int d = 128 * part + 32 * qq;  // dim within this half
-          tmem_ld32(trow + (half == 0 ? 256u + d : uint32_t(d)), r);
-          tmem_wait_ld();
-          if (row < rows_valid) {
-            float* dst = tile + size_t(256 * half + d) * kHeads + row;
+    if (ok) ok = warp_wait(&bars->o_half, 0, abort, wait_ns);
+    // Epilogue: O straight from TMEM to the workspace, in the chunk's
+    // dim-major tile [512 dims][128 heads]: a warp's 32 lanes are 32
+    // consecutive heads, so every store is a coalesced 128-byte run. Dims
+    // 0..255 (TMEM columns 256..511) go out while the tensor core still
+    // computes dims 256..511 (columns 0..255).
+    const size_t slot0 = ((size_t(b) * HG + hg) * C + c) * kHeads;
+    const int rows_valid = min(kHeads, H - hg * kHeads);
+    float* tile = opart + slot0 * DSA_DV;
+    bool live = ok && !*abort;
+    for (int half = 0; half < 2 && live; ++half) {
+      if (half == 1) {
+        live = warp_wait(&bars->o_full, 0, abort, wait_ns) && !*abort;
+        if (!live) break;
+      }
+      tc_fence_after();
+      uint32_t r[32];
+      for (int qq = 0; qq < 4; ++qq) {
+        const int d = 128 * part + 32 * qq;  // dim within this half
+        tmem_ld32(trow + (half == 0 ? 256u + d : uint32_t(d)), r);
+        tmem_wait_ld();
+        if (row < rows_valid) {
+          float* dst = tile + size_t(256 * half + d) * kHeads + row;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) dst[i * kHeads] = __uint_as_float(r[i]);
-          }
+          for (int i = 0; i < 32; ++i) dst[i * kHeads] = __uint_as_float(r[i]);
         }
       }
-      if (live && part == 0 && row < rows_valid) ml[slot0 + row] = make_float2(m, l);
-    } else {
-      merge_in_cluster(bars, base, trow, row, part, m, l, ok, abort, wait_ns, H, C, hg, b, out,
-                       lse);
     }
-  }
-  if constexpr (kMerge) {
-    // the TMA and MMA warps take part in the merge's two cluster barriers
-    if (warp < 2 || warp >= 10) {
-      __syncwarp();
-      cluster_sync_all();
-      cluster_sync_all();
-    }
+    if (live && part == 0 && row < rows_valid) ml[slot0 + row] = make_float2(m, l);
   }
 
   // ---------------- teardown ----------------
@@ -777,20 +636,12 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t batch, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The chunks of a (request, head tile) merge inside one cluster when they are
-// 1, 2 or 4 (C = ceil(k / 512)); otherwise through the workspace and a second
-// kernel.
-bool sfa_merges_in_cluster(int k) {
-  const int C = (k + kChunk - 1) / kChunk;
-  return C == 1 || C == 2 || C == 4;
-}
-
-// The attention's launches, from a selection buffer (sel_l, ps unused) or
-// straight from a staged-layout pool (kPool: pool_l with ps).
+// The attention's two launches, from a selection buffer (sel_l; ps unused) or
+// straight from a staged-layout pool (kPool: ps): the chunks, then their merge.
 template <bool kPool>
-ts_status launch_attention(const void* q, const void* rows, const PoolSrc& ps,
-                           int B, int H, int k, float scale, void* out, float* lse, void* ws,
-                           int32_t* err, cudaStream_t stream) {
+ts_status launch_attention(const void* q, const void* rows, const PoolSrc& ps, int B, int H,
+                           int k, float scale, void* out, float* lse, void* ws, int32_t* err,
+                           cudaStream_t stream) {
   const int HG = (H + kHeads - 1) / kHeads, C = (k + kChunk - 1) / kChunk;
   // the tile variant loads through tensor maps; the pool variant's loader
   // warps copy with plain addresses (its maps stay unused)
@@ -798,45 +649,17 @@ ts_status launch_attention(const void* q, const void* rows, const PoolSrc& ps,
   if (!kPool && (!make_map(&tm_q, q, H, B, kHeads) || !make_map(&tm_k, rows, k, B, kHalfRows) ||
                  !make_map(&tm_v, rows, k, B, 64)))
     return TS_ERR_CUDA;
-  const uint64_t wait_ns = wait_limit_ns(kWaitLimit);
   const uint32_t smem = kPool ? kPoolSmemBytes : kSmemBytes;
   const int threads = kPool ? kPoolThreads : kThreads;
-  if (sfa_merges_in_cluster(k)) {
-    static std::atomic<uint64_t> smem_set{0};
-    if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<true, kPool>),
-                          static_cast<int>(smem), smem_set))
-      return TS_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(C, HG, B);
-    cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = C;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    float* no_part = nullptr;
-    float2* no_ml = nullptr;
-    if (cudaLaunchKernelEx(&cfg, sfa_chunk_kernel<true, kPool>, tm_q, tm_k, tm_v, H, k, HG, C,
-                           scale * kLog2e, no_part, no_ml, static_cast<__nv_bfloat16*>(out), lse,
-                           wait_ns, ps, err) != cudaSuccess) {
-      cudaGetLastError();
-      return TS_ERR_CUDA;
-    }
-    return TS_OK;
-  }
   const size_t slots = size_t(B) * HG * C * kHeads;
   float* opart = static_cast<float*>(ws);
   float2* ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + align256(slots * DSA_DV * 4));
   static std::atomic<uint64_t> smem_set{0};
-  if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<false, kPool>),
+  if (!raise_smem_limit(reinterpret_cast<const void*>(sfa_chunk_kernel<kPool>),
                         static_cast<int>(smem), smem_set))
     return TS_ERR_CUDA;
-  sfa_chunk_kernel<false, kPool><<<dim3(C, HG, B), threads, smem, stream>>>(
-      tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, nullptr, nullptr, wait_ns, ps,
+  sfa_chunk_kernel<kPool><<<dim3(C, HG, B), threads, smem, stream>>>(
+      tm_q, tm_k, tm_v, H, k, HG, C, scale * kLog2e, opart, ml, wait_limit_ns(kWaitLimit), ps,
       err);
   if (launch_status() != TS_OK) return TS_ERR_CUDA;
   sfa_combine_kernel<<<dim3(DSA_DV / kCombineDims, HG, B), kHeads, 0, stream>>>(

@@ -47,7 +47,7 @@ def _sfa(d, q, sel, B, H, k, scale):
     return out, d.ts_read_error(err)
 
 
-@pytest.mark.parametrize("k", [2048, 1279])   # chunks merged in a cluster; merged by a second kernel
+@pytest.mark.parametrize("k", [2048, 1279])   # 4 chunks; 3 chunks, the last one ragged
 def test_attention_wait_that_runs_out_reports_and_recovers(d, k):
     from decode_dsa_kv_gb300 import _abi
     B, H = 2, 128
