@@ -50,6 +50,9 @@ constexpr int kPipeWarps = 16;                     // warps per gather CTA
 constexpr uint64_t kBulkWaitNs = 100000000ull;     // 100 ms
 constexpr size_t kPipeWarpBytes = kPipeSlots * (DSA_ROW_BYTES + 24);  // ring, barriers, targets
 constexpr size_t kPipeSmemBytes = kPipeWarps * kPipeWarpBytes;
+// most requests whose miss-count prefix fits beside the pipes (dynamic hand-out)
+constexpr int kMaxDynamicB = 1024;
+static_assert(kPipeSmemBytes + (kMaxDynamicB + 1) * 4 + 40 * 4 <= 227 * 1024, "shared memory");
 
 struct RowPipe {
   uint8_t* ring;
@@ -65,9 +68,11 @@ struct RowPipe {
   uint32_t pend_end;
   int nw;
   uint32_t *count, *done, seq;
+  uint32_t* ticket;  // dynamic miss hand-out: reset by the last warp of the last layer
+  int last;
 
   __device__ void init(uint8_t* warp_smem, int nw_, uint32_t* count_, uint32_t* done_,
-                       uint32_t seq_) {
+                       uint32_t seq_, uint32_t* ticket_, int last_) {
     ring = warp_smem;
     bars = reinterpret_cast<uint64_t*>(warp_smem + kPipeSlots * DSA_ROW_BYTES);
     to = reinterpret_cast<uint4**>(bars + kPipeSlots);
@@ -80,6 +85,8 @@ struct RowPipe {
     count = count_;
     done = done_;
     seq = seq_;
+    ticket = ticket_;
+    last = last_;
     for (int s = 0; s < kPipeSlots; ++s) mbar_init(bars + s, 1);
     mbar_fence_init();
   }
@@ -92,6 +99,8 @@ struct RowPipe {
     if (atomicAdd(count + l, 1u) == static_cast<uint32_t>(nw) - 1) {
       __threadfence();
       count[l] = 0;
+      // every warp has taken its last ticket before counting out of the last layer
+      if (ticket && l == last) *ticket = 0;
       atomicExch(done + l, seq);
     }
   }
@@ -155,6 +164,50 @@ struct GatherLayer {
   uint4* sel;
 };
 
+// Source and targets of miss i of request b (the plan's miss list): the host
+// row, its place in the selection (or staging rows), and, for an install with
+// code 1, its victim slot. False (with bits in `bad`) for a corrupt entry.
+__device__ __forceinline__ bool miss_targets(const GatherLayer& L, const int32_t* miss_ids,
+                                             const int32_t* miss_pos, const int32_t* victim,
+                                             const uint8_t* install, int b, int i, int k, int P,
+                                             int sel_rows, int pool_rows, int64_t ctx_stride,
+                                             const int32_t* ctx_len, const uint4*& from,
+                                             uint4*& to, uint4*& to2, int& bad) {
+  const bool in = i >= 0 && i < k;  // (a count past k is corrupt)
+  const int64_t s = int64_t(b) * k + i;
+  const int t = in ? __ldg(miss_ids + s) : -1;
+  const int j = in ? __ldg(miss_pos + s) : -1;
+  if (t < 0 || t >= __ldg(ctx_len + b) || t >= ctx_stride || j < 0 || j >= k) {
+    bad |= TS_DEVERR_ID_RANGE;
+    return false;
+  }
+  from = L.host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
+  to = L.sel + (int64_t(b) * sel_rows + j) * DSA_ROW_CHUNKS;
+  to2 = nullptr;
+  if (victim && __ldg(install + s) == 1) {
+    const int v = __ldg(victim + s);
+    if (v >= 0 && v < P) to2 = L.pool + (int64_t(b) * pool_rows + v) * DSA_ROW_CHUNKS;
+    else bad |= TS_DEVERR_SLOT_RANGE;
+  }
+  return true;
+}
+
+// Lane 0 pushes the rows of the lanes in `mask` through the warp's pipe.
+__device__ __forceinline__ void push_lanes(uint32_t mask, const uint4* from, uint4* to, uint4* to2,
+                                           int lane, RowPipe& pipe) {
+  while (mask) {
+    const int q = __ffs(mask) - 1;
+    mask &= mask - 1;
+    const uint4* f = reinterpret_cast<const uint4*>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(from), q));
+    uint4* t = reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(to), q));
+    uint4* t2 =
+        reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(to2), q));
+    if (lane == 0) pipe.push(f, t, t2);
+    __syncwarp();
+  }
+}
+
 // The misses of all requests, concatenated: the warp takes miss indices
 // m = w, w + nrole, ... (request b holds miss_count[b] of them), so every miss
 // warp gets the same number of host rows whatever the spread of misses over
@@ -188,26 +241,9 @@ __device__ __forceinline__ void gather_misses(const GatherLayer& L, const int32_
         if (++b < B) cnt = __ldg(miss_count + b);
       }
       bool valid = false;
-      if (b < B) {
-        const int i = ml - base;
-        const bool in = i >= 0 && i < k;  // (a count past k is corrupt)
-        const int64_t s = int64_t(b) * k + i;
-        const int t = in ? __ldg(miss_ids + s) : -1;
-        const int j = in ? __ldg(miss_pos + s) : -1;
-        if (t < 0 || t >= __ldg(ctx_len + b) || t >= ctx_stride || j < 0 || j >= k) {
-          bad |= TS_DEVERR_ID_RANGE;
-        } else {
-          my_from = host + (int64_t(b) * ctx_stride + t) * DSA_ROW_CHUNKS;
-          my_to = sel + (int64_t(b) * sel_rows + j) * DSA_ROW_CHUNKS;
-          my_to2 = nullptr;
-          if (victim && __ldg(install + s) == 1) {
-            const int v = __ldg(victim + s);
-            if (v >= 0 && v < P) my_to2 = L.pool + (int64_t(b) * pool_rows + v) * DSA_ROW_CHUNKS;
-            else bad |= TS_DEVERR_SLOT_RANGE;
-          }
-          valid = true;
-        }
-      }
+      if (b < B)
+        valid = miss_targets(L, miss_ids, miss_pos, victim, install, b, ml - base, k, P, sel_rows,
+                             pool_rows, ctx_stride, ctx_len, my_from, my_to, my_to2, bad);
       mask = __ballot_sync(0xffffffffu, valid);
       // lane 31 holds the furthest index: the walk resumes from there
       b1 = __shfl_sync(0xffffffffu, b, 31);
@@ -216,18 +252,63 @@ __device__ __forceinline__ void gather_misses(const GatherLayer& L, const int32_
       m1 += 32 * nrole;
       continue;
     }
-    while (mask) {
-      const int q = __ffs(mask) - 1;
-      mask &= mask - 1;
-      const uint4* f = reinterpret_cast<const uint4*>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_from), q));
-      uint4* t =
-          reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_to), q));
-      uint4* t2 = reinterpret_cast<uint4*>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_to2), q));
-      if (lane == 0) pipe.push(f, t, t2);
+    push_lanes(mask, my_from, my_to, my_to2, lane, pipe);
+    mask = 0;
+  }
+}
+
+// Every layer's misses handed out dynamically, layer after layer: a warp takes
+// the next batch of 32 misses (over all requests, concatenated) from the
+// launch's ticket word, so warps that read host memory faster take more
+// batches and every layer is done at about its share of the launch (measured
+// on GB300 at 128 requests x 32,768 rows: with the misses dealt out evenly
+// ahead of time, the fastest miss warps finished all four layers in half the
+// time of the slowest, and a layer's completion waited for the slowest). The
+// next ticket is fetched while the current batch is pushed. `prefix` holds the
+// requests' exclusive miss-count prefix (B + 1 entries, shared memory).
+__device__ __forceinline__ void gather_misses_dynamic(
+    uint4* pool, const uint4* host, uint4* sel, int64_t pool_stride, int64_t host_stride,
+    int64_t sel_stride, int layers, const int32_t* miss_ids, const int32_t* miss_pos,
+    const int32_t* victim, const uint8_t* install, const int* prefix, int B, int k, int P,
+    int sel_rows, int pool_rows, int64_t ctx_stride, const int32_t* ctx_len, uint32_t* ticket,
+    int lane, RowPipe& pipe, int& bad) {
+  const int total = prefix[B];
+  const uint32_t nb = static_cast<uint32_t>((total + 31) / 32);  // batches per layer
+  const uint32_t end = nb * static_cast<uint32_t>(layers);
+  uint32_t t = 0;
+  if (lane == 0) t = atomicAdd(ticket, 1u);
+  t = __shfl_sync(0xffffffffu, t, 0);
+  int cur = 0;  // the layer this warp's rows belong to
+  while (t < end) {
+    uint32_t next = 0;
+    if (lane == 0) next = atomicAdd(ticket, 1u);
+    const int l = static_cast<int>(t / nb);
+    for (; cur < l; ++cur) {  // every row of the earlier layers is pushed
+      if (lane == 0) pipe.end_layer(cur);
       __syncwarp();
     }
+    const GatherLayer L{pool + l * pool_stride, host + l * host_stride, sel + l * sel_stride};
+    const int g = static_cast<int>(t % nb) * 32 + lane;
+    const uint4* from = nullptr;
+    uint4* to = nullptr;
+    uint4* to2 = nullptr;
+    bool valid = false;
+    if (g < total) {
+      int lo = 0, hi = B;  // the request b with prefix[b] <= g < prefix[b + 1]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= g) lo = mid;
+        else hi = mid;
+      }
+      valid = miss_targets(L, miss_ids, miss_pos, victim, install, lo, g - prefix[lo], k, P,
+                           sel_rows, pool_rows, ctx_stride, ctx_len, from, to, to2, bad);
+    }
+    push_lanes(__ballot_sync(0xffffffffu, valid), from, to, to2, lane, pipe);
+    t = __shfl_sync(0xffffffffu, next, 0);
+  }
+  for (; cur < layers - 1; ++cur) {  // the finish counts out of the last layer
+    if (lane == 0) pipe.end_layer(cur);
+    __syncwarp();
   }
 }
 
@@ -309,8 +390,9 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
     const uint4* __restrict__ host, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
     uint4* __restrict__ sel, int layers, int64_t pool_stride, int64_t host_stride,
     int64_t sel_stride, uint32_t* __restrict__ done, uint32_t* __restrict__ count, uint32_t seq,
-    int miss_ctas, int sel_rows, int pool_rows, int32_t* err) {
+    int miss_ctas, int sel_rows, int pool_rows, uint32_t* ticket, int32_t* err) {
   extern __shared__ __align__(128) uint8_t gather_smem[];
+  __shared__ int scan_scratch[40];
   const int lane = threadIdx.x & 31;
   const int wc = threadIdx.x >> 5;  // warp in the CTA
   const int nw = static_cast<int>(gridDim.x) * kPipeWarps;
@@ -320,9 +402,31 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
   const int nrole = (miss_cta ? miss_ctas : static_cast<int>(gridDim.x) - miss_ctas) * kPipeWarps;
   int bad = 0;
   RowPipe pipe;
-  if (lane == 0) pipe.init(gather_smem + wc * kPipeWarpBytes, nw, count, done, seq);
+  if (lane == 0)
+    pipe.init(gather_smem + wc * kPipeWarpBytes, nw, count, done, seq, ticket, layers - 1);
   __syncwarp();
-  for (int l = 0; l < layers; ++l) {
+  if (miss_cta && ticket) {
+    // the requests' exclusive miss-count prefix, for the dynamic hand-out
+    int* prefix = reinterpret_cast<int*>(gather_smem + kPipeSmemBytes);
+    const int per = (B + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+    const int b0 = min(static_cast<int>(threadIdx.x) * per, B), b1 = min(b0 + per, B);
+    int c = 0;
+    for (int b = b0; b < b1; ++b) c += min(max(__ldg(miss_count + b), 0), k);
+    int total;
+    int o = block_exclusive_scan(c, scan_scratch, &total);
+    for (int b = b0; b < b1; ++b) {
+      prefix[b] = o;
+      o += min(max(__ldg(miss_count + b), 0), k);
+    }
+    if (threadIdx.x == 0) prefix[B] = total;
+    __syncthreads();
+    gather_misses_dynamic(pool, host, sel, pool_stride, host_stride, sel_stride, layers,
+                          miss_ids, miss_pos, victim, install, prefix, B, k, P, sel_rows,
+                          pool_rows, ctx_stride, ctx_len, ticket, lane, pipe, bad);
+    if (lane == 0) pipe.end_layer(layers - 1);
+    __syncwarp();
+  }
+  for (int l = 0; !(miss_cta && ticket) && l < layers; ++l) {
     const GatherLayer L{pool + l * pool_stride, host + l * host_stride, sel + l * sel_stride};
     if (miss_cta)
       gather_misses(L, miss_ids, miss_pos, miss_count, victim, install, B, k, P, sel_rows,
@@ -464,7 +568,8 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
                          const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream,
                          int layers, size_t pool_layer_bytes, size_t host_layer_bytes,
                          size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq,
-                         const int32_t* victim, const uint8_t* install, bool staged) {
+                         const int32_t* victim, const uint8_t* install, bool staged,
+                         uint32_t* ticket) {
   // At the decode_batch shape (32 x 2048 rows a layer, 9.7 GB of host KV):
   // kMissCtas + kHitCtas CTAs (24 SMs): the misses' share of them reads at
   // the host link's rate (measured alone: 8 SMs of bulk copies reach the
@@ -476,9 +581,15 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
   // 10 + 14, 12 + 12, 6 + 18, 4 + 20 CTAs), 8 or 32 warps per CTA.
   // The staged layout moves only the misses (the attention reads the hits
   // from the pool itself): the miss CTAs alone, into the staging rows.
+  // With `ticket` (the group step's), the misses are handed out dynamically
+  // in layer order, which needs the requests' miss-count prefix in shared
+  // memory beside the pipes.
+  const bool dynamic = ticket && count && B <= kMaxDynamicB;
+  const size_t smem = kPipeSmemBytes + (dynamic ? (size_t(B) + 1) * 4 : 0);
   static std::atomic<uint64_t> smem_set{0};
   if (!raise_smem_limit(reinterpret_cast<const void*>(gather_kernel),
-                        static_cast<int>(kPipeSmemBytes), smem_set))
+                        static_cast<int>(kPipeSmemBytes + (size_t(kMaxDynamicB) + 1) * 4),
+                        smem_set))
     return TS_ERR_CUDA;
   const double host_bytes =
       double(host_layer_bytes ? host_layer_bytes : size_t(B) * size_t(ctx_stride) * DSA_ROW_BYTES) *
@@ -490,11 +601,12 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
   uint4* pool = static_cast<uint4*>(const_cast<void*>(pool_l));
   uint4* sel = staged ? pool + size_t(P) * DSA_ROW_CHUNKS : static_cast<uint4*>(sel_l);
   if (staged) sel_layer_bytes = pool_layer_bytes;
-  gather_kernel<<<grid.miss + hit, kPipeWarps * 32, kPipeSmemBytes, stream>>>(
+  gather_kernel<<<grid.miss + hit, kPipeWarps * 32, smem, stream>>>(
       src_map, miss_ids, miss_pos, miss_count, miss_rows, victim, install, B, k, pool, P,
       static_cast<const uint4*>(host_l), ctx_stride, ctx_len, sel, layers,
       int64_t(pool_layer_bytes / 16), int64_t(host_layer_bytes / 16),
-      int64_t(sel_layer_bytes / 16), done, count, seq, grid.miss, sel_rows, pool_rows, err);
+      int64_t(sel_layer_bytes / 16), done, count, seq, grid.miss, sel_rows, pool_rows,
+      dynamic ? ticket : nullptr, err);
   return launch_status();
 }
 
@@ -564,7 +676,7 @@ extern "C" ts_status dsa_gather_kv(const int32_t* src_map, const int32_t* miss_i
   if (st != TS_OK) return st;
   return dsakv::gather_enqueue(src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, pool_l,
                                P, host_l, ctx_stride, ctx_len, sel_l, err, stream, 1, 0, 0, 0,
-                               nullptr, nullptr, 0, nullptr, nullptr, false);
+                               nullptr, nullptr, 0, nullptr, nullptr, false, nullptr);
 }
 
 extern "C" ts_status dsa_stage_misses(const int32_t* miss_ids, const int32_t* miss_pos,
@@ -578,7 +690,7 @@ extern "C" ts_status dsa_stage_misses(const int32_t* miss_ids, const int32_t* mi
   if ((victim == nullptr) != (install == nullptr)) return TS_ERR_INVALID_ARG;
   return dsakv::gather_enqueue(nullptr, miss_ids, miss_pos, miss_count, nullptr, B, k, pool_l, P,
                                host_l, ctx_stride, ctx_len, nullptr, err, stream, 1, 0, 0, 0,
-                               nullptr, nullptr, 0, victim, install, true);
+                               nullptr, nullptr, 0, victim, install, true, nullptr);
 }
 
 extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* miss_pos,

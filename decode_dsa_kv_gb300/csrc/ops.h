@@ -53,7 +53,9 @@ ts_status gather_check(const int32_t* src_map, const int32_t* miss_ids, const in
 // selection start l * *_layer_bytes after pool_l / host_l / sel_l). With
 // `done` non-null the kernel writes seq into done[l] once layer l's rows are
 // all written (count: `layers` device words, zero between launches; the
-// kernel leaves them zero). With `victim` and `install` (dsa_plan's) given,
+// kernel leaves them zero). With `ticket` too (one device word, zero between
+// launches; the kernel leaves it zero) and B <= 1024, the misses are handed
+// out to the warps dynamically, layer after layer. With `victim` and `install` (dsa_plan's) given,
 // the misses with install code 1 are also written into their victim slots
 // of the pool as they arrive (the refill then needs only min_install = 2).
 ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const int32_t* miss_pos,
@@ -62,7 +64,8 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
                          const int32_t* ctx_len, void* sel_l, int32_t* err, cudaStream_t stream,
                          int layers, size_t pool_layer_bytes, size_t host_layer_bytes,
                          size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq,
-                         const int32_t* victim, const uint8_t* install, bool staged);
+                         const int32_t* victim, const uint8_t* install, bool staged,
+                         uint32_t* ticket);
 
 // The staged layout: a layer's pool tensor is [B][P + k][576]; rows P .. P+k-1
 // of a request hold the step's missed rows at their first positions, so the

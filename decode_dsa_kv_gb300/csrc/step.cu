@@ -153,6 +153,7 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
   uint32_t* gathered = g.sync + kGathered;
   uint32_t* counts = g.sync + kGathered + L;  // the gather's per-layer warp counts
   uint32_t* attended = g.sync + kGathered + 2 * L;  // staged layout: a layer's attention is done
+  uint32_t* ticket = g.sync + kGathered + 3 * L;    // the gather's miss hand-out
   auto rec = [&](int slot, int end, cudaStream_t s) {
     return timing ? cudaEventRecord(timing[2 * slot + end], s) == cudaSuccess : true;
   };
@@ -182,7 +183,7 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
        gather_enqueue(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k, pool,
                       P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel, g.err, gs, L, lb.pool,
                       lb.host, lb.sel, gathered, counts, seq, reuse ? nullptr : g.victim,
-                      reuse ? nullptr : g.install, staged) == TS_OK &&
+                      reuse ? nullptr : g.install, staged, ticket) == TS_OK &&
        rec(2, 1, gs);
   // per layer: the attention on the main stream, the refill beside it on the
   // side stream; the last refill also updates the metadata. The staged

@@ -251,7 +251,7 @@ class DecodeGroup:
         self.side = torch.cuda.Stream(device=dev, priority=0)
         # cross-stream signals: device words written and waited on by the
         # streams themselves (zero before the first step)
-        self.sync = torch.zeros((2 + 3 * layers,), **i32)
+        self.sync = torch.zeros((3 + 3 * layers,), **i32)
         self.desc = self._descriptor()
 
     def staged_rows(self, l: int, b: int):

@@ -415,8 +415,7 @@ ts_status sfa_mla_decode_pool(const void* q, const void* pool_l, int P, const in
  *   topk_ws / sfa_ws                        workspaces of ts_topk and
  *                                           sfa_mla_decode (sizes as theirs)
  *   err       int32 device error word (or NULL)
- *   sync      uint32 [2 + 2 * layers] device words (2 + 3 * layers with the
- *             staged layout), zero before the first step
+ *   sync      uint32 [3 + 3 * layers] device words, zero before the first step
  *             and touched by nothing else; step = 0 before the first step.
  *             Each call uses sequence number step + 1 and stores it in
  *             `step` (with the reuse policy it also swaps the buffers named
@@ -486,8 +485,8 @@ typedef struct {
    * step's missed rows at their first positions; only the misses cross into
    * HBM (dsa_stage_misses' kernel), the attention is sfa_mla_decode_pool's,
    * each layer's refill waits for that layer's attention (the hits it read
-   * stay in place until then), and `sel` is not used. Needs the FIFO policy
-   * and 2 + 3 * layers sync words. */
+   * stay in place until then), and `sel` is not used. Not with the reuse
+   * policy. */
   int layout;
   /* DSA_POLICY_LRU: the fully associative LRU pool of P = S*W entries per
    * request (dsa_plan_lru): lru_stamp uint32 [B][P] and lru_clock uint32 [B],
