@@ -644,6 +644,9 @@ def run_native(args, w, rank, world, local, overrides):
     bits = g.synchronize()
     if bits:
         raise RuntimeError(f"device error bits {bits:#x} in the timed region")
+    # the link's peak measured again after the timed region; the higher of
+    # the two is the denominator (one measurement alone has come out 25 % low)
+    link = max(link, link_peak_gbs(torch, link_buf))
     ms_step = max_over_ranks(ms_total / args.steps, world, "cuda")
     rows_step = w.rows_per_step * world
     value = rows_step / (ms_step * 1e-3)

@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
     // memory); then per stage every loader thread copies its 16-byte pieces
     // into the tile's 128-byte-swizzled layout (a piece c of a stage is row
     // c >> 3, 16-byte column c & 7; 8 consecutive threads read one 128-byte
-    // run). A stage is signalled two stages later: after cp.async.wait_group
+    // run). A stage is signalled a few stages later: after cp.async.wait_group
     // the thread makes its copies visible to the tensor cores' async proxy
     // and arrives on the stage's barrier (count: all 128 loaders). Positions
     // past k read row k-1 (their weights are zero); heads past H read head
@@ -271,24 +271,34 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
     loader_sync();
     const uint8_t* prow0 = ps.rows + int64_t(b) * ps.prow * DSA_ROW_BYTES;
     auto row_src = [&](int p) { return prow0 + int64_t(ridx[p]) * DSA_ROW_BYTES; };
-    uint64_t* lag0 = nullptr;  // the last stage issued, not yet signalled
-    uint64_t* lag1 = nullptr;  // the one before it
-    auto issued_stage = [&](uint64_t* bar) {
+    // stages issued but not yet signalled, oldest first: at most kLag of
+    // them (3 in the score phase, where the 4th earlier stage's slot is the
+    // next to be reused; 2 in the value phase, whose ring has 3 slots)
+    uint64_t *lag0 = nullptr, *lag1 = nullptr, *lag2 = nullptr;
+    int nlag = 0;
+    auto issued_stage = [&](uint64_t* bar, int max_lag) {
       cp_async_commit();
-      if (lag1) {
-        cp_async_wait<2>();
+      if (nlag == max_lag) {
+        if (max_lag == 3) cp_async_wait<3>();
+        else cp_async_wait<2>();
         fence_proxy_async_smem();
-        mbar_arrive(lag1);
+        mbar_arrive(lag0);
+        lag0 = lag1;
+        lag1 = lag2;
+        --nlag;
       }
-      lag1 = lag0;
-      lag0 = bar;
+      if (nlag == 0) lag0 = bar;
+      else if (nlag == 1) lag1 = bar;
+      else lag2 = bar;
+      ++nlag;
     };
     auto signal_all = [&]() {
       cp_async_wait<0>();
       fence_proxy_async_smem();
-      if (lag1) mbar_arrive(lag1);
-      if (lag0) mbar_arrive(lag0);
-      lag0 = lag1 = nullptr;
+      if (nlag > 0) mbar_arrive(lag0);
+      if (nlag > 1) mbar_arrive(lag1);
+      if (nlag > 2) mbar_arrive(lag2);
+      nlag = 0;
     };
     bool ok = true;
     for (int it = 0; it < kScoreLoads && ok; ++it) {
@@ -310,7 +320,7 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
         cp_async16(st + kQBytes + r * 128 + ((col ^ (r & 7)) << 4),
                    row_src(nh * kHalfRows + r) + kb * 128 + col * 16);
       }
-      issued_stage(&bars->full[s]);
+      issued_stage(&bars->full[s], 3);
     }
     signal_all();
     // value phase, once the scores are done (their slots are free then):
@@ -329,7 +339,7 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
         cp_async16(st + j * kVBox + r * 128 + ((col ^ (r & 7)) << 4),
                    row_src(rb * 64 + r) + (half * 256 + j * 64) * 2 + col * 16);
       }
-      issued_stage(&bars->vfull[s]);
+      issued_stage(&bars->vfull[s], 2);
     }
     signal_all();
   } else if (!kPool && warp == 0) {
