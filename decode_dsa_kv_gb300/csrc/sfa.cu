@@ -135,13 +135,10 @@ struct PoolSrc {
 };
 
 // 16-byte copies global -> shared that write shared memory as they land
-// (cp.async, cached in L2 only), committed and waited for in groups.
+// (cp.async, cached in L2 only); wait_group<0> waits for all of them.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
                : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -254,9 +251,9 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
     // memory); then per stage every loader thread copies its 16-byte pieces
     // into the tile's 128-byte-swizzled layout (a piece c of a stage is row
     // c >> 3, 16-byte column c & 7; 8 consecutive threads read one 128-byte
-    // run). A stage is signalled a few stages later: after cp.async.wait_group
-    // the thread makes its copies visible to the tensor cores' async proxy
-    // and arrives on the stage's barrier (count: all 128 loaders). Positions
+    // run). Each thread's arrival on the stage's barrier (count: all 128
+    // loaders) comes from the hardware once its copies have landed; the MMA
+    // thread then makes them visible to the tensor cores' async proxy. Positions
     // past k read row k-1 (their weights are zero); heads past H read head
     // H-1 (their outputs are not stored).
     const int lt = warp == 0 ? lane : (warp - 9) * 32 + lane;  // 0..127
@@ -271,34 +268,11 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
     loader_sync();
     const uint8_t* prow0 = ps.rows + int64_t(b) * ps.prow * DSA_ROW_BYTES;
     auto row_src = [&](int p) { return prow0 + int64_t(ridx[p]) * DSA_ROW_BYTES; };
-    // stages issued but not yet signalled, oldest first: at most kLag of
-    // them (3 in the score phase, where the 4th earlier stage's slot is the
-    // next to be reused; 2 in the value phase, whose ring has 3 slots)
-    uint64_t *lag0 = nullptr, *lag1 = nullptr, *lag2 = nullptr;
-    int nlag = 0;
-    auto issued_stage = [&](uint64_t* bar, int max_lag) {
-      cp_async_commit();
-      if (nlag == max_lag) {
-        if (max_lag == 3) cp_async_wait<3>();
-        else cp_async_wait<2>();
-        fence_proxy_async_smem();
-        mbar_arrive(lag0);
-        lag0 = lag1;
-        lag1 = lag2;
-        --nlag;
-      }
-      if (nlag == 0) lag0 = bar;
-      else if (nlag == 1) lag1 = bar;
-      else lag2 = bar;
-      ++nlag;
-    };
-    auto signal_all = [&]() {
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      if (nlag > 0) mbar_arrive(lag0);
-      if (nlag > 1) mbar_arrive(lag1);
-      if (nlag > 2) mbar_arrive(lag2);
-      nlag = 0;
+    // a stage's barrier gets this thread's arrival from the hardware once its
+    // copies so far have landed; the thread does not wait for them
+    auto issued_stage = [&](uint64_t* bar) {
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+                   : "memory");
     };
     bool ok = true;
     for (int it = 0; it < kScoreLoads && ok; ++it) {
@@ -320,9 +294,8 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
         cp_async16(st + kQBytes + r * 128 + ((col ^ (r & 7)) << 4),
                    row_src(nh * kHalfRows + r) + kb * 128 + col * 16);
       }
-      issued_stage(&bars->full[s], 3);
+      issued_stage(&bars->full[s]);
     }
-    signal_all();
     // value phase, once the scores are done (their slots are free then):
     // piece c of a stage is row c >> 5 of the 64-row block, dim box
     // (c >> 3) & 3, 16-byte column c & 7
@@ -339,9 +312,9 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
         cp_async16(st + j * kVBox + r * 128 + ((col ^ (r & 7)) << 4),
                    row_src(rb * 64 + r) + (half * 256 + j * 64) * 2 + col * 16);
       }
-      issued_stage(&bars->vfull[s], 2);
+      issued_stage(&bars->vfull[s]);
     }
-    signal_all();
+    cp_async_wait<0>();  // every copy landed before the CTA may leave
   } else if (!kPool && warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
@@ -389,6 +362,7 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
         const int s = it % kSSlots;
         ok = mbar_wait_bounded(&bars->full[s], (it / kSSlots) & 1, abort, wait_ns);
         if (!ok) break;
+        if (kPool) fence_proxy_async_smem();  // copies written by the loaders' cp.async
         tc_fence_after();
         const int kb = it % kKB, nh = it / kKB;
         const uint32_t qa = smem_addr(score_slot(s));
@@ -409,6 +383,7 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
         const int s = v % kVSlots;
         ok = mbar_wait_bounded(&bars->vfull[s], (v / kVSlots) & 1, abort, wait_ns);
         if (!ok) break;
+        if (kPool) fence_proxy_async_smem();
         tc_fence_after();
         const int half = v >> 3, rb = v & 7;
         const uint32_t d = tmem + (half == 0 ? 256u : 0u);
