@@ -85,7 +85,8 @@ struct Bars {
   uint64_t vempty[kVSlots];
   uint64_t s_half;  // score product of the first 256 rows complete
   uint64_t s_full;
-  uint64_t p_full;
+  uint64_t p_hi;    // P of rows 256..511 written (their S columns read)
+  uint64_t p_lo;    // P of rows 0..255 written
   uint64_t o_half;  // value product of dims 0..255 complete
   uint64_t o_full;
   uint64_t drain;
@@ -213,7 +214,8 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
     }
     mbar_init(&bars->s_half, 1);
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->p_full, kSoftmaxThreads);
+    mbar_init(&bars->p_hi, kSoftmaxThreads);
+    mbar_init(&bars->p_lo, kSoftmaxThreads);
     mbar_init(&bars->o_half, 1);
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->drain, 1);
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
       const int s = v % kVSlots;
       if (v >= kVSlots) ok = warp_wait(&bars->vempty[s], ((v / kVSlots) - 1) & 1, abort, wait_ns);
       if (!ok) break;
-      const int half = v >> 3, rb = v & 7;
+      const int half = v >> 3, rb = ((v & 7) + 4) & 7;
       uint8_t* st = stages + s * kVBytes;
 #pragma unroll
       for (int i = 0; i < 64 * 32 / kLoaderThreads; ++i) {
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
               !mbar_wait_bounded(&bars->vempty[s], ((v / kVSlots) - 1) & 1, abort, wait_ns))
             break;
           uint8_t* st = stages + s * kVBytes;
-          const int half = v >> 3, rb = v & 7;
+          const int half = v >> 3, rb = ((v & 7) + 4) & 7;
           mbar_expect_tx(&bars->vfull[s], kVBytes);
           for (int j = 0; j < 4; ++j)
             tma_load_3d(st + j * kVBox, &tm_v, &bars->vfull[s], half * 256 + j * 64,
@@ -374,25 +376,30 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
         tc_commit(&bars->empty[s]);
         if (it == kKB - 1) tc_commit(&bars->s_half);
       }
-      if (ok) {
-        tc_commit(&bars->s_full);
-        ok = mbar_wait_bounded(&bars->p_full, 0, abort, wait_ns);
-      }
-      if (ok) tc_fence_after();
+      if (ok) tc_commit(&bars->s_full);
+      // value products: row blocks 4..7 first, as soon as their weights are
+      // written (the softmax reads the S columns they overwrite first), then
+      // 0..3; dims 0..255 go to TMEM columns 256..511, dims 256..511 to
+      // columns 0..255 once every S column has been read
       for (int v = 0; v < kLoads - kScoreLoads && ok; ++v) {
         const int s = v % kVSlots;
+        if (v == 0 || v == 4) {
+          ok = mbar_wait_bounded(v == 0 ? &bars->p_hi : &bars->p_lo, 0, abort, wait_ns);
+          if (!ok) break;
+        }
         ok = mbar_wait_bounded(&bars->vfull[s], (v / kVSlots) & 1, abort, wait_ns);
         if (!ok) break;
         if (kPool) fence_proxy_async_smem();
         tc_fence_after();
-        const int half = v >> 3, rb = v & 7;
+        const int half = v >> 3, rb = ((v & 7) + 4) & 7;
         const uint32_t d = tmem + (half == 0 ? 256u : 0u);
         const uint32_t pa = smem_addr(p_tile) + rb * kPBlock;
         const uint32_t va = smem_addr(stages + s * kVBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_bf16(d, smem_desc_sw128(pa + kk * 32, 16, 1024),
-                      smem_desc_sw128(va + kk * 2048, kVBox, 1024), id_pv, (rb | kk) != 0);
+                      smem_desc_sw128(va + kk * 2048, kVBox, 1024), id_pv,
+                      ((v & 7) | kk) != 0);
         tc_commit(&bars->vempty[s]);
         if (v == 7) tc_commit(&bars->o_half);
       }
@@ -407,7 +414,6 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
     const int row = q4 * 32 + lane;     // head within the tile
     const uint32_t trow = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
     const int nvalid = min(kChunk, k - c * kChunk);
-    const int col0 = part * (kChunk / 2);
     float m = -INFINITY, l = 0.f;
     // Row max in two passes of 128 columns per thread: the first 256 rows'
     // scores are read while the tensor core computes the other 256.
@@ -443,7 +449,11 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
     if (ok) {
       if (part == 1) m = bars->red[row];
       uint32_t r[32];
-      for (int cb = 0; cb < kChunk / 2; cb += 32) {
+      // columns 256..511 first (their P blocks feed the first value
+      // products, and O's first half takes their TMEM columns), then 0..255
+      for (int ph = 0; ph < 2; ++ph) {
+      const int col0 = (ph == 0 ? kHalfRows : 0) + part * (kHalfRows / 2);
+      for (int cb = 0; cb < kHalfRows / 2; cb += 32) {
         tmem_ld32(trow + col0 + cb, r);
         tmem_wait_ld();
         uint32_t packed[16];
@@ -469,7 +479,8 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars->p_full);
+      mbar_arrive(ph == 0 ? &bars->p_hi : &bars->p_lo);
+      }
     }
     softmax_sync();  // part 1 has read the max
     if (ok && part == 1) bars->red[row] = l;
