@@ -698,21 +698,19 @@ def run_native(args, w, rank, world, local, overrides):
     # attention output copied back; the input stream keeps running forward
     e2e = None
     if n_e2e:
-        ins_s = torch.empty((w.B, w.ctx_stride), dtype=torch.float32, device="cuda")
-        ins_q = torch.empty((w.layers, w.B, w.H, 576), dtype=torch.int16, device="cuda")
-        s_bytes, q_bytes = ins_s.numel() * 4, ins_q.numel() * 2
+        s_bytes = w.B * w.ctx_stride * 4
+        q_bytes = w.layers * w.B * w.H * 576 * 2
         o_bytes = g.out.numel() * 2
 
         def e2e_step():
             i = cursor[0]
             cursor[0] += 1
-            # the step's inputs in and its attention output out, through the SMs
-            abi.check(abi.ts_copy(ins_s, scores_pin.dev + i * s_bytes, s_bytes, g.main),
-                      "ts_copy")
-            abi.check(abi.ts_copy(ins_q, q_pin.dev + (i % QS) * q_bytes, q_bytes, g.main),
-                      "ts_copy")
-            g.step(ins_s, ins_q)
-            abi.check(abi.ts_copy(out_pin.dev, g.out, o_bytes, g.main), "ts_copy")
+            # the step's inputs in and its attention output out, copied by the
+            # SMs inside the step (dsa_group_step_host): the scores ahead of the
+            # top-k, the queries beside the top-k and plan, each layer's output
+            # right after its attention
+            g.step_host(scores_pin.dev + i * s_bytes, q_pin.dev + (i % QS) * q_bytes,
+                        out_pin.dev)
 
         e2e_settle = (settle(torch, g, e2e_step, args.e2e_settle_steps)
                       if args.e2e_settle_steps > 0 else 0)
@@ -734,7 +732,8 @@ def run_native(args, w, rank, world, local, overrides):
         e2e = {"value": rows_step / (e2e_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": int(s_bytes + q_bytes), "d2h_bytes_per_step": int(o_bytes),
                "steps": n_e2e, "ms_per_step": e2e_ms, "settle_steps": e2e_settle,
-               "copies": "ts_copy (SM copies) from / to page-locked host memory (ts_host_alloc)"}
+               "copies": "inside the step (dsa_group_step_host: SM copies from / to page-locked "
+                         "host memory from ts_host_alloc, overlapped with the step's work)"}
 
     clocks = sampler.summary(t_wall0, t_wall1)
     scores_steps = scores_pin.array[:first_timed + args.steps].copy() if rank == 0 else None

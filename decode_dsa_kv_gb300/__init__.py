@@ -16,7 +16,7 @@ _ABI_NAMES = {
     "ts_topk_workspace_size", "ts_topk", "ts_topk_noalloc", "dsa_plan", "dsa_plan_reuse", "dsa_plan_lru",
     "dsa_gather_kv", "dsa_stage_misses", "dsa_refill_pool", "dsa_refill_pool_staged",
     "sfa_mla_decode_pool",
-    "sfa_workspace_size", "sfa_mla_decode", "dsa_group_step", "DsaGroup", "DsaKvError", "check", "status_string", "EXPORTS",
+    "sfa_workspace_size", "sfa_mla_decode", "dsa_group_step", "dsa_group_step_host", "DsaGroup", "DsaKvError", "check", "status_string", "EXPORTS",
     "LIB_PATH",
 }
 _RUNTIME_NAMES = {"HostKV", "DecodeGroup", "PinnedHost", "StepTiming"}

@@ -65,6 +65,7 @@ _SIGS = {
     "sfa_mla_decode_pool": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ,
                                  _P, _P]),
     "dsa_group_step": (_I, [_P, _P, _P, _P, _P]),
+    "dsa_group_step_host": (_I, [_P, _P, _P, _P, _P, _P, _P]),
 }
 
 EXPORTS = tuple(_SIGS)
@@ -288,3 +289,12 @@ def dsa_group_step(group: DsaGroup, scores, q, ids=None, timing=None) -> int:
     2 * (3 + 2 * layers) event handles."""
     return _lib.dsa_group_step(ctypes.byref(group), ptr(scores), ptr(q), ptr(ids),
                                None if timing is None else ctypes.cast(timing, _P))
+
+
+def dsa_group_step_host(group: DsaGroup, scores_h, q_h, out_h, scores_d, q_d,
+                        timing=None) -> int:
+    """One decode step with the inputs and the output in page-locked host
+    memory (device-accessible addresses), copied inside the step."""
+    return _lib.dsa_group_step_host(ctypes.byref(group), ptr(scores_h), ptr(q_h), ptr(out_h),
+                                    ptr(scores_d), ptr(q_d),
+                                    None if timing is None else ctypes.cast(timing, _P))

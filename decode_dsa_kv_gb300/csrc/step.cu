@@ -24,6 +24,16 @@ namespace {
 constexpr size_t kRowBytes = DSA_ROW_BYTES;
 enum : int { kPlanned = 0, kRefilled = 1, kGathered = 2 };
 
+// The step's inputs and output in page-locked host memory (device-accessible
+// addresses), with the device staging they cross into (dsa_group_step_host).
+struct HostIo {
+  const float* scores_h;
+  const void* q_h;
+  void* out_h;
+  float* scores_d;
+  void* q_d;  // two halves of [layers][B][H][576], used by step parity
+};
+
 template <typename T>
 T* at(T* base, int l, size_t layer_bytes) {
   using Byte = typename std::conditional<std::is_const<T>::value, const char, char>::type;
@@ -87,8 +97,10 @@ bool wait_for(cudaStream_t s, const uint32_t* word, uint32_t v) {
 
 using namespace dsakv;
 
-extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const void* q,
-                                    const int32_t* ids, cudaEvent_t* timing) {
+namespace {
+
+ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const int32_t* ids,
+                       cudaEvent_t* timing, const HostIo* io) {
   if (!gp || !q) return TS_ERR_INVALID_ARG;
   dsa_group& g = *gp;
   const int L = g.layers;
@@ -154,13 +166,22 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
   uint32_t* counts = g.sync + kGathered + L;  // the gather's per-layer warp counts
   uint32_t* attended = g.sync + kGathered + 2 * L;  // staged layout: a layer's attention is done
   uint32_t* ticket = g.sync + kGathered + 3 * L;    // the gather's miss hand-out
+  uint32_t* qcopied = ticket + 1;                   // host I/O: the queries are in
+
+  // with host I/O: the copies' sizes; this step's half of the query staging
+  const size_t scores_bytes = size_t(g.B) * size_t(g.ctx_stride) * 4;
+  const size_t q_bytes = size_t(L) * lb.q;
+  void* q_stage = io ? static_cast<char*>(io->q_d) + (seq & 1u) * q_bytes : nullptr;
+  if (io) q = q_stage;
   auto rec = [&](int slot, int end, cudaStream_t s) {
     return timing ? cudaEventRecord(timing[2 * slot + end], s) == cudaSuccess : true;
   };
 
   bool ok = true;
+  // with host I/O the scores cross first, on the main stream ahead of the top-k
+  if (io) ok = ts_copy(io->scores_d, io->scores_h, scores_bytes, m) == TS_OK;
   if (!ids) {
-    ok = rec(0, 0, m) &&
+    ok = ok && rec(0, 0, m) &&
          topk_enqueue(scores, g.ctx_stride, g.ctx_len, g.B, g.max_ctx, g.k, g.ids, g.topk_ws,
                       g.err, m) == TS_OK &&
          rec(0, 1, m);
@@ -185,19 +206,29 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
                       lb.host, lb.sel, gathered, counts, seq, reuse ? nullptr : g.victim,
                       reuse ? nullptr : g.install, staged, ticket) == TS_OK &&
        rec(2, 1, gs);
+  // with host I/O the queries cross on the side stream beside the top-k and
+  // the plan, into this step's staging half; that half's last reader, the
+  // attention of step seq - 2, came before planned >= seq - 1 on the main
+  // stream (the signal is enqueued already, so the wait ends)
+  if (io)
+    ok = ok && wait_for(side, planned, seq - 1) &&
+         ts_copy(q_stage, io->q_h, q_bytes, side) == TS_OK && signal(side, qcopied, seq);
   // per layer: the attention on the main stream, the refill beside it on the
   // side stream; the last refill also updates the metadata. The staged
   // attention reads hit rows from the pool itself, so the layer's refill
   // (which overwrites slots read as hits) waits for that attention
   for (int l = 0; ok && l < L; ++l) {
     float* lse_l = g.lse ? at(g.lse, l, lb.lse) : nullptr;
-    ok = wait_for(m, gathered + l, seq) && rec(3 + l, 0, m) &&
+    ok = wait_for(m, gathered + l, seq) && (!io || l > 0 || wait_for(m, qcopied, seq)) &&
+         rec(3 + l, 0, m) &&
          (staged ? sfa_pool_enqueue(at(q, l, lb.q), at(g.pool, l, lb.pool), P, g.src_map,
                                     g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.H,
                                     g.k, g.scale, at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m)
                  : sfa_enqueue(at(q, l, lb.q), at(g.sel, l, lb.sel), g.B, g.H, g.k, g.scale,
                                at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m)) == TS_OK &&
-         rec(3 + l, 1, m) && (!staged || signal(m, attended + l, seq));
+         rec(3 + l, 1, m) && (!staged || signal(m, attended + l, seq)) &&
+         // with host I/O each layer's output crosses back right after its attention
+         (!io || ts_copy(at(io->out_h, l, lb.out), at(g.out, l, lb.out), lb.out, m) == TS_OK);
     if (refills)
       ok = ok && wait_for(side, (staged ? attended : gathered) + l, seq) &&
            rec(3 + L + l, 0, side) &&
@@ -247,10 +278,29 @@ extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const vo
         cudaStreamWaitEvent(side, ev[i], 0);
     for (int i = 0; i < kGathered + L; ++i) signal(side, g.sync + i, seq);
     for (int i = 0; staged && i < L; ++i) signal(side, attended + i, seq);
+    if (io) signal(side, qcopied, seq);
     for (int i = 0; i < 2; ++i)
       if (ev[i]) cudaEventDestroy(ev[i]);
     cudaGetLastError();
     return TS_ERR_CUDA;
   }
   return TS_OK;
+}
+
+}  // namespace
+
+extern "C" ts_status dsa_group_step(dsa_group* gp, const float* scores, const void* q,
+                                    const int32_t* ids, cudaEvent_t* timing) {
+  return enqueue_step(gp, scores, q, ids, timing, nullptr);
+}
+
+extern "C" ts_status dsa_group_step_host(dsa_group* gp, const float* scores_h, const void* q_h,
+                                         void* out_h, float* scores_d, void* q_d,
+                                         cudaEvent_t* timing) {
+  if (!gp || !scores_h || !q_h || !out_h || !scores_d || !q_d) return TS_ERR_INVALID_ARG;
+  if (!aligned16(scores_h) || !aligned16(q_h) || !aligned16(out_h) || !aligned16(scores_d) ||
+      !aligned16(q_d))
+    return TS_ERR_INVALID_ARG;
+  const HostIo io{scores_h, q_h, out_h, scores_d, q_d};
+  return enqueue_step(gp, scores_d, q_d, nullptr, timing, &io);
 }

@@ -251,7 +251,10 @@ class DecodeGroup:
         self.side = torch.cuda.Stream(device=dev, priority=0)
         # cross-stream signals: device words written and waited on by the
         # streams themselves (zero before the first step)
-        self.sync = torch.zeros((3 + 3 * layers,), **i32)
+        self.sync = torch.zeros((4 + 3 * layers,), **i32)
+        # device staging of dsa_group_step_host (made on first use)
+        self._io_scores = None
+        self._io_q = None
         self.desc = self._descriptor()
 
     def staged_rows(self, l: int, b: int):
@@ -311,6 +314,29 @@ class DecodeGroup:
         if self.policy == "reuse":
             # the step swapped its buffers: this step's ids and selection are
             # now the descriptor's previous ones
+            self.ids = self._bufs[self.desc.prev_ids]
+            self.sel = self._bufs[self.desc.prev_sel]
+
+    def step_host(self, scores_h: int, q_h: int, out_h: int,
+                  timing: StepTiming | None = None) -> None:
+        """Enqueue one decode step whose inputs and output live in page-locked
+        host memory (device-accessible addresses of float32 [B][ctx_stride]
+        scores, bf16 [layers][B][H][576] queries and bf16 [layers][B][H][512]
+        output): the library copies them inside the step (dsa_group_step_host).
+        The output also lands in `out`."""
+        if self._io_scores is None:
+            dev = self.out.device
+            self._io_scores = torch.empty((self.B, self.ctx_stride), dtype=torch.float32,
+                                          device=dev)
+            self._io_q = torch.empty((2, self.L, self.B, self.H, D), dtype=torch.int16,
+                                     device=dev)
+        if timing is not None:
+            timing.with_topk = True
+        abi.check(abi.dsa_group_step_host(self.desc, scores_h, q_h, out_h, self._io_scores,
+                                          self._io_q,
+                                          None if timing is None else timing.array),
+                  "dsa_group_step_host")
+        if self.policy == "reuse":
             self.ids = self._bufs[self.desc.prev_ids]
             self.sel = self._bufs[self.desc.prev_sel]
 

@@ -415,7 +415,7 @@ ts_status sfa_mla_decode_pool(const void* q, const void* pool_l, int P, const in
  *   topk_ws / sfa_ws                        workspaces of ts_topk and
  *                                           sfa_mla_decode (sizes as theirs)
  *   err       int32 device error word (or NULL)
- *   sync      uint32 [3 + 3 * layers] device words, zero before the first step
+ *   sync      uint32 [4 + 3 * layers] device words, zero before the first step
  *             and touched by nothing else; step = 0 before the first step.
  *             Each call uses sequence number step + 1 and stores it in
  *             `step` (with the reuse policy it also swaps the buffers named
@@ -504,6 +504,28 @@ typedef struct {
 
 ts_status dsa_group_step(dsa_group* g, const float* scores, const void* q, const int32_t* ids,
                          cudaEvent_t* timing);
+
+/* dsa_group_step_host -- the same step with its inputs and its output in
+ * page-locked host memory (device-accessible addresses, e.g. from
+ * ts_host_alloc); every copy is inside the step, done by the SMs (ts_copy):
+ *   main : scores_h -> scores_d, then the step as dsa_group_step; after each
+ *          layer's attention, that layer's output -> out_h (it also stays in
+ *          the descriptor's `out`)
+ *   side : wait planned >= step - 1 -> q_h -> one half of q_d (chosen by the
+ *          step's parity) -> signal the sync word after the gather's ticket;
+ *          the first layer's attention waits for it
+ * So the queries cross beside the top-k and the plan rather than before them,
+ * and each layer's output crosses while later layers are still gathered. The
+ * staging half a step writes was last read by the attention of the step
+ * before the previous one, which precedes planned >= step - 1 on the main
+ * stream; that signal is enqueued before this wait, so the wait ends.
+ *   scores_h float [B][ctx_stride], q_h bf16 [layers][B][H][576],
+ *   out_h bf16 [layers][B][H][512]      host (device-accessible addresses)
+ *   scores_d float [B][ctx_stride], q_d bf16 2 x [layers][B][H][576]
+ *                                        device staging, caller-owned
+ * All 16-byte aligned. The top-k always runs. Returns as dsa_group_step. */
+ts_status dsa_group_step_host(dsa_group* g, const float* scores_h, const void* q_h, void* out_h,
+                              float* scores_d, void* q_d, cudaEvent_t* timing);
 
 #ifdef __cplusplus
 }

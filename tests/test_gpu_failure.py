@@ -162,3 +162,48 @@ def test_group_step_orders_streams_under_delays(d, layout):
                 (b, l)
     assert deferred > 0   # installs that had to wait for the layer's reads occurred
     host.close()
+
+
+@pytest.mark.parametrize("layout", ["selection", "staged"])
+def test_host_io_step_equals_device_input_step(d, layout):
+    # dsa_group_step_host copies the inputs in and the output out inside the
+    # step (the queries beside the top-k and plan, into a staging half chosen
+    # by step parity): steps enqueued back to back without a sync give the same
+    # plan, pool and attention output as steps on device-resident inputs
+    from decode_dsa_kv_gb300 import PinnedHost
+    w = wl.scaled(wl.DECODE_BATCH, B=2, ctx=16384, S=256)
+    T = 6
+    lens = wl.ctx_lens(w)
+    host = d.HostKV(w.layers, w.B, w.ctx_stride)
+    wl.fill_host_kv(w, host.array)
+    stream = wl.ScoreStream(w)
+    scores = np.stack([stream.next() for _ in range(T)])
+    qs = np.stack([wl.queries(w, t) for t in range(T)])
+    s_pin = PinnedHost(scores.shape, np.float32)
+    q_pin = PinnedHost(qs.shape, np.int16)
+    o_pin = PinnedHost((T, w.layers, w.B, w.H, 512), np.int16)
+    s_pin.array[...] = scores
+    q_pin.array[...] = qs.view(np.int16)
+    ga = d.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host, layout=layout)
+    gb = d.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host, layout=layout)
+    s_b, q_b, o_b = scores[0].nbytes, qs[0].nbytes, o_pin.array[0].nbytes
+    outs = torch.empty((T,) + tuple(gb.out.shape), dtype=torch.bfloat16, device="cuda")
+    for t in range(T):
+        ga.step_host(s_pin.dev + t * s_b, q_pin.dev + t * q_b, o_pin.dev + t * o_b)
+    scores_d = torch.from_numpy(scores).cuda()
+    q_d = torch.from_numpy(qs.view(np.int16)).cuda()
+    torch.cuda.synchronize()
+    for t in range(T):
+        gb.step(scores_d[t], q_d[t])
+        with torch.cuda.stream(gb.main):
+            outs[t].copy_(gb.out)
+    assert ga.synchronize() == 0 and gb.synchronize() == 0
+    for t in range(T):
+        got = o_pin.array[t].view(np.uint16)
+        want = outs[t].cpu().view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, want), t
+    assert torch.equal(ga.tags, gb.tags) and torch.equal(ga.pool, gb.pool)
+    assert torch.equal(ga.ids, gb.ids) and torch.equal(ga.src_map, gb.src_map)
+    for pin in (s_pin, q_pin, o_pin):
+        pin.close()
+    host.close()
