@@ -32,6 +32,7 @@ def mutant(fname: str, old: str, new: str) -> types.ModuleType:
     src = (ORACLE / fname).read_text()
     assert src.count(old) == 1, f"{fname}: the planted change must match once: {old!r}"
     mod = types.ModuleType(f"mutant_{fname[:-3]}")
+    mod.__package__ = "oracle"  # its relative imports resolve to the oracle's modules
     exec(compile(src.replace(old, new), f"<mutant of {fname}>", "exec"), mod.__dict__)
     return mod
 
@@ -162,6 +163,26 @@ def test_lru_pins_catch():
     assert failing_pins(oracle, {"LruPool": m.LruPool}, pins)
 
 
+LRU_SLOT_MUTANTS = {
+    "hits not touched": ("                self.last_use[int(src_map[j])] = self.clock", "                pass"),
+    "victims in slot order, not least recently used":
+        ("key=lambda s: (self.tags[s] >= 0, self.last_use[s], s)",
+         "key=lambda s: (self.tags[s] >= 0, s)"),
+    "misses installed in descending id": ("miss_ids = sorted(first_pos)",
+                                          "miss_ids = sorted(first_pos, reverse=True)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(LRU_SLOT_MUTANTS))
+def test_lru_slot_pins_catch(name):
+    old, new = LRU_SLOT_MUTANTS[name]
+    m = mutant("lru.py", old, new)
+    pins = [test_policy_hit_rates.test_lru_slots_hand_worked] + \
+        [lambda a=a: test_policy_hit_rates.test_lru_slots_against_brute_force(*a)
+         for a in ((20, 12, 60), (8, 12, 30))]
+    assert failing_pins(oracle, {"LruSlots": m.LruSlots}, pins), name
+
+
 def test_unchanged_copies_pass_every_pin():
     """The harness itself: copies with no change pass all the pins."""
     same = {f: mutant(f, "import numpy as np", "import numpy as np")
@@ -169,3 +190,7 @@ def test_unchanged_copies_pass_every_pin():
     assert not failing_pins(test_oracle_topk, {"topk_ids": same["topk.py"].topk_ids}, TOPK_PINS)
     assert not failing_pins(test_oracle_plan, {"dsa_plan": same["plan.py"].dsa_plan}, PLAN_PINS)
     assert not failing_pins(test_oracle_sfa, {"sfa_decode": same["sfa.py"].sfa_decode}, SFA_PINS)
+    lru_same = mutant("lru.py", "import numpy as np", "import numpy as np")
+    lru_pins = [test_policy_hit_rates.test_lru_slots_hand_worked,
+                lambda: test_policy_hit_rates.test_lru_slots_against_brute_force(20, 12, 60)]
+    assert not failing_pins(oracle, {"LruSlots": lru_same.LruSlots}, lru_pins)
