@@ -288,20 +288,23 @@ def device_digest(source: str) -> str:
                             open(os.path.join(csrc, "common.cuh")).read())
 
 
-def traffic_record(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current device code of that kernel's source file (else None)."""
+def traffic_record(kernel: str, workload: str, layout: str = None):
+    """DRAM bytes per launch (and host-link bytes, where counted) from a
+    committed ncu summary, if it was taken on the current device code of that
+    kernel's source file: (dram, link), each None when unknown. A record for
+    the layout (`kernel/workload/layout`) is preferred to one for any layout."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
-        return None
-    rec = json.load(open(p)).get(f"{kernel}/{workload}")
+        return None, None
+    recs = json.load(open(p))
+    rec = (recs.get(f"{kernel}/{workload}/{layout}") if layout else None) \
+        or recs.get(f"{kernel}/{workload}")
     if not rec:
-        return None
+        return None, None
     src = os.path.join(ROOT, "decode_dsa_kv_gb300", "csrc", rec["source"])
-    if not os.path.exists(src):
-        return None
-    ok = device_digest(rec["source"]) == rec.get("device_digest")
-    return rec["bytes_per_launch"] if ok else None
+    if not os.path.exists(src) or device_digest(rec["source"]) != rec.get("device_digest"):
+        return None, None
+    return rec["bytes_per_launch"], rec.get("link_bytes_per_launch")
 
 
 # ---------------------------------------------------------------------------
@@ -674,6 +677,21 @@ def run_native(args, w, rank, world, local, overrides):
         ms = sum(launch_ms[n]) / len(launch_ms[n])
         per_kernel[n] = roofline_of(n, alg[n], ms, peaks, link)
         per_kernel[n]["launches_per_step"] = len(launch_ms[n]) / args.steps
+    # each timed step's span (its first launch's start to its last attention's
+    # end, CUDA events): how evenly the steps ran (a rare step on this platform
+    # stalls for milliseconds while its host reads slow down)
+    step_dist = None
+    if timings:
+        spans = []
+        for t in timings:
+            ev = t.events
+            first = ev[0] if t.with_topk else ev[2]
+            spans.append(first.elapsed_time(ev[2 * (3 + w.layers - 1) + 1]))
+        spans = np.asarray(spans)
+        med = float(np.median(spans))
+        step_dist = {"median_ms": round(med, 4), "p90_ms": round(float(np.percentile(spans, 90)), 4),
+                     "max_ms": round(float(spans.max()), 4),
+                     "steps_over_2x_median": int(np.sum(spans > 2 * med))}
     # where the launches of the last timed step sat, in microseconds after its
     # first launch began
     last_spans = None
@@ -689,9 +707,13 @@ def run_native(args, w, rank, world, local, overrides):
         rf = dict(per_kernel[dom])
         rf_line = {"kernel": dom, "bound": rf["bound"], "achieved": rf["achieved"],
                    "peak": rf["peak"], "unit": rf["unit"], "frac": rf["frac"],
-                   "traffic": traffic_record(dom, w.name),
+                   "traffic": None,
                    "peak_source": peaks["source"] if rf["bound"] != "host_link"
                    else "H2D DMA copy of registered host memory, measured in this run"}
+        dram, link_bytes = traffic_record(dom, w.name, g.layout)
+        rf_line["traffic"] = dram
+        if link_bytes is not None:
+            rf_line["link_traffic"] = link_bytes
 
     # end to end through the same schedule with host buffers: per step the
     # scores and queries are copied in from pinned host memory and the
@@ -770,6 +792,7 @@ def run_native(args, w, rank, world, local, overrides):
         "settle_steps": settled,
         "distinct_input_steps": cursor[0],
         "link_peak_gbs": link,
+        "step_span_distribution": step_dist,
         "last_step_spans_us": last_spans,
         "kernels": {n: {k2: (round(v, 4) if isinstance(v, float) else v)
                         for k2, v in per_kernel[n].items()} for n in per_kernel},

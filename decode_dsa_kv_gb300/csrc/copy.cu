@@ -52,6 +52,9 @@ constexpr size_t kPipeWarpBytes = kPipeSlots * (DSA_ROW_BYTES + 24);  // ring, b
 constexpr size_t kPipeSmemBytes = kPipeWarps * kPipeWarpBytes;
 // most requests whose miss-count prefix fits beside the pipes (dynamic hand-out)
 constexpr int kMaxDynamicB = 1024;
+// misses per ticket: a layer's completion waits for the last batch of it any
+// warp took, so smaller batches let the layers finish closer to their share
+constexpr int kTicketRows = 16;
 static_assert(kPipeSmemBytes + (kMaxDynamicB + 1) * 4 + 40 * 4 <= 227 * 1024, "shared memory");
 
 struct RowPipe {
@@ -258,7 +261,7 @@ __device__ __forceinline__ void gather_misses(const GatherLayer& L, const int32_
 }
 
 // Every layer's misses handed out dynamically, layer after layer: a warp takes
-// the next batch of 32 misses (over all requests, concatenated) from the
+// the next batch of kTicketRows misses (over all requests, concatenated) from the
 // launch's ticket word, so warps that read host memory faster take more
 // batches and every layer is done at about its share of the launch (measured
 // on GB300 at 128 requests x 32,768 rows: with the misses dealt out evenly
@@ -273,7 +276,7 @@ __device__ __forceinline__ void gather_misses_dynamic(
     int sel_rows, int pool_rows, int64_t ctx_stride, const int32_t* ctx_len, uint32_t* ticket,
     int lane, RowPipe& pipe, int& bad) {
   const int total = prefix[B];
-  const uint32_t nb = static_cast<uint32_t>((total + 31) / 32);  // batches per layer
+  const uint32_t nb = static_cast<uint32_t>((total + kTicketRows - 1) / kTicketRows);  // per layer
   const uint32_t end = nb * static_cast<uint32_t>(layers);
   uint32_t t = 0;
   if (lane == 0) t = atomicAdd(ticket, 1u);
@@ -288,12 +291,12 @@ __device__ __forceinline__ void gather_misses_dynamic(
       __syncwarp();
     }
     const GatherLayer L{pool + l * pool_stride, host + l * host_stride, sel + l * sel_stride};
-    const int g = static_cast<int>(t % nb) * 32 + lane;
+    const int g = static_cast<int>(t % nb) * kTicketRows + lane;
     const uint4* from = nullptr;
     uint4* to = nullptr;
     uint4* to2 = nullptr;
     bool valid = false;
-    if (g < total) {
+    if (lane < kTicketRows && g < total) {
       int lo = 0, hi = B;  // the request b with prefix[b] <= g < prefix[b + 1]
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;

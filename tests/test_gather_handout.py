@@ -23,11 +23,14 @@ def request_of(prefix, B, g):
     return lo
 
 
+ROWS = 16   # misses per ticket (kTicketRows)
+
+
 def simulate(counts, k, layers, nwarps, rng):
     B = len(counts)
     prefix = prefix_of(counts, k)
     total = int(prefix[B])
-    nb = (total + 31) // 32
+    nb = (total + ROWS - 1) // ROWS
     end = nb * layers
     ticket = 0
     moved = []
@@ -54,8 +57,8 @@ def simulate(counts, k, layers, nwarps, rng):
             events[w].append(("out", cur[w]))
             cur[w] += 1
         for lane in range(32):
-            g = (t % nb) * 32 + lane
-            if g < total:
+            g = (t % nb) * ROWS + lane
+            if lane < ROWS and g < total:
                 b = request_of(prefix, B, g)
                 i = g - int(prefix[b])
                 assert 0 <= b < B and 0 <= i < min(max(counts[b], 0), k)
