@@ -154,7 +154,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -602,6 +602,14 @@ def run_native(args, w, rank, world, local, overrides):
         cursor[0] += 1
         g.step(scores_d[i], q_d[i % QS], timing=timing)
 
+    # the clock sampler starts before the settle steps: the GPU then never
+    # idles between them, the warm-up and the timed region (after an idle
+    # pause of a fraction of a second the first host reads of a step run
+    # slowly, measured on GB300: after 20 s idle, 14.5 GB/s for the first
+    # gigabyte read against 210 GB/s once busy)
+    sampler = ClockSampler(local)
+    if not args.only:
+        sampler.start()
     settled = settle(torch, g, step, args.settle_steps) if args.settle_steps > 0 else 0
     for _ in range(args.warmup):
         step()
@@ -621,9 +629,6 @@ def run_native(args, w, rank, world, local, overrides):
     timings = (None if args.no_kernel_events
                else [g.timing() for _ in range(args.steps)])
     torch.cuda.synchronize()
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
@@ -840,6 +845,13 @@ def run_only(args, w, g, scores, q, peaks, link, lens, host, rank):
     torch.cuda.synchronize()
     misses = g.miss_count.double().sum().item()
     hit = 1.0 - misses / (B * k)
+    # a quarter second of launches right before the timed ones: host reads
+    # run slowly for a while after the GPU idles
+    t_end = time.time() + 0.25
+    while time.time() < t_end:
+        for _ in range(8):
+            abi.check(launch(), args.only)
+        torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(m)

@@ -53,7 +53,7 @@ _SIGS = {
     "ts_topk_noalloc": (_I, [_P, _I64, _P, _I, _I, _I, _P, _P, _P]),
     "dsa_plan": (_I, [_P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dsa_plan_reuse": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
-    "dsa_plan_lru": (_I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "dsa_plan_lru": (_I, [_P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dsa_gather_kv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _I, _P, _I64, _P, _P, _P, _P]),
     "dsa_stage_misses": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _I, _P, _I64, _P, _P, _P]),
     "dsa_refill_pool": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _I, _I,
@@ -100,8 +100,7 @@ class DsaGroup(ctypes.Structure):
         ("prev_ids", _P),
         ("prev_sel", _P),
         ("layout", _I),
-        ("lru_stamp", _P),
-        ("lru_clock", _P),
+        ("lru_order", _P),
     ]
 
 for _name, (_res, _args) in _SIGS.items():
@@ -226,13 +225,11 @@ def dsa_plan_reuse(ids, prev_ids, ctx_len, B, k, src_map, miss_ids, miss_pos, mi
                                ptr(err), stream_handle(stream))
 
 
-def dsa_plan_lru(ids, ctx_len, B, k, pool_tags, lru_stamp, lru_clock, P, src_map, miss_ids,
-                 miss_pos, victim, install, miss_count, miss_rows, err=None, stream=None) -> int:
-    return _lib.dsa_plan_lru(ptr(ids), ptr(ctx_len), B, k, ptr(pool_tags), ptr(lru_stamp),
-                             ptr(lru_clock), P, ptr(src_map), ptr(miss_ids), ptr(miss_pos),
-                             ptr(victim), ptr(install), ptr(miss_count), ptr(miss_rows), ptr(err),
-                             stream_handle(stream))
-
+def dsa_plan_lru(ids, ctx_len, B, k, pool_tags, lru_order, P, src_map, miss_ids, miss_pos,
+                 victim, install, miss_count, miss_rows, err=None, stream=None) -> int:
+    return _lib.dsa_plan_lru(ptr(ids), ptr(ctx_len), B, k, ptr(pool_tags), ptr(lru_order), P,
+                             ptr(src_map), ptr(miss_ids), ptr(miss_pos), ptr(victim), ptr(install),
+                             ptr(miss_count), ptr(miss_rows), ptr(err), stream_handle(stream))
 
 def dsa_gather_kv(src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, pool_l, P, host_l,
                   ctx_stride, ctx_len, sel_l, err=None, stream=None) -> int:

@@ -35,14 +35,14 @@ ts_status plan_reuse_enqueue(const int32_t* ids, const int32_t* prev_ids, const 
                              cudaStream_t stream);
 
 ts_status plan_lru_check(const int32_t* ids, const int32_t* ctx_len, int B, int k,
-                         const int32_t* pool_tags, const uint32_t* lru_stamp,
-                         const uint32_t* lru_clock, int P, int32_t* src_map, int32_t* miss_ids,
-                         int32_t* miss_pos, int32_t* victim, uint8_t* install,
+                         const int32_t* pool_tags, const int32_t* lru_order, int P,
+                         int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
+                         int32_t* victim, uint8_t* install,
                          int32_t* miss_count, int32_t* miss_rows);
 ts_status plan_lru_enqueue(const int32_t* ids, const int32_t* ctx_len, int B, int k,
-                           int32_t* pool_tags, uint32_t* lru_stamp, uint32_t* lru_clock, int P,
-                           int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
-                           int32_t* victim, uint8_t* install, int32_t* miss_count,
+                           int32_t* pool_tags, int32_t* lru_order, int P, int32_t* src_map,
+                           int32_t* miss_ids, int32_t* miss_pos, int32_t* victim,
+                           uint8_t* install, int32_t* miss_count,
                            int32_t* miss_rows, int32_t* err, cudaStream_t stream);
 
 ts_status gather_check(const int32_t* src_map, const int32_t* miss_ids, const int32_t* miss_pos,

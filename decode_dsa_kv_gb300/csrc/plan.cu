@@ -348,20 +348,31 @@ __global__ void __launch_bounds__(kReuseThreads) dsa_plan_reuse_kernel(
 // dsa_plan_lru: the fully associative LRU pool (GLM-5.2 shared-Indexer KV Cache
 // Offload, §3: the 8192-entry device pool the pages built before the
 // set-associative FIFO). Same outputs as dsa_plan, plus the pool's metadata
-// updated in place: each touched hit and each installed miss takes the next
-// tick of the request's clock, hits first in position order, then the misses
-// in ascending id, each into the least recently used slot (empty slots first,
-// lowest index first). One CTA per request: every slot's tag is looked up in
-// the (ascending) selected ids by binary search, the slots the step does not
-// hit are sorted by (empty first, last use, index) with a shared-memory
-// bitonic sort, and the i-th miss takes the i-th of them. With k <= P a step
-// never misses more tokens than it has slots it does not hit, so every
-// victim is a slot no position of the step reads (install code 1).
+// updated in place. The policy: the step's hits are touched in position
+// order, then its misses are installed in ascending id, each into the least
+// recently used slot (empty slots first, lowest index first).
+//
+// The metadata is the slots' recency order itself (lru_order, least recently
+// used first) rather than a clock and per-slot stamps, so no plan sorts: with
+// k <= P a step misses at most as many tokens as it has slots it does not hit,
+// so its victims are the first M of those slots in the old order, and the
+// new order is
+//     [slots neither hit nor evicted, old order] ++ [hit slots, position order]
+//     ++ [victims, install order]
+// (the touched hits are more recent than anything untouched, the installs
+// more recent than the hits). A cold pool is all empty with the identity
+// order, which lists the empty slots first in index order, and every step
+// keeps them so. One CTA per request: every slot's tag is looked up in the
+// (ascending) selected ids by binary search; two block-wide scans place the
+// hits (over positions) and the slots not hit (over the old order).
 // ---------------------------------------------------------------------------
 constexpr int kLruThreads = 1024;
 
 __host__ __device__ inline size_t lru_smem_bytes(int P, int k) {
-  return size_t(pow2_at_least(P)) * 8 + size_t(k) * 12 + 64 * 4 + 16;
+  // old order [P] int; hit flags [P] bytes; seen bitmap [P/32] words;
+  // ids, hit slots, miss ids [k] ints each; scan scratch
+  return size_t(P) * 4 + ((size_t(P) + 15) & ~size_t(15)) + size_t((P + 31) / 32) * 4 +
+         size_t(k) * 12 + 64 * 4 + 16;
 }
 
 __device__ __forceinline__ int find_sorted(const int* v, int n, int t) {
@@ -376,25 +387,25 @@ __device__ __forceinline__ int find_sorted(const int* v, int n, int t) {
 
 __global__ void __launch_bounds__(kLruThreads) dsa_plan_lru_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ ctx_len, int k,
-    int32_t* __restrict__ pool_tags, uint32_t* __restrict__ lru_stamp,
-    uint32_t* __restrict__ lru_clock, int P, int32_t* __restrict__ src_map,
-    int32_t* __restrict__ miss_ids, int32_t* __restrict__ miss_pos, int32_t* __restrict__ victim,
+    int32_t* __restrict__ pool_tags, int32_t* __restrict__ lru_order, int P,
+    int32_t* __restrict__ src_map, int32_t* __restrict__ miss_ids,
+    int32_t* __restrict__ miss_pos, int32_t* __restrict__ victim,
     uint8_t* __restrict__ install, int32_t* __restrict__ miss_count,
     int32_t* __restrict__ miss_rows, int32_t* err) {
   extern __shared__ __align__(16) char smem_raw[];
-  const int P2 = pow2_at_least(P);
-  uint64_t* key = reinterpret_cast<uint64_t*>(smem_raw);   // [P2]
-  int* id_s = reinterpret_cast<int*>(key + P2);            // [k]
-  int* src_s = id_s + k;                                   // [k]
-  int* mid_s = src_s + k;                                  // [k]
-  int* scratch = mid_s + k;                                // [64]
+  int* order_s = reinterpret_cast<int*>(smem_raw);                              // [P]
+  uint8_t* hit_s = reinterpret_cast<uint8_t*>(order_s + P);                     // [P]
+  uint32_t* seen = reinterpret_cast<uint32_t*>(hit_s + ((P + 15) & ~15));       // [P/32]
+  int* id_s = reinterpret_cast<int*>(seen + (P + 31) / 32);                     // [k]
+  int* src_s = id_s + k;                                                        // [k]
+  int* mid_s = src_s + k;                                                       // [k]
+  int* scratch = mid_s + k;                                                     // [64]
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int n = ctx_len[b];
   const int32_t* id_row = ids + int64_t(b) * k;
   int32_t* tag_row = pool_tags + int64_t(b) * P;
-  uint32_t* stamp_row = lru_stamp + int64_t(b) * P;
-  const uint32_t clock = lru_clock[b];
+  int32_t* order_row = lru_order + int64_t(b) * P;
 
   bool ascending = true, bad_id = false;
   for (int j = tid; j < k; j += kLruThreads) {
@@ -404,26 +415,36 @@ __global__ void __launch_bounds__(kLruThreads) dsa_plan_lru_kernel(
     id_s[j] = t;
     src_s[j] = -1;
   }
+  for (int w = tid; w < (P + 31) / 32; w += kLruThreads) seen[w] = 0;
   if (bad_id) report(err, TS_DEVERR_ID_RANGE);
   ascending = __syncthreads_and(ascending);
   if (!ascending && tid == 0) report(err, TS_DEVERR_ORDER);
 
-  // every slot: the position that hits it (-> src_s), or its eviction key
-  for (int s = tid; s < P2; s += kLruThreads) {
-    uint64_t e = ~0ull;
-    if (s < P) {
-      const int t = tag_row[s];
-      const int j = t >= 0 ? find_sorted(id_s, k, t) : -1;
-      if (j >= 0) src_s[j] = s;
-      else if (t < 0) e = uint64_t(s);
-      else e = ((uint64_t(stamp_row[s]) + 1) << 32) | uint32_t(s);
+  // the old order (a permutation of the slots), and every slot's hit position
+  bool bad_order = false;
+  int hit_slots = 0;
+  for (int i = tid; i < P; i += kLruThreads) {
+    int s = order_row[i];
+    if (s < 0 || s >= P) {
+      bad_order = true;
+      s = 0;
+    } else if (atomicOr(seen + (s >> 5), 1u << (s & 31)) & (1u << (s & 31))) {
+      bad_order = true;
     }
-    key[s] = e;
+    order_s[i] = s;
+    const int t = tag_row[i];
+    const int j = t >= 0 ? find_sorted(id_s, k, t) : -1;
+    if (j >= 0) {
+      src_s[j] = i;
+      ++hit_slots;
+    }
+    hit_s[i] = j >= 0;
   }
-  __syncthreads();
+  bad_order = __syncthreads_or(bad_order);
 
-  // source map; hits touched in position order; misses compacted in position
-  // order, which is ascending id. Each thread owns a contiguous run.
+  // source map; hits placed in position order after the untouched slots;
+  // misses compacted in position order, which is ascending id. Each thread
+  // owns a contiguous run of positions.
   const int per = (k + kLruThreads - 1) / kLruThreads;
   const int j0 = min(tid * per, k), j1 = min(j0 + per, k);
   int nh = 0, nm = 0;
@@ -432,16 +453,22 @@ __global__ void __launch_bounds__(kLruThreads) dsa_plan_lru_kernel(
     if (src_s[j] >= 0) ++nh;
     else if (t >= 0 && t < n) ++nm;
   }
-  int H, M;
+  int H, M, HS;
   int h = block_exclusive_scan(nh, scratch, &H);
   int mi = block_exclusive_scan(nm, scratch, &M);
+  block_exclusive_scan(hit_slots, scratch, &HS);
+  // a token held by two slots, or an order that is not a permutation of the
+  // slots: the pool's metadata is corrupt (the plan is then undefined)
+  const bool corrupt = bad_order || HS != H;
+  if (corrupt && tid == 0) report(err, TS_DEVERR_SLOT_RANGE);
   for (int j = j0; j < j1; ++j) {
     const int t = id_s[j];
     const int slot = src_s[j];
     int src;
     if (slot >= 0) {
       src = slot;
-      stamp_row[slot] = clock + 1u + uint32_t(h++);
+      if (!corrupt) order_row[P - M - H + h] = slot;
+      ++h;
     } else if (t >= 0 && t < n) {
       src = -1 - t;
       mid_s[mi] = t;
@@ -454,39 +481,39 @@ __global__ void __launch_bounds__(kLruThreads) dsa_plan_lru_kernel(
     src_map[int64_t(b) * k + j] = src;
   }
 
-  // the slots no position hits, least recently used first
-  for (int size = 2; size <= P2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < P2 / 2; i += kLruThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const uint64_t a = key[lo], c = key[hi];
-        if ((a > c) == up) {
-          key[lo] = c;
-          key[hi] = a;
-        }
+  // the slots no position hits, in the old order: the first M are the
+  // victims (least recently used first), the rest move to the front
+  const int per2 = (P + kLruThreads - 1) / kLruThreads;
+  const int i0 = min(tid * per2, P), i1 = min(i0 + per2, P);
+  int nn = 0;
+  for (int i = i0; i < i1; ++i) nn += hit_s[order_s[i]] ? 0 : 1;
+  int NH;
+  int r = block_exclusive_scan(nn, scratch, &NH);  // (a barrier: mid_s is complete)
+  for (int i = i0; i < i1; ++i) {
+    const int s = order_s[i];
+    if (hit_s[s]) continue;
+    if (r < M) {
+      const int64_t g = int64_t(b) * k + r;
+      if (corrupt) {
+        victim[g] = 0;
+        install[g] = 0;
+      } else {
+        victim[g] = s;
+        install[g] = 1;
+        tag_row[s] = mid_s[r];
+        order_row[P - M + r] = s;
       }
-      __syncthreads();
+    } else if (!corrupt) {
+      order_row[r - M] = s;
     }
+    ++r;
   }
-  for (int i = tid; i < M; i += kLruThreads) {
-    const uint64_t e = key[i];
-    const int64_t g = int64_t(b) * k + i;
-    if (e == ~0ull) {  // more misses than free slots: only when k > P (refused on the host)
-      report(err, TS_DEVERR_SLOT_RANGE);
-      victim[g] = 0;
-      install[g] = 0;
-      continue;
+  if (corrupt)  // (victims past the slots not hit: only with corrupt metadata)
+    for (int i = NH + tid; i < M; i += kLruThreads) {
+      victim[int64_t(b) * k + i] = 0;
+      install[int64_t(b) * k + i] = 0;
     }
-    const int v = static_cast<int>(e & 0xffffffffu);
-    victim[g] = v;
-    install[g] = 1;
-    tag_row[v] = mid_s[i];
-    stamp_row[v] = clock + 1u + uint32_t(H) + uint32_t(i);
-  }
   if (tid == 0) {
-    lru_clock[b] = clock + uint32_t(H) + uint32_t(M);
     miss_count[b] = M;
     miss_rows[b] = M;
   }
@@ -589,11 +616,11 @@ extern "C" ts_status dsa_plan_reuse(const int32_t* ids, const int32_t* prev_ids,
 namespace dsakv {
 
 ts_status plan_lru_check(const int32_t* ids, const int32_t* ctx_len, int B, int k,
-                         const int32_t* pool_tags, const uint32_t* lru_stamp,
-                         const uint32_t* lru_clock, int P, int32_t* src_map, int32_t* miss_ids,
-                         int32_t* miss_pos, int32_t* victim, uint8_t* install,
+                         const int32_t* pool_tags, const int32_t* lru_order, int P,
+                         int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
+                         int32_t* victim, uint8_t* install,
                          int32_t* miss_count, int32_t* miss_rows) {
-  if (!ids || !ctx_len || !pool_tags || !lru_stamp || !lru_clock || !src_map || !miss_ids ||
+  if (!ids || !ctx_len || !pool_tags || !lru_order || !src_map || !miss_ids ||
       !miss_pos || !victim || !install || !miss_count || !miss_rows)
     return TS_ERR_INVALID_ARG;
   if (B <= 0 || k <= 0 || P <= 0 || B > 65535) return TS_ERR_INVALID_ARG;
@@ -602,34 +629,32 @@ ts_status plan_lru_check(const int32_t* ids, const int32_t* ctx_len, int B, int 
 }
 
 ts_status plan_lru_enqueue(const int32_t* ids, const int32_t* ctx_len, int B, int k,
-                           int32_t* pool_tags, uint32_t* lru_stamp, uint32_t* lru_clock, int P,
-                           int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
-                           int32_t* victim, uint8_t* install, int32_t* miss_count,
+                           int32_t* pool_tags, int32_t* lru_order, int P, int32_t* src_map,
+                           int32_t* miss_ids, int32_t* miss_pos, int32_t* victim, uint8_t* install, int32_t* miss_count,
                            int32_t* miss_rows, int32_t* err, cudaStream_t stream) {
   const size_t smem = lru_smem_bytes(P, k);
   static std::atomic<uint64_t> smem_set{0};
   if (!raise_smem_limit(reinterpret_cast<const void*>(dsa_plan_lru_kernel),
                         static_cast<int>(kMaxSmem), smem_set))
     return TS_ERR_CUDA;
-  dsa_plan_lru_kernel<<<B, kLruThreads, smem, stream>>>(ids, ctx_len, k, pool_tags, lru_stamp,
-                                                        lru_clock, P, src_map, miss_ids, miss_pos,
-                                                        victim, install, miss_count, miss_rows,
-                                                        err);
+  dsa_plan_lru_kernel<<<B, kLruThreads, smem, stream>>>(ids, ctx_len, k, pool_tags, lru_order,
+                                                        P, src_map, miss_ids, miss_pos, victim,
+                                                        install, miss_count, miss_rows, err);
   return launch_status();
 }
 
 }  // namespace dsakv
 
 extern "C" ts_status dsa_plan_lru(const int32_t* ids, const int32_t* ctx_len, int B, int k,
-                                  int32_t* pool_tags, uint32_t* lru_stamp, uint32_t* lru_clock,
-                                  int P, int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
+                                  int32_t* pool_tags, int32_t* lru_order, int P,
+                                  int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos,
                                   int32_t* victim, uint8_t* install, int32_t* miss_count,
                                   int32_t* miss_rows, int32_t* err, cudaStream_t stream) {
-  const ts_status st = dsakv::plan_lru_check(ids, ctx_len, B, k, pool_tags, lru_stamp, lru_clock,
-                                             P, src_map, miss_ids, miss_pos, victim, install,
+  const ts_status st = dsakv::plan_lru_check(ids, ctx_len, B, k, pool_tags, lru_order, P,
+                                             src_map, miss_ids, miss_pos, victim, install,
                                              miss_count, miss_rows);
   if (st != TS_OK) return st;
-  return dsakv::plan_lru_enqueue(ids, ctx_len, B, k, pool_tags, lru_stamp, lru_clock, P, src_map,
+  return dsakv::plan_lru_enqueue(ids, ctx_len, B, k, pool_tags, lru_order, P, src_map,
                                  miss_ids, miss_pos, victim, install, miss_count, miss_rows, err,
                                  stream);
 }

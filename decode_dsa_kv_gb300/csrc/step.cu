@@ -134,9 +134,9 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   if (st == TS_OK)
     st = reuse ? plan_reuse_check(plan_ids, g.prev_ids, g.ctx_len, g.B, g.k, g.src_map, g.miss_ids,
                                   g.miss_pos, g.miss_count, g.miss_rows)
-         : lru ? plan_lru_check(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.lru_stamp,
-                                g.lru_clock, P, g.src_map, g.miss_ids, g.miss_pos, g.victim,
-                                g.install, g.miss_count, g.miss_rows)
+         : lru ? plan_lru_check(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.lru_order, P,
+                                g.src_map, g.miss_ids, g.miss_pos, g.victim, g.install,
+                                g.miss_count, g.miss_rows)
                : plan_check(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.fifo_ptr, g.S, g.W,
                             g.src_map, g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count,
                             g.miss_rows, g.ptr_next);
@@ -189,9 +189,9 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   ok = ok && wait_for(m, refilled, seq - 1) && rec(1, 0, m) &&
        (reuse ? plan_reuse_enqueue(plan_ids, g.prev_ids, g.ctx_len, g.B, g.k, g.src_map,
                                    g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.err, m)
-        : lru ? plan_lru_enqueue(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.lru_stamp,
-                                 g.lru_clock, P, g.src_map, g.miss_ids, g.miss_pos, g.victim,
-                                 g.install, g.miss_count, g.miss_rows, g.err, m)
+        : lru ? plan_lru_enqueue(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.lru_order, P,
+                                 g.src_map, g.miss_ids, g.miss_pos, g.victim, g.install,
+                                 g.miss_count, g.miss_rows, g.err, m)
               : plan_enqueue(plan_ids, g.ctx_len, g.B, g.k, g.pool_tags, g.fifo_ptr, g.S, g.W,
                              g.src_map, g.miss_ids, g.miss_pos, g.victim, g.install,
                              g.miss_count, g.miss_rows, g.ptr_next, g.err, m)) == TS_OK &&

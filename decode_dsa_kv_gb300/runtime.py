@@ -177,13 +177,13 @@ class DecodeGroup:
 
     policy "fifo": the set-associative FIFO pool of S sets x W ways;
     policy "lru": a fully associative pool of S x W entries, least recently
-    used first (tags, last-use stamps and a clock per request);
+    used first (tags and the slots' recency order per request);
     policy "reuse": the base design's adjacent-step reuse, where the device
     keeps only the previous step's selection (S and W are then unused).
     After a step, `ids` and `sel` hold that step's ids and selection.
 
     layout "selection": every layer's rows are gathered into `sel`, which the
-    attention reads; layout "staged" (FIFO only): the attention reads its rows
+    attention reads; layout "staged" (FIFO or LRU): the attention reads its rows
     straight from the pool, which then holds P + k rows per request (rows P..
     stage the step's misses at their first positions) and `sel` is None."""
 
@@ -214,9 +214,10 @@ class DecodeGroup:
         self.pool = torch.zeros((layers, B, rows, D), dtype=torch.int16, device=dev)
         self.tags = torch.full((B, P), -1, **i32)
         self.fifo_ptr = torch.zeros((B, S if policy == "fifo" else 1), **i32)
-        # LRU pool: each slot's last-use tick and each request's clock (uint32)
-        self.lru_stamp = torch.zeros((B, P) if policy == "lru" else (1,), **i32)
-        self.lru_clock = torch.zeros((B,) if policy == "lru" else (1,), **i32)
+        # LRU pool: each request's slots from least to most recently used
+        # (the identity order of a cold pool)
+        self.lru_order = (torch.arange(P, **i32).repeat(B, 1) if policy == "lru"
+                          else torch.zeros((1,), **i32))
         # plan outputs
         self.ids = torch.empty((B, k), **i32)
         self.src_map = torch.empty((B, k), **i32)
@@ -285,8 +286,7 @@ class DecodeGroup:
         d.err = self.err.data_ptr()
         if self.policy == "lru":
             d.policy = abi.DSA_POLICY_LRU
-            d.lru_stamp = self.lru_stamp.data_ptr()
-            d.lru_clock = self.lru_clock.data_ptr()
+            d.lru_order = self.lru_order.data_ptr()
         if self.policy == "reuse":
             d.policy = abi.DSA_POLICY_REUSE
             d.prev_ids = self.prev_ids.data_ptr()

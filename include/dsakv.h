@@ -219,27 +219,27 @@ ts_status dsa_plan_reuse(const int32_t* ids, const int32_t* prev_ids, const int3
  * in any slot. Per step: every selected token already resident is a hit (its
  * slot); the hits are touched in position order, then the distinct misses are
  * installed in ascending id, each into the least recently used slot (empty
- * slots first, lowest index first). Each touch and each install takes the
- * next tick of the request's clock.
+ * slots first, lowest index first).
  *
  *   ids        int32 [B][k]   strictly ascending per request (ts_topk's output)
  *   pool_tags  int32 [B][P]   token held by each slot, -1 = empty (in/out)
- *   lru_stamp  uint32 [B][P]  tick of each slot's last use (in/out)
- *   lru_clock  uint32 [B]     tick of each request's latest use (in/out; 0 with
- *                             a cold pool; wraps after 2^32 ticks, about two
- *                             million steps of k = 2048)
+ *   lru_order  int32 [B][P]   the slots from least to most recently used (in/out;
+ *                             a permutation of 0..P-1; a cold pool has every
+ *                             tag -1 and the identity order)
  * Outputs as dsa_plan's; every install has code 1 (with k <= P a victim is
  * never a slot the step reads, so the gather may write it on arrival) and no
- * refill is needed. Unlike dsa_plan, the pool's tags, stamps and clock are
- * updated here, at plan time: nothing else reads them, and the next plan runs
- * after this one. Requires k <= P, k <= 4096, 8 * pow2(P) + 12 * k bytes <=
- * 200 KiB (P <= 16384 at k = 2048). Ids not strictly ascending set
- * TS_DEVERR_ORDER (the plan is then undefined).
+ * refill is needed. Unlike dsa_plan, the pool's tags and order are updated
+ * here, at plan time: nothing else reads them, and the next plan runs after
+ * this one. Requires k <= P, k <= 4096, 5 * P + P / 8 + 12 * k bytes <= 200 KiB
+ * (P <= 32768 at k = 2048). Ids not strictly ascending set TS_DEVERR_ORDER; an
+ * order that is not a permutation of the slots, or a token held by two slots,
+ * sets TS_DEVERR_SLOT_RANGE, writes no install and leaves the order as it was
+ * (in either case the plan is undefined).
  * ------------------------------------------------------------------------- */
 ts_status dsa_plan_lru(const int32_t* ids, const int32_t* ctx_len, int B, int k,
-                       int32_t* pool_tags, uint32_t* lru_stamp, uint32_t* lru_clock, int P,
-                       int32_t* src_map, int32_t* miss_ids, int32_t* miss_pos, int32_t* victim,
-                       uint8_t* install, int32_t* miss_count, int32_t* miss_rows, int32_t* err,
+                       int32_t* pool_tags, int32_t* lru_order, int P, int32_t* src_map,
+                       int32_t* miss_ids, int32_t* miss_pos, int32_t* victim, uint8_t* install,
+                       int32_t* miss_count, int32_t* miss_rows, int32_t* err,
                        cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
@@ -489,11 +489,11 @@ typedef struct {
    * policy. */
   int layout;
   /* DSA_POLICY_LRU: the fully associative LRU pool of P = S*W entries per
-   * request (dsa_plan_lru): lru_stamp uint32 [B][P] and lru_clock uint32 [B],
-   * zero for a cold pool; fifo_ptr, ptr_next are not used and no refill runs
-   * (every install is written by the gather as its row arrives). */
-  uint32_t* lru_stamp;
-  uint32_t* lru_clock;
+   * request (dsa_plan_lru): lru_order int32 [B][P], the slots from least to
+   * most recently used (the identity for a cold pool); fifo_ptr, ptr_next
+   * are not used and no refill runs (every install is written by the gather
+   * as its row arrives). */
+  int32_t* lru_order;
 } dsa_group;
 
 #define DSA_POLICY_FIFO 0

@@ -2,8 +2,9 @@
 step's LRU policy; GLM-5.2 shared-Indexer KV Cache Offload, §3, the pool the
 pages measured before the set-associative FIFO of §4.3), against the oracle's
 slot-level LRU pool (oracle.LruSlots): bit-exact source maps, miss lists,
-victims, install flags, tags, last-use stamps and clocks, step after step; and
-whole decode steps (both layouts) with the pool's rows."""
+victims, install flags, tags and the slots' recency order (the oracle's slots
+sorted by empty first, then last use, then index), step after step; and whole
+decode steps (both layouts) with the pool's rows."""
 import math
 
 import numpy as np
@@ -33,8 +34,7 @@ def test_plan_lru_matches_oracle_step_by_step(d, B, P, k, ctx, steps):
     rng = np.random.default_rng(P + k)
     i32 = dict(dtype=torch.int32, device="cuda")
     tags = torch.full((B, P), -1, **i32)
-    stamp = torch.zeros((B, P), **i32)
-    clock = torch.zeros((B,), **i32)
+    order = torch.arange(P, **i32).repeat(B, 1)
     out = {n: torch.empty((B, k), **i32) for n in ("src", "mids", "mpos", "victim")}
     install = torch.empty((B, k), dtype=torch.uint8, device="cuda")
     mcnt = torch.empty((B,), **i32)
@@ -51,7 +51,7 @@ def test_plan_lru_matches_oracle_step_by_step(d, B, P, k, ctx, steps):
             new = rng.choice(np.setdiff1d(np.arange(ctx), keep), k - keep.size, replace=False)
             base[b] = np.sort(np.concatenate([keep, new]))
             ids[b] = base[b]
-        assert d.dsa_plan_lru(torch.from_numpy(ids).cuda(), lens, B, k, tags, stamp, clock, P,
+        assert d.dsa_plan_lru(torch.from_numpy(ids).cuda(), lens, B, k, tags, order, P,
                               out["src"], out["mids"], out["mpos"], out["victim"], install, mcnt,
                               mrows, err) == 0
         assert d.ts_read_error(err) == 0
@@ -65,10 +65,9 @@ def test_plan_lru_matches_oracle_step_by_step(d, B, P, k, ctx, steps):
             assert np.array_equal(out["victim"][b, :M].cpu().numpy(), plan.victim), (step, b)
             assert np.array_equal(install[b, :M].cpu().numpy(), plan.install_code)
             assert np.array_equal(tags[b].cpu().numpy(), np.asarray(pools[b].tags))
-            occupied = np.asarray(pools[b].tags) >= 0
-            st = stamp[b].cpu().numpy().view(np.uint32)
-            assert np.array_equal(st[occupied], np.asarray(pools[b].last_use)[occupied])
-            assert int(clock[b]) == pools[b].clock
+            want = sorted(range(P), key=lambda s: (pools[b].tags[s] >= 0,
+                                                   pools[b].last_use[s], s))
+            assert np.array_equal(order[b].cpu().numpy(), want), (step, b)
 
 
 def test_plan_lru_flags_unsorted_ids(d):
@@ -78,16 +77,47 @@ def test_plan_lru_flags_unsorted_ids(d):
     z = lambda *s: torch.zeros(s, **i32)
     err = z(1)
     assert d.dsa_plan_lru(ids, torch.tensor([100], **i32), B, k, torch.full((B, P), -1, **i32),
-                          z(B, P), z(B), P, z(B, k), z(B, k), z(B, k), z(B, k),
+                          torch.arange(P, **i32)[None], P, z(B, k), z(B, k), z(B, k), z(B, k),
                           torch.zeros((B, k), dtype=torch.uint8, device="cuda"), z(B), z(B),
                           err) == 0
     assert d.ts_read_error(err) & 0x80
     from decode_dsa_kv_gb300 import _abi
     # k above the pool size is refused on the host
-    assert d.dsa_plan_lru(ids, torch.tensor([100], **i32), B, k, z(B, 2), z(B, 2), z(B), 2,
-                          z(B, k), z(B, k), z(B, k), z(B, k),
+    assert d.dsa_plan_lru(ids, torch.tensor([100], **i32), B, k, z(B, 2), z(B, 2), 2, z(B, k),
+                          z(B, k), z(B, k), z(B, k),
                           torch.zeros((B, k), dtype=torch.uint8, device="cuda"), z(B), z(B),
                           err) == _abi.TS_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("fault", ["order_repeats_a_slot", "order_out_of_range", "tag_twice"])
+def test_plan_lru_flags_corrupt_metadata(d, fault):
+    """A recency order that is not a permutation of the slots, or a token held
+    by two slots, is reported; the plan installs nothing and leaves the order
+    as it was."""
+    i32 = dict(dtype=torch.int32, device="cuda")
+    B, P, k = 1, 64, 4
+    ids = torch.tensor([[3, 5, 9, 11]], **i32)
+    tags = torch.full((B, P), -1, **i32)
+    tags[0, 10] = 5
+    order = torch.arange(P, **i32)[None].clone()
+    if fault == "order_repeats_a_slot":
+        order[0, 7] = 6
+    elif fault == "order_out_of_range":
+        order[0, 7] = P
+    else:
+        tags[0, 20] = 5
+    before = order.clone()
+    z = lambda *s: torch.zeros(s, **i32)
+    victim = torch.full((B, k), 77, **i32)
+    install = torch.ones((B, k), dtype=torch.uint8, device="cuda")
+    err = z(1)
+    mcnt = z(B)
+    assert d.dsa_plan_lru(ids, torch.tensor([100], **i32), B, k, tags, order, P, z(B, k), z(B, k),
+                          z(B, k), victim, install, mcnt, z(B), err) == 0
+    assert d.ts_read_error(err) & 0x04
+    assert torch.equal(order, before)
+    M = int(mcnt[0])
+    assert M == 3 and int(install[0, :M].sum()) == 0
 
 
 @pytest.mark.parametrize("layout", ["selection", "staged"])
