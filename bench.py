@@ -86,6 +86,10 @@ def parse(argv=None):
                     help="staged: the attention reads its rows straight from the pool (only "
                          "the misses are staged in HBM); selection: every row is gathered "
                          "into a selection buffer first")
+    ap.add_argument("--layer-waits", action="store_true",
+                    help="staged layout: each layer's attention waits for the whole layer's "
+                         "rows (default: streamed, each attention CTA waits for its own "
+                         "request's rows while the gather runs)")
     ap.add_argument("--mtp", type=int, default=0, choices=(0, 1, 2, 3),
                     help="MTP draft steps whose queries are folded into the heads "
                          "(the step attends (1 + N) x H query rows over one selection)")
@@ -366,6 +370,8 @@ def config_of(args, w: wl.Workload, world: int) -> dict:
             "ctx": w.ctx, "sets": w.S, "ways": w.W, "heads": w.H,
             "mtp_draft_steps": args.mtp, "pool_policy": args.policy,
             "layout": args.layout,
+            "attention_start": ("layer waits" if args.layer_waits or args.layout != "staged"
+                                else "streamed per request"),
             "requests_per_gpu": w.B,
             "score_stream": "forward only: every step run (settle, warm-up, timed, end to end) "
                             "is the next step of the workload's score process; none is replayed",
@@ -591,7 +597,8 @@ def run_native(args, w, rank, world, local, overrides):
     del touch
     staged = args.layout == "staged" and args.policy != "reuse"
     g = dk.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host,
-                       policy=args.policy, layout="staged" if staged else "selection")
+                       policy=args.policy, layout="staged" if staged else "selection",
+                       streamed=not args.layer_waits)
     peaks = measured_peaks()
     link = link_peak_gbs(torch, link_buf)
 

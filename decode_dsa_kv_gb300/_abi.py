@@ -101,6 +101,7 @@ class DsaGroup(ctypes.Structure):
         ("prev_sel", _P),
         ("layout", _I),
         ("lru_order", _P),
+        ("arrived", _P),
     ]
 
 for _name, (_res, _args) in _SIGS.items():

@@ -201,6 +201,25 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Bounded wait, from one thread, until a device word written by another
+// running kernel reaches `target` (an acquire: what the writer stored before
+// its release is visible after). Gives up, returning false, when *stop
+// becomes non-zero or after `limit_ns` nanoseconds of the global timer.
+__device__ __forceinline__ bool wait_word_geq(const uint32_t* word, uint32_t target,
+                                              const uint32_t* stop, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t nap = 32;
+  for (;;) {
+    uint32_t v, s;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(word) : "memory");
+    if (v >= target) return true;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(s) : "l"(stop) : "memory");
+    if (s != 0 || globaltimer_ns() - t0 > limit_ns) return false;
+    __nanosleep(nap);
+    if (nap < 512) nap *= 2;
+  }
+}
+
 // Wait for a phase with only a time limit (teardown after an abort).
 __device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity,
                                                 uint64_t limit_ns) {

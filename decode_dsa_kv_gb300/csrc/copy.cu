@@ -48,10 +48,11 @@ constexpr int kPipeAhead = kPipeSlots - kPipeLag;  // loads in flight per warp
 constexpr int kPipeRetire = 4;  // stores after a layer's last before it counts out
 constexpr int kPipeWarps = 16;                     // warps per gather CTA
 constexpr uint64_t kBulkWaitNs = 100000000ull;     // 100 ms
-constexpr size_t kPipeWarpBytes = kPipeSlots * (DSA_ROW_BYTES + 24);  // ring, barriers, targets
+constexpr int kTagRing = 32;  // stored rows' request tags, by row number (see RowPipe::confirm)
+constexpr int kNoTag = 0xFFFF;  // a row counted into no request's arrivals
+constexpr size_t kPipeWarpBytes =
+    kPipeSlots * (DSA_ROW_BYTES + 24) + kTagRing * 2;  // ring, barriers, targets, tags
 constexpr size_t kPipeSmemBytes = kPipeWarps * kPipeWarpBytes;
-// most requests whose miss-count prefix fits beside the pipes (dynamic hand-out)
-constexpr int kMaxDynamicB = 1024;
 // misses per ticket: a layer's completion waits for the last batch of it any
 // warp took, so smaller batches let the layers finish closer to their share
 constexpr int kTicketRows = 16;
@@ -73,9 +74,15 @@ struct RowPipe {
   uint32_t *count, *done, seq;
   uint32_t* ticket;  // dynamic miss hand-out: reset by the last warp of the last layer
   int last;
+  // per-request arrival counts (streamed attention): row i's counter index
+  // (layer * B + request, or kNoTag) sits in tags[i % kTagRing] from its
+  // push until it is confirmed stored; rows below `confirmed` are counted
+  uint32_t* arrived;
+  uint16_t* tags;
+  uint32_t confirmed;
 
   __device__ void init(uint8_t* warp_smem, int nw_, uint32_t* count_, uint32_t* done_,
-                       uint32_t seq_, uint32_t* ticket_, int last_) {
+                       uint32_t seq_, uint32_t* ticket_, int last_, uint32_t* arrived_) {
     ring = warp_smem;
     bars = reinterpret_cast<uint64_t*>(warp_smem + kPipeSlots * DSA_ROW_BYTES);
     to = reinterpret_cast<uint4**>(bars + kPipeSlots);
@@ -90,6 +97,9 @@ struct RowPipe {
     seq = seq_;
     ticket = ticket_;
     last = last_;
+    arrived = arrived_;
+    tags = reinterpret_cast<uint16_t*>(to2 + kPipeSlots);
+    confirmed = 0;
     for (int s = 0; s < kPipeSlots; ++s) mbar_init(bars + s, 1);
     mbar_fence_init();
   }
@@ -107,6 +117,27 @@ struct RowPipe {
       atomicExch(done + l, seq);
     }
   }
+  // Rows below n are stored (the caller waited for their store groups):
+  // add them to their requests' arrival counts, one atomic per run of rows
+  // of one request, after making the bulk stores visible (a release).
+  __device__ void confirm(uint32_t n) {
+    if (!arrived || failed || n <= confirmed) return;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
+    int tag = tags[confirmed % kTagRing];
+    uint32_t run = 0;
+    for (uint32_t i = confirmed; i < n; ++i) {
+      const int t = tags[i % kTagRing];
+      if (t != tag) {
+        if (tag != kNoTag) atomicAdd(arrived + tag, run);
+        tag = t;
+        run = 0;
+      }
+      ++run;
+    }
+    if (tag != kNoTag) atomicAdd(arrived + tag, run);
+    confirmed = n;
+  }
   // Store the oldest row in flight (or, after a failure, only wait for it).
   __device__ void store_one() {
     const uint32_t i = stored++;
@@ -122,11 +153,16 @@ struct RowPipe {
       // every store group but the last kPipeRetire (all after pend_end) done
       if (failed) bulk_wait_all();
       else bulk_wait<kPipeRetire>();
+      confirm(stored - kPipeRetire);
       signal(pend);
       pend = -1;
+    } else if (arrived && (stored & 3u) == 0 && stored > kPipeRetire) {
+      // every fourth store: the rows whose stores are done are counted
+      bulk_wait<kPipeRetire>();
+      confirm(stored - kPipeRetire);
     }
   }
-  __device__ void push(const uint4* from, uint4* dst, uint4* dst2 = nullptr) {
+  __device__ void push(const uint4* from, uint4* dst, uint4* dst2 = nullptr, int tag = kNoTag) {
     if (failed) return;
     while (stored + kPipeAhead <= issued) store_one();
     if (failed) return;
@@ -134,6 +170,7 @@ struct RowPipe {
     const int s = static_cast<int>(issued % kPipeSlots);
     to[s] = dst;
     to2[s] = dst2;
+    tags[issued % kTagRing] = static_cast<uint16_t>(tag);
     mbar_expect_tx(bars + s, DSA_ROW_BYTES);
     bulk_load(ring + s * DSA_ROW_BYTES, from, DSA_ROW_BYTES, bars + s);
     ++issued;
@@ -145,6 +182,7 @@ struct RowPipe {
       while (stored < issued) store_one();
       if (pend >= 0) {
         bulk_wait_all();
+        confirm(stored);
         signal(pend);
       }
     }
@@ -155,6 +193,7 @@ struct RowPipe {
   __device__ void finish() {
     while (stored < issued) store_one();
     bulk_wait_all();
+    confirm(stored);
     if (pend >= 0) signal(pend);
     pend = -1;
   }
@@ -197,7 +236,7 @@ __device__ __forceinline__ bool miss_targets(const GatherLayer& L, const int32_t
 
 // Lane 0 pushes the rows of the lanes in `mask` through the warp's pipe.
 __device__ __forceinline__ void push_lanes(uint32_t mask, const uint4* from, uint4* to, uint4* to2,
-                                           int lane, RowPipe& pipe) {
+                                           int lane, RowPipe& pipe, int tag = kNoTag) {
   while (mask) {
     const int q = __ffs(mask) - 1;
     mask &= mask - 1;
@@ -206,7 +245,8 @@ __device__ __forceinline__ void push_lanes(uint32_t mask, const uint4* from, uin
     uint4* t = reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(to), q));
     uint4* t2 =
         reinterpret_cast<uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(to2), q));
-    if (lane == 0) pipe.push(f, t, t2);
+    const int tg = __shfl_sync(0xffffffffu, tag, q);
+    if (lane == 0) pipe.push(f, t, t2, tg);
     __syncwarp();
   }
 }
@@ -296,6 +336,7 @@ __device__ __forceinline__ void gather_misses_dynamic(
     uint4* to = nullptr;
     uint4* to2 = nullptr;
     bool valid = false;
+    int tag = kNoTag;
     if (lane < kTicketRows && g < total) {
       int lo = 0, hi = B;  // the request b with prefix[b] <= g < prefix[b + 1]
       while (hi - lo > 1) {
@@ -305,8 +346,12 @@ __device__ __forceinline__ void gather_misses_dynamic(
       }
       valid = miss_targets(L, miss_ids, miss_pos, victim, install, lo, g - prefix[lo], k, P,
                            sel_rows, pool_rows, ctx_stride, ctx_len, from, to, to2, bad);
+      tag = l * B + lo;
+      // a corrupt entry moves no row but still counts as arrived (its
+      // request's attention then runs on, with the error reported)
+      if (!valid && pipe.arrived) atomicAdd(pipe.arrived + tag, 1u);
     }
-    push_lanes(__ballot_sync(0xffffffffu, valid), from, to, to2, lane, pipe);
+    push_lanes(__ballot_sync(0xffffffffu, valid), from, to, to2, lane, pipe, tag);
     t = __shfl_sync(0xffffffffu, next, 0);
   }
   for (; cur < layers - 1; ++cur) {  // the finish counts out of the last layer
@@ -393,7 +438,8 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
     const uint4* __restrict__ host, int64_t ctx_stride, const int32_t* __restrict__ ctx_len,
     uint4* __restrict__ sel, int layers, int64_t pool_stride, int64_t host_stride,
     int64_t sel_stride, uint32_t* __restrict__ done, uint32_t* __restrict__ count, uint32_t seq,
-    int miss_ctas, int sel_rows, int pool_rows, uint32_t* ticket, int32_t* err) {
+    int miss_ctas, int sel_rows, int pool_rows, uint32_t* ticket, uint32_t* arrived,
+    int32_t* err) {
   extern __shared__ __align__(128) uint8_t gather_smem[];
   __shared__ int scan_scratch[40];
   const int lane = threadIdx.x & 31;
@@ -404,9 +450,16 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
   const int w = cta * kPipeWarps + wc;
   const int nrole = (miss_cta ? miss_ctas : static_cast<int>(gridDim.x) - miss_ctas) * kPipeWarps;
   int bad = 0;
+  if (arrived && threadIdx.x == 0) {
+    // every CTA of the launch is running once the last one counts in: the
+    // attention that waits for rows inside its kernel may start then
+    uint32_t* started = arrived + size_t(layers) * B;
+    if (atomicAdd(started, 1u) == gridDim.x - 1) atomicExch(started + 1, seq);
+  }
   RowPipe pipe;
   if (lane == 0)
-    pipe.init(gather_smem + wc * kPipeWarpBytes, nw, count, done, seq, ticket, layers - 1);
+    pipe.init(gather_smem + wc * kPipeWarpBytes, nw, count, done, seq, ticket, layers - 1,
+              arrived);
   __syncwarp();
   if (miss_cta && ticket) {
     // the requests' exclusive miss-count prefix, for the dynamic hand-out
@@ -442,7 +495,11 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
   }
   if (lane == 0) {
     pipe.finish();
-    if (pipe.failed) bad |= TS_DEVERR_TIMEOUT;
+    if (pipe.failed) {
+      bad |= TS_DEVERR_TIMEOUT;
+      // the attention waiting for this launch's rows stops waiting
+      if (arrived) atomicExch(arrived + size_t(layers) * B + 2, 1u);
+    }
   }
   bad = __reduce_or_sync(0xffffffffu, bad);  // lookups are per lane
   if (bad && lane == 0) report(err, bad);
@@ -572,7 +629,7 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
                          int layers, size_t pool_layer_bytes, size_t host_layer_bytes,
                          size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq,
                          const int32_t* victim, const uint8_t* install, bool staged,
-                         uint32_t* ticket) {
+                         uint32_t* ticket, uint32_t* arrived) {
   // At the decode_batch shape (32 x 2048 rows a layer, 9.7 GB of host KV):
   // kMissCtas + kHitCtas CTAs (24 SMs): the misses' share of them reads at
   // the host link's rate (measured alone: 8 SMs of bulk copies reach the
@@ -588,6 +645,8 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
   // in layer order, which needs the requests' miss-count prefix in shared
   // memory beside the pipes.
   const bool dynamic = ticket && count && B <= kMaxDynamicB;
+  // per-request arrival counts come from the dynamic hand-out's row tags
+  if (arrived && !(dynamic && staged && gather_streams(B, layers))) return TS_ERR_INVALID_ARG;
   const size_t smem = kPipeSmemBytes + (dynamic ? (size_t(B) + 1) * 4 : 0);
   static std::atomic<uint64_t> smem_set{0};
   if (!raise_smem_limit(reinterpret_cast<const void*>(gather_kernel),
@@ -609,7 +668,7 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
       static_cast<const uint4*>(host_l), ctx_stride, ctx_len, sel, layers,
       int64_t(pool_layer_bytes / 16), int64_t(host_layer_bytes / 16),
       int64_t(sel_layer_bytes / 16), done, count, seq, grid.miss, sel_rows, pool_rows,
-      dynamic ? ticket : nullptr, err);
+      dynamic ? ticket : nullptr, arrived, err);
   return launch_status();
 }
 
@@ -679,7 +738,7 @@ extern "C" ts_status dsa_gather_kv(const int32_t* src_map, const int32_t* miss_i
   if (st != TS_OK) return st;
   return dsakv::gather_enqueue(src_map, miss_ids, miss_pos, miss_count, miss_rows, B, k, pool_l,
                                P, host_l, ctx_stride, ctx_len, sel_l, err, stream, 1, 0, 0, 0,
-                               nullptr, nullptr, 0, nullptr, nullptr, false, nullptr);
+                               nullptr, nullptr, 0, nullptr, nullptr, false, nullptr, nullptr);
 }
 
 extern "C" ts_status dsa_stage_misses(const int32_t* miss_ids, const int32_t* miss_pos,
@@ -693,7 +752,7 @@ extern "C" ts_status dsa_stage_misses(const int32_t* miss_ids, const int32_t* mi
   if ((victim == nullptr) != (install == nullptr)) return TS_ERR_INVALID_ARG;
   return dsakv::gather_enqueue(nullptr, miss_ids, miss_pos, miss_count, nullptr, B, k, pool_l, P,
                                host_l, ctx_stride, ctx_len, nullptr, err, stream, 1, 0, 0, 0,
-                               nullptr, nullptr, 0, victim, install, true, nullptr);
+                               nullptr, nullptr, 0, victim, install, true, nullptr, nullptr);
 }
 
 extern "C" ts_status dsa_refill_pool(const int32_t* miss_ids, const int32_t* miss_pos,

@@ -58,6 +58,11 @@ ts_status gather_check(const int32_t* src_map, const int32_t* miss_ids, const in
 // out to the warps dynamically, layer after layer. With `victim` and `install` (dsa_plan's) given,
 // the misses with install code 1 are also written into their victim slots
 // of the pool as they arrive (the refill then needs only min_install = 2).
+// With `arrived` (staged, dynamic and gather_streams(B, layers) only:
+// uint32 [layers * B + 3], zero before the launch) the kernel adds every
+// stored row to arrived[l * B + b], counts its CTAs in word layers * B,
+// writes seq into word layers * B + 1 once every CTA runs, and sets word
+// layers * B + 2 if it gives up (sfa_pool_enqueue's `arrived` waits on these).
 ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const int32_t* miss_pos,
                          const int32_t* miss_count, const int32_t* miss_rows, int B, int k,
                          const void* pool_l, int P, const void* host_l, int64_t ctx_stride,
@@ -65,7 +70,16 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
                          int layers, size_t pool_layer_bytes, size_t host_layer_bytes,
                          size_t sel_layer_bytes, uint32_t* done, uint32_t* count, uint32_t seq,
                          const int32_t* victim, const uint8_t* install, bool staged,
-                         uint32_t* ticket);
+                         uint32_t* ticket, uint32_t* arrived);
+
+// most requests whose miss-count prefix fits beside the gather's pipes (its
+// dynamic hand-out)
+constexpr int kMaxDynamicB = 1024;
+// whether a group of B requests x `layers` layers can count arrivals per
+// request (the dynamic hand-out, and 16-bit row tags layer * B + b)
+inline bool gather_streams(int B, int layers) {
+  return B <= kMaxDynamicB && int64_t(layers) * B < 0xFFFF;
+}
 
 // The staged layout: a layer's pool tensor is [B][P + k][576]; rows P .. P+k-1
 // of a request hold the step's missed rows at their first positions, so the
@@ -107,6 +121,7 @@ ts_status sfa_pool_enqueue(const void* q, const void* pool_l, int P, const int32
                            const int32_t* miss_ids, const int32_t* miss_pos,
                            const int32_t* miss_count, const int32_t* miss_rows, int B, int H,
                            int k, float scale, void* out, float* lse, void* ws, int32_t* err,
-                           cudaStream_t stream);
+                           cudaStream_t stream, const uint32_t* arrived = nullptr,
+                           const uint32_t* gather_failed = nullptr);
 
 }  // namespace dsakv

@@ -133,6 +133,11 @@ struct PoolSrc {
   const uint8_t* rows;  // the pool tensor, [B][prow][576] bf16
   const uint8_t* q;     // the queries, [B][H][576] bf16
   int P, prow;
+  // streamed: request b's loaders start once arrived[b] reaches its miss
+  // count (the gather still running counts the staged rows in); they give up
+  // when *gather_failed is set. Null: the rows are all in at launch.
+  const uint32_t* arrived;
+  const uint32_t* gather_failed;
 };
 
 // 16-byte copies global -> shared that write shared memory as they land
@@ -267,6 +272,14 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
       ridx[p] = static_cast<uint16_t>(pool_row(ps, b, k, min(j0 + p, k - 1), M, repeats, bad));
     bad = __reduce_or_sync(0xffffffffu, bad);
     if (bad && lane == 0) report(err, bad);
+    // streamed: the request's staged rows of this layer are all stored (the
+    // other loaders' copies follow the barrier, which orders them after this
+    // thread's acquire)
+    if (ps.arrived && lt == 0 &&
+        !wait_word_geq(ps.arrived + b, static_cast<uint32_t>(M), ps.gather_failed, wait_ns)) {
+      report(err, TS_DEVERR_TIMEOUT);
+      *abort = 1;
+    }
     loader_sync();
     const uint8_t* prow0 = ps.rows + int64_t(b) * ps.prow * DSA_ROW_BYTES;
     auto row_src = [&](int p) { return prow0 + int64_t(ridx[p]) * DSA_ROW_BYTES; };
@@ -276,7 +289,7 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
                    : "memory");
     };
-    bool ok = true;
+    bool ok = *abort == 0;
     for (int it = 0; it < kScoreLoads && ok; ++it) {
       const int s = it % kSSlots;
       if (it >= kSSlots) ok = warp_wait(&bars->empty[s], ((it / kSSlots) - 1) & 1, abort, wait_ns);
@@ -710,9 +723,12 @@ ts_status sfa_pool_enqueue(const void* q, const void* pool_l, int P, const int32
                            const int32_t* miss_ids, const int32_t* miss_pos,
                            const int32_t* miss_count, const int32_t* miss_rows, int B, int H,
                            int k, float scale, void* out, float* lse, void* ws, int32_t* err,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const uint32_t* arrived,
+                           const uint32_t* gather_failed) {
+  if (arrived && !gather_failed) return TS_ERR_INVALID_ARG;
   const PoolSrc ps{src_map, miss_ids, miss_pos, miss_count, miss_rows,
-                   static_cast<const uint8_t*>(pool_l), static_cast<const uint8_t*>(q), P, P + k};
+                   static_cast<const uint8_t*>(pool_l), static_cast<const uint8_t*>(q), P, P + k,
+                   arrived, gather_failed};
   return launch_attention<true>(q, pool_l, ps, B, H, k, scale, out, lse, ws, err, stream);
 }
 

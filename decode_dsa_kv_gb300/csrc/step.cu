@@ -116,7 +116,11 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   if (reuse && (ids || !g.prev_ids || !g.prev_sel)) return TS_ERR_INVALID_ARG;
   if (g.S <= 0 || g.W <= 0 || int64_t(g.S) * g.W > (1 << 24)) return TS_ERR_INVALID_ARG;
   if (!g.sync || (reinterpret_cast<uintptr_t>(g.sync) & 3u) != 0) return TS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(g.arrived) & 3u) != 0) return TS_ERR_INVALID_ARG;
   if (!aligned16(q)) return TS_ERR_INVALID_ARG;
+  // streamed attention: each layer's attention CTAs wait inside the kernel
+  // for their own request's staged rows, counted by the running gather
+  const bool streamed = staged && g.arrived && gather_streams(g.B, L);
   // with reuse, the "pool" is the previous step's selection: k rows per request
   const int P = reuse ? g.k : g.S * g.W;
   Layers lb = layer_bytes(g);
@@ -167,6 +171,10 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   uint32_t* attended = g.sync + kGathered + 2 * L;  // staged layout: a layer's attention is done
   uint32_t* ticket = g.sync + kGathered + 3 * L;    // the gather's miss hand-out
   uint32_t* qcopied = ticket + 1;                   // host I/O: the queries are in
+  // streamed: per (layer, request) arrival counts, then the gather's started
+  // CTAs, the started flag and the gave-up flag
+  uint32_t* started = streamed ? g.arrived + size_t(L) * g.B + 1 : nullptr;
+  uint32_t* gave_up = streamed ? started + 1 : nullptr;
 
   // with host I/O: the copies' sizes; this step's half of the query staging
   const size_t scores_bytes = size_t(g.B) * size_t(g.ctx_stride) * 4;
@@ -186,6 +194,11 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
                       g.err, m) == TS_OK &&
          rec(0, 1, m);
   }
+  // streamed: the counts start from zero (the previous step's attention,
+  // their last reader, ran earlier on this stream; this step's gather waits
+  // for the plan, after this)
+  if (streamed)
+    ok = ok && cudaMemsetAsync(g.arrived, 0, (size_t(L) * g.B + 3) * 4, m) == cudaSuccess;
   ok = ok && wait_for(m, refilled, seq - 1) && rec(1, 0, m) &&
        (reuse ? plan_reuse_enqueue(plan_ids, g.prev_ids, g.ctx_len, g.B, g.k, g.src_map,
                                    g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.err, m)
@@ -204,7 +217,8 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
        gather_enqueue(g.src_map, g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.k, pool,
                       P, g.host_kv, g.ctx_stride, g.ctx_len, g.sel, g.err, gs, L, lb.pool,
                       lb.host, lb.sel, gathered, counts, seq, reuse ? nullptr : g.victim,
-                      reuse ? nullptr : g.install, staged, ticket) == TS_OK &&
+                      reuse ? nullptr : g.install, staged, ticket,
+                      streamed ? g.arrived : nullptr) == TS_OK &&
        rec(2, 1, gs);
   // with host I/O the queries cross on the side stream beside the top-k and
   // the plan, into this step's staging half; that half's last reader, the
@@ -217,13 +231,17 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   // side stream; the last refill also updates the metadata. The staged
   // attention reads hit rows from the pool itself, so the layer's refill
   // (which overwrites slots read as hits) waits for that attention
+  // Streamed, the first layer's attention launches once every gather CTA
+  // runs (so the gather that its CTAs wait for never waits for SMs they
+  // hold) and the later layers follow it on the stream.
   for (int l = 0; ok && l < L; ++l) {
     float* lse_l = g.lse ? at(g.lse, l, lb.lse) : nullptr;
-    ok = wait_for(m, gathered + l, seq) && (!io || l > 0 || wait_for(m, qcopied, seq)) &&
-         rec(3 + l, 0, m) &&
+    ok = (streamed ? (l > 0 || wait_for(m, started, seq)) : wait_for(m, gathered + l, seq)) &&
+         (!io || l > 0 || wait_for(m, qcopied, seq)) && rec(3 + l, 0, m) &&
          (staged ? sfa_pool_enqueue(at(q, l, lb.q), at(g.pool, l, lb.pool), P, g.src_map,
                                     g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.H,
-                                    g.k, g.scale, at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m)
+                                    g.k, g.scale, at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m,
+                                    streamed ? g.arrived + size_t(l) * g.B : nullptr, gave_up)
                  : sfa_enqueue(at(q, l, lb.q), at(g.sel, l, lb.sel), g.B, g.H, g.k, g.scale,
                                at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m)) == TS_OK &&
          rec(3 + l, 1, m) && (!staged || signal(m, attended + l, seq)) &&
@@ -278,6 +296,10 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
         cudaStreamWaitEvent(side, ev[i], 0);
     for (int i = 0; i < kGathered + L; ++i) signal(side, g.sync + i, seq);
     for (int i = 0; staged && i < L; ++i) signal(side, attended + i, seq);
+    if (streamed) {  // and no attention CTA keeps waiting for rows
+      signal(side, started, seq);
+      signal(side, gave_up, seq);
+    }
     if (io) signal(side, qcopied, seq);
     for (int i = 0; i < 2; ++i)
       if (ev[i]) cudaEventDestroy(ev[i]);

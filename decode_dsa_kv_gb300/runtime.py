@@ -185,12 +185,15 @@ class DecodeGroup:
     layout "selection": every layer's rows are gathered into `sel`, which the
     attention reads; layout "staged" (FIFO or LRU): the attention reads its rows
     straight from the pool, which then holds P + k rows per request (rows P..
-    stage the step's misses at their first positions) and `sel` is None."""
+    stage the step's misses at their first positions) and `sel` is None.
+    With `streamed` (staged only; B <= 1024) each layer's attention starts
+    while the gather runs, every CTA waiting for its own request's rows;
+    otherwise each layer's attention waits for the whole layer."""
 
     def __init__(self, B: int, layers: int, k: int, S: int, W: int, H: int,
                  ctx_len, ctx_stride: int, host: HostKV, scale: float | None = None,
                  device: str = "cuda", max_ctx: int | None = None, policy: str = "fifo",
-                 layout: str = "selection"):
+                 layout: str = "selection", streamed: bool = True):
         if policy not in ("fifo", "reuse", "lru"):
             raise ValueError(policy)
         if layout not in ("selection", "staged") or (layout == "staged" and policy == "reuse"):
@@ -253,6 +256,10 @@ class DecodeGroup:
         # cross-stream signals: device words written and waited on by the
         # streams themselves (zero before the first step)
         self.sync = torch.zeros((4 + 3 * layers,), **i32)
+        # staged layout: per (layer, request) arrival counts of the gather, so
+        # that each attention CTA starts once its own request's rows are in
+        self.arrived = (torch.zeros((layers * B + 3,), **i32)
+                        if layout == "staged" and streamed else None)
         # device staging of dsa_group_step_host (made on first use)
         self._io_scores = None
         self._io_q = None
@@ -284,6 +291,7 @@ class DecodeGroup:
         d.topk_ws, d.topk_ws_bytes = self.topk_ws.data_ptr(), self.topk_ws_bytes
         d.sfa_ws, d.sfa_ws_bytes = self.sfa_ws.data_ptr(), self.sfa_ws_bytes
         d.err = self.err.data_ptr()
+        d.arrived = 0 if self.arrived is None else self.arrived.data_ptr()
         if self.policy == "lru":
             d.policy = abi.DSA_POLICY_LRU
             d.lru_order = self.lru_order.data_ptr()

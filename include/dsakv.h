@@ -494,6 +494,17 @@ typedef struct {
    * are not used and no refill runs (every install is written by the gather
    * as its row arrives). */
   int32_t* lru_order;
+  /* DSA_LAYOUT_STAGED only, optional: uint32 [layers * B + 3] device words
+   * (zeroed by each step itself). When given (and B <= 1024, layers * B <
+   * 65535), each layer's attention starts as soon as the gather is running
+   * and each of its CTAs waits, inside the kernel, for its own request's
+   * missed rows of that layer (the gather counts every stored row into
+   * arrived[l * B + b]); words layers * B .. + 2 count the gather's CTAs that
+   * started, hold the step number once all have, and flag a gather that gave
+   * up. The attention of a request then overlaps the gather of the requests
+   * after it, and only the last requests' attention follows the gather's
+   * end. NULL: each layer's attention waits for the whole layer's rows. */
+  uint32_t* arrived;
 } dsa_group;
 
 #define DSA_POLICY_FIFO 0

@@ -292,3 +292,34 @@ def test_staged_large_batch_full_size(d):
 def test_staged_decode_batch_full_size(d):
     run_staged_steps(d, wl.DECODE_BATCH, 3, sample=[0, 31], sfa_layers=[0, 3],
                      sfa_heads=slice(0, 128, 9))
+
+
+@pytest.mark.parametrize("w,steps", [(wl.LARGE_BATCH, 6), (wl.DECODE_BATCH, 4)])
+def test_streamed_attention_equals_layer_waits(d, w, steps):
+    """Streamed attention (each CTA waits inside the kernel for its own
+    request's staged rows while the gather still runs) against attention that
+    waits for the whole layer: the same outputs and pool, bit for bit, step
+    after step at full size (the streamed group is the one the whole-step
+    tests above check against the oracle)."""
+    lens = wl.ctx_lens(w)
+    host = d.HostKV(w.layers, w.B, w.ctx_stride)
+    wl.fill_host_kv(w, host.array)
+    gs = [d.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host,
+                        layout="staged", streamed=s) for s in (True, False)]
+    assert gs[0].arrived is not None and gs[1].arrived is None
+    stream = wl.ScoreStream(w)
+    for step in range(steps):
+        scores = torch.from_numpy(stream.next()).cuda()
+        q = torch.from_numpy(wl.queries(w, step).view(np.int16)).cuda()
+        for g in gs:
+            g.step(scores, q)
+        for g in gs:
+            assert g.synchronize() == 0, step
+        assert torch.equal(gs[0].out.view(torch.int16), gs[1].out.view(torch.int16)), step
+        assert torch.equal(gs[0].src_map, gs[1].src_map), step
+        for l in range(w.layers):
+            assert torch.equal(gs[0].pool[l], gs[1].pool[l]), (step, l)
+        # every layer's arrival counts reached the requests' miss counts
+        arr = gs[0].arrived[:w.layers * w.B].view(w.layers, w.B)
+        assert torch.equal(arr, gs[0].miss_count[None].expand(w.layers, -1)), step
+    host.close()
