@@ -48,15 +48,38 @@ constexpr int kPipeAhead = kPipeSlots - kPipeLag;  // loads in flight per warp
 constexpr int kPipeRetire = 4;  // stores after a layer's last before it counts out
 constexpr int kPipeWarps = 16;                     // warps per gather CTA
 constexpr uint64_t kBulkWaitNs = 100000000ull;     // 100 ms
-constexpr int kTagRing = 32;  // stored rows' request tags, by row number (see RowPipe::confirm)
+constexpr int kTagRing = 48;  // pushed rows' request tags, by row number (see RowPipe::publish)
 constexpr int kNoTag = 0xFFFF;  // a row counted into no request's arrivals
-constexpr size_t kPipeWarpBytes =
-    kPipeSlots * (DSA_ROW_BYTES + 24) + kTagRing * 2;  // ring, barriers, targets, tags
+// A warp's shared memory: the ring, its barriers, the rows' targets, the
+// rows' tags, then the words it shares with the CTA's counting warp.
+constexpr size_t kPipeTagOffset = kPipeSlots * (DSA_ROW_BYTES + 24);
+constexpr size_t kPipeWordsOffset = kPipeTagOffset + kTagRing * 2;
+constexpr size_t kPipeWarpBytes = kPipeWordsOffset + 16;
+constexpr uint64_t kCountIdleNs = 1000000000ull;  // the counting warp gives up after 1 s idle
 constexpr size_t kPipeSmemBytes = kPipeWarps * kPipeWarpBytes;
 // misses per ticket: a layer's completion waits for the last batch of it any
 // warp took, so smaller batches let the layers finish closer to their share
 constexpr int kTicketRows = 16;
-static_assert(kPipeSmemBytes + (kMaxDynamicB + 1) * 4 + 40 * 4 <= 227 * 1024, "shared memory");
+// (the kernel's static shared memory, the scan scratch and what the compiler
+// adds, is counted as 256 bytes)
+static_assert(kPipeSmemBytes + (kMaxDynamicB + 1) * 4 + 256 <= 227 * 1024, "shared memory");
+static_assert(kPipeWarpBytes % 16 == 0, "rings start on 16-byte boundaries");
+constexpr int kGatherThreads = (kPipeWarps + 1) * 32;  // the pipes and the counting warp
+
+// Words a pipe warp shares with its CTA's counting warp (streamed attention):
+// rows [0, published) of the warp are stored, rows [0, consumed) are counted,
+// finished once the warp has published its last row.
+struct PipeWords {
+  uint32_t published, consumed, finished, pad;
+};
+__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
 
 struct RowPipe {
   uint8_t* ring;
@@ -76,13 +99,17 @@ struct RowPipe {
   int last;
   // per-request arrival counts (streamed attention): row i's counter index
   // (layer * B + request, or kNoTag) sits in tags[i % kTagRing] from its
-  // push until it is confirmed stored; rows below `confirmed` are counted
+  // push until the counting warp has read it; rows below `published` are
+  // stored, which the warp tells the counting warp through `words`
   uint32_t* arrived;
   uint16_t* tags;
-  uint32_t confirmed;
+  PipeWords* words;
+  uint32_t published, consumed;
+  bool self_count;  // the warp releases and counts its rows itself (no counting warp)
 
   __device__ void init(uint8_t* warp_smem, int nw_, uint32_t* count_, uint32_t* done_,
-                       uint32_t seq_, uint32_t* ticket_, int last_, uint32_t* arrived_) {
+                       uint32_t seq_, uint32_t* ticket_, int last_, uint32_t* arrived_,
+                       bool self_count_) {
     ring = warp_smem;
     bars = reinterpret_cast<uint64_t*>(warp_smem + kPipeSlots * DSA_ROW_BYTES);
     to = reinterpret_cast<uint4**>(bars + kPipeSlots);
@@ -98,8 +125,11 @@ struct RowPipe {
     ticket = ticket_;
     last = last_;
     arrived = arrived_;
-    tags = reinterpret_cast<uint16_t*>(to2 + kPipeSlots);
-    confirmed = 0;
+    tags = reinterpret_cast<uint16_t*>(warp_smem + kPipeTagOffset);
+    words = reinterpret_cast<PipeWords*>(warp_smem + kPipeWordsOffset);
+    published = consumed = 0;
+    self_count = self_count_;
+    words->published = words->consumed = words->finished = 0;
     for (int s = 0; s < kPipeSlots; ++s) mbar_init(bars + s, 1);
     mbar_fence_init();
   }
@@ -118,25 +148,36 @@ struct RowPipe {
     }
   }
   // Rows below n are stored (the caller waited for their store groups):
-  // add them to their requests' arrival counts, one atomic per run of rows
-  // of one request, after making the bulk stores visible (a release).
-  __device__ void confirm(uint32_t n) {
-    if (!arrived || failed || n <= confirmed) return;
+  // make them count. Either this thread releases them at GPU scope and adds
+  // them to their requests' arrival counts itself (self_count), or it tells
+  // the CTA's counting warp, which does (their bulk writes ordered before the
+  // shared word by a CTA-scope release). A GPU-scope fence on an SM whose
+  // warps keep host reads in flight waits microseconds (measured on GB300:
+  // 7 us on average from a pipe thread at 128 x 32,768, 1.9 us at 32 x
+  // 65,536, 30 us from a separate warp at 128 x 32,768); the pipes only
+  // afford it when the launch has reads in flight to spare (see
+  // gather_enqueue).
+  __device__ void publish(uint32_t n) {
+    if (!arrived || failed || n <= published) return;
     asm volatile("fence.proxy.async.global;" ::: "memory");
-    __threadfence();
-    int tag = tags[confirmed % kTagRing];
-    uint32_t run = 0;
-    for (uint32_t i = confirmed; i < n; ++i) {
-      const int t = tags[i % kTagRing];
-      if (t != tag) {
-        if (tag != kNoTag) atomicAdd(arrived + tag, run);
-        tag = t;
-        run = 0;
+    if (self_count) {
+      __threadfence();
+      int tag = tags[published % kTagRing];
+      uint32_t run = 0;
+      for (uint32_t i = published; i < n; ++i) {
+        const int t = tags[i % kTagRing];
+        if (t != tag) {
+          if (tag != kNoTag) atomicAdd(arrived + tag, run);
+          tag = t;
+          run = 0;
+        }
+        ++run;
       }
-      ++run;
+      if (tag != kNoTag) atomicAdd(arrived + tag, run);
+    } else {
+      st_release_cta(&words->published, n);
     }
-    if (tag != kNoTag) atomicAdd(arrived + tag, run);
-    confirmed = n;
+    published = n;
   }
   // Store the oldest row in flight (or, after a failure, only wait for it).
   __device__ void store_one() {
@@ -153,19 +194,30 @@ struct RowPipe {
       // every store group but the last kPipeRetire (all after pend_end) done
       if (failed) bulk_wait_all();
       else bulk_wait<kPipeRetire>();
-      confirm(stored - kPipeRetire);
+      publish(stored - kPipeRetire);
       signal(pend);
       pend = -1;
     } else if (arrived && (stored & 3u) == 0 && stored > kPipeRetire) {
-      // every fourth store: the rows whose stores are done are counted
+      // every fourth store: the rows whose stores are done are published
       bulk_wait<kPipeRetire>();
-      confirm(stored - kPipeRetire);
+      publish(stored - kPipeRetire);
     }
   }
   __device__ void push(const uint4* from, uint4* dst, uint4* dst2 = nullptr, int tag = kNoTag) {
     if (failed) return;
     while (stored + kPipeAhead <= issued) store_one();
     if (failed) return;
+    if (arrived && !self_count && issued - consumed >= kTagRing) {
+      // the tag entry this row takes is still to be read by the counting warp
+      const uint64_t t0 = globaltimer_ns();
+      while (issued - (consumed = ld_acquire_cta(&words->consumed)) >= kTagRing) {
+        if (globaltimer_ns() - t0 > kBulkWaitNs) {
+          failed = true;
+          return;
+        }
+        __nanosleep(64);
+      }
+    }
     bulk_wait_read<kPipeLag>();
     const int s = static_cast<int>(issued % kPipeSlots);
     to[s] = dst;
@@ -182,7 +234,7 @@ struct RowPipe {
       while (stored < issued) store_one();
       if (pend >= 0) {
         bulk_wait_all();
-        confirm(stored);
+        publish(stored);
         signal(pend);
       }
     }
@@ -193,11 +245,67 @@ struct RowPipe {
   __device__ void finish() {
     while (stored < issued) store_one();
     bulk_wait_all();
-    confirm(stored);
+    publish(stored);
+    if (arrived && !self_count) st_release_cta(&words->finished, 1u);
     if (pend >= 0) signal(pend);
     pend = -1;
   }
 };
+
+// The counting warp of a streamed gather CTA: lane w follows pipe warp w's
+// published rows and adds them to their requests' arrival counts, one
+// atomic per run of rows of one request, after a GPU-scope fence (the rows'
+// writes, ordered before `published`, become visible to the attention before
+// the counts). The lanes sweep together, so a sweep with new rows in any pipe
+// costs one fence for the warp (on an SM whose pipes keep host reads in
+// flight a fence takes microseconds; one per lane and sweep fell behind the
+// pipes at the large_batch shape). Gives up after kCountIdleNs without progress.
+__device__ void count_arrivals(uint8_t* smem, uint32_t* arrived, uint32_t* gave_up, int lane) {
+  const bool mine = lane < kPipeWarps;
+  uint8_t* base = smem + size_t(mine ? lane : 0) * kPipeWarpBytes;
+  const uint16_t* tags = reinterpret_cast<const uint16_t*>(base + kPipeTagOffset);
+  PipeWords* words = reinterpret_cast<PipeWords*>(base + kPipeWordsOffset);
+  uint32_t seen = 0;
+  bool done = !mine;
+  uint64_t t_idle = globaltimer_ns();
+  for (;;) {
+    uint32_t fin = 1, p = seen;
+    if (!done) {
+      fin = ld_acquire_cta(&words->finished);  // (read first: p is then the last value)
+      p = ld_acquire_cta(&words->published);
+    }
+    const bool work = p > seen;
+    if (__any_sync(0xffffffffu, work)) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      if (work) {
+        int tag = tags[seen % kTagRing];
+        uint32_t run = 0;
+        for (uint32_t i = seen; i < p; ++i) {
+          const int t = tags[i % kTagRing];
+          if (t != tag) {
+            if (tag != kNoTag) atomicAdd(arrived + tag, run);
+            tag = t;
+            run = 0;
+          }
+          ++run;
+        }
+        if (tag != kNoTag) atomicAdd(arrived + tag, run);
+        seen = p;
+        st_release_cta(&words->consumed, seen);
+      }
+      t_idle = globaltimer_ns();
+    } else {
+      if (fin) done = true;
+      if (__all_sync(0xffffffffu, done)) break;
+      // (lane 0's clock decides for the warp, which leaves the loop together)
+      if (__shfl_sync(0xffffffffu, globaltimer_ns() - t_idle > kCountIdleNs ? 1 : 0, 0)) {
+        if (lane == 0) atomicExch(gave_up, 1u);  // the attention stops waiting for these counts
+        break;
+      }
+      __nanosleep(128);
+    }
+  }
+}
 
 // Row lists of one layer (see gather_kernel).
 struct GatherLayer {
@@ -430,7 +538,7 @@ __device__ __forceinline__ void gather_positions(
 // writes `seq` into done[l]: another stream's stream-memory wait on done[l]
 // then orders the layer's consumers after its rows. The launch's own
 // completion orders them for the per-layer call.
-__global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
+__global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(
     const int32_t* __restrict__ src_map, const int32_t* __restrict__ miss_ids,
     const int32_t* __restrict__ miss_pos, const int32_t* __restrict__ miss_count,
     const int32_t* __restrict__ miss_rows, const int32_t* __restrict__ victim,
@@ -439,7 +547,7 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
     uint4* __restrict__ sel, int layers, int64_t pool_stride, int64_t host_stride,
     int64_t sel_stride, uint32_t* __restrict__ done, uint32_t* __restrict__ count, uint32_t seq,
     int miss_ctas, int sel_rows, int pool_rows, uint32_t* ticket, uint32_t* arrived,
-    int32_t* err) {
+    int self_count, int32_t* err) {
   extern __shared__ __align__(128) uint8_t gather_smem[];
   __shared__ int scan_scratch[40];
   const int lane = threadIdx.x & 31;
@@ -456,10 +564,11 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
     uint32_t* started = arrived + size_t(layers) * B;
     if (atomicAdd(started, 1u) == gridDim.x - 1) atomicExch(started + 1, seq);
   }
+  const bool counter = wc == kPipeWarps;  // the CTA's counting warp (no pipe)
   RowPipe pipe;
-  if (lane == 0)
+  if (lane == 0 && !counter)
     pipe.init(gather_smem + wc * kPipeWarpBytes, nw, count, done, seq, ticket, layers - 1,
-              arrived);
+              arrived, self_count != 0);
   __syncwarp();
   if (miss_cta && ticket) {
     // the requests' exclusive miss-count prefix, for the dynamic hand-out
@@ -476,13 +585,18 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
     }
     if (threadIdx.x == 0) prefix[B] = total;
     __syncthreads();
-    gather_misses_dynamic(pool, host, sel, pool_stride, host_stride, sel_stride, layers,
-                          miss_ids, miss_pos, victim, install, prefix, B, k, P, sel_rows,
-                          pool_rows, ctx_stride, ctx_len, ticket, lane, pipe, bad);
-    if (lane == 0) pipe.end_layer(layers - 1);
-    __syncwarp();
+    if (counter) {
+      if (arrived && !self_count)
+        count_arrivals(gather_smem, arrived, arrived + size_t(layers) * B + 2, lane);
+    } else {
+      gather_misses_dynamic(pool, host, sel, pool_stride, host_stride, sel_stride, layers,
+                            miss_ids, miss_pos, victim, install, prefix, B, k, P, sel_rows,
+                            pool_rows, ctx_stride, ctx_len, ticket, lane, pipe, bad);
+      if (lane == 0) pipe.end_layer(layers - 1);
+      __syncwarp();
+    }
   }
-  for (int l = 0; !(miss_cta && ticket) && l < layers; ++l) {
+  for (int l = 0; !counter && !(miss_cta && ticket) && l < layers; ++l) {
     const GatherLayer L{pool + l * pool_stride, host + l * host_stride, sel + l * sel_stride};
     if (miss_cta)
       gather_misses(L, miss_ids, miss_pos, miss_count, victim, install, B, k, P, sel_rows,
@@ -493,7 +607,7 @@ __global__ void __launch_bounds__(kPipeWarps * 32, 1) gather_kernel(
     if (lane == 0) pipe.end_layer(l);
     __syncwarp();
   }
-  if (lane == 0) {
+  if (lane == 0 && !counter) {
     pipe.finish();
     if (pipe.failed) {
       bad |= TS_DEVERR_TIMEOUT;
@@ -657,18 +771,26 @@ ts_status gather_enqueue(const int32_t* src_map, const int32_t* miss_ids, const 
       double(host_layer_bytes ? host_layer_bytes : size_t(B) * size_t(ctx_stride) * DSA_ROW_BYTES) *
       layers;
   const GatherGrid grid = gather_grid(B, k, host_bytes);
+  // Streamed arrival counts: with three or more units of miss CTAs the
+  // launch keeps far more host rows in flight than the link needs, and the
+  // pipe threads release their rows themselves (the counts then lag the rows
+  // least); with fewer, every stall of a pipe costs link time, and the CTA's
+  // counting warp releases them. Measured per step (GB300): 128 x 32,768
+  // (32 miss CTAs) 1.55 ms with the pipes' own releases, 1.73 with counting
+  // warps; 32 x 65,536 (8 miss CTAs) 0.73 and 0.55.
+  const bool self_count = grid.miss >= 3 * kMissCtas;
   const int hit = staged ? 0 : grid.hit;
   const int pool_rows = staged ? P + k : P;
   const int sel_rows = staged ? P + k : k;
   uint4* pool = static_cast<uint4*>(const_cast<void*>(pool_l));
   uint4* sel = staged ? pool + size_t(P) * DSA_ROW_CHUNKS : static_cast<uint4*>(sel_l);
   if (staged) sel_layer_bytes = pool_layer_bytes;
-  gather_kernel<<<grid.miss + hit, kPipeWarps * 32, smem, stream>>>(
+  gather_kernel<<<grid.miss + hit, kGatherThreads, smem, stream>>>(
       src_map, miss_ids, miss_pos, miss_count, miss_rows, victim, install, B, k, pool, P,
       static_cast<const uint4*>(host_l), ctx_stride, ctx_len, sel, layers,
       int64_t(pool_layer_bytes / 16), int64_t(host_layer_bytes / 16),
       int64_t(sel_layer_bytes / 16), done, count, seq, grid.miss, sel_rows, pool_rows,
-      dynamic ? ticket : nullptr, arrived, err);
+      dynamic ? ticket : nullptr, arrived, self_count ? 1 : 0, err);
   return launch_status();
 }
 
