@@ -703,7 +703,8 @@ def run_native(args, w, rank, world, local, overrides):
         med = float(np.median(spans))
         step_dist = {"median_ms": round(med, 4), "p90_ms": round(float(np.percentile(spans, 90)), 4),
                      "max_ms": round(float(spans.max()), 4),
-                     "steps_over_2x_median": int(np.sum(spans > 2 * med))}
+                     "steps_over_2x_median": int(np.sum(spans > 2 * med)),
+                     "spans_ms": [round(float(x), 3) for x in spans]}
     # where the launches of the last timed step sat, in microseconds after its
     # first launch began
     last_spans = None
@@ -714,8 +715,12 @@ def run_native(args, w, rank, world, local, overrides):
                       for n, v in t_last.spans(first).items()}
     rf_line = None
     if per_kernel:
-        dom = max(per_kernel, key=lambda n: per_kernel[n]["ms_per_launch"]
-                  * per_kernel[n]["launches_per_step"])
+        # the gather bounds the step: its host-link reads are the step's
+        # largest transfer (with streamed attention, an attention launch's
+        # events also span its wait for the gather's rows)
+        dom = "gather" if "gather" in per_kernel else max(
+            per_kernel, key=lambda n: per_kernel[n]["ms_per_launch"]
+            * per_kernel[n]["launches_per_step"])
         rf = dict(per_kernel[dom])
         rf_line = {"kernel": dom, "bound": rf["bound"], "achieved": rf["achieved"],
                    "peak": rf["peak"], "unit": rf["unit"], "frac": rf["frac"],

@@ -224,9 +224,14 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   // the plan, into this step's staging half; that half's last reader, the
   // attention of step seq - 2, came before planned >= seq - 1 on the main
   // stream (the signal is enqueued already, so the wait ends)
-  if (io)
-    ok = ok && wait_for(side, planned, seq - 1) &&
-         ts_copy(q_stage, io->q_h, q_bytes, side) == TS_OK && signal(side, qcopied, seq);
+  // layer by layer, each copy followed by the word's next value seq * L + l,
+  // which layer l's attention waits for (values grow step after step)
+  if (io) {
+    ok = ok && wait_for(side, planned, seq - 1);
+    for (int l = 0; ok && l < L; ++l)
+      ok = ts_copy(at(q_stage, l, lb.q), at(io->q_h, l, lb.q), lb.q, side) == TS_OK &&
+           signal(side, qcopied, seq * uint32_t(L) + l);
+  }
   // per layer: the attention on the main stream, the refill beside it on the
   // side stream; the last refill also updates the metadata. The staged
   // attention reads hit rows from the pool itself, so the layer's refill
@@ -237,7 +242,7 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   for (int l = 0; ok && l < L; ++l) {
     float* lse_l = g.lse ? at(g.lse, l, lb.lse) : nullptr;
     ok = (streamed ? (l > 0 || wait_for(m, started, seq)) : wait_for(m, gathered + l, seq)) &&
-         (!io || l > 0 || wait_for(m, qcopied, seq)) && rec(3 + l, 0, m) &&
+         (!io || wait_for(m, qcopied, seq * uint32_t(L) + l)) && rec(3 + l, 0, m) &&
          (staged ? sfa_pool_enqueue(at(q, l, lb.q), at(g.pool, l, lb.pool), P, g.src_map,
                                     g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.H,
                                     g.k, g.scale, at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m,
@@ -300,7 +305,7 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
       signal(side, started, seq);
       signal(side, gave_up, seq);
     }
-    if (io) signal(side, qcopied, seq);
+    if (io) signal(side, qcopied, seq * uint32_t(L) + L - 1);
     for (int i = 0; i < 2; ++i)
       if (ev[i]) cudaEventDestroy(ev[i]);
     cudaGetLastError();

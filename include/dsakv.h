@@ -522,11 +522,13 @@ ts_status dsa_group_step(dsa_group* g, const float* scores, const void* q, const
  *   main : scores_h -> scores_d, then the step as dsa_group_step; after each
  *          layer's attention, that layer's output -> out_h (it also stays in
  *          the descriptor's `out`)
- *   side : wait planned >= step - 1 -> q_h -> one half of q_d (chosen by the
- *          step's parity) -> signal the sync word after the gather's ticket;
- *          the first layer's attention waits for it
+ *   side : wait planned >= step - 1 -> layer by layer, q_h[l] -> layer l
+ *          of one half of q_d (chosen by the step's parity) -> write
+ *          step * layers + l into the sync word after the gather's ticket;
+ *          layer l's attention waits for that value
  * So the queries cross beside the top-k and the plan rather than before them,
- * and each layer's output crosses while later layers are still gathered. The
+ * each layer's attention waits only for its own layer's queries, and each
+ * layer's output crosses while later layers are still gathered. The
  * staging half a step writes was last read by the attention of the step
  * before the previous one, which precedes planned >= step - 1 on the main
  * stream; that signal is enqueued before this wait, so the wait ends.
