@@ -619,10 +619,16 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(
   if (bad && lane == 0) report(err, bad);
 }
 
-// The installs of every layer of the call: 32 (request, miss) entries per
-// warp at a time, then one row after the other with the whole warp (72
-// pieces per row, lanes stride by 32). Layer l's selection and pool start
-// sel_stride and pool_stride 16-byte pieces after layer l-1's.
+// The installs of every layer of the call, one CTA per request: its misses
+// (the first miss_count[b] entries of its plan) 256 at a time with coalesced
+// loads, then each warp copies the rows of its entries that need it, one
+// after the other (72 pieces per row, lanes stride by 32). Layer l's
+// selection and pool start sel_stride and pool_stride 16-byte pieces after
+// layer l-1's. Requests hold a few hundred misses and the refill copies only
+// the few whose victim slot the step read: scanning each request's own
+// entries replaces a scan of all B x k positions (measured on GB300 at 128 x
+// 32,768, the last layer's refill and metadata update: 35 us over all
+// positions from one CTA per SM).
 constexpr int kRefillThreads = 256;
 __global__ void __launch_bounds__(kRefillThreads) refill_kernel(
     const int32_t* __restrict__ miss_ids, const int32_t* __restrict__ miss_pos,
@@ -633,26 +639,22 @@ __global__ void __launch_bounds__(kRefillThreads) refill_kernel(
     const int32_t* __restrict__ ptr_next, int S, int W, int min_install, int sel_rows,
     int pool_rows, int32_t* err) {
   const int lane = threadIdx.x & 31;
-  const int warp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  const int nwarps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
-  const int rows = B * k;  // < 2^31: B <= 65535, k <= 8192
-  // 32 entries at a time, one per lane; then the warp copies the rows that
-  // need it, one after the other
-  for (int r0 = warp * 32; r0 < rows; r0 += nwarps * 32) {
-    const int r = r0 + lane;
+  const int b = blockIdx.x;
+  const int M = min(max(__ldg(miss_count + b), 0), k);
+  const int64_t base = int64_t(b) * k;
+  for (int i0 = 0; i0 < M; i0 += kRefillThreads) {
+    const int i = i0 + static_cast<int>(threadIdx.x);
     bool need = false;
     int64_t from_row = 0, to_row = 0;
-    if (r < rows) {
-      const int b = r / k;
-      const int i = r - b * k;
-      const int code = i < __ldg(miss_count + b) ? __ldg(install + r) : 0;
+    if (i < M) {
+      const int code = __ldg(install + base + i);
       if (code) {
-        const int v = __ldg(victim + r);
-        const int j = __ldg(miss_pos + r);
+        const int v = __ldg(victim + base + i);
+        const int j = __ldg(miss_pos + base + i);
         if (v < 0 || v >= P || j < 0 || j >= k) {
           report(err, TS_DEVERR_SLOT_RANGE);
         } else {
-          if (update_metadata) pool_tags[int64_t(b) * P + v] = __ldg(miss_ids + r);
+          if (update_metadata) pool_tags[int64_t(b) * P + v] = __ldg(miss_ids + base + i);
           // (rows with a lower code went in with the gather)
           need = code >= min_install;
           from_row = int64_t(b) * sel_rows + j;
@@ -678,15 +680,13 @@ __global__ void __launch_bounds__(kRefillThreads) refill_kernel(
     }
   }
   if (update_metadata) {
-    const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t nth = int64_t(gridDim.x) * blockDim.x;
-    for (int64_t q = tid; q < int64_t(B) * S; q += nth) {
-      const int p = __ldg(ptr_next + q);
+    for (int s = threadIdx.x; s < S; s += kRefillThreads) {
+      const int p = __ldg(ptr_next + int64_t(b) * S + s);
       if (p < 0 || p >= W) {
         report(err, TS_DEVERR_PTR_RANGE);
         continue;
       }
-      fifo_ptr[q] = p;
+      fifo_ptr[int64_t(b) * S + s] = p;
     }
   }
 }
@@ -826,21 +826,14 @@ ts_status refill_enqueue(const int32_t* miss_ids, const int32_t* miss_pos, const
                          int W, int32_t* err, cudaStream_t stream, int layers,
                          size_t sel_layer_bytes, size_t pool_layer_bytes, int min_install,
                          bool staged) {
-  // one warp per (request, miss); one small CTA per SM, which fits beside an
-  // attention CTA (measured best of 16 or 38 1024-thread CTAs and 76 or 152
-  // 256-thread ones, beside the attention and the next layer's gather). The
+  // one CTA per request (a small one: it fits beside an attention CTA). The
   // staged layout refills from the pool's own staging rows.
-  const int64_t warps = int64_t(B) * k;
-  int64_t blocks = (warps * 32 + kRefillThreads - 1) / kRefillThreads;
-  const int64_t cap = sm_count();
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
   const int pool_rows = staged ? P + k : P;
   const int sel_rows = staged ? P + k : k;
   const uint4* sel = staged ? static_cast<const uint4*>(pool_l) + size_t(P) * DSA_ROW_CHUNKS
                             : static_cast<const uint4*>(sel_l);
   if (staged) sel_layer_bytes = pool_layer_bytes;
-  refill_kernel<<<static_cast<unsigned>(blocks), kRefillThreads, 0, stream>>>(
+  refill_kernel<<<static_cast<unsigned>(B), kRefillThreads, 0, stream>>>(
       miss_ids, miss_pos, victim, install, miss_count, B, k, sel, static_cast<uint4*>(pool_l), P,
       layers, int64_t(sel_layer_bytes / 16), int64_t(pool_layer_bytes / 16), update_metadata,
       pool_tags, fifo_ptr, ptr_next, S, W, min_install, sel_rows, pool_rows, err);
