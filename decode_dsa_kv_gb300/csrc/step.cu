@@ -171,6 +171,7 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   uint32_t* attended = g.sync + kGathered + 2 * L;  // staged layout: a layer's attention is done
   uint32_t* ticket = g.sync + kGathered + 3 * L;    // the gather's miss hand-out
   uint32_t* qcopied = ticket + 1;                   // host I/O: the queries are in
+  uint32_t* outcopied = ticket + 2;                 // host I/O: a layer's output is out
   // streamed: per (layer, request) arrival counts, then the gather's started
   // CTAs, the started flag and the gave-up flag
   uint32_t* started = streamed ? g.arrived + size_t(L) * g.B + 1 : nullptr;
@@ -239,19 +240,25 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   // Streamed, the first layer's attention launches once every gather CTA
   // runs (so the gather that its CTAs wait for never waits for SMs they
   // hold) and the later layers follow it on the stream.
+  // Each layer's output crosses to the host (host I/O) on the side stream,
+  // after the layer's refill; outcopied then holds seq * L + l. Every step's
+  // attention of layer l first waits for the previous step's copy of that
+  // layer's output (a step without host I/O writes the value itself), since
+  // it overwrites `out`.
+  const uint32_t seqL = seq * uint32_t(L);
   for (int l = 0; ok && l < L; ++l) {
     float* lse_l = g.lse ? at(g.lse, l, lb.lse) : nullptr;
     ok = (streamed ? (l > 0 || wait_for(m, started, seq)) : wait_for(m, gathered + l, seq)) &&
-         (!io || wait_for(m, qcopied, seq * uint32_t(L) + l)) && rec(3 + l, 0, m) &&
+         (!io || wait_for(m, qcopied, seqL + l)) &&
+         (seq == 1 || wait_for(m, outcopied, seqL - L + l)) && rec(3 + l, 0, m) &&
          (staged ? sfa_pool_enqueue(at(q, l, lb.q), at(g.pool, l, lb.pool), P, g.src_map,
                                     g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.H,
                                     g.k, g.scale, at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m,
                                     streamed ? g.arrived + size_t(l) * g.B : nullptr, gave_up)
                  : sfa_enqueue(at(q, l, lb.q), at(g.sel, l, lb.sel), g.B, g.H, g.k, g.scale,
                                at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m)) == TS_OK &&
-         rec(3 + l, 1, m) && (!staged || signal(m, attended + l, seq)) &&
-         // with host I/O each layer's output crosses back right after its attention
-         (!io || ts_copy(at(io->out_h, l, lb.out), at(g.out, l, lb.out), lb.out, m) == TS_OK);
+         rec(3 + l, 1, m) && signal(m, attended + l, seq) &&
+         (io || signal(m, outcopied, seqL + l));
     if (refills)
       ok = ok && wait_for(side, (staged ? attended : gathered) + l, seq) &&
            rec(3 + L + l, 0, side) &&
@@ -259,7 +266,13 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
                           staged ? nullptr : at(g.sel, l, lb.sel), at(g.pool, l, lb.pool), P,
                           l == L - 1, g.pool_tags, g.fifo_ptr, g.ptr_next, g.S, g.W, g.err, side,
                           1, lb.sel, lb.pool, 2, staged) == TS_OK &&
-           rec(3 + L + l, 1, side);
+           rec(3 + L + l, 1, side) &&
+           // the next plan waits for the last refill, not for the last copy
+           (l < L - 1 || signal(side, refilled, seq));
+    if (io)
+      ok = ok && wait_for(side, attended + l, seq) &&
+           ts_copy(at(io->out_h, l, lb.out), at(g.out, l, lb.out), lb.out, side) == TS_OK &&
+           signal(side, outcopied, seqL + l);
   }
   if (lru) {
     // no refill: the plan updated the pool's metadata and the gather wrote
@@ -283,8 +296,6 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
       g.sel = g.prev_sel;
       g.prev_sel = t_sel;
     }
-  } else {
-    ok = ok && signal(side, refilled, seq);
   }
   if (!ok) {
     // give every signal word this step's number, so that no wait enqueued
@@ -300,12 +311,13 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
           cudaEventRecord(ev[i], others[i]) == cudaSuccess)
         cudaStreamWaitEvent(side, ev[i], 0);
     for (int i = 0; i < kGathered + L; ++i) signal(side, g.sync + i, seq);
-    for (int i = 0; staged && i < L; ++i) signal(side, attended + i, seq);
+    for (int i = 0; i < L; ++i) signal(side, attended + i, seq);
     if (streamed) {  // and no attention CTA keeps waiting for rows
       signal(side, started, seq);
       signal(side, gave_up, seq);
     }
-    if (io) signal(side, qcopied, seq * uint32_t(L) + L - 1);
+    if (io) signal(side, qcopied, seqL + L - 1);
+    signal(side, outcopied, seqL + L - 1);
     for (int i = 0; i < 2; ++i)
       if (ev[i]) cudaEventDestroy(ev[i]);
     cudaGetLastError();

@@ -255,7 +255,7 @@ class DecodeGroup:
         self.side = torch.cuda.Stream(device=dev, priority=0)
         # cross-stream signals: device words written and waited on by the
         # streams themselves (zero before the first step)
-        self.sync = torch.zeros((4 + 3 * layers,), **i32)
+        self.sync = torch.zeros((5 + 3 * layers,), **i32)
         # staged layout: per (layer, request) arrival counts of the gather, so
         # that each attention CTA starts once its own request's rows are in
         self.arrived = (torch.zeros((layers * B + 3,), **i32)

@@ -415,7 +415,7 @@ ts_status sfa_mla_decode_pool(const void* q, const void* pool_l, int P, const in
  *   topk_ws / sfa_ws                        workspaces of ts_topk and
  *                                           sfa_mla_decode (sizes as theirs)
  *   err       int32 device error word (or NULL)
- *   sync      uint32 [4 + 3 * layers] device words, zero before the first step
+ *   sync      uint32 [5 + 3 * layers] device words, zero before the first step
  *             and touched by nothing else; step = 0 before the first step.
  *             Each call uses sequence number step + 1 and stores it in
  *             `step` (with the reuse policy it also swaps the buffers named
@@ -519,9 +519,10 @@ ts_status dsa_group_step(dsa_group* g, const float* scores, const void* q, const
 /* dsa_group_step_host -- the same step with its inputs and its output in
  * page-locked host memory (device-accessible addresses, e.g. from
  * ts_host_alloc); every copy is inside the step, done by the SMs (ts_copy):
- *   main : scores_h -> scores_d, then the step as dsa_group_step; after each
- *          layer's attention, that layer's output -> out_h (it also stays in
- *          the descriptor's `out`)
+ *   main : scores_h -> scores_d, then the step as dsa_group_step
+ *   side : after each layer's attention (and that layer's refill), the
+ *          layer's output -> out_h (it also stays in the descriptor's `out`);
+ *          the next step's attention of that layer waits for the copy
  *   side : wait planned >= step - 1 -> layer by layer, q_h[l] -> layer l
  *          of one half of q_d (chosen by the step's parity) -> write
  *          step * layers + l into the sync word after the gather's ticket;

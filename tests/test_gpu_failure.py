@@ -164,12 +164,16 @@ def test_group_step_orders_streams_under_delays(d, layout):
     host.close()
 
 
-@pytest.mark.parametrize("layout", ["selection", "staged"])
-def test_host_io_step_equals_device_input_step(d, layout):
+@pytest.mark.parametrize("layout,mixed", [("selection", False), ("staged", False),
+                                          ("staged", True)])
+def test_host_io_step_equals_device_input_step(d, layout, mixed):
     # dsa_group_step_host copies the inputs in and the output out inside the
     # step (the queries beside the top-k and plan, into a staging half chosen
-    # by step parity): steps enqueued back to back without a sync give the same
-    # plan, pool and attention output as steps on device-resident inputs
+    # by step parity; each layer's output on the side stream, which the next
+    # step's attention of that layer waits for before it overwrites the
+    # output): steps enqueued back to back without a sync give the same plan,
+    # pool and attention output as steps on device-resident inputs. `mixed`:
+    # host-I/O steps alternate with device-input steps on the same group.
     from decode_dsa_kv_gb300 import PinnedHost
     w = wl.scaled(wl.DECODE_BATCH, B=2, ctx=16384, S=256)
     T = 6
@@ -188,10 +192,17 @@ def test_host_io_step_equals_device_input_step(d, layout):
     gb = d.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host, layout=layout)
     s_b, q_b, o_b = scores[0].nbytes, qs[0].nbytes, o_pin.array[0].nbytes
     outs = torch.empty((T,) + tuple(gb.out.shape), dtype=torch.bfloat16, device="cuda")
-    for t in range(T):
-        ga.step_host(s_pin.dev + t * s_b, q_pin.dev + t * q_b, o_pin.dev + t * o_b)
     scores_d = torch.from_numpy(scores).cuda()
     q_d = torch.from_numpy(qs.view(np.int16)).cuda()
+    outs_a = torch.empty((T,) + tuple(ga.out.shape), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    for t in range(T):
+        if mixed and t % 2:
+            ga.step(scores_d[t], q_d[t])
+            with torch.cuda.stream(ga.main):
+                outs_a[t].copy_(ga.out)
+        else:
+            ga.step_host(s_pin.dev + t * s_b, q_pin.dev + t * q_b, o_pin.dev + t * o_b)
     torch.cuda.synchronize()
     for t in range(T):
         gb.step(scores_d[t], q_d[t])
@@ -199,7 +210,8 @@ def test_host_io_step_equals_device_input_step(d, layout):
             outs[t].copy_(gb.out)
     assert ga.synchronize() == 0 and gb.synchronize() == 0
     for t in range(T):
-        got = o_pin.array[t].view(np.uint16)
+        got = (outs_a[t].cpu().view(torch.int16).numpy() if mixed and t % 2
+               else o_pin.array[t]).view(np.uint16)
         want = outs[t].cpu().view(torch.int16).numpy().view(np.uint16)
         assert np.array_equal(got, want), t
     assert torch.equal(ga.tags, gb.tags) and torch.equal(ga.pool, gb.pool)
