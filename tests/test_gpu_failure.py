@@ -219,3 +219,44 @@ def test_host_io_step_equals_device_input_step(d, layout, mixed):
     for pin in (s_pin, q_pin, o_pin):
         pin.close()
     host.close()
+
+
+@pytest.mark.parametrize("w", [wl.scaled(wl.DECODE_BATCH, B=4, ctx=16384, S=256),
+                               wl.scaled(wl.LARGE_BATCH, B=8, ctx=8192, S=128)])
+def test_streamed_attention_wait_that_runs_out_reports_and_recovers(d, w):
+    # streamed attention: with the wait limit at 1 ns every attention CTA
+    # gives up waiting for its request's rows at once; the step reports
+    # TS_DEVERR_TIMEOUT through the error word (no trap, no hang), the gather
+    # and the refills still complete, and the steps after it, at the default
+    # limit, equal those of a group that never timed out (outputs and pool,
+    # bit for bit)
+    from decode_dsa_kv_gb300 import _abi
+    lens = wl.ctx_lens(w)
+    host = d.HostKV(w.layers, w.B, w.ctx_stride)
+    wl.fill_host_kv(w, host.array)
+    ga = d.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host,
+                       layout="staged")
+    gb = d.DecodeGroup(w.B, w.layers, w.k, w.S, w.W, w.H, lens, w.ctx_stride, host,
+                       layout="staged")
+    assert ga.arrived is not None
+    stream = wl.ScoreStream(w)
+    for t in range(5):
+        scores = torch.from_numpy(stream.next()).cuda()
+        q = torch.from_numpy(wl.queries(w, t).view(np.int16)).cuda()
+        if t == 2:
+            d.ts_set_wait_limit_ns(1)
+            try:
+                ga.step(scores, q)
+                bits = ga.synchronize()
+            finally:
+                d.ts_set_wait_limit_ns(0)
+            assert bits & _abi.TS_DEVERR_TIMEOUT, bits
+        else:
+            ga.step(scores, q)
+            assert ga.synchronize() == 0, t
+        gb.step(scores, q)
+        assert gb.synchronize() == 0, t
+        assert torch.equal(ga.pool, gb.pool), t
+        if t != 2:
+            assert torch.equal(ga.out.view(torch.int16), gb.out.view(torch.int16)), t
+    host.close()
