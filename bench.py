@@ -689,6 +689,16 @@ def run_native(args, w, rank, world, local, overrides):
         ms = sum(launch_ms[n]) / len(launch_ms[n])
         per_kernel[n] = roofline_of(n, alg[n], ms, peaks, link)
         per_kernel[n]["launches_per_step"] = len(launch_ms[n]) / args.steps
+    if g.arrived is not None and "sfa" in per_kernel:
+        # a streamed attention launch's events also span its wait for the
+        # gather's rows: its own time comes from launches back to back on the
+        # last timed step's rows (layer 0, every row in place)
+        span_ms = per_kernel["sfa"]["ms_per_launch"]
+        sfa_ms = sfa_alone_ms(torch, g, q_d[(cursor[0] - 1) % QS])
+        per_kernel["sfa"] = roofline_of("sfa", alg["sfa"], sfa_ms, peaks, link)
+        per_kernel["sfa"].update({"launches_per_step": w.layers, "in_step_span_ms": span_ms,
+                                  "timing": "alone: 10 launches back to back on the last timed "
+                                            "step's layer-0 rows (chunks + merge)"})
     # each timed step's span (its first launch's start to its last attention's
     # end, CUDA events): how evenly the steps ran (a rare step on this platform
     # stalls for milliseconds while its host reads slow down)
@@ -815,6 +825,30 @@ def run_native(args, w, rank, world, local, overrides):
                         for k2, v in per_kernel[n].items()} for n in per_kernel},
     }
     print(json.dumps(line), flush=True)
+
+
+def sfa_alone_ms(torch, g, q, n=10):
+    """Mean CUDA-event time of the staged attention (chunks + merge) on layer
+    0's rows as the last step left them, launched n times back to back on
+    the main stream after 3 untimed launches."""
+    from decode_dsa_kv_gb300 import _abi as abi
+
+    def launch():
+        abi.check(abi.sfa_mla_decode_pool(q[0], g.pool[0], g.P, g.src_map, g.miss_ids,
+                                          g.miss_pos, g.miss_count, g.miss_rows, g.B, g.H, g.k,
+                                          g.scale, g.out[0], g.lse[0], g.sfa_ws, g.sfa_ws_bytes,
+                                          g.err, g.main), "sfa_mla_decode_pool")
+    g.join(g.main)
+    for _ in range(3):
+        launch()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(g.main)
+    for _ in range(n):
+        launch()
+    e1.record(g.main)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / n
 
 
 def run_only(args, w, g, scores, q, peaks, link, lens, host, rank):
