@@ -18,8 +18,10 @@
 // memory; the CTAs merge their histograms through distributed shared memory,
 // rank 0 resolves the exact threshold and broadcasts it, and every CTA writes
 // its own slice of the sorted output. Longer contexts: hist and select spread
-// over many CTAs per request (8,192 positions each) in two launches; the last
-// select CTA of a request to finish (a completion counter) runs the finish.
+// over many CTAs per request (8,192 positions each); the last select CTA of a
+// request to finish (a completion counter) resolves the threshold and each
+// chunk's first output slot, and an output launch writes every chunk's
+// positions in order, one CTA per chunk.
 #include <mutex>
 
 #include "common.cuh"
@@ -41,7 +43,8 @@ struct TopkWs {
   uint32_t* cand_count;  // [B] candidates listed, then [B] select CTAs done
   uint64_t* cand;        // [B][max_ctx]  (key << 32 | position)
   uint32_t* bitmap;      // [B][words]
-  int64_t words;
+  uint32_t* chunk;       // [B][chunks] selected positions of each select chunk, then its offset
+  int64_t words, chunks;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -57,6 +60,9 @@ inline TopkWs carve(void* ws, int B, int max_ctx) {
   p += align256(size_t(B) * max_ctx * 8);
   w.bitmap = reinterpret_cast<uint32_t*>(p);
   w.words = (max_ctx + 31) / 32;
+  p += align256(size_t(B) * w.words * 4);
+  w.chunk = reinterpret_cast<uint32_t*>(p);
+  w.chunks = (max_ctx + kChunk - 1) / kChunk;
   return w;
 }
 
@@ -77,14 +83,6 @@ __device__ __forceinline__ uint32_t score_key(float f, bool& nan) {
 }
 
 __device__ __forceinline__ bool ctx_ok(int n, int k, int max_ctx) { return n >= k && n <= max_ctx; }
-
-// Add one to hist[bin] for every lane of the warp with bin >= 0, one atomic
-// per distinct bin (the lanes of a warp agree on few bins: scores cluster).
-__device__ __forceinline__ void warp_hist_add(uint32_t* hist, int bin) {
-  const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-  const int lane = threadIdx.x & 31;
-  if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
-}
 
 // The bin t of an nbins histogram (walked from the preferred end: high bins
 // first when high_first) with before(t) < need <= before(t) + hist[t]; also
@@ -224,11 +222,16 @@ __device__ __forceinline__ bool taken(uint64_t e, uint32_t T, uint32_t cut) {
 }
 
 // Resolve the threshold, set the chosen candidates' bits in the request's
-// global bitmap, and write the set positions in ascending order.
+// global bitmap and add them to their chunks' counts (which hold each select
+// chunk's positions above the threshold bin), then turn the counts into each
+// chunk's first output slot (an exclusive scan over the request's chunks).
+// topk_output_kernel then writes every chunk's positions in order, one CTA
+// per chunk. A total other than k sets TS_DEVERR_COUNT, writes -1 ids and
+// marks every chunk so that nothing more is written.
 template <typename C>
-__device__ void finish_request(const C& cand, uint32_t c, int t1, int need1, uint32_t* bits,
-                               int n, int k, int32_t* out, uint32_t* hist, int* sbuf,
-                               int32_t* err) {
+__device__ void finish_chunks(const C& cand, uint32_t c, int t1, int need1, uint32_t* bits,
+                              uint32_t* counts, int n, int k, int32_t* out, uint32_t* hist,
+                              int* sbuf, int32_t* err) {
   uint32_t T, cut;
   resolve_threshold(cand, c, t1, need1, hist, sbuf, &T, &cut);
   for (uint32_t i = threadIdx.x; i < c; i += blockDim.x) {
@@ -236,43 +239,27 @@ __device__ void finish_request(const C& cand, uint32_t c, int t1, int need1, uin
     if (taken(e, T, cut)) {
       const uint32_t pos = static_cast<uint32_t>(e);
       atomicOr(bits + (pos >> 5), 1u << (pos & 31));
+      atomicAdd(counts + pos / kChunk, 1u);
     }
   }
   __syncthreads();
-  // each thread owns a run of consecutive words; kRun of them are loaded
-  // before any is used, so the loads of a long bitmap overlap
-  constexpr int kRun = 16;
-  const int64_t nwords = (int64_t(n) + 31) / 32;
-  const int64_t per = (nwords + blockDim.x - 1) / blockDim.x;
-  const int64_t w0 = int64_t(threadIdx.x) * per;
-  const int64_t w1 = min(w0 + per, nwords);
+  const int nch = (n + kChunk - 1) / kChunk;
+  const int per = (nch + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+  const int j0 = min(static_cast<int>(threadIdx.x) * per, nch), j1 = min(j0 + per, nch);
   int cnt = 0;
-  for (int64_t w = w0; w < w1; w += kRun) {
-    uint32_t m[kRun];
-#pragma unroll
-    for (int u = 0; u < kRun; ++u) m[u] = w + u < w1 ? __ldcg(bits + w + u) : 0u;
-#pragma unroll
-    for (int u = 0; u < kRun; ++u) cnt += __popc(m[u]);
-  }
+  for (int j = j0; j < j1; ++j) cnt += static_cast<int>(__ldcg(counts + j));
   int total;
-  int pos = block_exclusive_scan(cnt, sbuf, &total);
+  int off = block_exclusive_scan(cnt, sbuf, &total);
   if (total != k) {
     if (threadIdx.x == 0) report(err, TS_DEVERR_COUNT);
     for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
+    for (int j = threadIdx.x; j < nch; j += blockDim.x) counts[j] = kAll;
     return;
   }
-  for (int64_t w = w0; w < w1; w += kRun) {
-    uint32_t m[kRun];
-#pragma unroll
-    for (int u = 0; u < kRun; ++u) m[u] = w + u < w1 ? __ldcg(bits + w + u) : 0u;
-#pragma unroll
-    for (int u = 0; u < kRun; ++u) {
-      while (m[u]) {
-        const int bit = __ffs(m[u]) - 1;
-        m[u] &= m[u] - 1;
-        out[pos++] = static_cast<int32_t>((w + u) * 32 + bit);
-      }
-    }
+  for (int j = j0; j < j1; ++j) {
+    const int c_j = static_cast<int>(__ldcg(counts + j));
+    counts[j] = static_cast<uint32_t>(off);
+    off += c_j;
   }
 }
 
@@ -514,6 +501,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(
   __shared__ uint32_t dig[2048];
   __shared__ uint64_t cand_s[kFinishCandCap];
   __shared__ int last;
+  __shared__ uint32_t chunk_above;
   const int b = blockIdx.y;
   const int n = ctx_len[b];
   if (!ctx_ok(n, k, max_ctx)) {
@@ -526,6 +514,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(
   }
   const int64_t start = int64_t(blockIdx.x) * kChunk;
   if (start >= n) return;
+  if (threadIdx.x == 0) chunk_above = 0;  // (select_bin's barriers come before its use)
   // threshold bin from the request's histogram
   int t1, above, cnt1;
   select_bin(ws.hist + int64_t(b) * kBins, kBins, true, k, sbuf, &t1, &above, &cnt1);
@@ -536,6 +525,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(
   const int lane = threadIdx.x & 31;
   // each warp covers 4 x 32 consecutive positions per iteration: 4 bitmap words
   const int warp = threadIdx.x >> 5;
+  uint32_t n_above = 0;  // this warp's positions above the threshold bin
   for (int64_t base = start + warp * 128; base < end; base += (kThreads / 32) * 128) {
     float v[4];
 #pragma unroll
@@ -555,6 +545,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(
       }
       const uint32_t above_mask = __ballot_sync(0xffffffffu, bin > t1);
       const uint32_t tie_mask = __ballot_sync(0xffffffffu, bin == t1);
+      n_above += __popc(above_mask);
       if (lane == 0 && base + u * 32 < end) bits[(base + u * 32) >> 5] = above_mask;
       if (tie_mask) {
         uint32_t pos0 = 0;
@@ -567,7 +558,11 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(
       }
     }
   }
-  // the last CTA of this request to get here runs the finish
+  // the chunk's count of positions above the bin, then the last CTA of this
+  // request to get here runs the finish
+  if (lane == 0) atomicAdd(&chunk_above, n_above);
+  __syncthreads();
+  if (threadIdx.x == 0) ws.chunk[int64_t(b) * ws.chunks + blockIdx.x] = chunk_above;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -584,7 +579,35 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(
     cand_s[i] = __ldcg(cand + i);
   __syncthreads();
   Cands cl{cand_s, cand, kFinishCandCap};
-  finish_request(cl, c, t1, k - above, bits, n, k, ids + int64_t(b) * k, dig, sbuf, err);
+  finish_chunks(cl, c, t1, k - above, bits, ws.chunk + int64_t(b) * ws.chunks, n, k,
+                ids + int64_t(b) * k, dig, sbuf, err);
+}
+
+// Each select chunk's selected positions, in order, at the chunk's first
+// output slot (finish_chunks): one CTA per chunk, one bitmap word per thread.
+constexpr int kOutThreads = kChunk / 32;
+__global__ void __launch_bounds__(kOutThreads) topk_output_kernel(
+    const int32_t* __restrict__ ctx_len, int k, int max_ctx, TopkWs ws,
+    int32_t* __restrict__ ids) {
+  __shared__ int scratch[40];
+  const int b = blockIdx.y, j = blockIdx.x;
+  const int n = ctx_len[b];
+  if (!ctx_ok(n, k, max_ctx)) return;  // (the select kernel wrote the request's -1 ids)
+  const int64_t start = int64_t(j) * kChunk;
+  if (start >= n) return;
+  const uint32_t off = __ldcg(ws.chunk + int64_t(b) * ws.chunks + j);
+  if (off == kAll) return;  // (a count other than k: reported, ids -1)
+  const int64_t nwords = (int64_t(n) + 31) / 32;
+  const int64_t w = start / 32 + threadIdx.x;
+  uint32_t m = w < nwords ? __ldcg(ws.bitmap + int64_t(b) * ws.words + w) : 0u;
+  int total;
+  const int pos = block_exclusive_scan(__popc(m), scratch, &total);
+  int32_t* o = ids + int64_t(b) * k + off + pos;
+  while (m) {
+    const int bit = __ffs(m) - 1;
+    m &= m - 1;
+    *o++ = static_cast<int32_t>(w * 32 + bit);
+  }
 }
 
 
@@ -637,6 +660,7 @@ ts_status launch_topk(const float* scores, int64_t ctx_stride, const int32_t* ct
                                                                          err);
   topk_select_kernel<<<grid, kThreads, 0, stream>>>(scores, ctx_stride, ctx_len, k, max_ctx, w,
                                                     ids, err);
+  topk_output_kernel<<<grid, kOutThreads, 0, stream>>>(ctx_len, k, max_ctx, w, ids);
   return launch_status();
 }
 
@@ -658,8 +682,10 @@ extern "C" size_t ts_topk_workspace_size(int B, int max_ctx, int k) {
   (void)k;
   if (B <= 0 || max_ctx <= 0) return 0;
   const int64_t words = (int64_t(max_ctx) + 31) / 32;
+  const int64_t chunks = (int64_t(max_ctx) + kChunk - 1) / kChunk;
   return align256(size_t(B) * kBins * 4) + align256(size_t(B) * 8) +
-         align256(size_t(B) * max_ctx * 8) + align256(size_t(B) * words * 4);
+         align256(size_t(B) * max_ctx * 8) + align256(size_t(B) * words * 4) +
+         align256(size_t(B) * chunks * 4);
 }
 
 namespace dsakv {
@@ -704,7 +730,8 @@ constexpr size_t kNoAllocScratchBytes =
     ((size_t(kNoAllocMaxB) * kBins * 4 + 255) & ~size_t(255)) +
     ((size_t(kNoAllocMaxB) * 8 + 255) & ~size_t(255)) +
     ((size_t(kNoAllocMaxPositions) * 8 + 255) & ~size_t(255)) +
-    ((size_t(kNoAllocMaxPositions / 32 + kNoAllocMaxB) * 4 + 255) & ~size_t(255));
+    ((size_t(kNoAllocMaxPositions / 32 + kNoAllocMaxB) * 4 + 255) & ~size_t(255)) +
+    ((size_t(kNoAllocMaxPositions / kChunk + kNoAllocMaxB) * 4 + 255) & ~size_t(255));
 
 // Module-scope scratch: every device that loads the library holds it (about
 // 34.5 MiB) until the process exits. Host code must not pass the symbol
