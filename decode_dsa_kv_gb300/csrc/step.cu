@@ -187,19 +187,20 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   };
 
   bool ok = true;
+  // streamed: the counts start from zero, ahead of the top-k (the previous
+  // step's attention, their last reader, ran earlier on this stream, and
+  // every count it waited for was complete; this step's gather waits for the
+  // plan, after this)
+  if (streamed)
+    ok = cudaMemsetAsync(g.arrived, 0, (size_t(L) * g.B + 3) * 4, m) == cudaSuccess;
   // with host I/O the scores cross first, on the main stream ahead of the top-k
-  if (io) ok = ts_copy(io->scores_d, io->scores_h, scores_bytes, m) == TS_OK;
+  if (io) ok = ok && ts_copy(io->scores_d, io->scores_h, scores_bytes, m) == TS_OK;
   if (!ids) {
     ok = ok && rec(0, 0, m) &&
          topk_enqueue(scores, g.ctx_stride, g.ctx_len, g.B, g.max_ctx, g.k, g.ids, g.topk_ws,
                       g.err, m) == TS_OK &&
          rec(0, 1, m);
   }
-  // streamed: the counts start from zero (the previous step's attention,
-  // their last reader, ran earlier on this stream; this step's gather waits
-  // for the plan, after this)
-  if (streamed)
-    ok = ok && cudaMemsetAsync(g.arrived, 0, (size_t(L) * g.B + 3) * 4, m) == cudaSuccess;
   ok = ok && wait_for(m, refilled, seq - 1) && rec(1, 0, m) &&
        (reuse ? plan_reuse_enqueue(plan_ids, g.prev_ids, g.ctx_len, g.B, g.k, g.src_map,
                                    g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.err, m)
