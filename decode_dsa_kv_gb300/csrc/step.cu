@@ -222,14 +222,15 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
                       reuse ? nullptr : g.install, staged, ticket,
                       streamed ? g.arrived : nullptr) == TS_OK &&
        rec(2, 1, gs);
-  // with host I/O the queries cross on the side stream beside the top-k and
-  // the plan, into this step's staging half; that half's last reader, the
-  // attention of step seq - 2, came before planned >= seq - 1 on the main
-  // stream (the signal is enqueued already, so the wait ends)
-  // layer by layer, each copy followed by the word's next value seq * L + l,
-  // which layer l's attention waits for (values grow step after step)
+  // with host I/O the queries cross on the side stream once this step's plan
+  // is done (the scores the top-k waits for then cross the host link alone),
+  // into this step's staging half; that half's last reader, the attention of
+  // step seq - 2, came before planned >= seq - 1 on the main stream (the
+  // signal is enqueued already, so the wait ends). Layer by layer, each copy
+  // followed by the word's next value seq * L + l, which layer l's attention
+  // waits for (values grow step after step)
   if (io) {
-    ok = ok && wait_for(side, planned, seq - 1);
+    ok = ok && wait_for(side, planned, seq);
     for (int l = 0; ok && l < L; ++l)
       ok = ts_copy(at(q_stage, l, lb.q), at(io->q_h, l, lb.q), lb.q, side) == TS_OK &&
            signal(side, qcopied, seq * uint32_t(L) + l);
