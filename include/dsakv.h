@@ -520,19 +520,19 @@ ts_status dsa_group_step(dsa_group* g, const float* scores, const void* q, const
  * page-locked host memory (device-accessible addresses, e.g. from
  * ts_host_alloc); every copy is inside the step, done by the SMs (ts_copy):
  *   main : scores_h -> scores_d, then the step as dsa_group_step
+ *   side : wait planned >= step (this step's plan) -> layer by layer,
+ *          q_h[l] -> layer l of one half of q_d (chosen by the step's parity)
+ *          -> write step * layers + l into the sync word after the gather's
+ *          ticket; layer l's attention waits for that value
  *   side : after each layer's attention (and that layer's refill), the
  *          layer's output -> out_h (it also stays in the descriptor's `out`);
  *          the next step's attention of that layer waits for the copy
- *   side : wait planned >= step - 1 -> layer by layer, q_h[l] -> layer l
- *          of one half of q_d (chosen by the step's parity) -> write
- *          step * layers + l into the sync word after the gather's ticket;
- *          layer l's attention waits for that value
- * So the queries cross beside the top-k and the plan rather than before them,
- * each layer's attention waits only for its own layer's queries, and each
- * layer's output crosses while later layers are still gathered. The
- * staging half a step writes was last read by the attention of the step
- * before the previous one, which precedes planned >= step - 1 on the main
- * stream; that signal is enqueued before this wait, so the wait ends.
+ * So the scores the top-k waits for cross the host link alone, the queries
+ * cross beside the gather, each layer's attention waits only for its own
+ * layer's queries, and each layer's output crosses while later layers are
+ * still gathered. The staging half a step writes was last read by the
+ * attention of the step before the previous one, which precedes this step's
+ * plan on the main stream.
  *   scores_h float [B][ctx_stride], q_h bf16 [layers][B][H][576],
  *   out_h bf16 [layers][B][H][512]      host (device-accessible addresses)
  *   scores_d float [B][ctx_stride], q_d bf16 2 x [layers][B][H][576]
