@@ -55,10 +55,13 @@ constexpr int kScoreLoads = 2 * kKB;                 // 18 score stages
 constexpr int kLoads = kScoreLoads + 16;             // + 16 value stages (8 row blocks x 2 halves)
 constexpr int kSoftmaxThreads = 256;                 // warps 2..9
 constexpr int kThreads = 64 + kSoftmaxThreads;
-// The pool variant loads its tiles with 16-byte cp.async copies from four
-// loader warps (warp 0 and warps 10..12): 128 threads.
-constexpr int kLoaderThreads = 128;
-constexpr int kPoolThreads = kThreads + 96;
+// The pool variant loads its tiles with 16-byte cp.async copies from eight
+// loader warps (warp 0 and warps 10..16): 256 threads. Measured on GB300 (L2
+// flushed, 128 heads x 2048 rows): 51.9 -> 45.7 us a layer at 8 requests and
+// 198.6 -> 184.2 us at 128 against four loader warps (the copies' issue rate
+// bounded the CTA; with 544 threads the kernel fits in 88 registers).
+constexpr int kLoaderThreads = 256;
+constexpr int kPoolThreads = kThreads + kLoaderThreads - 32;
 constexpr uint32_t kBarBytes = 704;
 // barriers first, then the 1024-byte aligned tiles (worst-case padding
 // included). The total leaves room on the SM for a 0-byte CTA of another
@@ -151,9 +154,9 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Barrier among the pool variant's four loader warps (named barrier 2).
+// Barrier among the pool variant's loader warps (named barrier 2).
 __device__ __forceinline__ void loader_sync() {
-  asm volatile("bar.sync 2, 128;" ::: "memory");
+  asm volatile("bar.sync 2, 256;" ::: "memory");
 }
 
 // Row of request b's part of the pool tensor that position j reads: a hit's
@@ -181,7 +184,7 @@ __device__ __forceinline__ int pool_row(const PoolSrc& ps, int b, int k, int j, 
 // O, the row max and the row sum of the chunk go to the workspace for
 // sfa_combine_kernel. kPool = false: the rows are the selection buffer's, loaded as TMA tiles
 // (tm_q, tm_k, tm_v). kPool = true: the rows are read straight from a
-// staged-layout pool by the plan (`ps`), by four loader warps with 16-byte
+// staged-layout pool by the plan (`ps`), by eight loader warps with 16-byte
 // cp.async copies (the maps are unused). Measured on GB300: TMA 4-row gathers
 // (one instruction per 4 rows x 64 dims) kept the attention at 117 us a layer
 // at the decode_batch shape against 46 us for tile loads; the TMA unit's
@@ -263,7 +266,7 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
     // thread then makes them visible to the tensor cores' async proxy. Positions
     // past k read row k-1 (their weights are zero); heads past H read head
     // H-1 (their outputs are not stored).
-    const int lt = warp == 0 ? lane : (warp - 9) * 32 + lane;  // 0..127
+    const int lt = warp == 0 ? lane : (warp - 9) * 32 + lane;  // 0..255
     const int M = min(max(__ldg(ps.miss_count + b), 0), k);
     const bool repeats = __ldg(ps.miss_rows + b) != __ldg(ps.miss_count + b);
     const int j0 = c * kChunk;

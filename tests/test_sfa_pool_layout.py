@@ -1,6 +1,6 @@
 """Index arithmetic of the attention variant that reads its rows straight from
 the pool (csrc/sfa.cu, the kPool loader warps), restated on the CPU: over every
-score and value stage, the 16-byte copies of the 128 loader threads land inside
+score and value stage, the 16-byte copies of the 256 loader threads land inside
 their stage's tile, cover it exactly once, and put 16-byte column c of
 selection row p where a 128-byte-swizzled tile load of the selection would
 (row p at p * 128, column c at (c ^ (p & 7)) * 16); every source piece lies
@@ -13,7 +13,7 @@ kQBytes = kHeads * 128
 kKBytes = kHalf * 128
 kVBox = 64 * 128
 kVBytes = 4 * kVBox
-kLoaders = 128
+kLoaders = 256
 INT_MIN = -(1 << 31)
 
 
