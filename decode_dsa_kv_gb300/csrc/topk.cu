@@ -13,8 +13,8 @@
 //            digits, then the lowest positions among exact ties), set their
 //            bits, and write the set positions of the bitmap in order: the
 //            output comes out sorted without a sort.
-// Contexts up to 131,072 positions: one launch, one thread-block cluster of
-// 1 to 4 CTAs per request, each holding the keys of 32,768 positions in shared
+// Contexts up to 262,144 positions: one launch, one thread-block cluster of
+// 1 to 8 CTAs per request, each holding the keys of up to 32,768 positions in shared
 // memory; the CTAs merge their histograms through distributed shared memory,
 // rank 0 resolves the exact threshold and broadcasts it, and every CTA writes
 // its own slice of the sorted output. Longer contexts: hist and select spread
@@ -32,6 +32,9 @@ namespace {
 
 constexpr int kBins = 4096;    // top 12 bits of the key
 constexpr int kChunk = 8192;   // positions per CTA in the multi-CTA select
+constexpr int kSlice = 32768;  // positions per CTA of the cluster kernel (at most)
+constexpr int kClusterMaxG = 8;   // CTAs per request's cluster (the portable cluster size)
+constexpr int kClusterFillG = 4;  // at most this many only to fill the SMs (short contexts)
 constexpr int kHistChunk = 32768;  // positions per CTA in the multi-CTA hist (one wave at 4 x 1M)
 constexpr int kThreads = 512;  // multi-CTA kernels
 constexpr int kMaxK = 8192;
@@ -138,10 +141,12 @@ struct Cands {
 // A candidate list in up to four global segments (one per CTA of a cluster):
 // entry i lies in the segment s with off[s] <= i < off[s+1].
 struct SegCands {
-  const uint64_t* seg[4];
-  uint32_t off[5];
+  const uint64_t* seg[kClusterMaxG];
+  uint32_t off[kClusterMaxG + 1];
   __device__ __forceinline__ uint64_t operator()(uint32_t i) const {
-    const int s = (i >= off[1]) + (i >= off[2]) + (i >= off[3]);
+    int s = 0;
+#pragma unroll
+    for (int g = 1; g < kClusterMaxG; ++g) s += i >= off[g];
     return __ldcg(seg[s] + (i - off[s]));
   }
 };
@@ -268,8 +273,6 @@ __device__ void finish_chunks(const C& cand, uint32_t c, int t1, int need1, uint
 // per request, every CTA holding the keys of its 32,768-position slice in
 // shared memory; histograms merge through distributed shared memory.
 // ---------------------------------------------------------------------------
-constexpr int kSlice = 32768;
-constexpr int kClusterMaxG = 4;
 constexpr int kClusterMaxCtx = kSlice * kClusterMaxG;
 constexpr int kClThreads = 1024;
 constexpr int kClCandCap = 4096;  // candidates kept in shared memory by rank 0
@@ -374,12 +377,12 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_kernel(
   if (rank == 0 && ok) {
     SegCands cl;
     cl.off[0] = 0;
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < kClusterMaxG; ++g) {
       const uint32_t cg = g < G ? ld_dsmem_u32(dsmem_addr(&sm.ncand, g)) : 0u;
       cl.seg[g] = ws.cand + int64_t(b) * max_ctx + int64_t(g) * slice;
       cl.off[g + 1] = cl.off[g] + cg;
     }
-    const uint32_t c = cl.off[4];
+    const uint32_t c = cl.off[kClusterMaxG];
     uint32_t T, cut;
     if (c <= kClCandCap) {
       // the common case: the whole list in shared memory
@@ -621,14 +624,14 @@ ts_status launch_topk(const float* scores, int64_t ctx_stride, const int32_t* ct
     if (!raise_smem_limit(reinterpret_cast<const void*>(topk_cluster_kernel),
                           int(sizeof(ClSmem)), smem_set))
       return TS_ERR_CUDA;
-    // enough CTAs per request to fill half of the SMs when the requests are
-    // few (up to kClusterMaxG; the other half stays free for the kernels of
+    // enough CTAs per request for slices of at most kSlice positions (a
+    // multiple of 1024), and, when the requests are few, to fill half of the
+    // SMs (up to kClusterFillG; the other half stays free for the kernels of
     // the previous step still running, which would otherwise delay this
-    // launch), each with a slice of at most kSlice positions (a multiple of
-    // 1024)
+    // launch)
     int G = (max_ctx + kSlice - 1) / kSlice;
     const int fill = sm_count() / (2 * B);
-    if (fill > G) G = fill < kClusterMaxG ? fill : kClusterMaxG;
+    if (fill > G) G = max(G, min(fill, kClusterFillG));
     const int slice = ((max_ctx + G - 1) / G + 1023) / 1024 * 1024;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G, B, 1);
@@ -642,10 +645,30 @@ ts_status launch_topk(const float* scores, int64_t ctx_stride, const int32_t* ct
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, ctx_stride, ctx_len, k, max_ctx,
-                           slice, w, ids, err) != cudaSuccess)
-      return TS_ERR_CUDA;
-    return TS_OK;
+    // clusters above kClusterFillG CTAs of this size need a GPC with that many
+    // free SMs: asked of the device once per size (contexts that need them
+    // otherwise take the multi-launch path below)
+    bool fits = true;
+    if (G > kClusterFillG) {
+      static std::atomic<int> fit_known[kClusterMaxG + 1];  // 0 unknown, 1 yes, 2 no
+      int known = fit_known[G].load(std::memory_order_relaxed);
+      if (known == 0) {
+        int n = 0;
+        known = cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel, &cfg) == cudaSuccess &&
+                        n > 0
+                    ? 1
+                    : 2;
+        cudaGetLastError();
+        fit_known[G].store(known, std::memory_order_relaxed);
+      }
+      fits = known == 1;
+    }
+    if (fits) {
+      if (cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, ctx_stride, ctx_len, k, max_ctx,
+                             slice, w, ids, err) != cudaSuccess)
+        return TS_ERR_CUDA;
+      return TS_OK;
+    }
   }
   // histograms, list counters and completion counters start at zero
   if (cudaMemsetAsync(ws, 0, counters_bytes(B), stream) != cudaSuccess) return TS_ERR_CUDA;
