@@ -93,6 +93,9 @@ def parse(argv=None):
     ap.add_argument("--mtp", type=int, default=0, choices=(0, 1, 2, 3),
                     help="MTP draft steps whose queries are folded into the heads "
                          "(the step attends (1 + N) x H query rows over one selection)")
+    ap.add_argument("--profile-steps", type=int, default=10,
+                    help="steps after the timed region with every launch's timing events "
+                         "(the per-kernel figures other than the gather's)")
     ap.add_argument("--no-kernel-events", action="store_true",
                     help="time the steps without per-kernel events (no per-kernel roofline)")
     ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
@@ -568,7 +571,8 @@ def run_native(args, w, rank, world, local, overrides):
     # end-to-end steps each take the next step of the score process
     n_e2e = 0 if args.no_e2e else min(args.e2e_steps, args.steps)
     e2e_steps = (args.e2e_settle_steps + args.warmup + n_e2e) if n_e2e else 0
-    T = args.settle_steps + args.warmup + args.steps + e2e_steps
+    n_prof = 0 if args.no_kernel_events else max(1, args.profile_steps)
+    T = args.settle_steps + args.warmup + args.steps + n_prof + e2e_steps
     QS = max(1, min(args.query_slots, T))
     stream = wl.ScoreStream(w, first)
     # every registered host buffer of the run is made here, before any timing
@@ -632,9 +636,17 @@ def run_native(args, w, rank, world, local, overrides):
     # timed region: K steps, per-kernel events on the launching streams
     first_timed = cursor[0]
     miss_log = torch.zeros((args.steps, w.B), dtype=torch.int32, device="cuda")
-    # per-launch timing events of every timed step, created before the region
+    # timing events of every timed step, created before the region: only the
+    # step's first start, the gather's start and end (on its own stream) and
+    # the last attention's end -- every recorded event costs the streams time
+    # (measured: long_context 0.285 ms a step without any, 0.315 with every
+    # launch's); the other launches are timed on the steps after the region
     timings = (None if args.no_kernel_events
-               else [g.timing() for _ in range(args.steps)])
+               else [g.timing(light=True) for _ in range(args.steps)])
+    # every launch's events on n_prof steps enqueued right behind the timed
+    # region (the GPU does not idle in between; host reads after an idle
+    # pause run slowly)
+    prof = [g.timing() for _ in range(n_prof)]
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -650,15 +662,20 @@ def run_native(args, w, rank, world, local, overrides):
     t_enq1 = time.perf_counter()
     g.join(g.main)
     e1.record(g.main)
-    torch.cuda.synchronize()
+    for t in prof:
+        step(t)
+    e1.synchronize()
     t_wall1 = time.time()
+    g.join()
+    torch.cuda.synchronize()
     barrier(world)
     time.sleep(0.2)
     sampler.stop()
     ms_total = e0.elapsed_time(e1)
     bits = g.synchronize()
     if bits:
-        raise RuntimeError(f"device error bits {bits:#x} in the timed region")
+        raise RuntimeError(f"device error bits {bits:#x} in the timed region or the steps "
+                           "after it")
     # the link's peak measured again after the timed region; the higher of
     # the two is the denominator (one measurement alone has come out 25 % low)
     link = max(link, link_peak_gbs(torch, link_buf))
@@ -683,12 +700,22 @@ def run_native(args, w, rank, world, local, overrides):
     for t in timings or []:
         for n, v in t.ms().items():
             launch_ms[n].extend(v)
+    # every other launch's time from the n_prof steps run right after the
+    # timed region with all events (the input stream keeps running forward);
+    # the gather's stays the timed region's own
+    for t in prof:
+        for n, v in t.ms().items():
+            if n != "gather":
+                launch_ms[n].extend(v)
     for n in KERNELS:
         if not launch_ms[n]:
             continue
         ms = sum(launch_ms[n]) / len(launch_ms[n])
         per_kernel[n] = roofline_of(n, alg[n], ms, peaks, link)
-        per_kernel[n]["launches_per_step"] = len(launch_ms[n]) / args.steps
+        steps_n = args.steps if n == "gather" else n_prof
+        per_kernel[n]["launches_per_step"] = len(launch_ms[n]) / steps_n
+        per_kernel[n]["timed_in"] = ("the timed region" if n == "gather"
+                                     else f"{n_prof} steps after the timed region")
     if g.arrived is not None and "sfa" in per_kernel:
         # a streamed attention launch's events also span its wait for the
         # gather's rows: its own time comes from launches back to back on the
@@ -715,11 +742,11 @@ def run_native(args, w, rank, world, local, overrides):
                      "max_ms": round(float(spans.max()), 4),
                      "steps_over_2x_median": int(np.sum(spans > 2 * med)),
                      "spans_ms": [round(float(x), 3) for x in spans]}
-    # where the launches of the last timed step sat, in microseconds after its
-    # first launch began
+    # where the launches of the last profiled step sat, in microseconds after
+    # its first launch began
     last_spans = None
-    if timings:
-        t_last = timings[-1]
+    if prof:
+        t_last = prof[-1]
         first = t_last.events[0] if t_last.with_topk else t_last.events[2]
         last_spans = {n: [(round(a, 1), round(b, 1)) for a, b in v]
                       for n, v in t_last.spans(first).items()}

@@ -182,8 +182,10 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   const size_t q_bytes = size_t(L) * lb.q;
   void* q_stage = io ? static_cast<char*>(io->q_d) + (seq & 1u) * q_bytes : nullptr;
   if (io) q = q_stage;
+  // (a NULL entry of `timing` is left out: a caller may time only some launches)
   auto rec = [&](int slot, int end, cudaStream_t s) {
-    return timing ? cudaEventRecord(timing[2 * slot + end], s) == cudaSuccess : true;
+    cudaEvent_t e = timing ? timing[2 * slot + end] : nullptr;
+    return e ? cudaEventRecord(e, s) == cudaSuccess : true;
   };
 
   bool ok = true;

@@ -130,26 +130,36 @@ class HostKV:
 class StepTiming:
     """CUDA timing events for the launches of one step, created (and recorded
     once, which makes them valid) ahead of use, in the order dsa_group_step
-    fills them: top-k, plan, gather (every layer), sfa[l], refill[l]."""
+    fills them: top-k, plan, gather (every layer), sfa[l], refill[l].
+    light=True hands the step only the top-k's start, the gather's start and
+    end and the last attention's end (the step's span and the gather's time);
+    the other entries stay unrecorded."""
 
-    def __init__(self, layers: int, stream=None, refills: bool = True):
+    def __init__(self, layers: int, stream=None, refills: bool = True, light: bool = False):
         self.layers = layers
         self.refills = refills  # the reuse policy runs no refill
+        self.light = light
         n = 2 * (3 + 2 * layers)
         st = torch.cuda.current_stream() if stream is None else stream
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         for e in self.events:
             e.record(st)
-        self.array = (ctypes.c_void_p * n)(*[e.cuda_event for e in self.events])
+        keep = {0, 4, 5, 2 * (3 + layers - 1) + 1} if light else set(range(n))
+        self.array = (ctypes.c_void_p * n)(*[e.cuda_event if i in keep else None
+                                             for i, e in enumerate(self.events)])
         self.with_topk = True
 
     def ms(self) -> dict:
-        """name -> per-launch milliseconds (after the step completed)."""
+        """name -> per-launch milliseconds (after the step completed); with
+        light timing the gather only."""
         L = self.layers
         ev = self.events
 
         def pair(i):
             return ev[2 * i].elapsed_time(ev[2 * i + 1])
+
+        if self.light:
+            return {"gather": [pair(2)]}
 
         out = {"topk": [pair(0)] if self.with_topk else [], "plan": [pair(1)]}
         out["gather"] = [pair(2)]
@@ -271,9 +281,9 @@ class DecodeGroup:
         position j, the other rows are stale)."""
         return self.pool[l, b, self.P:]
 
-    def timing(self) -> StepTiming:
+    def timing(self, light: bool = False) -> StepTiming:
         """Timing events for one step of this group (see StepTiming)."""
-        return StepTiming(self.L, self.main, refills=self.policy == "fifo")
+        return StepTiming(self.L, self.main, refills=self.policy == "fifo", light=light)
 
     def _descriptor(self):
         d = abi.DsaGroup()

@@ -426,7 +426,9 @@ ts_status sfa_mla_decode_pool(const void* q, const void* pool_l, int P, const in
  * timing: NULL, or 2 * (3 + 2 * layers) events created by the caller, filled
  * as (start, end) pairs recorded on the launching stream around every
  * launch, in the order top-k, plan, gather (all layers), sfa[0..layers),
- * refill[0..layers) (the top-k pair is left alone when ids are given).
+ * refill[0..layers) (the top-k pair is left alone when ids are given); a
+ * NULL entry is not recorded (each recorded event costs the stream a little
+ * time, so a caller may time only the launches it needs).
  * Every operation's arguments are validated before anything is enqueued;
  * 1 <= layers <= TS_MAX_LAYERS. If a launch fails after the first one, every
  * sync word still receives this step's number, written on the side stream
