@@ -45,13 +45,18 @@ LAUNCHES_PLAN, LAUNCHES_GATHER = 1, 1
 
 
 def topk_launches(w) -> int:
-    return 1 if w.ctx <= 131072 else 2
+    """One cluster launch up to 262,144 positions (up to 8 CTAs a request),
+    else histogram, select and output launches."""
+    return 1 if w.ctx <= 262144 else 3
 
 
 def sfa_launches(w) -> int:
-    """1 when the chunks of a head tile (ceil(k / 512) of them) merge inside
-    one cluster (1, 2 or 4 chunks), else chunk kernel + merge kernel."""
-    return 1 if -(-w.k // 512) in (1, 2, 4) else 2
+    """The chunk kernel and the merge kernel of a layer's attention."""
+    return 2
+
+
+# after each layer's attention a one-thread kernel writes the layer's words
+LAUNCHES_POST = 1
 
 
 def parse(argv=None):
@@ -837,7 +842,7 @@ def run_native(args, w, rank, world, local, overrides):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * (topk_launches(w) + LAUNCHES_PLAN + LAUNCHES_GATHER
-                                      + w.layers * (sfa_launches(w)
+                                      + w.layers * (sfa_launches(w) + LAUNCHES_POST
                                                     + (1 if args.policy == "fifo" else 0))),
         "clocks": clocks,
         "hit_rate": hit_frac,

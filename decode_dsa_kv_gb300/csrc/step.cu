@@ -6,11 +6,13 @@
 //
 // Cross-stream ordering uses device words holding the step's sequence number:
 // a signal is a stream memory write issued on the producing stream (it lands
-// when the stream's prior work is complete) or, for the per-layer gather
-// signals, a write by the gather kernel itself once a layer's rows are in; a
-// wait is a stream memory wait that blocks the consuming stream until the
-// word, compared wrap-around, has reached that number. No kernel waits on
-// another: only the streams' front end polls the words, in HBM.
+// when the stream's prior work is complete), a one-thread kernel's write
+// after a layer's attention, or, for the per-layer gather signals, a write by
+// the gather kernel itself once a layer's rows are in; a wait is a stream
+// memory wait that blocks the consuming stream until the word, compared
+// wrap-around, has reached that number. No kernel waits on another (except
+// the streamed attention's bounded wait for its request's rows): only the
+// streams' front end polls the words, in HBM.
 #include <cuda.h>
 
 #include <type_traits>
@@ -90,6 +92,24 @@ bool signal(cudaStream_t s, uint32_t* word, uint32_t v) {
 bool wait_for(cudaStream_t s, const uint32_t* word, uint32_t v) {
   return memops().wait(reinterpret_cast<CUstream>(s), reinterpret_cast<CUdeviceptr>(word), v,
                        CU_STREAM_WAIT_VALUE_GEQ) == CUDA_SUCCESS;
+}
+
+// One thread writes a layer's words once the stream's earlier kernels are
+// complete (their writes are then visible on the GPU). A stream memory write
+// does the same but first takes a system-wide memory barrier, which waits
+// tens of microseconds while the gather keeps the host link busy (measured on
+// GB300 at the large_batch shape: the two writes between two layers' attention
+// launches held the next launch back by ~60 us; 18 us at decode_batch); a
+// kernel's own stores need no such barrier.
+__global__ void post_kernel(uint32_t* a, uint32_t va, uint32_t* b, uint32_t vb) {
+  __threadfence();
+  atomicExch(a, va);
+  if (b) atomicExch(b, vb);
+}
+
+bool post(cudaStream_t s, uint32_t* a, uint32_t va, uint32_t* b = nullptr, uint32_t vb = 0) {
+  post_kernel<<<1, 1, 0, s>>>(a, va, b, vb);
+  return launch_status() == TS_OK;
 }
 
 }  // namespace
@@ -213,6 +233,13 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
                              g.src_map, g.miss_ids, g.miss_pos, g.victim, g.install,
                              g.miss_count, g.miss_rows, g.ptr_next, g.err, m)) == TS_OK &&
        rec(1, 1, m) && signal(m, planned, seq) && wait_for(gs, planned, seq);
+  // every attention of this step overwrites `out`: with host I/O in the step
+  // before, the side stream copied each layer of it out, and the last copy
+  // wrote (seq - 1) * L + L - 1 (without, the step wrote that itself). One
+  // wait here, on the main stream ahead of the gather's traffic, covers
+  // every layer
+  const uint32_t seqL = seq * uint32_t(L);
+  ok = ok && (seq == 1 || wait_for(m, outcopied, seqL - 1));
   // one launch gathers every layer and writes seq into gathered[l] from the
   // device as soon as layer l's rows are in (no ramp between layers); it also
   // installs the misses whose victim slots no hit of the step reads (install
@@ -235,7 +262,7 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
     ok = ok && wait_for(side, planned, seq);
     for (int l = 0; ok && l < L; ++l)
       ok = ts_copy(at(q_stage, l, lb.q), at(io->q_h, l, lb.q), lb.q, side) == TS_OK &&
-           signal(side, qcopied, seq * uint32_t(L) + l);
+           post(side, qcopied, seq * uint32_t(L) + l);
   }
   // per layer: the attention on the main stream, the refill beside it on the
   // side stream; the last refill also updates the metadata. The staged
@@ -245,27 +272,27 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   // runs (so the gather that its CTAs wait for never waits for SMs they
   // hold) and the later layers follow it on the stream.
   // Each layer's output crosses to the host (host I/O) on the side stream,
-  // after the layer's refill; outcopied then holds seq * L + l. Every step's
-  // attention of layer l first waits for the previous step's copy of that
-  // layer's output (a step without host I/O writes the value itself), since
-  // it overwrites `out`.
-  const uint32_t seqL = seq * uint32_t(L);
+  // after the layer's refill; outcopied then holds seq * L + l (a step
+  // without host I/O writes the value itself, with attended[l]). Between two
+  // layers' attention launches the main stream holds only kernels: the words
+  // are written by post_kernel, not by stream memory writes.
   for (int l = 0; ok && l < L; ++l) {
     float* lse_l = g.lse ? at(g.lse, l, lb.lse) : nullptr;
     ok = (streamed ? (l > 0 || wait_for(m, started, seq)) : wait_for(m, gathered + l, seq)) &&
-         (!io || wait_for(m, qcopied, seqL + l)) &&
-         (seq == 1 || wait_for(m, outcopied, seqL - L + l)) && rec(3 + l, 0, m) &&
+         (!io || wait_for(m, qcopied, seqL + l)) && rec(3 + l, 0, m) &&
          (staged ? sfa_pool_enqueue(at(q, l, lb.q), at(g.pool, l, lb.pool), P, g.src_map,
                                     g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.H,
                                     g.k, g.scale, at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m,
                                     streamed ? g.arrived + size_t(l) * g.B : nullptr, gave_up)
                  : sfa_enqueue(at(q, l, lb.q), at(g.sel, l, lb.sel), g.B, g.H, g.k, g.scale,
                                at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m)) == TS_OK &&
-         rec(3 + l, 1, m) && signal(m, attended + l, seq) &&
-         (io || signal(m, outcopied, seqL + l));
+         rec(3 + l, 1, m) && post(m, attended + l, seq, io ? nullptr : outcopied, seqL + l);
+    // (staged: the refill copies staged rows into victim slots; an attention
+    // ends after its requests' rows are in unless its wait for them ran out,
+    // so the refill also waits for the gather's layer)
     if (refills)
       ok = ok && wait_for(side, (staged ? attended : gathered) + l, seq) &&
-           rec(3 + L + l, 0, side) &&
+           (!staged || wait_for(side, gathered + l, seq)) && rec(3 + L + l, 0, side) &&
            refill_enqueue(g.miss_ids, g.miss_pos, g.victim, g.install, g.miss_count, g.B, g.k,
                           staged ? nullptr : at(g.sel, l, lb.sel), at(g.pool, l, lb.pool), P,
                           l == L - 1, g.pool_tags, g.fifo_ptr, g.ptr_next, g.S, g.W, g.err, side,
@@ -276,7 +303,7 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
     if (io)
       ok = ok && wait_for(side, attended + l, seq) &&
            ts_copy(at(io->out_h, l, lb.out), at(g.out, l, lb.out), lb.out, side) == TS_OK &&
-           signal(side, outcopied, seqL + l);
+           post(side, outcopied, seqL + l);
   }
   if (lru) {
     // no refill: the plan updated the pool's metadata and the gather wrote

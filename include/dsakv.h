@@ -376,6 +376,7 @@ ts_status sfa_mla_decode_pool(const void* q, const void* pool_l, int P, const in
  * streams it issues:
  *
  *   main   : ts_topk(scores) -> wait refilled -> dsa_plan -> signal planned
+ *            -> wait for the previous step's output copies (host I/O only)
  *            -> for each layer l: wait gathered[l] -> sfa_mla_decode(l)
  *   gather : wait planned -> one launch gathering every layer (as
  *            dsa_gather_kv per layer, in layer order); the kernel itself
@@ -386,7 +387,10 @@ ts_status sfa_mla_decode_pool(const void* q, const void* pool_l, int P, const in
  *
  * Signals are writes of the step's sequence number into the caller's device
  * words `sync`: stream memory writes (cuStreamWriteValue32) for planned and
- * refilled, and the gather kernel's own writes for gathered[l]. Waits are
+ * refilled, the gather kernel's own writes for gathered[l], and a one-thread
+ * kernel's after each layer's attention (a stream memory write first takes a
+ * system-wide memory barrier, slow while the gather keeps the host link
+ * busy). Waits are
  * stream memory waits (cuStreamWaitValue32, compared wrap-around): the GPU's
  * front end polls device memory, with no event round trip, and no kernel
  * ever waits on another. Ordering: refill(l) evicts slots
@@ -399,9 +403,9 @@ ts_status sfa_mla_decode_pool(const void* q, const void* pool_l, int P, const in
  *
  * With layout = DSA_LAYOUT_STAGED the gather launch moves only the misses
  * (as dsa_stage_misses per layer), the attention is sfa_mla_decode_pool(l),
- * the main stream writes attended[l] after it, and refill(l) waits for
- * attended[l] instead of gathered[l] (the attention reads the hit slots in
- * place; the refill overwrites some of them).
+ * attended[l] is written after it on the main stream, and refill(l) waits for
+ * attended[l] as well as gathered[l] (the attention reads the hit slots in
+ * place; the refill overwrites some of them, from the staged rows).
  *
  * The descriptor holds the group's buffers (the caller owns all of them):
  *   ctx_len   int32 [B]                     k <= ctx_len[b] <= max_ctx
@@ -528,7 +532,7 @@ ts_status dsa_group_step(dsa_group* g, const float* scores, const void* q, const
  *          ticket; layer l's attention waits for that value
  *   side : after each layer's attention (and that layer's refill), the
  *          layer's output -> out_h (it also stays in the descriptor's `out`);
- *          the next step's attention of that layer waits for the copy
+ *          the next step's first attention waits for every layer's copy
  * So the scores the top-k waits for cross the host link alone, the queries
  * cross beside the gather, each layer's attention waits only for its own
  * layer's queries, and each layer's output crosses while later layers are
