@@ -575,8 +575,9 @@ def run_native(args, w, rank, world, local, overrides):
     # the input stream runs forward only: settle, warm-up, timed and
     # end-to-end steps each take the next step of the score process
     n_e2e = 0 if args.no_e2e else min(args.e2e_steps, args.steps)
-    e2e_steps = (args.e2e_settle_steps + args.warmup + n_e2e) if n_e2e else 0
     n_prof = 0 if args.no_kernel_events else max(1, args.profile_steps)
+    n_e2e_prof = min(3, n_prof) if n_e2e else 0
+    e2e_steps = (args.e2e_settle_steps + args.warmup + n_e2e + n_e2e_prof) if n_e2e else 0
     T = args.settle_steps + args.warmup + args.steps + n_prof + e2e_steps
     QS = max(1, min(args.query_slots, T))
     stream = wl.ScoreStream(w, first)
@@ -783,20 +784,23 @@ def run_native(args, w, rank, world, local, overrides):
         q_bytes = w.layers * w.B * w.H * 576 * 2
         o_bytes = g.out.numel() * 2
 
-        def e2e_step():
+        def e2e_step(timing=None):
             i = cursor[0]
             cursor[0] += 1
             # the step's inputs in and its attention output out, copied by the
             # SMs inside the step (dsa_group_step_host): the scores ahead of the
-            # top-k, the queries beside the top-k and plan, each layer's output
-            # right after its attention
+            # top-k, the queries beside the gather, each layer's output after
+            # its attention and refill
             g.step_host(scores_pin.dev + i * s_bytes, q_pin.dev + (i % QS) * q_bytes,
-                        out_pin.dev)
+                        out_pin.dev, timing=timing)
 
         e2e_settle = (settle(torch, g, e2e_step, args.e2e_settle_steps)
                       if args.e2e_settle_steps > 0 else 0)
         for _ in range(args.warmup):
             e2e_step()
+        # every launch's events on a few end-to-end steps right behind the
+        # timed ones (the copies themselves are not timed)
+        e2e_prof = [g.timing() for _ in range(n_e2e_prof)]
         torch.cuda.synchronize()
         barrier(world)
         f0 = torch.cuda.Event(enable_timing=True)
@@ -806,6 +810,8 @@ def run_native(args, w, rank, world, local, overrides):
             e2e_step()
         g.join(g.main)
         f1.record(g.main)
+        for t in e2e_prof:
+            e2e_step(t)
         torch.cuda.synchronize()
         if g.synchronize():
             raise RuntimeError("device error in the end-to-end steps")
@@ -815,6 +821,13 @@ def run_native(args, w, rank, world, local, overrides):
                "steps": n_e2e, "ms_per_step": e2e_ms, "settle_steps": e2e_settle,
                "copies": "inside the step (dsa_group_step_host: SM copies from / to page-locked "
                          "host memory from ts_host_alloc, overlapped with the step's work)"}
+        if e2e_prof:
+            # the launches of the last profiled end-to-end step, in microseconds
+            # after its top-k began (the scores' copy comes before it)
+            t_last = e2e_prof[-1]
+            e2e["last_step_spans_us"] = {
+                n: [(round(a, 1), round(b, 1)) for a, b in v]
+                for n, v in t_last.spans(t_last.events[0]).items()}
 
     clocks = sampler.summary(t_wall0, t_wall1)
     scores_steps = scores_pin.array[:first_timed + args.steps].copy() if rank == 0 else None
