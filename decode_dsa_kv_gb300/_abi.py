@@ -102,6 +102,7 @@ class DsaGroup(ctypes.Structure):
         ("layout", _I),
         ("lru_order", _P),
         ("arrived", _P),
+        ("layer_streams", _P),
     ]
 
 for _name, (_res, _args) in _SIGS.items():

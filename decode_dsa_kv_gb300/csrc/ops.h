@@ -111,6 +111,8 @@ ts_status sfa_check(const void* q, const void* sel_l, int B, int H, int k, float
                     void* out, const void* ws, size_t ws_bytes);
 ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, float scale,
                       void* out, float* lse, void* ws, int32_t* err, cudaStream_t stream);
+// CTAs of one attention launch's chunk kernel (chunks x head tiles x requests).
+uint32_t sfa_chunk_ctas(int B, int H, int k);
 // The attention reading its rows straight from a staged-layout pool by the
 // plan (hits: the slot; misses: the staged row at P + first position).
 ts_status sfa_pool_check(const void* q, const void* pool_l, int P, const int32_t* src_map,
@@ -122,6 +124,7 @@ ts_status sfa_pool_enqueue(const void* q, const void* pool_l, int P, const int32
                            const int32_t* miss_count, const int32_t* miss_rows, int B, int H,
                            int k, float scale, void* out, float* lse, void* ws, int32_t* err,
                            cudaStream_t stream, const uint32_t* arrived = nullptr,
-                           const uint32_t* gather_failed = nullptr);
+                           const uint32_t* gather_failed = nullptr,
+                           uint32_t* started = nullptr);
 
 }  // namespace dsakv

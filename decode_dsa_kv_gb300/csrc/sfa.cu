@@ -141,6 +141,9 @@ struct PoolSrc {
   // when *gather_failed is set. Null: the rows are all in at launch.
   const uint32_t* arrived;
   const uint32_t* gather_failed;
+  // optional: every CTA adds one as it starts (so the next layer's attention
+  // can be launched once all of this launch's CTAs hold their SMs)
+  uint32_t* started;
 };
 
 // 16-byte copies global -> shared that write shared memory as they land
@@ -212,6 +215,7 @@ __global__ void __launch_bounds__(kPool ? kPoolThreads : kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    if (kPool && ps.started) atomicAdd(ps.started, 1u);
     for (int s = 0; s < kSSlots; ++s) {
       mbar_init(&bars->full[s], kPool ? kLoaderThreads : 1);
       mbar_init(&bars->empty[s], 1);
@@ -704,6 +708,10 @@ ts_status sfa_check(const void* q, const void* sel_l, int B, int H, int k, float
   return TS_OK;
 }
 
+uint32_t sfa_chunk_ctas(int B, int H, int k) {
+  return uint32_t((k + kChunk - 1) / kChunk) * uint32_t((H + kHeads - 1) / kHeads) * uint32_t(B);
+}
+
 ts_status sfa_enqueue(const void* q, const void* sel_l, int B, int H, int k, float scale,
                       void* out, float* lse, void* ws, int32_t* err, cudaStream_t stream) {
   return launch_attention<false>(q, sel_l, PoolSrc{}, B, H, k, scale, out, lse, ws, err, stream);
@@ -727,11 +735,11 @@ ts_status sfa_pool_enqueue(const void* q, const void* pool_l, int P, const int32
                            const int32_t* miss_count, const int32_t* miss_rows, int B, int H,
                            int k, float scale, void* out, float* lse, void* ws, int32_t* err,
                            cudaStream_t stream, const uint32_t* arrived,
-                           const uint32_t* gather_failed) {
+                           const uint32_t* gather_failed, uint32_t* started) {
   if (arrived && !gather_failed) return TS_ERR_INVALID_ARG;
   const PoolSrc ps{src_map, miss_ids, miss_pos, miss_count, miss_rows,
                    static_cast<const uint8_t*>(pool_l), static_cast<const uint8_t*>(q), P, P + k,
-                   arrived, gather_failed};
+                   arrived, gather_failed, started};
   return launch_attention<true>(q, pool_l, ps, B, H, k, scale, out, lse, ws, err, stream);
 }
 

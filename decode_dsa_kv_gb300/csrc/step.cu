@@ -141,6 +141,21 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   // streamed attention: each layer's attention CTAs wait inside the kernel
   // for their own request's staged rows, counted by the running gather
   const bool streamed = staged && g.arrived && gather_streams(g.B, L);
+  // streamed, with layer streams: layer l's attention on its own stream, with
+  // its own workspace (sfa_workspace_size each), where one layer's attention
+  // CTAs fill at most half of the SMs. Measured on GB300 (streams against one
+  // stream): long_context 0.189 against 0.292 ms a step, adversarial 0.343
+  // against 0.374; at large_batch, whose every layer fills the SMs several
+  // times over, the later layers' waiting CTAs held the SMs the refills
+  // needed, and the step took 1.579 against 1.546 ms
+  const size_t ws_layer = sfa_workspace_size(g.B, g.H, g.k);
+  if (streamed && g.layer_streams) {
+    for (int l = 0; l < L; ++l)
+      if (!g.layer_streams[l]) return TS_ERR_INVALID_ARG;
+    if (g.sfa_ws_bytes < size_t(L) * ws_layer) return TS_ERR_WORKSPACE;
+  }
+  const bool lanes = streamed && g.layer_streams &&
+                     2 * int64_t(sfa_chunk_ctas(g.B, g.H, g.k)) <= int64_t(sm_count());
   // with reuse, the "pool" is the previous step's selection: k rows per request
   const int P = reuse ? g.k : g.S * g.W;
   Layers lb = layer_bytes(g);
@@ -196,6 +211,10 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   // CTAs, the started flag and the gave-up flag
   uint32_t* started = streamed ? g.arrived + size_t(L) * g.B + 1 : nullptr;
   uint32_t* gave_up = streamed ? started + 1 : nullptr;
+  // streamed: per layer, the attention CTAs that have started
+  uint32_t* lstarted = streamed ? g.arrived + size_t(L) * g.B + 3 : nullptr;
+  const uint32_t nctas = sfa_chunk_ctas(g.B, g.H, g.k);
+  auto astream = [&](int l) { return lanes ? g.layer_streams[l] : m; };
 
   // with host I/O: the copies' sizes; this step's half of the query staging
   const size_t scores_bytes = size_t(g.B) * size_t(g.ctx_stride) * 4;
@@ -214,7 +233,7 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   // every count it waited for was complete; this step's gather waits for the
   // plan, after this)
   if (streamed)
-    ok = cudaMemsetAsync(g.arrived, 0, (size_t(L) * g.B + 3) * 4, m) == cudaSuccess;
+    ok = cudaMemsetAsync(g.arrived, 0, (size_t(L) * g.B + 3 + L) * 4, m) == cudaSuccess;
   // with host I/O the scores cross first, on the main stream ahead of the top-k
   if (io) ok = ok && ts_copy(io->scores_d, io->scores_h, scores_bytes, m) == TS_OK;
   if (!ids) {
@@ -238,8 +257,9 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   // wrote (seq - 1) * L + L - 1 (without, the step wrote that itself). One
   // wait here, on the main stream ahead of the gather's traffic, covers
   // every layer
+  // (with layer streams each layer's stream waits for its own layer's copy)
   const uint32_t seqL = seq * uint32_t(L);
-  ok = ok && (seq == 1 || wait_for(m, outcopied, seqL - 1));
+  ok = ok && (lanes || seq == 1 || wait_for(m, outcopied, seqL - 1));
   // one launch gathers every layer and writes seq into gathered[l] from the
   // device as soon as layer l's rows are in (no ramp between layers); it also
   // installs the misses whose victim slots no hit of the step reads (install
@@ -271,22 +291,37 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   // Streamed, the first layer's attention launches once every gather CTA
   // runs (so the gather that its CTAs wait for never waits for SMs they
   // hold) and the later layers follow it on the stream.
+  // With layer streams, layer l's attention runs on layer_streams[l] and
+  // launches once every CTA of layer l - 1's attention has started, so the
+  // CTAs still reach the SMs in the gather's layer-then-request order (no
+  // waiting CTA of a later layer takes an SM a CTA of an earlier layer
+  // needs) while the layers overlap where one layer's CTAs leave SMs idle;
+  // every layer stream first waits for this step's gather to run (after the
+  // counts were zeroed), and for the step before's copy of its layer's output.
   // Each layer's output crosses to the host (host I/O) on the side stream,
   // after the layer's refill; outcopied then holds seq * L + l (a step
-  // without host I/O writes the value itself, with attended[l]). Between two
-  // layers' attention launches the main stream holds only kernels: the words
-  // are written by post_kernel, not by stream memory writes.
+  // without host I/O writes the value itself: with attended[l], or with
+  // layer streams once on the main stream after every layer). Between two
+  // layers' attention launches a stream holds only kernels: the words are
+  // written by post_kernel, not by stream memory writes.
   for (int l = 0; ok && l < L; ++l) {
     float* lse_l = g.lse ? at(g.lse, l, lb.lse) : nullptr;
-    ok = (streamed ? (l > 0 || wait_for(m, started, seq)) : wait_for(m, gathered + l, seq)) &&
-         (!io || wait_for(m, qcopied, seqL + l)) && rec(3 + l, 0, m) &&
+    const cudaStream_t a = astream(l);
+    void* ws_l = lanes ? static_cast<char*>(g.sfa_ws) + size_t(l) * ws_layer : g.sfa_ws;
+    ok = (streamed ? ((l > 0 && !lanes) || wait_for(a, started, seq))
+                   : wait_for(a, gathered + l, seq)) &&
+         (!lanes || l == 0 || wait_for(a, lstarted + l - 1, nctas)) &&
+         (!lanes || seq == 1 || wait_for(a, outcopied, seqL - L + l)) &&
+         (!io || wait_for(a, qcopied, seqL + l)) && rec(3 + l, 0, a) &&
          (staged ? sfa_pool_enqueue(at(q, l, lb.q), at(g.pool, l, lb.pool), P, g.src_map,
                                     g.miss_ids, g.miss_pos, g.miss_count, g.miss_rows, g.B, g.H,
-                                    g.k, g.scale, at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m,
-                                    streamed ? g.arrived + size_t(l) * g.B : nullptr, gave_up)
+                                    g.k, g.scale, at(g.out, l, lb.out), lse_l, ws_l, g.err, a,
+                                    streamed ? g.arrived + size_t(l) * g.B : nullptr, gave_up,
+                                    streamed ? lstarted + l : nullptr)
                  : sfa_enqueue(at(q, l, lb.q), at(g.sel, l, lb.sel), g.B, g.H, g.k, g.scale,
-                               at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, m)) == TS_OK &&
-         rec(3 + l, 1, m) && post(m, attended + l, seq, io ? nullptr : outcopied, seqL + l);
+                               at(g.out, l, lb.out), lse_l, g.sfa_ws, g.err, a)) == TS_OK &&
+         rec(3 + l, 1, a) &&
+         post(a, attended + l, seq, (io || lanes) ? nullptr : outcopied, seqL + l);
     // (staged: the refill copies staged rows into victim slots; an attention
     // ends after its requests' rows are in unless its wait for them ran out,
     // so the refill also waits for the gather's layer)
@@ -304,6 +339,13 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
       ok = ok && wait_for(side, attended + l, seq) &&
            ts_copy(at(io->out_h, l, lb.out), at(g.out, l, lb.out), lb.out, side) == TS_OK &&
            post(side, outcopied, seqL + l);
+  }
+  // with layer streams the main stream then waits for every layer's
+  // attention: what follows on it (the next step's plan, which the next
+  // gather waits for) comes after every attention of this step
+  if (lanes) {
+    for (int l = 0; ok && l < L; ++l) ok = wait_for(m, attended + l, seq);
+    ok = ok && (io || post(m, outcopied, seqL + L - 1));
   }
   if (lru) {
     // no refill: the plan updated the pool's metadata and the gather wrote
@@ -331,13 +373,15 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
   if (!ok) {
     // give every signal word this step's number, so that no wait enqueued
     // now or by the next call is left without its signal. The side stream
-    // first waits for everything already enqueued on the other two streams
+    // first waits for everything already enqueued on the other streams
     // (every wait enqueued there has its signal: a per-layer wait is
-    // enqueued only after the gather launch that writes it), so no signal
-    // lands while a kernel of this step still reads or writes the pool
-    cudaEvent_t ev[2] = {nullptr, nullptr};
-    const cudaStream_t others[2] = {m, gs};
-    for (int i = 0; i < 2; ++i)
+    // enqueued only after the launch that writes it), so no signal lands
+    // while a kernel of this step still reads or writes the pool
+    cudaEvent_t ev[2 + TS_MAX_LAYERS] = {};
+    cudaStream_t others[2 + TS_MAX_LAYERS] = {m, gs};
+    const int n_others = 2 + (lanes ? L : 0);
+    for (int l = 0; lanes && l < L; ++l) others[2 + l] = g.layer_streams[l];
+    for (int i = 0; i < n_others; ++i)
       if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess &&
           cudaEventRecord(ev[i], others[i]) == cudaSuccess)
         cudaStreamWaitEvent(side, ev[i], 0);
@@ -349,7 +393,7 @@ ts_status enqueue_step(dsa_group* gp, const float* scores, const void* q, const 
     }
     if (io) signal(side, qcopied, seqL + L - 1);
     signal(side, outcopied, seqL + L - 1);
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < n_others; ++i)
       if (ev[i]) cudaEventDestroy(ev[i]);
     cudaGetLastError();
     return TS_ERR_CUDA;

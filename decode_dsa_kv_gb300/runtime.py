@@ -197,8 +197,9 @@ class DecodeGroup:
     straight from the pool, which then holds P + k rows per request (rows P..
     stage the step's misses at their first positions) and `sel` is None.
     With `streamed` (staged only; B <= 1024) each layer's attention starts
-    while the gather runs, every CTA waiting for its own request's rows;
-    otherwise each layer's attention waits for the whole layer."""
+    while the gather runs, every CTA waiting for its own request's rows, each
+    layer on a stream of its own (launched once the previous layer's CTAs all
+    run); otherwise each layer's attention waits for the whole layer."""
 
     def __init__(self, B: int, layers: int, k: int, S: int, W: int, H: int,
                  ctx_len, ctx_stride: int, host: HostKV, scale: float | None = None,
@@ -253,7 +254,9 @@ class DecodeGroup:
         self.lse = torch.empty((layers, B, H), dtype=torch.float32, device=dev)
         # workspaces and the device error word
         self.topk_ws_bytes = abi.ts_topk_workspace_size(B, self.max_ctx, k)
-        self.sfa_ws_bytes = abi.sfa_workspace_size(B, H, k)
+        streamed = layout == "staged" and streamed
+        # streamed: one attention workspace per layer (the layers overlap)
+        self.sfa_ws_bytes = abi.sfa_workspace_size(B, H, k) * (layers if streamed else 1)
         self.topk_ws = torch.empty(self.topk_ws_bytes, dtype=torch.uint8, device=dev)
         self.sfa_ws = torch.empty(self.sfa_ws_bytes, dtype=torch.uint8, device=dev)
         self.err = torch.zeros((1,), **i32)
@@ -263,13 +266,19 @@ class DecodeGroup:
         self.main = torch.cuda.Stream(device=dev, priority=-1)
         self.gstream = torch.cuda.Stream(device=dev, priority=0)
         self.side = torch.cuda.Stream(device=dev, priority=0)
+        # streamed: each layer's attention on its own stream
+        self.lstreams = ([torch.cuda.Stream(device=dev, priority=-1) for _ in range(layers)]
+                         if streamed else [])
+        self._lstream_handles = (ctypes.c_void_p * max(1, layers))(
+            *[st.cuda_stream for st in self.lstreams])
         # cross-stream signals: device words written and waited on by the
         # streams themselves (zero before the first step)
         self.sync = torch.zeros((5 + 3 * layers,), **i32)
         # staged layout: per (layer, request) arrival counts of the gather, so
-        # that each attention CTA starts once its own request's rows are in
-        self.arrived = (torch.zeros((layers * B + 3,), **i32)
-                        if layout == "staged" and streamed else None)
+        # that each attention CTA starts once its own request's rows are in;
+        # the gather's start words; each layer's started attention CTAs
+        self.arrived = (torch.zeros((layers * B + 3 + layers,), **i32)
+                        if streamed else None)
         # device staging of dsa_group_step_host (made on first use)
         self._io_scores = None
         self._io_q = None
@@ -302,6 +311,7 @@ class DecodeGroup:
         d.sfa_ws, d.sfa_ws_bytes = self.sfa_ws.data_ptr(), self.sfa_ws_bytes
         d.err = self.err.data_ptr()
         d.arrived = 0 if self.arrived is None else self.arrived.data_ptr()
+        d.layer_streams = (ctypes.addressof(self._lstream_handles) if self.lstreams else 0)
         if self.policy == "lru":
             d.policy = abi.DSA_POLICY_LRU
             d.lru_order = self.lru_order.data_ptr()
@@ -364,10 +374,14 @@ class DecodeGroup:
         st.wait_stream(self.main)
         st.wait_stream(self.gstream)
         st.wait_stream(self.side)
+        for ls in self.lstreams:
+            st.wait_stream(ls)
 
     def synchronize(self) -> int:
         """Wait for everything and return (and clear) the device error bits."""
         self.main.synchronize()
         self.gstream.synchronize()
         self.side.synchronize()
+        for ls in self.lstreams:
+            ls.synchronize()
         return abi.ts_read_error(self.err, self.main)

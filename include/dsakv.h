@@ -378,6 +378,7 @@ ts_status sfa_mla_decode_pool(const void* q, const void* pool_l, int P, const in
  *   main   : ts_topk(scores) -> wait refilled -> dsa_plan -> signal planned
  *            -> wait for the previous step's output copies (host I/O only)
  *            -> for each layer l: wait gathered[l] -> sfa_mla_decode(l)
+ *            (or on the layer streams below)
  *   gather : wait planned -> one launch gathering every layer (as
  *            dsa_gather_kv per layer, in layer order); the kernel itself
  *            writes gathered[l] once layer l's rows are all in
@@ -500,17 +501,31 @@ typedef struct {
    * are not used and no refill runs (every install is written by the gather
    * as its row arrives). */
   int32_t* lru_order;
-  /* DSA_LAYOUT_STAGED only, optional: uint32 [layers * B + 3] device words
-   * (zeroed by each step itself). When given (and B <= 1024, layers * B <
-   * 65535), each layer's attention starts as soon as the gather is running
-   * and each of its CTAs waits, inside the kernel, for its own request's
-   * missed rows of that layer (the gather counts every stored row into
-   * arrived[l * B + b]); words layers * B .. + 2 count the gather's CTAs that
-   * started, hold the step number once all have, and flag a gather that gave
-   * up. The attention of a request then overlaps the gather of the requests
-   * after it, and only the last requests' attention follows the gather's
-   * end. NULL: each layer's attention waits for the whole layer's rows. */
+  /* DSA_LAYOUT_STAGED only, optional: uint32 [layers * B + 3 + layers]
+   * device words (zeroed by each step itself). When given (and B <= 1024,
+   * layers * B < 65535), each layer's attention starts as soon as the gather
+   * is running and each of its CTAs waits, inside the kernel, for its own
+   * request's missed rows of that layer (the gather counts every stored row
+   * into arrived[l * B + b]); words layers * B .. + 2 count the gather's CTAs
+   * that started, hold the step number once all have, and flag a gather that
+   * gave up; the last `layers` words count each layer's attention CTAs that
+   * started. The attention of a request then overlaps the gather of the
+   * requests after it, and only the last requests' attention follows the
+   * gather's end. NULL: each layer's attention waits for the whole layer's
+   * rows. */
   uint32_t* arrived;
+  /* With `arrived`, optional: `layers` streams (none of them NULL), and
+   * sfa_ws must then hold one workspace per layer, layers *
+   * sfa_workspace_size(B, H, k) bytes. Where one layer's attention has at
+   * most half as many CTAs as the GPU has SMs (ceil(k / 512) * ceil(H / 128)
+   * * B of them: few requests), layer l's attention (its two launches and
+   * its words) then runs on layer_streams[l], launched once every CTA of
+   * layer l - 1's attention has started (the CTAs still reach the SMs in the
+   * gather's layer-then-request order), so the layers' attention overlaps,
+   * and the main stream waits for every layer's attention at the end of the
+   * step. Otherwise, or NULL: every layer's attention on the main stream, one
+   * after another. */
+  cudaStream_t* layer_streams;
 } dsa_group;
 
 #define DSA_POLICY_FIFO 0

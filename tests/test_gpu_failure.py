@@ -98,14 +98,16 @@ def test_group_step_orders_streams_under_delays(d, layout):
             "install": torch.empty((T, w.B, w.k), dtype=torch.uint8, device="cuda"),
             "mc": torch.empty((T, w.B), dtype=torch.int32, device="cuda")}
     torch.cuda.synchronize()
-    delayed = (g.side, g.gstream, g.main)
+    delayed = (g.side, g.gstream, g.main) + tuple(g.lstreams[1:2])
     for t in range(T):
         # about 2 ms of spinning ahead of this step's work on one stream:
         # the refill (then the next plan must wait for it), the gather (the
-        # attention and the refill must wait), or the top-k, plan and
+        # attention and the refill must wait), the top-k, plan and
         # attention (the gather must wait for the plan; with the staged layout
-        # the refill must wait for the attention)
-        with torch.cuda.stream(delayed[t % 3]):
+        # the refill must wait for the attention), or (streamed) layer 1's
+        # attention stream (the later layers, that layer's refill and the
+        # next step's plan must wait for it)
+        with torch.cuda.stream(delayed[t % len(delayed)]):
             torch.cuda._sleep(4_000_000)
         g.step(scores_d[t], q_d[t])
         with torch.cuda.stream(g.main):   # after the step's last attention
