@@ -58,8 +58,9 @@ ts_status gather_check(const int32_t* src_map, const int32_t* miss_ids, const in
 // out to the warps dynamically, layer after layer. With `victim` and `install` (dsa_plan's) given,
 // the misses with install code 1 are also written into their victim slots
 // of the pool as they arrive (the refill then needs only min_install = 2).
-// With `arrived` (staged, dynamic and gather_streams(B, layers) only:
-// uint32 [layers * B + 3], zero before the launch) the kernel adds every
+// With `arrived` (staged, dynamic and gather_streams(B, layers) only: its
+// first layers * B + 3 uint32 words, zero before the launch; the attention's
+// per-layer start counts follow them) the kernel adds every
 // stored row to arrived[l * B + b], counts its CTAs in word layers * B,
 // writes seq into word layers * B + 1 once every CTA runs, and sets word
 // layers * B + 2 if it gives up (sfa_pool_enqueue's `arrived` waits on these).

@@ -187,3 +187,21 @@ def test_group_step_refusals():
     assert L.dsa_group_step(ctypes.byref(g), A, A, None, None) == INVALID     # unknown policy
     g.policy, g.sync = 0, A + 2
     assert L.dsa_group_step(ctypes.byref(g), A, A, None, None) == INVALID     # sync word misaligned
+
+
+def test_group_step_layer_stream_refusals():
+    # layer streams (streamed staged layout): none of them NULL, and one
+    # attention workspace per layer; refused before anything is enqueued
+    g = _abi.DsaGroup()
+    g.B, g.layers, g.k, g.S, g.W, g.H = 2, 2, 16, 8, 4, 128
+    g.layout, g.policy = _abi.DSA_LAYOUT_STAGED, _abi.DSA_POLICY_FIFO
+    g.sync, g.arrived = A, A2
+    streams = (ctypes.c_void_p * 2)(0x1234, None)
+    g.layer_streams = ctypes.addressof(streams)
+    assert L.dsa_group_step(ctypes.byref(g), A, A, None, None) == INVALID     # a NULL layer stream
+    streams[1] = 0x5678
+    g.sfa_ws_bytes = L.sfa_workspace_size(2, 128, 16)                          # one layer's only
+    assert L.dsa_group_step(ctypes.byref(g), A, A, None, None) == _abi.TS_ERR_WORKSPACE
+    g.sfa_ws_bytes = 2 * L.sfa_workspace_size(2, 128, 16)
+    assert L.dsa_group_step(ctypes.byref(g), A, A, None, None) == INVALID     # null buffers next
+    assert g.step == 0
