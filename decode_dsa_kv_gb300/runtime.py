@@ -377,6 +377,47 @@ class DecodeGroup:
         for ls in self.lstreams:
             st.wait_stream(ls)
 
+    # -- checkpoint / resume ---------------------------------------------
+    def state(self) -> dict:
+        """The pool's state after the steps so far, as host arrays (numpy): its
+        metadata (tags, FIFO pointers, LRU order) and every layer's slot rows;
+        with the reuse policy the previous step's ids and selection instead of
+        the pool. Waits for the group's streams first (raises if the device
+        reported an error). load_state puts it into a group of the same
+        shapes, after which that group continues as this one would; a test
+        resumes the oracle from the same arrays (tags, pointers and rows of
+        one request)."""
+        if self.synchronize():
+            raise RuntimeError("device error bits set before the checkpoint")
+        st = {"tags": self.tags.cpu().numpy(), "fifo_ptr": self.fifo_ptr.cpu().numpy(),
+              "lru_order": self.lru_order.cpu().numpy()}
+        if self.policy == "reuse":
+            st["prev_ids"] = self._bufs[self.desc.prev_ids].cpu().numpy()
+            st["prev_sel"] = self._bufs[self.desc.prev_sel].cpu().numpy()
+        else:
+            st["pool"] = self.pool[:, :, :self.P].cpu().numpy()
+        return st
+
+    def load_state(self, st: dict) -> None:
+        """Put a state from state() into this group (its streams idle); the
+        group's own step count and ordering words carry on as they are."""
+        self.synchronize()
+
+        def put(t: torch.Tensor, a: np.ndarray):
+            if tuple(t.shape) != a.shape:
+                raise ValueError(f"state of shape {a.shape} for a buffer of {tuple(t.shape)}")
+            t.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+
+        put(self.tags, st["tags"])
+        put(self.fifo_ptr, st["fifo_ptr"])
+        put(self.lru_order, st["lru_order"])
+        if self.policy == "reuse":
+            put(self._bufs[self.desc.prev_ids], st["prev_ids"])
+            put(self._bufs[self.desc.prev_sel], st["prev_sel"])
+        else:
+            put(self.pool[:, :, :self.P], st["pool"])
+        torch.cuda.synchronize(self.pool.device)
+
     def synchronize(self) -> int:
         """Wait for everything and return (and clear) the device error bits."""
         self.main.synchronize()
