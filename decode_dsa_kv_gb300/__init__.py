@@ -19,7 +19,7 @@ _ABI_NAMES = {
     "sfa_workspace_size", "sfa_mla_decode", "dsa_group_step", "dsa_group_step_host", "DsaGroup", "DsaKvError", "check", "status_string", "EXPORTS",
     "LIB_PATH",
 }
-_RUNTIME_NAMES = {"HostKV", "DecodeGroup", "PinnedHost", "StepTiming"}
+_RUNTIME_NAMES = {"HostKV", "DecodeGroup", "PinnedHost", "StepTiming", "plan_metrics"}
 
 
 def __getattr__(name):

@@ -38,6 +38,33 @@ D = 576
 DV = 512
 
 
+def plan_metrics(miss_rows, miss_count, miss_ids, install, k: int, S: int) -> dict:
+    """Per-request counts of one step's plan, from its outputs as host arrays
+    ([B], [B], [B][k], [B][k] or None): positions that hit (k minus the
+    positions that miss, repeats included), distinct misses, misses installed
+    (install code 1 or 2) and overflow sets (sets that missed more tokens than
+    they have ways: their earliest misses are not installed). Each a list of
+    B ints; installs and overflow sets are None without an install array
+    (the reuse policy installs nothing)."""
+    miss_rows = np.asarray(miss_rows)
+    miss_count = np.asarray(miss_count)
+    B = miss_count.shape[0]
+    out = {"hits": [int(k - miss_rows[b]) for b in range(B)],
+           "misses": [int(miss_count[b]) for b in range(B)],
+           "installs": None, "overflow_sets": None}
+    if install is not None:
+        install = np.asarray(install)
+        miss_ids = np.asarray(miss_ids)
+        out["installs"], out["overflow_sets"] = [], []
+        for b in range(B):
+            M = int(miss_count[b])
+            codes = install[b, :M]
+            out["installs"].append(int(np.count_nonzero(codes)))
+            dropped = miss_ids[b, :M][codes == 0]
+            out["overflow_sets"].append(int(np.unique(dropped % S).size))
+    return out
+
+
 class PinnedHost:
     """A page-locked host buffer the device reads and writes in place, seen as
     a numpy array (zero-filled). kind="alloc" (default): ts_host_alloc memory,
@@ -376,6 +403,12 @@ class DecodeGroup:
         st.wait_stream(self.side)
         for ls in self.lstreams:
             st.wait_stream(ls)
+
+    def metrics(self) -> dict:
+        """plan_metrics of the last step's plan (after synchronize())."""
+        install = None if self.policy == "reuse" else self.install.cpu().numpy()
+        return plan_metrics(self.miss_rows.cpu().numpy(), self.miss_count.cpu().numpy(),
+                            self.miss_ids.cpu().numpy(), install, self.k, self.S)
 
     # -- checkpoint / resume ---------------------------------------------
     def state(self) -> dict:
