@@ -61,3 +61,38 @@ def test_group_step_validation_without_gpu():
     assert d.dsa_group_step(g, q, q + 8) == _abi.TS_ERR_INVALID_ARG         # q misaligned
     assert d.dsa_group_step(g, q, q) == _abi.TS_ERR_INVALID_ARG             # null buffers
     assert g.step == 0                                                      # nothing enqueued
+
+
+def header_struct_fields(name, path=None):
+    """(field, C type) of `typedef struct { ... } name;` in the header, in order."""
+    import re
+
+    from _util import HEADER
+    text = open(path or HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    body = re.search(r"typedef struct \{(.*?)\}\s*" + name + r"\s*;", text, flags=re.S).group(1)
+    fields = []
+    for decl in body.split(";"):
+        decl = " ".join(decl.split())
+        if not decl:
+            continue
+        m = re.match(r"((?:const )?\w+)\s*(.*)", decl)
+        base, rest = m.group(1), m.group(2)
+        for item in rest.split(","):
+            item = item.strip()
+            stars = item.count("*")
+            fields.append((item.replace("*", "").strip(), base + "*" * stars))
+    return fields
+
+
+def test_binding_descriptor_matches_the_header_field_by_field():
+    # the ctypes descriptor must lay out exactly what dsa_group_step reads:
+    # the same fields, in the same order, each of the same size
+    from decode_dsa_kv_gb300 import _abi
+    c_size = {"int": 4, "int64_t": 8, "float": 4, "size_t": 8, "uint32_t": 4}
+    header = header_struct_fields("dsa_group")
+    binding = _abi.DsaGroup._fields_
+    assert [f for f, _ in header] == [f for f, _ in binding]
+    for (f, ctype), (_, pytype) in zip(header, binding):
+        want = 8 if ctype.endswith("*") or ctype == "cudaStream_t" else c_size[ctype]
+        assert ctypes.sizeof(pytype) == want, (f, ctype, pytype)
