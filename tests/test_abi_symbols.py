@@ -96,3 +96,25 @@ def test_binding_descriptor_matches_the_header_field_by_field():
     for (f, ctype), (_, pytype) in zip(header, binding):
         want = 8 if ctype.endswith("*") or ctype == "cudaStream_t" else c_size[ctype]
         assert ctypes.sizeof(pytype) == want, (f, ctype, pytype)
+
+
+def header_param_counts(path=None):
+    """name -> number of parameters of every function the header declares."""
+    import re
+
+    from _util import HEADER
+    text = open(path or HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(([^)]*)\)\s*;", text, flags=re.M):
+        params = " ".join(m.group(2).split())
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_take_as_many_arguments_as_the_header():
+    from decode_dsa_kv_gb300 import _abi
+    counts = header_param_counts()
+    assert set(counts) == set(header_functions())
+    for name, n in counts.items():
+        assert len(_abi._SIGS[name][1]) == n, name
