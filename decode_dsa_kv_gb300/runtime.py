@@ -282,7 +282,9 @@ class DecodeGroup:
         # workspaces and the device error word
         self.topk_ws_bytes = abi.ts_topk_workspace_size(B, self.max_ctx, k)
         streamed = layout == "staged" and streamed
-        # streamed: one attention workspace per layer (the layers overlap)
+        # streamed: one attention workspace per layer and a stream per layer
+        # (the library runs the layers' attention side by side where one
+        # layer's CTAs fill at most half of the SMs, else on the main stream)
         self.sfa_ws_bytes = abi.sfa_workspace_size(B, H, k) * (layers if streamed else 1)
         self.topk_ws = torch.empty(self.topk_ws_bytes, dtype=torch.uint8, device=dev)
         self.sfa_ws = torch.empty(self.sfa_ws_bytes, dtype=torch.uint8, device=dev)
@@ -293,7 +295,6 @@ class DecodeGroup:
         self.main = torch.cuda.Stream(device=dev, priority=-1)
         self.gstream = torch.cuda.Stream(device=dev, priority=0)
         self.side = torch.cuda.Stream(device=dev, priority=0)
-        # streamed: each layer's attention on its own stream
         self.lstreams = ([torch.cuda.Stream(device=dev, priority=-1) for _ in range(layers)]
                          if streamed else [])
         self._lstream_handles = (ctypes.c_void_p * max(1, layers))(
